@@ -1,0 +1,225 @@
+/*
+ * mtkv.h — C ABI of libmtkv: grouped-query decode attention over a paged KV
+ * cache, and the kernels that feed it, for NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ *  - Plain pointers and sizes only. "device" pointers are CUDA device
+ *    addresses (for example from a torch tensor's data_ptr()), "host"
+ *    pointers are ordinary CPU memory.
+ *  - Ownership: the caller owns every buffer. The library allocates no
+ *    device memory; calls that need scratch take a caller-provided
+ *    workspace whose size comes from the matching *_workspace_bytes call.
+ *  - Execution: compute calls are asynchronous on `stream` (a cudaStream_t;
+ *    NULL is the legacy default stream). Arguments that can be checked on
+ *    the host are checked before anything is launched; a failed check
+ *    returns a status and launches nothing. Checks that need device data
+ *    (block ids, context lengths, cells) run inside the kernels: an
+ *    out-of-range value is skipped (never dereferenced) and recorded in a
+ *    caller-owned 32-bit device status word, read back with
+ *    mt_check_device_status().
+ *  - Errors: every call returns mt_status; mt_last_error() gives a
+ *    human-readable reason for the last failure on the calling thread.
+ *  - The storage format is an explicit argument of every call; there is no
+ *    process-wide format setting.
+ *  - No call aborts or traps; device-side waits are bounded and report
+ *    MT_ERR_TIMEOUT through the status word instead of hanging.
+ */
+#ifndef MTKV_H
+#define MTKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *mt_stream; /* a cudaStream_t */
+
+/* KV storage formats — "KV Cache Design — cells, format, sessions",
+ * section 3 (KvFormat {f32, f16, q8_0}). An unknown value is an error. */
+typedef enum { MT_KV_F32 = 0, MT_KV_F16 = 1, MT_KV_Q8_0 = 2 } mt_kv_format;
+
+typedef enum {
+  MT_OK = 0,
+  MT_ERR_INVALID_ARG = 1,  /* null pointer, negative size, inconsistent shape  */
+  MT_ERR_UNSUPPORTED = 2,  /* valid but outside the built kernels' shape set   */
+  MT_ERR_ORDER = 3,        /* move list would overwrite a row not yet copied   */
+  MT_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out               */
+  MT_ERR_DEVICE_CHECK = 5, /* a kernel met an out-of-range id / length / cell  */
+  MT_ERR_CUDA = 6          /* a CUDA runtime call failed                       */
+} mt_status;
+
+/* Device status word bits (see mt_check_device_status). */
+#define MT_STATUS_BIT_DEVICE_CHECK 1u
+#define MT_STATUS_BIT_TIMEOUT 2u
+
+/* Hole marker in a block table — "Tiered KV cache — architecture",
+ * sections "The paged-attention block model" (item 3, holes) and "Kernel
+ * dispatch" (kInvalidBlockTableEntry): its positions get logit -infinity. */
+#define MT_INVALID_BLOCK_ID (-1)
+
+/* A run of `len` rows (cells) moving from cell `src` to cell `dst`. */
+typedef struct {
+  int64_t src;
+  int64_t dst;
+  int64_t len;
+} mt_move;
+
+/* Bytes of one cell (one token's K, or V, for all KV heads).
+ * "KV Cache Design — cells, format, sessions", section 3: f32 4*Hkv*d,
+ * f16 2*Hkv*d, q8_0 a whole number of 34-byte Q8_0 blocks ({f16 scale,
+ * int8 q[32]}; head h owns blocks [h*d/32, (h+1)*d/32)) rounded up to whole
+ * 4-byte words. Returns 0 for an unknown format, non-positive sizes, or
+ * q8_0 with head_dim % 32 != 0. Host function. */
+size_t mt_kv_row_bytes(mt_kv_format fmt, int n_kv_heads, int head_dim);
+
+/* KV store: write freshly projected rows into their resolved cells.
+ * "KV Cache Design — cells, format, sessions", section 1 (positions vs
+ * cells: the store writes the cell the allocator resolved) and section 3
+ * (one store quantiser: q8_0 scale amax/127 stored as f16, codes
+ * round-ties-even of x divided by the float32 amax/127, clamped to
+ * +-127; f16 round-to-nearest-even; f32 verbatim).
+ *   k_pool, v_pool  device, n_cells rows of mt_kv_row_bytes(fmt, ...) bytes
+ *                   each, 16-byte aligned.
+ *   k_new, v_new    device float32 [n_rows][n_kv_heads*head_dim].
+ *   cells           device int64 [n_rows]; a negative cell skips that row;
+ *                   a cell >= n_cells is skipped and flagged in *status.
+ *   status          device uint32 status word, or NULL (no reporting).
+ * Rows with the same cell: the last one wins is NOT guaranteed (caller
+ * error). */
+mt_status mt_kv_store(mt_kv_format fmt, void *k_pool, void *v_pool, int64_t n_cells,
+                      int n_kv_heads, int head_dim, const float *k_new, const float *v_new,
+                      const int64_t *cells, int n_rows, uint32_t *status, mt_stream stream);
+
+/* Arguments of paged decode attention (one query token per sequence). */
+typedef struct {
+  mt_kv_format fmt;
+  const float *q;              /* device float32 [n_seqs][n_heads][head_dim]        */
+  const void *k_pool;          /* device, n_phys_blocks*block_size cells, 16B-aligned */
+  const void *v_pool;          /* same shape as k_pool                                */
+  const int32_t *block_table;  /* device int32 [n_seqs][max_blocks]; entry = physical
+                                  block id in [0, n_phys_blocks) or MT_INVALID_BLOCK_ID */
+  const int32_t *context_lens; /* device int32 [n_seqs], each in [0, max_blocks*block_size] */
+  const int32_t *spans;        /* device int32 [n_seqs][2] windows [lo, hi), or NULL  */
+  float *out;                  /* device float32 [n_seqs][n_heads][head_dim]          */
+  float *lse;                  /* device float32 [n_seqs][n_heads] or NULL            */
+  int n_seqs;
+  int n_heads;                 /* query heads; a multiple of n_kv_heads               */
+  int n_kv_heads;
+  int head_dim;
+  int block_size;
+  int max_blocks;
+  int64_t n_phys_blocks;
+  float scale;                 /* softmax scale applied to q.k                        */
+  int n_ctas;                  /* 0 = one persistent CTA per SM; >0 forces the split  */
+} mt_paged_attn_args;
+
+/* Workspace bytes mt_paged_attn_decode needs for `args` (0 on invalid args).
+ * The first 4 bytes of the workspace are the call's device status word:
+ * zero them once after allocating the workspace; mt_check_device_status()
+ * reads and clears them. */
+size_t mt_paged_attn_workspace_bytes(const mt_paged_attn_args *args);
+
+/* Grouped-query decode attention read through a paged KV cache.
+ * "Tiered KV cache — architecture", sections "The paged-attention block
+ * model" (position p of sequence s lives in physical block
+ * block_table[s][p / block_size], slot p % block_size, i.e. cell
+ * block_table[s][p/bs]*bs + p%bs of each pool) and "Kernel dispatch"
+ * (block table, context lengths; MT_INVALID_BLOCK_ID positions get logit
+ * -infinity, so zero weight). "KV Cache Design — cells, format, sessions",
+ * section 1: the optional window [lo, hi) of each query, read as logical
+ * positions intersected with [0, context_len).
+ * For each sequence s and query head h (KV head h / (n_heads/n_kv_heads)):
+ *   out[s][h] = sum_p softmax_p(scale * q[s][h] . k_p) v_p over the valid
+ *   positions p; lse[s][h] = log sum_p exp(scale * q . k_p) (natural log).
+ * A sequence with no valid position gets out = 0 and lse = -infinity.
+ * Shapes built: head_dim in {64, 128, 256}, block_size in {16, 32},
+ * n_kv_heads <= 8, n_heads/n_kv_heads <= 8; others return
+ * MT_ERR_UNSUPPORTED. Out-of-range block ids and context lengths are
+ * skipped and flagged in the workspace status word. */
+mt_status mt_paged_attn_decode(const mt_paged_attn_args *args, void *workspace,
+                               size_t workspace_bytes, mt_stream stream);
+
+/* order_moves — "KV Cache Design — cells, format, sessions", section 2:
+ * upward moves (dst > src) first, top-down (source descending), then
+ * downward moves bottom-up (source ascending), so a destination never lands
+ * on a row that has not been copied yet. Sorts `moves` (host) in place,
+ * dropping moves with len <= 0 or dst == src; *n_out receives the new
+ * count. Host function. */
+mt_status mt_order_moves(mt_move *moves, int n_moves, int *n_out);
+
+/* Validate a move list (host): MT_OK if no move writes a row that a later
+ * move still reads and every run lies in [0, n_cells); MT_ERR_ORDER
+ * otherwise, with the index of the first offending move in *first_bad
+ * (may be NULL). Host function. */
+mt_status mt_check_moves(const mt_move *moves, int n_moves, int64_t n_cells, int *first_bad);
+
+/* copy_cells: apply an ordered move list to every pool, rows verbatim.
+ * "KV Cache Design — cells, format, sessions", section 2 (compaction moves
+ * rows verbatim; overlapping runs copy ascending when sliding down and
+ * descending when sliding up). The result equals applying each move in
+ * list order as a memmove of len*row_bytes bytes in every pool.
+ *   pools      host array of n_pools (<= 256) device pointers, 16-byte
+ *              aligned, each n_cells rows of row_bytes bytes (% 4 == 0).
+ *   moves      host array, already ordered (mt_order_moves). It is checked
+ *              with mt_check_moves first; MT_ERR_ORDER launches nothing.
+ * The schedule travels in kernel parameters (no workspace, no host-device
+ * copy): consecutive moves share a launch (at most 1024, one CTA each) while
+ * none writes rows another of them reads or writes; each move copies in
+ * chunks of min(|dst-src|, len) rows in slide order with a barrier between
+ * chunks. */
+mt_status mt_copy_cells(void *const *pools, int n_pools, size_t row_bytes, int64_t n_cells,
+                        const mt_move *moves, int n_moves, mt_stream stream);
+
+/* Cold-tier int4 quantise — "Tiered KV cache — architecture", section
+ * "The three-tier model": per block one float32 scale and ceil(n_elts/2)
+ * packed int4 nibbles. Reading: scale = amax/7 (float32), q =
+ * clamp(rint(x/scale), -8, 7), nibble = q + 8, element 2j in the low nibble
+ * of byte j; amax == 0 gives scale 0 and nibbles 8. A block's elements are
+ * its block_size*n_kv_heads*head_dim values in pool order [slot][head][dim].
+ *   fmt      MT_KV_F16 or MT_KV_F32 (the pool's format).
+ *   pool     device pool of n_phys_blocks*block_size cells.
+ *   blocks   device int32 [n_blocks] physical ids to quantise.
+ *   scales   device float32 [n_blocks]; nibbles device uint8
+ *            [n_blocks][n_elts/2], 16-byte aligned.
+ *   status   device status word or NULL; out-of-range ids are skipped. */
+mt_status mt_kv_quant_int4(mt_kv_format fmt, const void *pool, int block_size, int n_kv_heads,
+                           int head_dim, int64_t n_phys_blocks, const int32_t *blocks,
+                           int n_blocks, float *scales, uint8_t *nibbles, uint32_t *status,
+                           mt_stream stream);
+
+/* Cold-tier int4 dequantise into (fresh) physical blocks: element =
+ * round_to_pool_type(float32(scale * (nibble - 8))). Same layout as
+ * mt_kv_quant_int4; dst_blocks lists the blocks written. */
+mt_status mt_kv_dequant_int4(mt_kv_format fmt, void *pool, int block_size, int n_kv_heads,
+                             int head_dim, int64_t n_phys_blocks, const int32_t *dst_blocks,
+                             int n_blocks, const float *scales, const uint8_t *nibbles,
+                             uint32_t *status, mt_stream stream);
+
+/* Grow-on-demand re-layout — "KV cache" (sipllm), section "Design": a
+ * [layer][pos][row] store with the capacity as per-layer stride; growing
+ * copies each layer's old_cap rows verbatim from stride old_cap (src) to
+ * stride new_cap (dst). Rows [old_cap, new_cap) of dst are not written.
+ * src, dst: device, 16-byte aligned, not overlapping; row_bytes % 4 == 0. */
+mt_status mt_kv_relayout(const void *src, void *dst, int n_layers, int64_t old_cap,
+                         int64_t new_cap, size_t row_bytes, mt_stream stream);
+
+/* The same page's capacity rule: double `cap` until it holds `need`
+ * positions, then cap at max_ctx. Returns -1 on invalid input. Host. */
+int64_t mt_kv_grow_capacity(int64_t cap, int64_t need, int64_t max_ctx);
+
+/* Synchronise `stream`, read the device status word, clear it, and map it
+ * to MT_OK, MT_ERR_TIMEOUT or MT_ERR_DEVICE_CHECK. */
+mt_status mt_check_device_status(uint32_t *status_word, mt_stream stream);
+
+/* Reason for the calling thread's last non-OK status ("" if none). */
+const char *mt_last_error(void);
+
+/* Library version string. */
+const char *mt_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MTKV_H */

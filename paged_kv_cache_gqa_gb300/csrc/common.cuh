@@ -1,0 +1,127 @@
+// Shared device helpers for the sm_103a kernels: mbarrier and bulk-copy
+// (TMA) wrappers written as inline PTX, bounded waits, and status reporting.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mtkv.h"
+
+namespace mtkv {
+
+// ---------------------------------------------------------------- status --
+
+__device__ __forceinline__ void report(uint32_t *status, uint32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// ------------------------------------------------------------- mbarriers --
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile(
+      "{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(
+          smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase with `parity` to complete. Gives up (returns false)
+// when *abort becomes non-zero or after `limit_ns` nanoseconds (checked
+// every 64 polls, and never more than 2^31 polls), so no wait can hang.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  volatile int *abort, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1; it < 0x80000000u; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (global_ns() - t0 > limit_ns) return false;
+    }
+  }
+  return false;
+}
+
+// ---------------------------------------------------- bulk (TMA) copies --
+
+// One contiguous global -> shared copy through the tensor-memory-access
+// engine, completing `bytes` of transaction count on `bar`. Both addresses
+// 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gsrc, uint32_t bytes,
+                                         uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+      "[%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Prefetch a contiguous global range into L2 (bytes a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *g, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(g), "r"(bytes) : "memory");
+}
+
+// ------------------------------------------------------------ numerics --
+
+__device__ __forceinline__ float2 h2_to_f2(uint32_t w) {
+  __half2 h = *reinterpret_cast<__half2 *>(&w);
+  return __half22float2(h);
+}
+
+// int8 code (two's complement, byte k of w) -> exact float, without the
+// integer-to-float conversion unit: place (q + 128) in the low mantissa
+// bits of 2^23 and subtract 2^23 + 128.
+__device__ __forceinline__ float i8_to_f(uint32_t w_biased, int k) {
+  const uint32_t sel = 0x7540u | (uint32_t)k;
+  uint32_t bits = __byte_perm(w_biased, 0x4B000000u, sel);
+  return __int_as_float((int)bits) - 8388736.0f;
+}
+
+}  // namespace mtkv

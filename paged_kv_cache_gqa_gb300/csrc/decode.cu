@@ -1,0 +1,862 @@
+// Paged grouped-query decode attention (split-K over a flattened block
+// stream) and its combine step, for sm_103a.
+//
+// What is computed — "Tiered KV cache — architecture", sections "The
+// paged-attention block model" (per-sequence logical -> physical block
+// table; position p in cell table[p/bs]*bs + p%bs) and "Kernel dispatch"
+// (block table + context lengths; kInvalidBlockId positions get logit
+// -infinity, i.e. zero weight); "KV Cache Design — cells, format, sessions",
+// section 1 (each query's window [lo, hi)) and section 3 (f32 / f16 / q8_0
+// storage; q8_0 is read packed and dequantised in registers).
+//
+// How (GB300-first design, not the pages' kernels):
+//  * Work is the stream of all sequences' (window-clipped) logical blocks,
+//    cut into equal contiguous ranges, one per persistent CTA (one CTA per
+//    SM). Every CTA derives its range from the context lengths itself, so
+//    long and short sequences balance without a planning launch. A CTA's
+//    range covers all KV heads of its blocks: the block's cells for all
+//    heads are one contiguous span of the pool, fetched by a single bulk
+//    (TMA) copy per K and per V.
+//  * Warp specialisation: one producer warp walks the range, reads block
+//    ids (32 at a time), skips holes, and issues bulk copies of the rows the
+//    window needs into a 2-4 stage shared-memory ring guarded by mbarriers.
+//    Consumer warps own one KV head each (several warps per head when there
+//    are fewer than 8 heads, splitting the block's tokens).
+//  * Consumer math on the FP32 pipes: lanes own 16-dim (8 when the group
+//    has more than 4 heads) slices of the head for one token; the G group
+//    heads' partial dot products are reduced across the token's lanes by
+//    recursive halving (G values cost G/2 + G/4 + ... shuffles instead of
+//    G per level); online softmax in base 2 with the max shared by the
+//    group; P.V with each lane owning head_dim/32 output dims of every head.
+//  * Each (CTA, sequence) segment writes an unnormalised partial (o, m, l);
+//    the combine kernel merges them (log-sum-exp) and normalises.
+//  * Every mbarrier wait is bounded; a timeout sets the status word, stops
+//    the CTA's producer after its copies in flight have landed, and returns.
+#include "common.cuh"
+#include "internal.h"
+
+#include <math.h>
+
+namespace mtkv {
+namespace {
+
+constexpr int kMaxConsumerWarps = 8;
+constexpr int kThreads = 32 * (kMaxConsumerWarps + 1);
+constexpr int kMaxStages = 4;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr unsigned kFull = 0xffffffffu;
+
+enum : int { F_NEW = 1, F_END = 2, F_DATA = 4, F_EXIT = 8 };
+
+struct StageInfo {
+  int seq;
+  int r0;     // first valid row of the block (relative to the block)
+  int r1;     // one past the last valid row
+  int flags;  // F_* bits | (first block row held by the stage) << 8
+};
+
+struct Params {
+  const float *q;
+  const uint8_t *k_pool;
+  const uint8_t *v_pool;
+  const int32_t *table;
+  const int32_t *ctx;
+  const int32_t *spans;
+  float *out;
+  float *lse;
+  float *part_o;       // [P][Hq][D] unnormalised partial outputs
+  float *part_ml;      // [P][Hq][2] partial (max, sum) in base-2 logits
+  int32_t *seq_start;  // [B+1] stream offset of each sequence's first block
+  uint32_t *status;
+  int B, Hq, Hkv, G, bs, max_blocks;
+  long long n_phys;
+  int row_bytes;
+  int blk_pad;   // bytes of one staged K (or V) row chunk, padded to 128
+  int rows;      // block rows per stage (block_size, or a divisor of it for wide rows)
+  int stages;
+  int wph;       // consumer warps per KV head
+  int n_cw;      // consumer warps = Hkv * wph
+  int n_ctas;
+  float qscale;  // softmax scale * log2(e)
+  uint64_t wait_ns;
+};
+
+// Shared memory: [barriers | stage infos | abort] header, per-warp softmax
+// scratch, then the stage ring.
+constexpr int kHdrBytes = 256;
+
+template <int GP>
+__host__ __device__ constexpr int scratch_floats_per_warp() {
+  return 32 * GP + GP;  // p[32 tokens][GP] and alpha[GP]
+}
+
+__device__ __forceinline__ int seq_window(const Params &p, int s, int &lo, int &hi) {
+  int c = p.ctx[s];
+  const int cmax = p.max_blocks * p.bs;
+  if (c < 0 || c > cmax) {
+    report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
+    c = c < 0 ? 0 : cmax;
+  }
+  lo = 0;
+  hi = c;
+  if (p.spans) {
+    lo = max(p.spans[2 * s], 0);
+    hi = min(p.spans[2 * s + 1], c);
+  }
+  if (hi <= lo) {
+    lo = hi = 0;
+    return 0;
+  }
+  return (hi - 1) / p.bs - lo / p.bs + 1;
+}
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// Recursive-halving reduction of N partial sums across the lanes selected by
+// offsets OFF, OFF/2, ..., 1: at each of the first log2(N) levels a lane keeps
+// the half of its values chosen by its lane bit and adds the partner's copy of
+// that half; the remaining levels are plain butterflies. Afterwards acc[0]
+// holds the full sum of value index j / (2*OFF/N) (the top log2(N) bits of j).
+template <int N, int OFF>
+__device__ __forceinline__ void halve(float *acc, int j) {
+  if constexpr (OFF > 0) {
+    if constexpr (N > 1) {
+      const bool upper = (j & OFF) != 0;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        const float send = upper ? acc[i] : acc[i + N / 2];
+        const float keep = upper ? acc[i + N / 2] : acc[i];
+        acc[i] = keep + __shfl_xor_sync(kFull, send, OFF);
+      }
+      halve<N / 2, OFF / 2>(acc, j);
+    } else {
+      acc[0] += __shfl_xor_sync(kFull, acc[0], OFF);
+      halve<1, OFF / 2>(acc, j);
+    }
+  }
+}
+
+template <int FMT, int D, int GP>
+struct Cfg {
+  static constexpr int DPL = (GP >= 8) ? 8 : 16;   // dims per lane in Q.K
+  static constexpr int LPT = D / DPL;              // lanes per token
+  static constexpr int TPS = 32 / LPT;             // tokens per step
+  static constexpr int REP = LPT / GP;             // lanes holding each score
+  static constexpr int DV = D / 32;                // P.V dims per lane
+  static constexpr int ES = FMT == MT_KV_F32 ? 4 : (FMT == MT_KV_F16 ? 2 : 1);
+  static constexpr int CH = FMT == MT_KV_Q8_0 ? DPL : 16 / ES;  // elems per chunk
+  static constexpr int NCL = DPL / CH;             // chunks per lane per token
+  static constexpr int MAXSTEPS = 32 / TPS;        // steps of a 32-token block
+  static_assert(GP <= LPT, "one score per lane");
+  static_assert(LPT >= 4 && LPT <= 32, "lane layout");
+};
+
+template <int FMT, int D, int GP>
+__global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params p) {
+  using C = Cfg<FMT, D, GP>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+  uint64_t *empty = full + kMaxStages;
+  StageInfo *infos = reinterpret_cast<StageInfo *>(smem + 64);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 128);
+  float *scratch = reinterpret_cast<float *>(smem + kHdrBytes);
+  uint8_t *ring = smem + kHdrBytes +
+                  ((kMaxConsumerWarps * scratch_floats_per_warp<GP>() * 4 + 127) & ~127);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = p.stages;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], p.n_cw);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == p.n_cw) {
+    // ------------------------------------------------------ producer warp
+    const uint64_t pol = policy_evict_first();
+    // pass 1: total stream length (CTA 0 also publishes the prefix)
+    int total = 0;
+    for (int base = 0; base < p.B; base += 32) {
+      const int s = base + lane;
+      int lo, hi;
+      const int nb = s < p.B ? seq_window(p, s, lo, hi) : 0;
+      const int incl = warp_incl_scan(nb, lane);
+      if (blockIdx.x == 0 && s < p.B) p.seq_start[s] = total + incl - nb;
+      total += __shfl_sync(kFull, incl, 31);
+    }
+    if (blockIdx.x == 0 && lane == 0) p.seq_start[p.B] = total;
+    const int per = total > 0 ? (total + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    const long long b0 = (long long)blockIdx.x * per;
+    const long long b1 = min((long long)total, b0 + per);
+
+    uint32_t it = 0;
+    bool alive = true;
+    // Publish one stage. Lane 0 waits for the slot and issues; the others
+    // learn the outcome through the shuffle.
+    auto emit = [&](int flags, int s, int r0, int r1, int phys, int base) -> bool {
+      const int slot = (int)(it % (uint32_t)S);
+      const uint32_t round = it / (uint32_t)S;
+      int okv = 1;
+      if (lane == 0) {
+        if (it >= (uint32_t)S && !mbar_wait_bounded(&empty[slot], (round - 1) & 1u, abort_flag,
+                                                    p.wait_ns))
+          okv = 0;
+        if (okv) {
+          infos[slot] = StageInfo{s, r0, r1, flags | (base << 8)};
+          if (flags & F_DATA) {
+            // rows [ra, rb): the valid rows widened to whole 4-row groups, so
+            // both addresses and the size stay multiples of 16 bytes
+            const int ra = r0 & ~3;
+            const int rb = min(base + p.rows, (r1 + 3) & ~3);
+            const uint32_t bytes = (uint32_t)((rb - ra) * p.row_bytes);
+            uint8_t *dk = ring + (size_t)slot * 2 * p.blk_pad + (size_t)(ra - base) * p.row_bytes;
+            const size_t src = ((size_t)phys * p.bs + ra) * (size_t)p.row_bytes;
+            mbar_arrive_expect_tx(&full[slot], 2 * bytes);
+            bulk_g2s(dk, p.k_pool + src, bytes, &full[slot], pol);
+            bulk_g2s(dk + p.blk_pad, p.v_pool + src, bytes, &full[slot], pol);
+          } else {
+            mbar_arrive(&full[slot]);
+          }
+        }
+      }
+      okv = __shfl_sync(kFull, okv, 0);
+      if (okv) ++it;
+      return okv != 0;
+    };
+
+    if (b0 < b1) {
+      // pass 2: first sequence whose blocks reach past b0
+      int s_first = p.B, start_first = 0, run = 0;
+      for (int base = 0; base < p.B; base += 32) {
+        const int s = base + lane;
+        int lo, hi;
+        const int nb = s < p.B ? seq_window(p, s, lo, hi) : 0;
+        const int incl = warp_incl_scan(nb, lane);
+        const unsigned hit = __ballot_sync(kFull, s < p.B && nb > 0 && (long long)run + incl > b0);
+        if (hit) {
+          const int l = __ffs(hit) - 1;
+          s_first = base + l;
+          start_first = run + __shfl_sync(kFull, incl - nb, l);
+          break;
+        }
+        run += __shfl_sync(kFull, incl, 31);
+      }
+      long long x = b0;
+      int start = start_first;
+      for (int s = s_first; alive && x < b1 && s < p.B; ++s) {
+        int lo, hi;
+        const int nb = seq_window(p, s, lo, hi);
+        const long long seg_lo = max(x, (long long)start);
+        const long long seg_hi = min(b1, (long long)start + nb);
+        if (seg_hi > seg_lo) {
+          if (lane == 0)
+            bulk_prefetch_l2(p.q + (size_t)s * p.Hq * D, (uint32_t)(p.Hq * D * sizeof(float)));
+          bool first = true;
+          const int lb0 = lo / p.bs;
+          const int32_t *trow = p.table + (size_t)s * p.max_blocks;
+          for (long long y0 = seg_lo; alive && y0 < seg_hi; y0 += 32) {
+            const long long y = y0 + lane;
+            int ent = MT_INVALID_BLOCK_ID;
+            if (y < seg_hi) ent = trow[lb0 + (int)(y - start)];
+            const int cnt = (int)min(32LL, seg_hi - y0);
+            for (int i = 0; i < cnt; ++i) {
+              const int phys = __shfl_sync(kFull, ent, i);
+              if (phys == MT_INVALID_BLOCK_ID) continue;
+              if (phys < 0 || (long long)phys >= p.n_phys) {
+                if (lane == 0) report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
+                continue;
+              }
+              const int lb = lb0 + (int)(y0 + i - start);
+              const int r0 = max(lo - lb * p.bs, 0);
+              const int r1 = min(hi - lb * p.bs, p.bs);
+              for (int c0 = (r0 / p.rows) * p.rows; c0 < r1; c0 += p.rows) {
+                if (!emit(F_DATA | (first ? F_NEW : 0), s, max(r0, c0), min(r1, c0 + p.rows),
+                          phys, c0)) {
+                  alive = false;
+                  break;
+                }
+                first = false;
+              }
+              if (!alive) break;
+            }
+          }
+          if (alive && !emit(F_END | (first ? F_NEW : 0), s, 0, 0, -1, 0)) alive = false;
+          x = seg_hi;
+        }
+        start += nb;
+      }
+    }
+    if (alive) alive = emit(F_EXIT, 0, 0, 0, -1, 0);
+    if (!alive) {
+      // Stop: flag the others, then let every copy already issued land in
+      // shared memory before this warp (and so the CTA) can retire.
+      if (lane == 0) {
+        *abort_flag = 1;
+        report(p.status, MT_STATUS_BIT_TIMEOUT);
+        const uint32_t first_live = it > (uint32_t)S ? it - (uint32_t)S : 0;
+        for (uint32_t k = first_live; k < it; ++k) {
+          const int slot = (int)(k % (uint32_t)S);
+          volatile int never = 0;
+          mbar_wait_bounded(&full[slot], (k / (uint32_t)S) & 1u, &never, p.wait_ns);
+        }
+      }
+      __syncwarp();
+    }
+    return;
+  }
+
+  if (warp >= p.n_cw) return;
+
+  // ------------------------------------------------------- consumer warps
+  const int kvh = warp / p.wph;
+  const int sub = warp % p.wph;
+  const int tq = lane / C::LPT;           // token within a step
+  const int j = lane % C::LPT;            // slice within the token
+  const int hidx = j / C::REP;            // group head whose score this lane ends with
+  const bool rep0 = (j % C::REP) == 0;
+  const int rot = (C::LPT == 4 && C::NCL > 1) ? (tq & 1) : 0;  // bank-conflict rotation
+  float *p_s = scratch + warp * scratch_floats_per_warp<GP>();
+  float *a_s = p_s + 32 * GP;
+  const int nsteps = p.bs / C::TPS;
+  const int G = p.G;
+
+  float qr[GP][C::DPL];
+  float o_acc[GP][C::DV];
+  float m_run = -INFINITY, l_run = 0.f;
+
+  // element offset (within the head) of this lane's chunk k
+  auto chunk_elem = [&](int k) -> int {
+    if constexpr (FMT == MT_KV_Q8_0) {
+      return C::DPL * j;
+    } else {
+      return (j + C::LPT * ((k + rot) % C::NCL)) * C::CH;
+    }
+  };
+
+  for (uint32_t it = 0;; ++it) {
+    const int slot = (int)(it % (uint32_t)S);
+    int okv = 1;
+    if (lane == 0)
+      okv = mbar_wait_bounded(&full[slot], (it / (uint32_t)S) & 1u, abort_flag, p.wait_ns) ? 1 : 0;
+    okv = __shfl_sync(kFull, okv, 0);
+    if (!okv) {
+      if (lane == 0) {
+        *abort_flag = 1;
+        report(p.status, MT_STATUS_BIT_TIMEOUT);
+      }
+      break;
+    }
+    struct {
+      int seq, r0, r1, flags, base;
+    } inf;
+    {
+      const volatile int *vi = reinterpret_cast<const volatile int *>(&infos[slot]);
+      inf.seq = vi[0];
+      inf.r0 = vi[1];
+      inf.r1 = vi[2];
+      inf.flags = vi[3] & 0xff;
+      inf.base = vi[3] >> 8;
+    }
+    if (inf.flags & F_EXIT) break;
+    const int seq = inf.seq;
+
+    if (inf.flags & F_NEW) {
+      const float *qb = p.q + ((size_t)seq * p.Hq + (size_t)kvh * G) * D;
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+#pragma unroll
+        for (int k = 0; k < C::NCL; ++k) {
+          const int e0 = chunk_elem(k);
+#pragma unroll
+          for (int e = 0; e < C::CH; e += 4) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (g < G) v = *reinterpret_cast<const float4 *>(qb + (size_t)g * D + e0 + e);
+            qr[g][k * C::CH + e + 0] = v.x * p.qscale;
+            qr[g][k * C::CH + e + 1] = v.y * p.qscale;
+            qr[g][k * C::CH + e + 2] = v.z * p.qscale;
+            qr[g][k * C::CH + e + 3] = v.w * p.qscale;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < C::DV; ++e) o_acc[g][e] = 0.f;
+      }
+      m_run = -INFINITY;
+      l_run = 0.f;
+    }
+
+    if (inf.flags & F_DATA) {
+      // stage rows start at block row inf.base; steps never straddle stages
+      const uint8_t *kst = ring + (size_t)slot * 2 * p.blk_pad - (ptrdiff_t)inf.base * p.row_bytes;
+      const uint8_t *vst = kst + p.blk_pad;
+      const int r0 = inf.r0, r1 = inf.r1;
+      // ---- scores: Q.K for this lane's slice, reduced across the token's lanes
+      // Raw scores go to this warp's scratch row p_s[token][head]; each lane
+      // later reads back only the entries it wrote itself.
+      float mloc = -INFINITY;
+#pragma unroll 1
+      for (int st = sub; st < nsteps; st += p.wph) {
+        const int t0 = st * C::TPS;
+        const int tok = t0 + tq;
+        if (t0 + C::TPS <= r0 || t0 >= r1) {  // whole step outside the window
+          if (rep0) p_s[tok * GP + hidx] = -INFINITY;
+          continue;
+        }
+        float acc[GP];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) acc[g] = 0.f;
+        if constexpr (FMT == MT_KV_Q8_0) {
+          const uint8_t *rowp = kst + (size_t)tok * p.row_bytes + kvh * (D / 32) * 34;
+          const int b = (C::DPL * j) >> 5, o = (C::DPL * j) & 31;
+          const uint8_t *qa = rowp + b * 34 + 2 + o;
+          const uintptr_t a = reinterpret_cast<uintptr_t>(qa);
+          const uint32_t *w = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
+          const int sh = (int)(a & 3) * 8;
+          constexpr int NW = C::DPL / 4;
+          uint32_t raw[NW + 1];
+#pragma unroll
+          for (int i2 = 0; i2 <= NW; ++i2) raw[i2] = w[i2];
+          const float dsc = __half2float(*reinterpret_cast<const __half *>(rowp + b * 34));
+#pragma unroll
+          for (int i2 = 0; i2 < NW; ++i2) {
+            const uint32_t u = __funnelshift_r(raw[i2], raw[i2 + 1], sh) ^ 0x80808080u;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float x = i8_to_f(u, k);
+#pragma unroll
+              for (int g = 0; g < GP; ++g) acc[g] = fmaf(qr[g][i2 * 4 + k], x, acc[g]);
+            }
+          }
+#pragma unroll
+          for (int g = 0; g < GP; ++g) acc[g] *= dsc;
+        } else {
+          const uint8_t *rowp = kst + (size_t)tok * p.row_bytes + (size_t)kvh * D * C::ES;
+#pragma unroll
+          for (int k = 0; k < C::NCL; ++k) {
+            const uint4 raw = *reinterpret_cast<const uint4 *>(rowp + chunk_elem(k) * C::ES);
+            float x[C::CH];
+            if constexpr (FMT == MT_KV_F32) {
+              x[0] = __uint_as_float(raw.x);
+              x[1] = __uint_as_float(raw.y);
+              x[2] = __uint_as_float(raw.z);
+              x[3] = __uint_as_float(raw.w);
+            } else {
+              float2 f;
+              f = h2_to_f2(raw.x); x[0] = f.x; x[1] = f.y;
+              f = h2_to_f2(raw.y); x[2] = f.x; x[3] = f.y;
+              f = h2_to_f2(raw.z); x[4] = f.x; x[5] = f.y;
+              f = h2_to_f2(raw.w); x[6] = f.x; x[7] = f.y;
+            }
+#pragma unroll
+            for (int e = 0; e < C::CH; ++e)
+#pragma unroll
+              for (int g = 0; g < GP; ++g) acc[g] = fmaf(qr[g][k * C::CH + e], x[e], acc[g]);
+          }
+        }
+        halve<GP, C::LPT / 2>(acc, j);
+        const bool valid = tok >= r0 && tok < r1 && hidx < G;
+        const float sc = valid ? acc[0] : -INFINITY;
+        if (rep0) p_s[tok * GP + hidx] = sc;
+        mloc = fmaxf(mloc, sc);
+      }
+      // ---- online softmax (base 2); the group's heads share nothing but
+      // each head's max is common to all lanes that hold that head
+#pragma unroll
+      for (int o = C::LPT; o < 32; o <<= 1) mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, o));
+      const float m_new = fmaxf(m_run, mloc);
+      const bool none = m_new == -INFINITY;
+      const float alpha = none ? 1.f : exp2f(m_run - m_new);
+      l_run *= alpha;
+      if (rep0) {
+#pragma unroll 1
+        for (int st = sub; st < nsteps; st += p.wph) {
+          float *ps = p_s + (st * C::TPS + tq) * GP + hidx;
+          const float pr = none ? 0.f : exp2f(*ps - m_new);
+          l_run += pr;
+          *ps = pr;
+        }
+      }
+      m_run = m_new;
+      if (tq == 0 && rep0) a_s[hidx] = alpha;
+      __syncwarp();
+      // ---- P.V: lane owns dims [lane*DV, lane*DV + DV) of every group head
+      float al[GP];
+#pragma unroll
+      for (int g = 0; g < GP; ++g) al[g] = a_s[g];
+#pragma unroll
+      for (int g = 0; g < GP; ++g)
+#pragma unroll
+        for (int e = 0; e < C::DV; ++e) o_acc[g][e] *= al[g];
+      for (int i = 0; i < C::MAXSTEPS; ++i) {
+        const int st = sub + p.wph * i;
+        if (st >= nsteps) break;
+        const int ta = max(st * C::TPS, r0), tb = min(st * C::TPS + C::TPS, r1);
+        for (int tok = ta; tok < tb; ++tok) {
+          float pg[GP];
+          if constexpr (GP == 1) {
+            pg[0] = p_s[tok];
+          } else if constexpr (GP == 2) {
+            const float2 v2 = *reinterpret_cast<const float2 *>(p_s + tok * 2);
+            pg[0] = v2.x;
+            pg[1] = v2.y;
+          } else {
+#pragma unroll
+            for (int g = 0; g < GP; g += 4) {
+              const float4 v4 = *reinterpret_cast<const float4 *>(p_s + tok * GP + g);
+              pg[g] = v4.x;
+              pg[g + 1] = v4.y;
+              pg[g + 2] = v4.z;
+              pg[g + 3] = v4.w;
+            }
+          }
+          float x[C::DV];
+          if constexpr (FMT == MT_KV_Q8_0) {
+            const uint8_t *rowp = vst + (size_t)tok * p.row_bytes + kvh * (D / 32) * 34;
+            const int dim0 = lane * C::DV;
+            const int b = dim0 >> 5, o = dim0 & 31;
+            const uintptr_t a = reinterpret_cast<uintptr_t>(rowp + b * 34 + 2 + o);
+            const uint32_t *w = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
+            const int sh = (int)(a & 3) * 8;
+            constexpr int NWV = C::DV >= 4 ? C::DV / 4 : 1;
+            uint32_t raw[NWV + 1];
+#pragma unroll
+            for (int i2 = 0; i2 <= NWV; ++i2) raw[i2] = w[i2];
+            const float dsc = __half2float(*reinterpret_cast<const __half *>(rowp + b * 34));
+#pragma unroll
+            for (int i2 = 0; i2 < NWV; ++i2) {
+              const uint32_t u = __funnelshift_r(raw[i2], raw[i2 + 1], sh) ^ 0x80808080u;
+#pragma unroll
+              for (int k = 0; k < 4 && i2 * 4 + k < C::DV; ++k) x[i2 * 4 + k] = i8_to_f(u, k);
+            }
+#pragma unroll
+            for (int g = 0; g < GP; ++g) pg[g] *= dsc;
+          } else if constexpr (FMT == MT_KV_F32) {
+            const float *vp = reinterpret_cast<const float *>(vst + (size_t)tok * p.row_bytes) +
+                              (size_t)kvh * D + lane * C::DV;
+            if constexpr (C::DV == 2) {
+              const float2 v2 = *reinterpret_cast<const float2 *>(vp);
+              x[0] = v2.x;
+              x[1] = v2.y;
+            } else {
+#pragma unroll
+              for (int e = 0; e < C::DV; e += 4) {
+                const float4 v4 = *reinterpret_cast<const float4 *>(vp + e);
+                x[e] = v4.x;
+                x[e + 1] = v4.y;
+                x[e + 2] = v4.z;
+                x[e + 3] = v4.w;
+              }
+            }
+          } else {
+            const uint8_t *vp = vst + (size_t)tok * p.row_bytes + ((size_t)kvh * D + lane * C::DV) * 2;
+            if constexpr (C::DV == 2) {
+              const float2 f = h2_to_f2(*reinterpret_cast<const uint32_t *>(vp));
+              x[0] = f.x;
+              x[1] = f.y;
+            } else if constexpr (C::DV == 4) {
+              const uint2 r = *reinterpret_cast<const uint2 *>(vp);
+              float2 f = h2_to_f2(r.x);
+              x[0] = f.x; x[1] = f.y;
+              f = h2_to_f2(r.y);
+              x[2] = f.x; x[3] = f.y;
+            } else {
+              const uint4 r = *reinterpret_cast<const uint4 *>(vp);
+              float2 f = h2_to_f2(r.x);
+              x[0] = f.x; x[1] = f.y;
+              f = h2_to_f2(r.y);
+              x[2] = f.x; x[3] = f.y;
+              f = h2_to_f2(r.z);
+              x[4] = f.x; x[5] = f.y;
+              f = h2_to_f2(r.w);
+              x[6] = f.x; x[7] = f.y;
+            }
+          }
+#pragma unroll
+          for (int g = 0; g < GP; ++g)
+#pragma unroll
+            for (int e = 0; e < C::DV; ++e) o_acc[g][e] = fmaf(pg[g], x[e], o_acc[g][e]);
+        }
+      }
+      __syncwarp();
+    }
+
+    if (inf.flags & F_END) {
+      float lsum = l_run;  // non-zero only on the rep0 lanes
+#pragma unroll
+      for (int o = C::LPT; o < 32; o <<= 1) lsum += __shfl_xor_sync(kFull, lsum, o);
+      const size_t P = ((size_t)blockIdx.x + seq) * p.wph + sub;
+      const size_t hq0 = P * p.Hq + (size_t)kvh * G;
+      if (tq == 0 && rep0 && hidx < G) {
+        p.part_ml[(hq0 + hidx) * 2 + 0] = m_run;
+        p.part_ml[(hq0 + hidx) * 2 + 1] = lsum;
+      }
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        if (g >= G) break;
+        float *dst = p.part_o + (hq0 + g) * D + lane * C::DV;
+#pragma unroll
+        for (int e = 0; e < C::DV; e += 2)
+          *reinterpret_cast<float2 *>(dst + e) = make_float2(o_acc[g][e], o_acc[g][e + 1]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+  }
+}
+
+// Merge every partial of (sequence, query head) by log-sum-exp and
+// normalise. One warp per (s, h); lane owns D/32 dims.
+template <int D>
+__global__ void __launch_bounds__(256) splitk_combine_kernel(const Params p) {
+  constexpr int DV = D / 32;
+  const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (w >= p.B * p.Hq) return;
+  const int s = w / p.Hq, h = w % p.Hq;
+  const int T = p.seq_start[p.B];
+  const int per = T > 0 ? (T + p.n_ctas - 1) / p.n_ctas : 1;
+  const int beg = p.seq_start[s], end = p.seq_start[s + 1];
+  float acc[DV];
+#pragma unroll
+  for (int e = 0; e < DV; ++e) acc[e] = 0.f;
+  float M = -INFINITY, L = 0.f;
+  if (end > beg) {
+    const int c0 = beg / per, c1 = (end - 1) / per;
+    for (int c = c0; c <= c1; ++c)
+      for (int u = 0; u < p.wph; ++u) {
+        const size_t P = ((size_t)c + s) * p.wph + u;
+        M = fmaxf(M, p.part_ml[(P * p.Hq + h) * 2]);
+      }
+    if (M > -INFINITY) {
+      for (int c = c0; c <= c1; ++c)
+        for (int u = 0; u < p.wph; ++u) {
+          const size_t P = ((size_t)c + s) * p.wph + u;
+          const float m = p.part_ml[(P * p.Hq + h) * 2];
+          const float l = p.part_ml[(P * p.Hq + h) * 2 + 1];
+          if (!(l > 0.f)) continue;
+          const float f = exp2f(m - M);
+          L += l * f;
+          const float *src = p.part_o + (P * p.Hq + h) * D + lane * DV;
+#pragma unroll
+          for (int e = 0; e < DV; e += 2) {
+            const float2 v = *reinterpret_cast<const float2 *>(src + e);
+            acc[e] = fmaf(f, v.x, acc[e]);
+            acc[e + 1] = fmaf(f, v.y, acc[e + 1]);
+          }
+        }
+    }
+  }
+  float *dst = p.out + ((size_t)s * p.Hq + h) * D + lane * DV;
+  const bool any = L > 0.f;
+#pragma unroll
+  for (int e = 0; e < DV; e += 2)
+    *reinterpret_cast<float2 *>(dst + e) =
+        any ? make_float2(acc[e] / L, acc[e + 1] / L) : make_float2(0.f, 0.f);
+  if (p.lse && lane == 0)
+    p.lse[(size_t)s * p.Hq + h] = any ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+}
+
+// --------------------------------------------------------------- host side
+
+struct Plan {
+  int D, GP, wph, n_cw, stages, n_ctas, blk_pad, rows, smem;
+  size_t ws_status, ws_seq, ws_ml, ws_o, ws_total;
+};
+
+int pad_group(int G) {
+  if (G <= 1) return 1;
+  if (G <= 2) return 2;
+  if (G <= 4) return 4;
+  if (G <= 8) return 8;
+  return 0;
+}
+
+mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
+  if (!a) return fail(MT_ERR_INVALID_ARG, "paged decode: null args");
+  const size_t rb = mt_kv_row_bytes(a->fmt, a->n_kv_heads, a->head_dim);
+  if (rb == 0) return fail(MT_ERR_INVALID_ARG, "paged decode: unknown format or bad head shape");
+  if (a->n_seqs < 0 || a->n_heads <= 0 || a->max_blocks < 0 || a->n_phys_blocks < 0 ||
+      a->block_size <= 0)
+    return fail(MT_ERR_INVALID_ARG, "paged decode: negative or zero size");
+  if (a->n_heads % a->n_kv_heads)
+    return fail(MT_ERR_INVALID_ARG, "paged decode: n_heads must be a multiple of n_kv_heads");
+  if (a->head_dim != 64 && a->head_dim != 128 && a->head_dim != 256)
+    return fail(MT_ERR_UNSUPPORTED, "paged decode: head_dim must be 64, 128 or 256");
+  if (a->block_size != 16 && a->block_size != 32)
+    return fail(MT_ERR_UNSUPPORTED, "paged decode: block_size must be 16 or 32");
+  if (a->n_kv_heads > kMaxConsumerWarps)
+    return fail(MT_ERR_UNSUPPORTED, "paged decode: at most 8 KV heads");
+  const int G = a->n_heads / a->n_kv_heads;
+  const int GP = pad_group(G);
+  if (!GP) return fail(MT_ERR_UNSUPPORTED, "paged decode: at most 8 query heads per KV head");
+  if (a->n_ctas < 0) return fail(MT_ERR_INVALID_ARG, "paged decode: negative n_ctas");
+  if ((long long)a->max_blocks * a->block_size > 0x7fffffffLL)
+    return fail(MT_ERR_UNSUPPORTED, "paged decode: max_blocks * block_size overflows int32");
+  pl->D = a->head_dim;
+  pl->GP = GP;
+  const int dpl = GP >= 8 ? 8 : 16;
+  const int tps = 32 / (a->head_dim / dpl);
+  const int nsteps = a->block_size / tps;
+  int wph = kMaxConsumerWarps / a->n_kv_heads;
+  if (wph > nsteps) wph = nsteps;
+  if (wph < 1) wph = 1;
+  pl->wph = wph;
+  pl->n_cw = a->n_kv_heads * wph;
+  const int fixed = kHdrBytes + ((kMaxConsumerWarps * (32 * GP + GP) * 4 + 127) & ~127) + 16;
+  int n_ctas = a->n_ctas;
+  int smem_cap = 232448;
+  if (need_device || n_ctas == 0) {
+    DeviceInfo di;
+    mt_status st = device_info(&di);
+    if (st != MT_OK) return st;
+    if (n_ctas == 0) n_ctas = di.n_sm;
+    smem_cap = di.smem_optin;
+  }
+  // Whole blocks per stage when at least two stages fit; otherwise halve the
+  // rows per stage (never below 8, a multiple of every token step) until
+  // they do.
+  int rows = a->block_size, stages = 0, pad = 0;
+  for (;;) {
+    pad = (int)(((size_t)rows * rb + 127) & ~(size_t)127);
+    stages = (smem_cap - fixed) / (2 * pad);
+    if (stages >= 2 || rows <= 8) break;
+    rows /= 2;
+  }
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 2)
+    return fail(MT_ERR_UNSUPPORTED, "paged decode: KV rows too wide to double-buffer 8 of them");
+  pl->rows = rows;
+  pl->blk_pad = pad;
+  pl->stages = stages;
+  pl->n_ctas = n_ctas;
+  pl->smem = fixed + stages * 2 * pl->blk_pad;
+  const size_t P = ((size_t)n_ctas + (size_t)a->n_seqs) * wph;
+  auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  pl->ws_status = 0;
+  pl->ws_seq = 256;
+  pl->ws_ml = pl->ws_seq + up(((size_t)a->n_seqs + 1) * 4);
+  pl->ws_o = pl->ws_ml + up(P * a->n_heads * 2 * 4);
+  pl->ws_total = pl->ws_o + up(P * a->n_heads * (size_t)a->head_dim * 4);
+  return MT_OK;
+}
+
+template <int FMT, int D, int GP>
+mt_status launch_decode(const Params &prm, const Plan &pl, cudaStream_t s) {
+  static int configured_dev = -1;
+  static int configured_smem = 0;
+  auto kern = paged_decode_kernel<FMT, D, GP>;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev || configured_smem < pl.smem) {
+    mt_status st = cuda_check(
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem),
+        "cudaFuncSetAttribute(decode smem)");
+    if (st != MT_OK) return st;
+    configured_dev = dev;
+    configured_smem = pl.smem;
+  }
+  kern<<<pl.n_ctas, 32 * (pl.n_cw + 1), pl.smem, s>>>(prm);
+  mt_status st = cuda_check(cudaGetLastError(), "paged decode launch");
+  if (st != MT_OK) return st;
+  const int warps = prm.B * prm.Hq;
+  if (warps > 0) {
+    splitk_combine_kernel<D><<<(warps + 7) / 8, 256, 0, s>>>(prm);
+    st = cuda_check(cudaGetLastError(), "split-K combine launch");
+  }
+  return st;
+}
+
+template <int FMT, int D>
+mt_status dispatch_gp(const Params &prm, const Plan &pl, cudaStream_t s) {
+  switch (pl.GP) {
+    case 1: return launch_decode<FMT, D, 1>(prm, pl, s);
+    case 2: return launch_decode<FMT, D, 2>(prm, pl, s);
+    case 4: return launch_decode<FMT, D, 4>(prm, pl, s);
+    default: return launch_decode<FMT, D, 8>(prm, pl, s);
+  }
+}
+
+template <int FMT>
+mt_status dispatch_d(const Params &prm, const Plan &pl, cudaStream_t s) {
+  switch (pl.D) {
+    case 64: return dispatch_gp<FMT, 64>(prm, pl, s);
+    case 128: return dispatch_gp<FMT, 128>(prm, pl, s);
+    default: return dispatch_gp<FMT, 256>(prm, pl, s);
+  }
+}
+
+}  // namespace
+}  // namespace mtkv
+
+using namespace mtkv;
+
+extern "C" size_t mt_paged_attn_workspace_bytes(const mt_paged_attn_args *args) {
+  Plan pl;
+  if (make_plan(args, &pl, false) != MT_OK) return 0;
+  return pl.ws_total;
+}
+
+extern "C" mt_status mt_paged_attn_decode(const mt_paged_attn_args *a, void *workspace,
+                                          size_t workspace_bytes, mt_stream stream) {
+  Plan pl;
+  mt_status st = make_plan(a, &pl, true);
+  if (st != MT_OK) return st;
+  if (a->n_seqs == 0) return ok();
+  if (!a->q || !a->k_pool || !a->v_pool || !a->block_table || !a->context_lens || !a->out)
+    return fail(MT_ERR_INVALID_ARG, "paged decode: null pointer");
+  if (!workspace || workspace_bytes < pl.ws_total)
+    return fail(MT_ERR_INVALID_ARG, "paged decode: workspace missing or too small (need " +
+                                        std::to_string(pl.ws_total) + " bytes)");
+  if (!aligned16(a->k_pool) || !aligned16(a->v_pool) || !aligned16(a->q) || !aligned16(a->out) ||
+      !aligned16(workspace))
+    return fail(MT_ERR_INVALID_ARG, "paged decode: q, pools, out and workspace must be 16-byte aligned");
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  Params prm;
+  prm.q = a->q;
+  prm.k_pool = static_cast<const uint8_t *>(a->k_pool);
+  prm.v_pool = static_cast<const uint8_t *>(a->v_pool);
+  prm.table = a->block_table;
+  prm.ctx = a->context_lens;
+  prm.spans = a->spans;
+  prm.out = a->out;
+  prm.lse = a->lse;
+  prm.status = reinterpret_cast<uint32_t *>(ws + pl.ws_status);
+  prm.seq_start = reinterpret_cast<int32_t *>(ws + pl.ws_seq);
+  prm.part_ml = reinterpret_cast<float *>(ws + pl.ws_ml);
+  prm.part_o = reinterpret_cast<float *>(ws + pl.ws_o);
+  prm.B = a->n_seqs;
+  prm.Hq = a->n_heads;
+  prm.Hkv = a->n_kv_heads;
+  prm.G = a->n_heads / a->n_kv_heads;
+  prm.bs = a->block_size;
+  prm.max_blocks = a->max_blocks;
+  prm.n_phys = a->n_phys_blocks;
+  prm.row_bytes = (int)mt_kv_row_bytes(a->fmt, a->n_kv_heads, a->head_dim);
+  prm.blk_pad = pl.blk_pad;
+  prm.rows = pl.rows;
+  prm.stages = pl.stages;
+  prm.wph = pl.wph;
+  prm.n_cw = pl.n_cw;
+  prm.n_ctas = pl.n_ctas;
+  prm.qscale = a->scale * 1.4426950408889634f;
+  prm.wait_ns = kWaitLimitNs;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (a->fmt) {
+    case MT_KV_F32: st = dispatch_d<MT_KV_F32>(prm, pl, s); break;
+    case MT_KV_F16: st = dispatch_d<MT_KV_F16>(prm, pl, s); break;
+    default: st = dispatch_d<MT_KV_Q8_0>(prm, pl, s); break;
+  }
+  return st == MT_OK ? ok() : st;
+}

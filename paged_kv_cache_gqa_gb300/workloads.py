@@ -287,7 +287,8 @@ def longctx_f16_int4(seed: int = 1005, n_seqs: int = 16, ctx: int = 32768,
     """Long-context tiered decode, f16 KV: 16/4 heads, d=256, bs=16.
 
     A fraction `hole_frac` of logical blocks become holes (never the last
-    block of a sequence). Of the remaining blocks, `cold_frac` are chosen for
+    block of a sequence). Of the remaining blocks other than the last (which
+    takes the decode token's row), `cold_frac` are chosen for
     the cold round trip: extra['cold_src'] lists their current physical ids
     and extra['cold_dst'] the fresh ids (from the pool's spare blocks) that
     the dequantised data lands in; extra['cold_where'] holds the (seq,
@@ -308,7 +309,8 @@ def longctx_f16_int4(seed: int = 1005, n_seqs: int = 16, ctx: int = 32768,
         for lb in np.nonzero(holes[s])[0]:
             pool.decref(int(table[s, lb]))
             seqs.tables[s][lb] = INVALID_BLOCK_ID
-    live = [(s, lb) for s in range(n_seqs) for lb in range(nb) if not holes[s, lb]]
+    # the last block holds the position being written: it stays hot
+    live = [(s, lb) for s in range(n_seqs) for lb in range(nb - 1) if not holes[s, lb]]
     pick = rng.random(len(live)) < cold_frac
     cold_where = [live[i] for i in np.nonzero(pick)[0]]
     cold_src = [seqs.tables[s][lb] for (s, lb) in cold_where]
