@@ -1,0 +1,434 @@
+"""Benchmark: paged GQA decode on the Llama-3-8B-shaped f16 workload.
+
+One step = for each of the 32 layers: the KV store of the decode token's new
+K/V rows into their resolved cells, then paged decode attention (split-K
+decode + combine) over that layer's paged f16 K/V pools. 64 sequences,
+context lengths log-uniform in [512, 16384], 32 query / 8 KV heads,
+head_dim 128, block_size 16, block tables drawn from a pool of 1.1x the
+blocks needed (seeded synthetic data; ~42 GB of K/V resident in HBM).
+
+Prints one JSON line. `value` is algorithmic KV bytes per second (K and V
+rows attended, block-table entries read, Q read, output written, rows
+stored), device-timed with CUDA events with inputs already in HBM; `e2e` is
+the same metric through the same C-ABI calls with each step's inputs copied
+from pinned host memory and the outputs copied back inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mtkv|reference]
+
+`--impl reference` times the CPU oracle (the only reference this method has)
+on a bounded sample of the same workload, on the host's cores.
+Under torchrun with N > 1 every rank runs an independent replica (the path
+has no exchange step); rank 0 prints the line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import os
+
+# the CPU oracle runs single-threaded; fix the BLAS pools before numpy loads
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import math
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_gqa_gb300 import workloads  # noqa: E402
+
+METRIC = "paged GQA decode: KV HBM GB/s (fraction of GB300 peak) and attended tokens/s"
+WORKLOAD = ("llama3-8b-shaped paged GQA decode, f16 KV: 32 layers, 64 seqs, ctx log-uniform "
+            "[512,16384], 32/8 heads, head_dim 128, block_size 16, pool 1.1x, store+attention "
+            "per layer")
+SEED = 1003
+N_LAYERS = 32
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _structure():
+    return workloads.llama3_f16(seed=SEED, hist=False)
+
+
+def decode_bytes(w, seqs=None):
+    """Algorithmic bytes of one decode call (one layer): K and V rows of the
+    attended positions for every KV head, the block-table entries those
+    positions use, the context lengths, Q read and the output written."""
+    seqs = range(w.n_seqs) if seqs is None else seqs
+    hkv, d, bs = w.n_kv_heads, w.head_dim, w.block_size
+    seg = d * 2  # f16 head segment
+    toks = sum(int(w.context_lens[s]) for s in seqs)
+    blocks = sum(-(-int(w.context_lens[s]) // bs) for s in seqs)
+    n = len(list(seqs))
+    return (toks * hkv * seg * 2 + blocks * 4 + n * 4 + 2 * n * w.n_heads * d * 4), toks
+
+
+def store_bytes(w):
+    row = w.n_kv_heads * w.head_dim
+    return w.n_seqs * (2 * row * 4 + 2 * row * 2 + 8)
+
+
+class Clocks:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.sel = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            self.sel = vis.split(",")[device_index] if vis else str(device_index)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.sel, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons, power = [], [], set(), []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in out.strip().splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def _traffic_from_profile():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode kernel source (else None)."""
+    prof = os.path.join(ROOT, "profiles", "paged_decode_llama3_f16.md")
+    src = os.path.join(ROOT, "paged_kv_cache_gqa_gb300", "csrc", "decode.cu")
+    try:
+        txt = open(prof).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        m_sha = re.search(r"decode\.cu sha256\[:16\]:\s*([0-9a-f]{16})", txt)
+        m_tr = re.search(r"traffic_bytes_per_launch_full:\s*([0-9.eE+]+)", txt)
+        if m_sha and m_tr and m_sha.group(1) == sha:
+            return float(m_tr.group(1))
+    except OSError:
+        pass
+    return None
+
+
+class OracleSample:
+    """The CPU oracle (store + decode of one layer) on the first `n`
+    sequences of the workload, on pool rows generated for those sequences."""
+
+    def __init__(self, w, n):
+        from oracle import formats as ofmt
+        self.w, self.n = w, n
+        rng = np.random.default_rng(SEED + 7)
+        hkv, d, bs = w.n_kv_heads, w.head_dim, w.block_size
+        rb = ofmt.row_bytes("f16", hkv, d)
+        self.kp = np.zeros((w.n_cells, rb), np.uint8)
+        self.vp = np.zeros((w.n_cells, rb), np.uint8)
+        for s in range(n):
+            nb = -(-int(w.context_lens[s]) // bs)
+            for b in w.block_table[s, :nb]:
+                rows = rng.standard_normal((2, bs, hkv * d), dtype=np.float32)
+                self.kp[b * bs:(b + 1) * bs] = ofmt.encode_rows("f16", rows[0], hkv, d)
+                self.vp[b * bs:(b + 1) * bs] = ofmt.encode_rows("f16", rows[1], hkv, d)
+        db, self.toks = decode_bytes(w, range(n))
+        self.bytes = db + store_bytes(w) * n // w.n_seqs
+
+    def run(self) -> float:
+        from oracle import attention as oatt
+        w, n = self.w, self.n
+        t0 = time.perf_counter()
+        oatt.kv_store("f16", self.kp, self.vp, w.k_new[:n], w.v_new[:n], w.new_cells[:n],
+                      w.n_kv_heads, w.head_dim)
+        oatt.paged_attn_decode("f16", w.q, self.kp, self.vp, w.block_table, w.context_lens, None,
+                               w.n_heads, w.n_kv_heads, w.head_dim, w.block_size, w.scale,
+                               seqs=range(n))
+        return time.perf_counter() - t0
+
+    @classmethod
+    def calibrated(cls, w, budget_s: float):
+        """Smallest prefix of sequences whose oracle run takes >= budget_s
+        (estimated from a one-sequence run)."""
+        one = cls(w, 1)
+        t1 = max(one.run(), 1e-4) / max(1, one.toks)
+        toks, n = 0, 0
+        while n < w.n_seqs and toks * t1 < budget_s:
+            toks += int(w.context_lens[n])
+            n += 1
+        return cls(w, max(1, n))
+
+
+def run_reference(args, rank):
+    """The reference arm: the CPU oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return None
+    w = _structure()
+    # size one step's sample so that all steps fit in about two minutes
+    per_step = max(0.02, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    smp = OracleSample.calibrated(w, per_step)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t = smp.run()
+        if i >= args.warmup:
+            times.append(t)
+    sec = statistics.median(times)
+    val = smp.bytes / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(val, 5), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "kv_format": "f16",
+                   "sample": f"first {smp.n} of 64 sequences, one layer per step"},
+        "attended_tokens_per_s": round(smp.toks / sec, 1),
+        "cpu_baseline": {"value": round(val, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"store+decode of the first {smp.n} sequences of one layer "
+                                   f"({smp.toks} attended positions), float64 numpy oracle"},
+        "e2e": {"value": round(val, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def run_gpu(args, rank, world, local_rank):
+    n_layers = args.layers
+    from paged_kv_cache_gqa_gb300 import mtkv
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = _structure()
+    hkv, d, bs, hq, B = w.n_kv_heads, w.head_dim, w.block_size, w.n_heads, w.n_seqs
+    n_cells = w.n_cells
+    g = torch.Generator(device=dev)
+    g.manual_seed(SEED + 100 * rank)
+    k_pools, v_pools, qs, k_news, v_news, outs = [], [], [], [], [], []
+    for _ in range(n_layers):
+        k_pools.append(torch.randn(n_cells, hkv * d, generator=g, device=dev, dtype=torch.float16))
+        v_pools.append(torch.randn(n_cells, hkv * d, generator=g, device=dev, dtype=torch.float16))
+        qs.append(torch.randn(B, hq, d, generator=g, device=dev, dtype=torch.float32))
+        k_news.append(torch.randn(B, hkv * d, generator=g, device=dev, dtype=torch.float32))
+        v_news.append(torch.randn(B, hkv * d, generator=g, device=dev, dtype=torch.float32))
+        outs.append(torch.empty(B, hq, d, device=dev, dtype=torch.float32))
+    table = torch.from_numpy(w.block_table).to(dev)
+    ctx = torch.from_numpy(w.context_lens).to(dev)
+    cells = torch.from_numpy(w.new_cells).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    args_l = [mtkv.paged_attn_args("f16", qs[l], k_pools[l], v_pools[l], table, ctx, outs[l],
+                                   n_kv_heads=hkv, block_size=bs, n_phys_blocks=w.n_phys_blocks,
+                                   scale=w.scale) for l in range(n_layers)]
+    ws = torch.zeros(mtkv.mt_paged_attn_workspace_bytes(args_l[0]), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n_layers)]
+
+    def step(record=False):
+        for l in range(n_layers):
+            mtkv.mt_kv_store("f16", k_pools[l], v_pools[l], hkv, d, k_news[l], v_news[l], cells,
+                             status=status)
+            if record:
+                ev[l][0].record(stream)
+            mtkv.mt_paged_attn_decode(args_l[l], ws)
+            if record:
+                ev[l][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert mtkv.mt_check_device_status(status) == 0, mtkv.mt_last_error()
+    assert mtkv.mt_check_device_status(ws) == 0, mtkv.mt_last_error()
+
+    clocks = Clocks(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    dec_ms = []
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+        # per-call decode durations of this step (read back after the run)
+        dec_ms.append([e for e in ev])
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n_layers)]
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t0.elapsed_time(t1)
+    dec_times = [a.elapsed_time(b) for st in dec_ms for (a, b) in st]
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    dbytes, toks = decode_bytes(w)
+    step_bytes = n_layers * (dbytes + store_bytes(w))
+    ms_per_step = total_ms / args.steps
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = _peak()
+    dec_avg_ms = statistics.mean(dec_times)
+    achieved = dbytes / (dec_avg_ms * 1e-3) / 1e9
+
+    # ---- end to end: inputs from pinned host memory, outputs back to host
+    h_q = [q.cpu().pin_memory() for q in qs]
+    h_k = [k.cpu().pin_memory() for k in k_news]
+    h_v = [v.cpu().pin_memory() for v in v_news]
+    h_table = torch.from_numpy(w.block_table).pin_memory()
+    h_ctx = torch.from_numpy(w.context_lens).pin_memory()
+    h_cells = torch.from_numpy(w.new_cells).pin_memory()
+    h_out = [torch.empty(B, hq, d, dtype=torch.float32).pin_memory() for _ in range(n_layers)]
+    h2d = sum(t.numel() * t.element_size() for t in h_q + h_k + h_v + [h_table, h_ctx, h_cells])
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def e2e_step():
+        table.copy_(h_table, non_blocking=True)
+        ctx.copy_(h_ctx, non_blocking=True)
+        cells.copy_(h_cells, non_blocking=True)
+        for l in range(n_layers):
+            qs[l].copy_(h_q[l], non_blocking=True)
+            k_news[l].copy_(h_k[l], non_blocking=True)
+            v_news[l].copy_(h_v[l], non_blocking=True)
+            mtkv.mt_kv_store("f16", k_pools[l], v_pools[l], hkv, d, k_news[l], v_news[l], cells,
+                             status=status)
+            mtkv.mt_paged_attn_decode(args_l[l], ws)
+            h_out[l].copy_(outs[l], non_blocking=True)
+
+    e2e_steps = max(3, args.steps // 4)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - e0) / e2e_steps
+    if world > 1:
+        tt = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+    assert mtkv.mt_check_device_status(status) == 0, mtkv.mt_last_error()
+    assert mtkv.mt_check_device_status(ws) == 0, mtkv.mt_last_error()
+
+    if rank != 0:
+        return None
+    cpu = None
+    if args.cpu_seconds > 0:
+        smp = OracleSample.calibrated(w, args.cpu_seconds / 3)
+        cpu_t = statistics.median([smp.run() for _ in range(3)])
+        cpu = {"value": round(smp.bytes / cpu_t / 1e9, 5), "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "attended_tokens_per_s": round(smp.toks / cpu_t, 1),
+               "sample": f"store+decode of the first {smp.n} of 64 sequences of one layer "
+                         f"({smp.toks} attended positions), float64 numpy oracle, median of "
+                         f"3 runs of {cpu_t:.2f} s"}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "kv_format": "f16", "n_layers": n_layers,
+                   "n_seqs": B, "attended_tokens_per_layer": toks,
+                   "l2": "inputs larger than L2 (1.3 GB of K/V per layer, 42 GB per step)",
+                   "parallelism": f"replicas x{world}"},
+        "frac_of_peak": round(value / peak, 4),
+        "attended_tokens_per_s": round(world * n_layers * toks / (ms_per_step * 1e-3), 1),
+        "roofline": {"bound": "hbm", "kernel": "mt_paged_attn_decode (split-K decode + combine)",
+                     "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "bytes_per_launch": dbytes, "avg_launch_ms": round(dec_avg_ms, 5),
+                     "traffic": _traffic_from_profile()},
+        "e2e": {"value": round(world * step_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_s * 1e3, 4)},
+        "gpu_launches": args.steps * n_layers * 3,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mtkv", choices=["mtkv", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="oracle baseline budget; 0 skips it (profiling runs)")
+    ap.add_argument("--layers", type=int, default=N_LAYERS,
+                    help="layers per step; fewer than 32 only for profiling captures")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group(backend)
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+    else:
+        line = run_gpu(args, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
