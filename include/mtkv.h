@@ -141,6 +141,31 @@ size_t mt_paged_attn_workspace_bytes(const mt_paged_attn_args *args);
 mt_status mt_paged_attn_decode(const mt_paged_attn_args *args, void *workspace,
                                size_t workspace_bytes, mt_stream stream);
 
+/* Bytes of the scratch array built into the library for
+ * mt_paged_attn_decode_static (8 MiB per device that loads the library). */
+#define MT_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/* Paged decode attention that allocates nothing and takes no workspace.
+ * This entry point has no counterpart in the paper; it is a convenience of
+ * this library. It computes exactly what mt_paged_attn_decode computes, for
+ * callers that cannot allocate device memory when they decode (a fixed
+ * memory budget that must not grow, an embedder that gets no allocator from
+ * its host, a thread that must not call into the CUDA allocator): the
+ * split-K scratch lives in one array of MT_STATIC_SCRATCH_BYTES inside the
+ * library, which every GPU that loads the library keeps until the process
+ * exits. The caller still passes inputs and outputs in `args`.
+ *   status  device uint32 status word, or NULL (no device-side reporting).
+ * Refused with MT_ERR_UNSUPPORTED, launching nothing, when the call needs
+ * more scratch than the array holds (compare
+ * mt_paged_attn_workspace_bytes with MT_STATIC_SCRATCH_BYTES).
+ * All calls on a device share the array and leave the last call's contents
+ * in it; nothing in it needs to start at zero, but calls whose kernels
+ * overlap on the GPU race on it, so order them on one stream. The first
+ * call on each device looks up the array's device address and caches it:
+ * make that first call before any stream capture begins. */
+mt_status mt_paged_attn_decode_static(const mt_paged_attn_args *args, uint32_t *status,
+                                      mt_stream stream);
+
 /* order_moves — "KV Cache Design — cells, format, sessions", section 2:
  * upward moves (dst > src) first, top-down (source descending), then
  * downward moves bottom-up (source ascending), so a destination never lands

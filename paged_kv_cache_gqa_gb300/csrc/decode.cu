@@ -37,6 +37,9 @@
 
 #include <math.h>
 
+#include <mutex>
+#include <string>
+
 namespace mtkv {
 namespace {
 
@@ -833,6 +836,123 @@ extern "C" mt_status mt_paged_attn_decode(const mt_paged_attn_args *a, void *wor
   prm.out = a->out;
   prm.lse = a->lse;
   prm.status = reinterpret_cast<uint32_t *>(ws + pl.ws_status);
+  prm.seq_start = reinterpret_cast<int32_t *>(ws + pl.ws_seq);
+  prm.part_ml = reinterpret_cast<float *>(ws + pl.ws_ml);
+  prm.part_o = reinterpret_cast<float *>(ws + pl.ws_o);
+  prm.B = a->n_seqs;
+  prm.Hq = a->n_heads;
+  prm.Hkv = a->n_kv_heads;
+  prm.G = a->n_heads / a->n_kv_heads;
+  prm.bs = a->block_size;
+  prm.max_blocks = a->max_blocks;
+  prm.n_phys = a->n_phys_blocks;
+  prm.row_bytes = (int)mt_kv_row_bytes(a->fmt, a->n_kv_heads, a->head_dim);
+  prm.blk_pad = pl.blk_pad;
+  prm.rows = pl.rows;
+  prm.stages = pl.stages;
+  prm.wph = pl.wph;
+  prm.n_cw = pl.n_cw;
+  prm.n_ctas = pl.n_ctas;
+  prm.qscale = a->scale * 1.4426950408889634f;
+  prm.wait_ns = kWaitLimitNs;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (a->fmt) {
+    case MT_KV_F32: st = dispatch_d<MT_KV_F32>(prm, pl, s); break;
+    case MT_KV_F16: st = dispatch_d<MT_KV_F16>(prm, pl, s); break;
+    default: st = dispatch_d<MT_KV_Q8_0>(prm, pl, s); break;
+  }
+  return st == MT_OK ? ok() : st;
+}
+
+// ------------------------------------------------ decode without allocation
+//
+// Some callers cannot allocate device memory at the moment they decode: code
+// running under a pre-sized memory budget that must not grow, plugins and
+// other embedders that get no allocator from their host, and callers that
+// must not call into the CUDA allocator on this thread (for example while
+// another component holds it). They cannot size and pass a workspace, so
+// this variant keeps the split-K scratch (sequence offsets and the per-split
+// partial results) in a fixed array that lives in the library itself.
+//
+// Limits and sharing:
+//  * The array holds MT_STATIC_SCRATCH_BYTES (8 MiB). Every GPU that loads
+//    the library keeps that much device memory for it until the process
+//    exits. A call whose scratch would not fit (mt_paged_attn_workspace_bytes
+//    larger than the array) is refused with MT_ERR_UNSUPPORTED before
+//    anything is launched.
+//  * All calls on a device share the one array and leave the last call's
+//    partial results in it. No byte of it has to start at zero: every byte
+//    a call reads was written earlier in the same call. Two calls whose
+//    kernels overlap on the GPU (different streams, no ordering between
+//    them) race on the array and may produce wrong results; order them on
+//    one stream, or use mt_paged_attn_decode with separate workspaces.
+//  * The first call on each device looks the array's device address up
+//    (cudaGetSymbolAddress, with that device current) and caches it; make
+//    that first call before any stream capture begins.
+//  * The device status word is the caller's `status` (may be NULL), not part
+//    of the array.
+namespace mtkv {
+namespace {
+
+constexpr size_t kStaticScratchBytes = MT_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_decode_scratch on the current device (host code only
+// sees a host-side stand-in when it names the array).
+mt_status static_scratch(uint8_t **out) {
+  static std::mutex mu;
+  static void *addr[kMaxDevices] = {};
+  int dev = 0;
+  mt_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != MT_OK) return st;
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(MT_ERR_UNSUPPORTED, "static-scratch decode: device index above 63");
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    st = cuda_check(cudaGetSymbolAddress(&p, g_decode_scratch),
+                    "cudaGetSymbolAddress(static decode scratch)");
+    if (st != MT_OK) return st;
+    addr[dev] = p;
+  }
+  *out = static_cast<uint8_t *>(addr[dev]);
+  return MT_OK;
+}
+
+}  // namespace
+}  // namespace mtkv
+
+extern "C" mt_status mt_paged_attn_decode_static(const mt_paged_attn_args *a, uint32_t *status,
+                                                 mt_stream stream) {
+  Plan pl;
+  mt_status st = make_plan(a, &pl, true);
+  if (st != MT_OK) return st;
+  if (pl.ws_total > kStaticScratchBytes)
+    return fail(MT_ERR_UNSUPPORTED,
+                "static-scratch decode: this call needs " + std::to_string(pl.ws_total) +
+                    " bytes of scratch but the library's array holds " +
+                    std::to_string(kStaticScratchBytes) +
+                    "; use mt_paged_attn_decode with a workspace");
+  if (a->n_seqs == 0) return ok();
+  if (!a->q || !a->k_pool || !a->v_pool || !a->block_table || !a->context_lens || !a->out)
+    return fail(MT_ERR_INVALID_ARG, "static-scratch decode: null pointer");
+  if (!aligned16(a->k_pool) || !aligned16(a->v_pool) || !aligned16(a->q) || !aligned16(a->out))
+    return fail(MT_ERR_INVALID_ARG, "static-scratch decode: q, pools and out must be 16-byte aligned");
+  uint8_t *ws = nullptr;
+  st = static_scratch(&ws);
+  if (st != MT_OK) return st;
+  Params prm;
+  prm.q = a->q;
+  prm.k_pool = static_cast<const uint8_t *>(a->k_pool);
+  prm.v_pool = static_cast<const uint8_t *>(a->v_pool);
+  prm.table = a->block_table;
+  prm.ctx = a->context_lens;
+  prm.spans = a->spans;
+  prm.out = a->out;
+  prm.lse = a->lse;
+  prm.status = status;
   prm.seq_start = reinterpret_cast<int32_t *>(ws + pl.ws_seq);
   prm.part_ml = reinterpret_cast<float *>(ws + pl.ws_ml);
   prm.part_o = reinterpret_cast<float *>(ws + pl.ws_o);

@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
         "mt_kv_store": (I, [I, P, P, I64, I, I, P, P, P, I, U32P, P]),
         "mt_paged_attn_workspace_bytes": (SZ, [ctypes.POINTER(mt_paged_attn_args)]),
         "mt_paged_attn_decode": (I, [ctypes.POINTER(mt_paged_attn_args), P, SZ, P]),
+        "mt_paged_attn_decode_static": (I, [ctypes.POINTER(mt_paged_attn_args), U32P, P]),
         "mt_order_moves": (I, [ctypes.POINTER(mt_move), I, ctypes.POINTER(I)]),
         "mt_check_moves": (I, [ctypes.POINTER(mt_move), I, I64, ctypes.POINTER(I)]),
         "mt_copy_cells": (I, [ctypes.POINTER(P), I, SZ, I64, ctypes.POINTER(mt_move), I, P]),
@@ -172,6 +173,16 @@ def mt_paged_attn_decode(args: mt_paged_attn_args, workspace, stream=None) -> No
     nbytes = workspace.numel() * workspace.element_size()
     _check(lib().mt_paged_attn_decode(ctypes.byref(args), _ptr(workspace), nbytes,
                                       _stream(stream)), "mt_paged_attn_decode")
+
+
+MT_STATIC_SCRATCH_BYTES = 8 << 20
+
+
+def mt_paged_attn_decode_static(args: mt_paged_attn_args, status=None, stream=None) -> None:
+    """Decode with the library's built-in scratch array instead of a workspace
+    (for callers that cannot allocate device memory when they decode)."""
+    _check(lib().mt_paged_attn_decode_static(ctypes.byref(args), _ptr(status), _stream(stream)),
+           "mt_paged_attn_decode_static")
 
 
 def _moves_array(moves):
