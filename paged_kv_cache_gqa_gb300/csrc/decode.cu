@@ -76,6 +76,9 @@ struct Params {
   int row_bytes;
   int blk_pad;   // bytes of one staged K (or V) row chunk, padded to 128
   int rows;      // block rows per stage (block_size, or a divisor of it for wide rows)
+  int pitch;     // shared-memory bytes between consecutive staged rows
+  int row_copies;  // 1: one bulk copy per row (padded pitch); 0: one per K and V range
+  int n_sub;     // partial records per (CTA, sequence) slot
   int stages;
   int wph;       // consumer warps per KV head
   int n_cw;      // consumer warps = Hkv * wph
@@ -161,7 +164,270 @@ struct Cfg {
   static_assert(LPT >= 4 && LPT <= 32, "lane layout");
 };
 
-template <int FMT, int D, int GP>
+// ------------------------------------------------------------ f16 on MMA
+//
+// Consumers for f16 pools that run Q.K and P.V on the tensor cores with
+// mma.sync.m16n8k16 (f16 inputs, f32 accumulation). Per 16-token step and
+// KV head a warp issues 2*(D/16) MMAs for Q.K and D/16 (its share of) MMAs
+// for P.V instead of ~1400 FP32-pipe instructions. Layouts:
+//   S = Qhl . K^T : A rows r<8 hold the high f16 half of q(head(r)) and rows
+//                   r+8 the low half (q - f16(q)), so S = hi + lo is accurate
+//                   to ~2^-22 relative; B = K rows straight from shared memory
+//                   (ldmatrix); thread (g, c) ends with head(g)'s scores for
+//                   tokens 8t + 2c, 8t + 2c + 1.
+//   O^T += V^T . P^T : dims on M (ldmatrix.trans of V rows), the N=8 columns
+//                   are (head, high/low half of p) pairs when G <= 4 and the
+//                   heads themselves when G > 4; each thread supplies column
+//                   g from its own probabilities, so P never leaves registers.
+// Rows of a stage sit `pitch` = row_bytes + 16 bytes apart, which makes every
+// ldmatrix phase hit 8 different bank groups.
+template <int D, int GP>
+struct MmaCfg {
+  static constexpr int KS = D / 16;              // Q.K k-steps over the head dims
+  static constexpr int MT = D / 16;              // P.V m-tiles over the head dims
+  static constexpr int MTW = MT < 8 ? MT : 8;    // m-tiles per warp
+  static constexpr int WPH = MT / MTW;           // warps per KV head (split over dims)
+  static constexpr bool HILO = GP <= 4;          // p split into two f16 columns
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+
+// high and low f16 halves of a float pair: x ~= hi + lo to ~2^-22 relative
+__device__ __forceinline__ void split_h2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  const float2 hf = __half22float2(h);
+  hi = h2_bits(h);
+  lo = h2_bits(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
+}
+
+template <int D, int GP>
+__device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uint64_t *empty,
+                                            StageInfo *infos, volatile int *abort_flag,
+                                            uint8_t *ring, int warp, int lane) {
+  using M = MmaCfg<D, GP>;
+  const int kvh = warp / M::WPH;
+  const int sub = warp % M::WPH;
+  const int g = lane >> 2, c = lane & 3;
+  const int G = p.G;
+  const int S = p.stages;
+  const int hrow = M::HILO ? (g >> 1) : g;  // head of A row g (and of B column g)
+  const bool row_ok = hrow < G;
+  const bool lo_col = M::HILO && (g & 1);   // B column g carries the low half of p
+  // lanes holding the softmax state of the heads of O^T columns 2c and 2c+1
+  const int src0 = M::HILO ? 8 * c : 8 * c;
+  const int src1 = M::HILO ? 8 * c : 8 * c + 4;
+  const size_t head_off = (size_t)kvh * D * 2;  // byte offset of this head in a row
+  const int dim0 = sub * M::MTW * 16;           // first output dim of this warp
+
+  uint32_t qa[M::KS][4];
+  float oacc[M::MTW][4];
+  float m_run = -INFINITY, l_run = 0.f;
+
+  for (uint32_t it = 0;; ++it) {
+    const int slot = (int)(it % (uint32_t)S);
+    int okv = 1;
+    if (lane == 0)
+      okv = mbar_wait_bounded(&full[slot], (it / (uint32_t)S) & 1u, abort_flag, p.wait_ns) ? 1 : 0;
+    okv = __shfl_sync(kFull, okv, 0);
+    if (!okv) {
+      if (lane == 0) {
+        *abort_flag = 1;
+        report(p.status, MT_STATUS_BIT_TIMEOUT);
+      }
+      return;
+    }
+    int seq, r0, r1, flags, base;
+    {
+      const volatile int *vi = reinterpret_cast<const volatile int *>(&infos[slot]);
+      seq = vi[0];
+      r0 = vi[1];
+      r1 = vi[2];
+      flags = vi[3] & 0xff;
+      base = vi[3] >> 8;
+    }
+    if (flags & F_EXIT) return;
+
+    if (flags & F_NEW) {
+      const float *qh = p.q + ((size_t)seq * p.Hq + (size_t)kvh * G + hrow) * D;
+#pragma unroll
+      for (int ks = 0; ks < M::KS; ++ks) {
+        float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
+        if (row_ok) {
+          x0 = *reinterpret_cast<const float2 *>(qh + 16 * ks + 2 * c);
+          x1 = *reinterpret_cast<const float2 *>(qh + 16 * ks + 2 * c + 8);
+        }
+        split_h2(x0.x * p.qscale, x0.y * p.qscale, qa[ks][0], qa[ks][1]);
+        split_h2(x1.x * p.qscale, x1.y * p.qscale, qa[ks][2], qa[ks][3]);
+      }
+#pragma unroll
+      for (int mt = 0; mt < M::MTW; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) oacc[mt][e] = 0.f;
+      m_run = -INFINITY;
+      l_run = 0.f;
+    }
+
+    if (flags & F_DATA) {
+      uint8_t *kst = ring + (size_t)slot * 2 * p.blk_pad - (ptrdiff_t)base * p.pitch;
+      uint8_t *vst = kst + p.blk_pad;
+      const int row_end = base + p.rows;
+      // Rows of the stage outside [r0, r1) hold stale bytes: P is 0 there but
+      // 0 * NaN would not be, so clear this head's V columns of those rows.
+      bool wrote = false;
+      if (r0 > base || r1 < row_end) {
+        constexpr int V16 = D * 2 / 16;  // 16-byte pieces of one head row
+        const int n_bad = (r0 - base) + (row_end - r1);
+        for (int i = lane; i < n_bad * V16; i += 32) {
+          const int k = i / V16;
+          const int row = k < r0 - base ? base + k : r1 + (k - (r0 - base));
+          *reinterpret_cast<uint4 *>(vst + (size_t)row * p.pitch + head_off + (i % V16) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        wrote = true;
+        __syncwarp();
+      }
+      // ---- S = Qhl . K^T over the stage's 8-token tiles
+      float pr[4][2];
+      float mloc = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        pr[t][0] = pr[t][1] = -INFINITY;
+        const int t0 = 8 * t;
+        if (t0 >= p.bs || t0 + 8 <= r0 || t0 >= r1) continue;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t kaddr = smem_u32(kst + (size_t)(t0 + (lane & 7)) * p.pitch + head_off) +
+                               (uint32_t)((lane >> 3) & 1) * 16 + (uint32_t)(lane >> 4) * 32;
+#pragma unroll
+        for (int ks = 0; ks < M::KS; ks += 2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kaddr + ks * 32, b0, b1, b2, b3);
+          mma_f16(acc, qa[ks], b0, b1);
+          mma_f16(acc, qa[ks + 1], b2, b3);
+        }
+        const int tk = t0 + 2 * c;
+        const float s0 = acc[0] + acc[2], s1 = acc[1] + acc[3];
+        pr[t][0] = (row_ok && tk >= r0 && tk < r1) ? s0 : -INFINITY;
+        pr[t][1] = (row_ok && tk + 1 >= r0 && tk + 1 < r1) ? s1 : -INFINITY;
+        mloc = fmaxf(mloc, fmaxf(pr[t][0], pr[t][1]));
+      }
+      // ---- online softmax (base 2) per head: the 4 lanes of group g agree
+      mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, 1));
+      mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, 2));
+      const float m_new = fmaxf(m_run, mloc);
+      const bool none = m_new == -INFINITY;
+      const float alpha = none ? 1.f : exp2f(m_run - m_new);
+      m_run = m_new;
+      float lsum = 0.f;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        pr[t][0] = none ? 0.f : exp2f(pr[t][0] - m_new);
+        pr[t][1] = none ? 0.f : exp2f(pr[t][1] - m_new);
+        lsum += pr[t][0] + pr[t][1];
+      }
+      l_run = l_run * alpha + lsum;
+      const float a0 = __shfl_sync(kFull, alpha, src0);
+      const float a1 = __shfl_sync(kFull, alpha, src1);
+      if (!__all_sync(kFull, a0 == 1.f && a1 == 1.f)) {
+#pragma unroll
+        for (int mt = 0; mt < M::MTW; ++mt) {
+          oacc[mt][0] *= a0;
+          oacc[mt][1] *= a1;
+          oacc[mt][2] *= a0;
+          oacc[mt][3] *= a1;
+        }
+      }
+      // ---- O^T += V^T . P^T over 16-token chunks
+#pragma unroll
+      for (int kc = 0; kc < 2; ++kc) {
+        const int t0 = 16 * kc;
+        if (t0 >= p.bs || t0 + 16 <= r0 || t0 >= r1) continue;
+        uint32_t b0, b1;
+        if (M::HILO) {
+          uint32_t h0, l0, h1, l1;
+          split_h2(pr[2 * kc][0], pr[2 * kc][1], h0, l0);
+          split_h2(pr[2 * kc + 1][0], pr[2 * kc + 1][1], h1, l1);
+          b0 = lo_col ? l0 : h0;
+          b1 = lo_col ? l1 : h1;
+        } else {
+          b0 = h2_bits(__floats2half2_rn(pr[2 * kc][0], pr[2 * kc][1]));
+          b1 = h2_bits(__floats2half2_rn(pr[2 * kc + 1][0], pr[2 * kc + 1][1]));
+        }
+        if (!row_ok) b0 = b1 = 0u;
+        const uint32_t vaddr =
+            smem_u32(vst + (size_t)(t0 + ((lane >> 4) & 1) * 8 + (lane & 7)) * p.pitch + head_off) +
+            (uint32_t)(dim0 + ((lane >> 3) & 1) * 8) * 2;
+#pragma unroll
+        for (int mt = 0; mt < M::MTW; ++mt) {
+          uint32_t a[4];
+          ldsm_x4_t(vaddr + mt * 32, a[0], a[1], a[2], a[3]);
+          mma_f16(oacc[mt], a, b0, b1);
+        }
+      }
+      if (wrote) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+
+    if (flags & F_END) {
+      float l = l_run;
+      l += __shfl_xor_sync(kFull, l, 1);
+      l += __shfl_xor_sync(kFull, l, 2);
+      const size_t P = (size_t)blockIdx.x + seq;
+      const size_t hq0 = P * p.Hq + (size_t)kvh * G;
+      if (sub == 0 && c == 0 && row_ok && !lo_col) {
+        p.part_ml[(hq0 + hrow) * 2 + 0] = m_run;
+        p.part_ml[(hq0 + hrow) * 2 + 1] = l;
+      }
+#pragma unroll
+      for (int mt = 0; mt < M::MTW; ++mt) {
+        const int dm = dim0 + mt * 16 + g;
+        if (M::HILO) {
+          if (c < G) {
+            float *dst = p.part_o + (hq0 + c) * D;
+            dst[dm] = oacc[mt][0] + oacc[mt][1];
+            dst[dm + 8] = oacc[mt][2] + oacc[mt][3];
+          }
+        } else {
+          if (2 * c < G) {
+            float *dst = p.part_o + (hq0 + 2 * c) * D;
+            dst[dm] = oacc[mt][0];
+            dst[dm + 8] = oacc[mt][2];
+          }
+          if (2 * c + 1 < G) {
+            float *dst = p.part_o + (hq0 + 2 * c + 1) * D;
+            dst[dm] = oacc[mt][1];
+            dst[dm + 8] = oacc[mt][3];
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+  }
+}
+
+template <int FMT, int D, int GP, bool MMA>
 __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params p) {
   using C = Cfg<FMT, D, GP>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -219,7 +485,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params 
           okv = 0;
         if (okv) {
           infos[slot] = StageInfo{s, r0, r1, flags | (base << 8)};
-          if (flags & F_DATA) {
+          if ((flags & F_DATA) && p.row_copies) {
+            mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * (r1 - r0) * p.row_bytes));
+          } else if (flags & F_DATA) {
             // rows [ra, rb): the valid rows widened to whole 4-row groups, so
             // both addresses and the size stay multiples of 16 bytes
             const int ra = r0 & ~3;
@@ -236,6 +504,20 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params 
         }
       }
       okv = __shfl_sync(kFull, okv, 0);
+      if (okv && (flags & F_DATA) && p.row_copies) {
+        // one bulk copy per row into rows of `pitch` bytes: the 16-byte pad
+        // shifts consecutive rows across banks for ldmatrix; lanes share them
+        const int n = r1 - r0;
+        const int slot2 = (int)(it % (uint32_t)S);
+        uint8_t *dk = ring + (size_t)slot2 * 2 * p.blk_pad;
+        for (int i = lane; i < 2 * n; i += 32) {
+          const int r = r0 + (i < n ? i : i - n);
+          const size_t src = ((size_t)phys * p.bs + r) * (size_t)p.row_bytes;
+          uint8_t *dst = dk + (i < n ? 0 : p.blk_pad) + (size_t)(r - base) * p.pitch;
+          bulk_g2s(dst, (i < n ? p.k_pool : p.v_pool) + src, (uint32_t)p.row_bytes, &full[slot2],
+                   pol);
+        }
+      }
       if (okv) ++it;
       return okv != 0;
     };
@@ -322,7 +604,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params 
   }
 
   if (warp >= p.n_cw) return;
-
+  if constexpr (MMA) {
+    consume_mma<D, GP>(p, full, empty, infos, abort_flag, ring, warp, lane);
+  } else {
   // ------------------------------------------------------- consumer warps
   const int kvh = warp / p.wph;
   const int sub = warp % p.wph;
@@ -599,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params 
       float lsum = l_run;  // non-zero only on the rep0 lanes
 #pragma unroll
       for (int o = C::LPT; o < 32; o <<= 1) lsum += __shfl_xor_sync(kFull, lsum, o);
-      const size_t P = ((size_t)blockIdx.x + seq) * p.wph + sub;
+      const size_t P = ((size_t)blockIdx.x + seq) * p.n_sub + sub;
       const size_t hq0 = P * p.Hq + (size_t)kvh * G;
       if (tq == 0 && rep0 && hidx < G) {
         p.part_ml[(hq0 + hidx) * 2 + 0] = m_run;
@@ -617,6 +901,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params 
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
   }
+  }  // SIMT consumers
 }
 
 // Merge every partial of (sequence, query head) by log-sum-exp and
@@ -638,14 +923,14 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(const Params p) {
   if (end > beg) {
     const int c0 = beg / per, c1 = (end - 1) / per;
     for (int c = c0; c <= c1; ++c)
-      for (int u = 0; u < p.wph; ++u) {
-        const size_t P = ((size_t)c + s) * p.wph + u;
+      for (int u = 0; u < p.n_sub; ++u) {
+        const size_t P = ((size_t)c + s) * p.n_sub + u;
         M = fmaxf(M, p.part_ml[(P * p.Hq + h) * 2]);
       }
     if (M > -INFINITY) {
       for (int c = c0; c <= c1; ++c)
-        for (int u = 0; u < p.wph; ++u) {
-          const size_t P = ((size_t)c + s) * p.wph + u;
+        for (int u = 0; u < p.n_sub; ++u) {
+          const size_t P = ((size_t)c + s) * p.n_sub + u;
           const float m = p.part_ml[(P * p.Hq + h) * 2];
           const float l = p.part_ml[(P * p.Hq + h) * 2 + 1];
           if (!(l > 0.f)) continue;
@@ -675,6 +960,8 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(const Params p) {
 
 struct Plan {
   int D, GP, wph, n_cw, stages, n_ctas, blk_pad, rows, smem;
+  bool mma;
+  int pitch, n_sub;
   size_t ws_status, ws_seq, ws_ml, ws_o, ws_total;
 };
 
@@ -709,14 +996,6 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
     return fail(MT_ERR_UNSUPPORTED, "paged decode: max_blocks * block_size overflows int32");
   pl->D = a->head_dim;
   pl->GP = GP;
-  const int dpl = GP >= 8 ? 8 : 16;
-  const int tps = 32 / (a->head_dim / dpl);
-  const int nsteps = a->block_size / tps;
-  int wph = kMaxConsumerWarps / a->n_kv_heads;
-  if (wph > nsteps) wph = nsteps;
-  if (wph < 1) wph = 1;
-  pl->wph = wph;
-  pl->n_cw = a->n_kv_heads * wph;
   const int fixed = kHdrBytes + ((kMaxConsumerWarps * (32 * GP + GP) * 4 + 127) & ~127) + 16;
   int n_ctas = a->n_ctas;
   int smem_cap = 232448;
@@ -727,25 +1006,49 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
     if (n_ctas == 0) n_ctas = di.n_sm;
     smem_cap = di.smem_optin;
   }
-  // Whole blocks per stage when at least two stages fit; otherwise halve the
-  // rows per stage (never below 8, a multiple of every token step) until
-  // they do.
-  int rows = a->block_size, stages = 0, pad = 0;
-  for (;;) {
-    pad = (int)(((size_t)rows * rb + 127) & ~(size_t)127);
-    stages = (smem_cap - fixed) / (2 * pad);
-    if (stages >= 2 || rows <= 8) break;
-    rows /= 2;
+  // Rows per stage: whole blocks when at least two stages fit, else halve
+  // (never below `min_rows`). Returns false when even that does not fit.
+  auto fit = [&](int pitch, int min_rows, int &rows, int &pad, int &stages) {
+    rows = a->block_size;
+    for (;;) {
+      pad = (int)(((size_t)rows * pitch + 127) & ~(size_t)127);
+      stages = (smem_cap - fixed) / (2 * pad);
+      if (stages >= 2 || rows <= min_rows) break;
+      rows /= 2;
+    }
+    if (stages > kMaxStages) stages = kMaxStages;
+    return stages >= 2 && rows >= min_rows;
+  };
+  int rows = 0, pad = 0, stages = 0, wph = 1;
+  // f16 pools use the tensor-core consumers when a warp per KV head (two for
+  // head_dim 256) fits in the 8 consumer warps and 16-row stages fit.
+  const int mma_wph = a->head_dim == 256 ? 2 : 1;
+  pl->mma = a->fmt == MT_KV_F16 && a->n_kv_heads * mma_wph <= kMaxConsumerWarps &&
+            fit((int)rb + 16, 16, rows, pad, stages);
+  if (pl->mma) {
+    wph = mma_wph;
+    pl->pitch = (int)rb + 16;
+    pl->n_sub = 1;
+  } else {
+    const int dpl = GP >= 8 ? 8 : 16;
+    const int tps = 32 / (a->head_dim / dpl);
+    const int nsteps = a->block_size / tps;
+    wph = kMaxConsumerWarps / a->n_kv_heads;
+    if (wph > nsteps) wph = nsteps;
+    if (wph < 1) wph = 1;
+    if (!fit((int)rb, 8, rows, pad, stages))
+      return fail(MT_ERR_UNSUPPORTED, "paged decode: KV rows too wide to double-buffer 8 of them");
+    pl->pitch = (int)rb;
+    pl->n_sub = wph;
   }
-  if (stages > kMaxStages) stages = kMaxStages;
-  if (stages < 2)
-    return fail(MT_ERR_UNSUPPORTED, "paged decode: KV rows too wide to double-buffer 8 of them");
+  pl->wph = wph;
+  pl->n_cw = a->n_kv_heads * wph;
   pl->rows = rows;
   pl->blk_pad = pad;
   pl->stages = stages;
   pl->n_ctas = n_ctas;
   pl->smem = fixed + stages * 2 * pl->blk_pad;
-  const size_t P = ((size_t)n_ctas + (size_t)a->n_seqs) * wph;
+  const size_t P = ((size_t)n_ctas + (size_t)a->n_seqs) * pl->n_sub;
   auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
   pl->ws_status = 0;
   pl->ws_seq = 256;
@@ -755,11 +1058,11 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
   return MT_OK;
 }
 
-template <int FMT, int D, int GP>
+template <int FMT, int D, int GP, bool MMA>
 mt_status launch_decode(const Params &prm, const Plan &pl, cudaStream_t s) {
   static int configured_dev = -1;
   static int configured_smem = 0;
-  auto kern = paged_decode_kernel<FMT, D, GP>;
+  auto kern = paged_decode_kernel<FMT, D, GP, MMA>;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev || configured_smem < pl.smem) {
@@ -781,22 +1084,68 @@ mt_status launch_decode(const Params &prm, const Plan &pl, cudaStream_t s) {
   return st;
 }
 
-template <int FMT, int D>
+template <int FMT, int D, bool MMA>
 mt_status dispatch_gp(const Params &prm, const Plan &pl, cudaStream_t s) {
   switch (pl.GP) {
-    case 1: return launch_decode<FMT, D, 1>(prm, pl, s);
-    case 2: return launch_decode<FMT, D, 2>(prm, pl, s);
-    case 4: return launch_decode<FMT, D, 4>(prm, pl, s);
-    default: return launch_decode<FMT, D, 8>(prm, pl, s);
+    case 1: return launch_decode<FMT, D, 1, MMA>(prm, pl, s);
+    case 2: return launch_decode<FMT, D, 2, MMA>(prm, pl, s);
+    case 4: return launch_decode<FMT, D, 4, MMA>(prm, pl, s);
+    default: return launch_decode<FMT, D, 8, MMA>(prm, pl, s);
   }
 }
 
-template <int FMT>
+template <int FMT, bool MMA>
 mt_status dispatch_d(const Params &prm, const Plan &pl, cudaStream_t s) {
   switch (pl.D) {
-    case 64: return dispatch_gp<FMT, 64>(prm, pl, s);
-    case 128: return dispatch_gp<FMT, 128>(prm, pl, s);
-    default: return dispatch_gp<FMT, 256>(prm, pl, s);
+    case 64: return dispatch_gp<FMT, 64, MMA>(prm, pl, s);
+    case 128: return dispatch_gp<FMT, 128, MMA>(prm, pl, s);
+    default: return dispatch_gp<FMT, 256, MMA>(prm, pl, s);
+  }
+}
+
+// Fill the kernel parameters shared by both decode entry points.
+void fill_params(Params &prm, const mt_paged_attn_args *a, const Plan &pl, uint8_t *ws,
+                 uint32_t *status) {
+  prm.q = a->q;
+  prm.k_pool = static_cast<const uint8_t *>(a->k_pool);
+  prm.v_pool = static_cast<const uint8_t *>(a->v_pool);
+  prm.table = a->block_table;
+  prm.ctx = a->context_lens;
+  prm.spans = a->spans;
+  prm.out = a->out;
+  prm.lse = a->lse;
+  prm.status = status;
+  prm.seq_start = reinterpret_cast<int32_t *>(ws + pl.ws_seq);
+  prm.part_ml = reinterpret_cast<float *>(ws + pl.ws_ml);
+  prm.part_o = reinterpret_cast<float *>(ws + pl.ws_o);
+  prm.B = a->n_seqs;
+  prm.Hq = a->n_heads;
+  prm.Hkv = a->n_kv_heads;
+  prm.G = a->n_heads / a->n_kv_heads;
+  prm.bs = a->block_size;
+  prm.max_blocks = a->max_blocks;
+  prm.n_phys = a->n_phys_blocks;
+  prm.row_bytes = (int)mt_kv_row_bytes(a->fmt, a->n_kv_heads, a->head_dim);
+  prm.blk_pad = pl.blk_pad;
+  prm.rows = pl.rows;
+  prm.pitch = pl.pitch;
+  prm.row_copies = pl.mma ? 1 : 0;
+  prm.n_sub = pl.n_sub;
+  prm.stages = pl.stages;
+  prm.wph = pl.wph;
+  prm.n_cw = pl.n_cw;
+  prm.n_ctas = pl.n_ctas;
+  prm.qscale = a->scale * 1.4426950408889634f;
+  prm.wait_ns = kWaitLimitNs;
+}
+
+mt_status dispatch(const Params &prm, const Plan &pl, mt_kv_format fmt, cudaStream_t s) {
+  switch (fmt) {
+    case MT_KV_F32: return dispatch_d<MT_KV_F32, false>(prm, pl, s);
+    case MT_KV_F16:
+      return pl.mma ? dispatch_d<MT_KV_F16, true>(prm, pl, s)
+                    : dispatch_d<MT_KV_F16, false>(prm, pl, s);
+    default: return dispatch_d<MT_KV_Q8_0, false>(prm, pl, s);
   }
 }
 
@@ -827,40 +1176,8 @@ extern "C" mt_status mt_paged_attn_decode(const mt_paged_attn_args *a, void *wor
     return fail(MT_ERR_INVALID_ARG, "paged decode: q, pools, out and workspace must be 16-byte aligned");
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   Params prm;
-  prm.q = a->q;
-  prm.k_pool = static_cast<const uint8_t *>(a->k_pool);
-  prm.v_pool = static_cast<const uint8_t *>(a->v_pool);
-  prm.table = a->block_table;
-  prm.ctx = a->context_lens;
-  prm.spans = a->spans;
-  prm.out = a->out;
-  prm.lse = a->lse;
-  prm.status = reinterpret_cast<uint32_t *>(ws + pl.ws_status);
-  prm.seq_start = reinterpret_cast<int32_t *>(ws + pl.ws_seq);
-  prm.part_ml = reinterpret_cast<float *>(ws + pl.ws_ml);
-  prm.part_o = reinterpret_cast<float *>(ws + pl.ws_o);
-  prm.B = a->n_seqs;
-  prm.Hq = a->n_heads;
-  prm.Hkv = a->n_kv_heads;
-  prm.G = a->n_heads / a->n_kv_heads;
-  prm.bs = a->block_size;
-  prm.max_blocks = a->max_blocks;
-  prm.n_phys = a->n_phys_blocks;
-  prm.row_bytes = (int)mt_kv_row_bytes(a->fmt, a->n_kv_heads, a->head_dim);
-  prm.blk_pad = pl.blk_pad;
-  prm.rows = pl.rows;
-  prm.stages = pl.stages;
-  prm.wph = pl.wph;
-  prm.n_cw = pl.n_cw;
-  prm.n_ctas = pl.n_ctas;
-  prm.qscale = a->scale * 1.4426950408889634f;
-  prm.wait_ns = kWaitLimitNs;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  switch (a->fmt) {
-    case MT_KV_F32: st = dispatch_d<MT_KV_F32>(prm, pl, s); break;
-    case MT_KV_F16: st = dispatch_d<MT_KV_F16>(prm, pl, s); break;
-    default: st = dispatch_d<MT_KV_Q8_0>(prm, pl, s); break;
-  }
+  fill_params(prm, a, pl, ws, reinterpret_cast<uint32_t *>(ws + pl.ws_status));
+  st = dispatch(prm, pl, a->fmt, reinterpret_cast<cudaStream_t>(stream));
   return st == MT_OK ? ok() : st;
 }
 
@@ -944,39 +1261,7 @@ extern "C" mt_status mt_paged_attn_decode_static(const mt_paged_attn_args *a, ui
   st = static_scratch(&ws);
   if (st != MT_OK) return st;
   Params prm;
-  prm.q = a->q;
-  prm.k_pool = static_cast<const uint8_t *>(a->k_pool);
-  prm.v_pool = static_cast<const uint8_t *>(a->v_pool);
-  prm.table = a->block_table;
-  prm.ctx = a->context_lens;
-  prm.spans = a->spans;
-  prm.out = a->out;
-  prm.lse = a->lse;
-  prm.status = status;
-  prm.seq_start = reinterpret_cast<int32_t *>(ws + pl.ws_seq);
-  prm.part_ml = reinterpret_cast<float *>(ws + pl.ws_ml);
-  prm.part_o = reinterpret_cast<float *>(ws + pl.ws_o);
-  prm.B = a->n_seqs;
-  prm.Hq = a->n_heads;
-  prm.Hkv = a->n_kv_heads;
-  prm.G = a->n_heads / a->n_kv_heads;
-  prm.bs = a->block_size;
-  prm.max_blocks = a->max_blocks;
-  prm.n_phys = a->n_phys_blocks;
-  prm.row_bytes = (int)mt_kv_row_bytes(a->fmt, a->n_kv_heads, a->head_dim);
-  prm.blk_pad = pl.blk_pad;
-  prm.rows = pl.rows;
-  prm.stages = pl.stages;
-  prm.wph = pl.wph;
-  prm.n_cw = pl.n_cw;
-  prm.n_ctas = pl.n_ctas;
-  prm.qscale = a->scale * 1.4426950408889634f;
-  prm.wait_ns = kWaitLimitNs;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  switch (a->fmt) {
-    case MT_KV_F32: st = dispatch_d<MT_KV_F32>(prm, pl, s); break;
-    case MT_KV_F16: st = dispatch_d<MT_KV_F16>(prm, pl, s); break;
-    default: st = dispatch_d<MT_KV_Q8_0>(prm, pl, s); break;
-  }
+  fill_params(prm, a, pl, ws, status);
+  st = dispatch(prm, pl, a->fmt, reinterpret_cast<cudaStream_t>(stream));
   return st == MT_OK ? ok() : st;
 }
