@@ -32,6 +32,9 @@
 //    the combine kernel merges them (log-sum-exp) and normalises.
 //  * Every mbarrier wait is bounded; a timeout sets the status word, stops
 //    the CTA's producer after its copies in flight have landed, and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -59,6 +62,8 @@ struct StageInfo {
 };
 
 struct Params {
+  CUtensorMap tmap_k;  // f16 tensor-core path: 3-D maps of the pools, see tma_block()
+  CUtensorMap tmap_v;
   const float *q;
   const uint8_t *k_pool;
   const uint8_t *v_pool;
@@ -77,7 +82,8 @@ struct Params {
   int blk_pad;   // bytes of one staged K (or V) row chunk, padded to 128
   int rows;      // block rows per stage (block_size, or a divisor of it for wide rows)
   int pitch;     // shared-memory bytes between consecutive staged rows
-  int row_copies;  // 1: one bulk copy per row (padded pitch); 0: one per K and V range
+  int use_tmap;  // 1: stage blocks with swizzled tensor copies (f16 tensor-core path)
+  int ncb;       // 128-byte chunks per staged row (odd), tensor path
   int n_sub;     // partial records per (CTA, sequence) slot
   int stages;
   int wph;       // consumer warps per KV head
@@ -164,6 +170,34 @@ struct Cfg {
   static_assert(LPT >= 4 && LPT <= 32, "lane layout");
 };
 
+// --------------------------------------------------- swizzled tensor copies
+//
+// On the f16 tensor-core path a pool is described to the TMA engine as a 3-D
+// tensor [cell][128-byte chunk of the row][64 f16], and one tensor copy
+// stages `rows` cells of a block with the 128-byte swizzle. The box spans
+// ncb chunks, one more than the row has when that count is even (the extra
+// chunk lies outside the tensor and is zero-filled, never read from memory),
+// so a staged row is an odd number of 128-byte lines: the swizzle then XORs
+// the 16-byte unit index with (line & 7) and the 8 rows an ldmatrix phase
+// reads land in 8 different bank groups.
+__device__ __forceinline__ void tma_block(void *smem_dst, const CUtensorMap *map, int cell,
+                                          uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(cell), "r"(smem_u32(bar)),
+      "l"(policy)
+      : "memory");
+}
+
+// Shared-memory address of the 16-byte unit holding elements [e, e+8) of
+// staged row `row` (relative to the stage): line = row*ncb + e/64, unit
+// (e/8)%8 XOR (line % 8).
+__device__ __forceinline__ uint32_t swz(uint32_t stage, int row, int e, int ncb) {
+  const int line = row * ncb + (e >> 6);
+  return stage + (uint32_t)line * 128u + ((uint32_t)(((e >> 3) & 7) ^ (line & 7)) << 4);
+}
+
 // ------------------------------------------------------------ f16 on MMA
 //
 // Consumers for f16 pools that run Q.K and P.V on the tensor cores with
@@ -239,7 +273,7 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
   // lanes holding the softmax state of the heads of O^T columns 2c and 2c+1
   const int src0 = M::HILO ? 8 * c : 8 * c;
   const int src1 = M::HILO ? 8 * c : 8 * c + 4;
-  const size_t head_off = (size_t)kvh * D * 2;  // byte offset of this head in a row
+  const int head_e = kvh * D;                   // first element of this head in a row
   const int dim0 = sub * M::MTW * 16;           // first output dim of this warp
 
   uint32_t qa[M::KS][4];
@@ -291,19 +325,22 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
     }
 
     if (flags & F_DATA) {
-      uint8_t *kst = ring + (size_t)slot * 2 * p.blk_pad - (ptrdiff_t)base * p.pitch;
-      uint8_t *vst = kst + p.blk_pad;
+      const uint32_t kst = smem_u32(ring + (size_t)slot * 2 * p.blk_pad);
+      const uint32_t vst = kst + p.blk_pad;
+      uint8_t *vst_ptr = ring + (size_t)slot * 2 * p.blk_pad + p.blk_pad;
       const int row_end = base + p.rows;
-      // Rows of the stage outside [r0, r1) hold stale bytes: P is 0 there but
-      // 0 * NaN would not be, so clear this head's V columns of those rows.
+      // Rows of the stage outside [r0, r1) hold bytes of other positions: P
+      // is 0 there but 0 * NaN would not be, so clear this head's V chunks of
+      // those rows (all 8 units of a chunk, so the swizzle does not matter).
       bool wrote = false;
       if (r0 > base || r1 < row_end) {
         constexpr int V16 = D * 2 / 16;  // 16-byte pieces of one head row
         const int n_bad = (r0 - base) + (row_end - r1);
         for (int i = lane; i < n_bad * V16; i += 32) {
           const int k = i / V16;
-          const int row = k < r0 - base ? base + k : r1 + (k - (r0 - base));
-          *reinterpret_cast<uint4 *>(vst + (size_t)row * p.pitch + head_off + (i % V16) * 16) =
+          const int row = k < r0 - base ? k : r1 - base + (k - (r0 - base));
+          const int line = row * p.ncb + (head_e >> 6) + (i % V16) / 8;
+          *reinterpret_cast<uint4 *>(vst_ptr + (size_t)line * 128 + (i % 8) * 16) =
               make_uint4(0, 0, 0, 0);
         }
         wrote = true;
@@ -318,12 +355,12 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
         const int t0 = 8 * t;
         if (t0 >= p.bs || t0 + 8 <= r0 || t0 >= r1) continue;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t kaddr = smem_u32(kst + (size_t)(t0 + (lane & 7)) * p.pitch + head_off) +
-                               (uint32_t)((lane >> 3) & 1) * 16 + (uint32_t)(lane >> 4) * 32;
+        const int krow = t0 + (lane & 7) - base;
+        const int ke = head_e + ((lane >> 3) & 1) * 8 + (lane >> 4) * 16;
 #pragma unroll
         for (int ks = 0; ks < M::KS; ks += 2) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(kaddr + ks * 32, b0, b1, b2, b3);
+          ldsm_x4(swz(kst, krow, ke + ks * 16, p.ncb), b0, b1, b2, b3);
           mma_f16(acc, qa[ks], b0, b1);
           mma_f16(acc, qa[ks + 1], b2, b3);
         }
@@ -376,13 +413,12 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
           b1 = h2_bits(__floats2half2_rn(pr[2 * kc + 1][0], pr[2 * kc + 1][1]));
         }
         if (!row_ok) b0 = b1 = 0u;
-        const uint32_t vaddr =
-            smem_u32(vst + (size_t)(t0 + ((lane >> 4) & 1) * 8 + (lane & 7)) * p.pitch + head_off) +
-            (uint32_t)(dim0 + ((lane >> 3) & 1) * 8) * 2;
+        const int vrow = t0 + ((lane >> 4) & 1) * 8 + (lane & 7) - base;
+        const int ve = head_e + dim0 + ((lane >> 3) & 1) * 8;
 #pragma unroll
         for (int mt = 0; mt < M::MTW; ++mt) {
           uint32_t a[4];
-          ldsm_x4_t(vaddr + mt * 32, a[0], a[1], a[2], a[3]);
+          ldsm_x4_t(swz(vst, vrow, ve + mt * 16, p.ncb), a[0], a[1], a[2], a[3]);
           mma_f16(oacc[mt], a, b0, b1);
         }
       }
@@ -428,7 +464,7 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
 }
 
 template <int FMT, int D, int GP, bool MMA>
-__global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_constant__ Params p) {
   using C = Cfg<FMT, D, GP>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
@@ -436,8 +472,10 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params 
   StageInfo *infos = reinterpret_cast<StageInfo *>(smem + 64);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 128);
   float *scratch = reinterpret_cast<float *>(smem + kHdrBytes);
+  // the ring starts on a 1024-byte boundary (the 128-byte swizzle's period)
   uint8_t *ring = smem + kHdrBytes +
                   ((kMaxConsumerWarps * scratch_floats_per_warp<GP>() * 4 + 127) & ~127);
+  ring += (1024u - (smem_u32(ring) & 1023u)) & 1023u;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -485,8 +523,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params 
           okv = 0;
         if (okv) {
           infos[slot] = StageInfo{s, r0, r1, flags | (base << 8)};
-          if ((flags & F_DATA) && p.row_copies) {
-            mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * (r1 - r0) * p.row_bytes));
+          if ((flags & F_DATA) && p.use_tmap) {
+            // the whole stage (rows [base, base + rows)) in two tensor copies
+            uint8_t *dk = ring + (size_t)slot * 2 * p.blk_pad;
+            const int cell = phys * p.bs + base;
+            mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * p.blk_pad));
+            tma_block(dk, &p.tmap_k, cell, &full[slot], pol);
+            tma_block(dk + p.blk_pad, &p.tmap_v, cell, &full[slot], pol);
           } else if (flags & F_DATA) {
             // rows [ra, rb): the valid rows widened to whole 4-row groups, so
             // both addresses and the size stay multiples of 16 bytes
@@ -504,20 +547,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const Params 
         }
       }
       okv = __shfl_sync(kFull, okv, 0);
-      if (okv && (flags & F_DATA) && p.row_copies) {
-        // one bulk copy per row into rows of `pitch` bytes: the 16-byte pad
-        // shifts consecutive rows across banks for ldmatrix; lanes share them
-        const int n = r1 - r0;
-        const int slot2 = (int)(it % (uint32_t)S);
-        uint8_t *dk = ring + (size_t)slot2 * 2 * p.blk_pad;
-        for (int i = lane; i < 2 * n; i += 32) {
-          const int r = r0 + (i < n ? i : i - n);
-          const size_t src = ((size_t)phys * p.bs + r) * (size_t)p.row_bytes;
-          uint8_t *dst = dk + (i < n ? 0 : p.blk_pad) + (size_t)(r - base) * p.pitch;
-          bulk_g2s(dst, (i < n ? p.k_pool : p.v_pool) + src, (uint32_t)p.row_bytes, &full[slot2],
-                   pol);
-        }
-      }
       if (okv) ++it;
       return okv != 0;
     };
@@ -961,7 +990,7 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(const Params p) {
 struct Plan {
   int D, GP, wph, n_cw, stages, n_ctas, blk_pad, rows, smem;
   bool mma;
-  int pitch, n_sub;
+  int pitch, n_sub, ncb;
   size_t ws_status, ws_seq, ws_ml, ws_o, ws_total;
 };
 
@@ -996,7 +1025,8 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
     return fail(MT_ERR_UNSUPPORTED, "paged decode: max_blocks * block_size overflows int32");
   pl->D = a->head_dim;
   pl->GP = GP;
-  const int fixed = kHdrBytes + ((kMaxConsumerWarps * (32 * GP + GP) * 4 + 127) & ~127) + 16;
+  // header, softmax scratch, 1024 bytes to align the ring, 16 bytes of tail
+  const int fixed = kHdrBytes + ((kMaxConsumerWarps * (32 * GP + GP) * 4 + 127) & ~127) + 1024 + 16;
   int n_ctas = a->n_ctas;
   int smem_cap = 232448;
   if (need_device || n_ctas == 0) {
@@ -1023,11 +1053,13 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
   // f16 pools use the tensor-core consumers when a warp per KV head (two for
   // head_dim 256) fits in the 8 consumer warps and 16-row stages fit.
   const int mma_wph = a->head_dim == 256 ? 2 : 1;
-  pl->mma = a->fmt == MT_KV_F16 && a->n_kv_heads * mma_wph <= kMaxConsumerWarps &&
-            fit((int)rb + 16, 16, rows, pad, stages);
+  const int nc = (int)(rb / 128);
+  pl->ncb = nc | 1;  // odd number of 128-byte lines per staged row
+  pl->mma = a->fmt == MT_KV_F16 && rb % 128 == 0 && pl->ncb <= 255 &&
+            a->n_kv_heads * mma_wph <= kMaxConsumerWarps && fit(128 * pl->ncb, 16, rows, pad, stages);
   if (pl->mma) {
     wph = mma_wph;
-    pl->pitch = (int)rb + 16;
+    pl->pitch = 128 * pl->ncb;
     pl->n_sub = 1;
   } else {
     const int dpl = GP >= 8 ? 8 : 16;
@@ -1103,9 +1135,49 @@ mt_status dispatch_d(const Params &prm, const Plan &pl, cudaStream_t s) {
   }
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once.
+mt_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000 *out) {
+  static std::mutex mu;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!fn) {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    mt_status st = cuda_check(
+        cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q),
+        "cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)");
+    if (st != MT_OK) return st;
+    if (q != cudaDriverEntryPointSuccess || !f)
+      return fail(MT_ERR_CUDA, "driver has no cuTensorMapEncodeTiled");
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  *out = fn;
+  return MT_OK;
+}
+
+// 3-D tensor map of a pool for the tensor-core path: [cells][row chunks of
+// 128 bytes][64 f16], box = (64, ncb, rows), 128-byte swizzle, zero fill.
+mt_status encode_pool_map(CUtensorMap *map, const void *pool, long long n_cells, size_t rb,
+                          const Plan &pl) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn;
+  mt_status st = encode_fn(&fn);
+  if (st != MT_OK) return st;
+  const cuuint64_t dims[3] = {64, (cuuint64_t)(rb / 128), (cuuint64_t)n_cells};
+  const cuuint64_t strides[2] = {128, (cuuint64_t)rb};
+  const cuuint32_t box[3] = {64, (cuuint32_t)pl.ncb, (cuuint32_t)pl.rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(pool), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MT_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string((int)r) + ")");
+  return MT_OK;
+}
+
 // Fill the kernel parameters shared by both decode entry points.
-void fill_params(Params &prm, const mt_paged_attn_args *a, const Plan &pl, uint8_t *ws,
-                 uint32_t *status) {
+mt_status fill_params(Params &prm, const mt_paged_attn_args *a, const Plan &pl, uint8_t *ws,
+                      uint32_t *status) {
   prm.q = a->q;
   prm.k_pool = static_cast<const uint8_t *>(a->k_pool);
   prm.v_pool = static_cast<const uint8_t *>(a->v_pool);
@@ -1129,7 +1201,8 @@ void fill_params(Params &prm, const mt_paged_attn_args *a, const Plan &pl, uint8
   prm.blk_pad = pl.blk_pad;
   prm.rows = pl.rows;
   prm.pitch = pl.pitch;
-  prm.row_copies = pl.mma ? 1 : 0;
+  prm.use_tmap = pl.mma ? 1 : 0;
+  prm.ncb = pl.ncb;
   prm.n_sub = pl.n_sub;
   prm.stages = pl.stages;
   prm.wph = pl.wph;
@@ -1137,6 +1210,15 @@ void fill_params(Params &prm, const mt_paged_attn_args *a, const Plan &pl, uint8
   prm.n_ctas = pl.n_ctas;
   prm.qscale = a->scale * 1.4426950408889634f;
   prm.wait_ns = kWaitLimitNs;
+  if (pl.mma) {
+    const long long n_cells = (long long)a->n_phys_blocks * a->block_size;
+    const size_t rb = (size_t)prm.row_bytes;
+    mt_status st = encode_pool_map(&prm.tmap_k, a->k_pool, n_cells, rb, pl);
+    if (st != MT_OK) return st;
+    st = encode_pool_map(&prm.tmap_v, a->v_pool, n_cells, rb, pl);
+    if (st != MT_OK) return st;
+  }
+  return MT_OK;
 }
 
 mt_status dispatch(const Params &prm, const Plan &pl, mt_kv_format fmt, cudaStream_t s) {
@@ -1176,7 +1258,8 @@ extern "C" mt_status mt_paged_attn_decode(const mt_paged_attn_args *a, void *wor
     return fail(MT_ERR_INVALID_ARG, "paged decode: q, pools, out and workspace must be 16-byte aligned");
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   Params prm;
-  fill_params(prm, a, pl, ws, reinterpret_cast<uint32_t *>(ws + pl.ws_status));
+  st = fill_params(prm, a, pl, ws, reinterpret_cast<uint32_t *>(ws + pl.ws_status));
+  if (st != MT_OK) return st;
   st = dispatch(prm, pl, a->fmt, reinterpret_cast<cudaStream_t>(stream));
   return st == MT_OK ? ok() : st;
 }
@@ -1261,7 +1344,8 @@ extern "C" mt_status mt_paged_attn_decode_static(const mt_paged_attn_args *a, ui
   st = static_scratch(&ws);
   if (st != MT_OK) return st;
   Params prm;
-  fill_params(prm, a, pl, ws, status);
+  st = fill_params(prm, a, pl, ws, status);
+  if (st != MT_OK) return st;
   st = dispatch(prm, pl, a->fmt, reinterpret_cast<cudaStream_t>(stream));
   return st == MT_OK ? ok() : st;
 }
