@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/mtkv.h"
 
 namespace mtkv {
@@ -106,6 +108,35 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 // Prefetch a contiguous global range into L2 (bytes a multiple of 16).
 __device__ __forceinline__ void bulk_prefetch_l2(const void *g, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(g), "r"(bytes) : "memory");
+}
+
+// ------------------------------------------- programmatic dependent launch --
+//
+// The decode-step kernels are launched with programmatic stream serialisation:
+// a kernel may be scheduled while its predecessor in the stream is still
+// running, so its launch latency overlaps that kernel's tail. Each such
+// kernel first waits until the predecessor has completed and its writes are
+// visible (griddepcontrol.wait; a no-op when launched normally), then lets its
+// own successor start launching.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // ------------------------------------------------------------ numerics --

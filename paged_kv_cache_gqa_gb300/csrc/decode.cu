@@ -480,6 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = p.stages;
+  pdl_enter();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -934,53 +935,75 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
 }
 
 // Merge every partial of (sequence, query head) by log-sum-exp and
-// normalise. One warp per (s, h); lane owns D/32 dims.
+// normalise. One warp per (s, h); lane owns D/32 output dims. The (m, l)
+// pairs of up to 32 partials arrive in one round (a lane each); the output
+// partials then stream in with several loads in flight; longer lists are
+// taken 32 at a time with an online rescale.
 template <int D>
 __global__ void __launch_bounds__(256) splitk_combine_kernel(const Params p) {
   constexpr int DV = D / 32;
+  pdl_enter();
   const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (w >= p.B * p.Hq) return;
   const int s = w / p.Hq, h = w % p.Hq;
   const int T = p.seq_start[p.B];
-  const int per = T > 0 ? (T + p.n_ctas - 1) / p.n_ctas : 1;
   const int beg = p.seq_start[s], end = p.seq_start[s + 1];
+  const int per = T > 0 ? (T + p.n_ctas - 1) / p.n_ctas : 1;
   float acc[DV];
 #pragma unroll
   for (int e = 0; e < DV; ++e) acc[e] = 0.f;
   float M = -INFINITY, L = 0.f;
   if (end > beg) {
-    const int c0 = beg / per, c1 = (end - 1) / per;
-    for (int c = c0; c <= c1; ++c)
-      for (int u = 0; u < p.n_sub; ++u) {
-        const size_t P = ((size_t)c + s) * p.n_sub + u;
-        M = fmaxf(M, p.part_ml[(P * p.Hq + h) * 2]);
+    const int c0 = beg / per;
+    const int NP = ((end - 1) / per - c0 + 1) * p.n_sub;  // partials, CTA-major
+    for (int base = 0; base < NP; base += 32) {
+      const int cnt = min(32, NP - base);
+      const int i = base + lane;
+      float m = -INFINITY, l = 0.f;
+      if (lane < cnt) {
+        const size_t P = ((size_t)c0 + i / p.n_sub + s) * p.n_sub + i % p.n_sub;
+        const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + (P * p.Hq + h) * 2);
+        m = ml.x;
+        l = ml.y;
       }
-    if (M > -INFINITY) {
-      for (int c = c0; c <= c1; ++c)
-        for (int u = 0; u < p.n_sub; ++u) {
-          const size_t P = ((size_t)c + s) * p.n_sub + u;
-          const float m = p.part_ml[(P * p.Hq + h) * 2];
-          const float l = p.part_ml[(P * p.Hq + h) * 2 + 1];
-          if (!(l > 0.f)) continue;
-          const float f = exp2f(m - M);
-          L += l * f;
-          const float *src = p.part_o + (P * p.Hq + h) * D + lane * DV;
+      if (!(l > 0.f)) m = -INFINITY;
+      float mc = m;
 #pragma unroll
-          for (int e = 0; e < DV; e += 2) {
-            const float2 v = *reinterpret_cast<const float2 *>(src + e);
-            acc[e] = fmaf(f, v.x, acc[e]);
-            acc[e + 1] = fmaf(f, v.y, acc[e + 1]);
-          }
+      for (int o = 16; o; o >>= 1) mc = fmaxf(mc, __shfl_xor_sync(kFull, mc, o));
+      const float m_new = fmaxf(M, mc);
+      if (m_new == -INFINITY) continue;  // nothing valid yet
+      const float f_old = exp2f(M - m_new);
+      const float f = m == -INFINITY ? 0.f : exp2f(m - m_new);
+      float lc = l * f;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) lc += __shfl_xor_sync(kFull, lc, o);
+      L = L * f_old + lc;
+      M = m_new;
+#pragma unroll
+      for (int e = 0; e < DV; ++e) acc[e] *= f_old;
+#pragma unroll 4
+      for (int k = 0; k < cnt; ++k) {
+        const float fk = __shfl_sync(kFull, f, k);
+        if (fk == 0.f) continue;
+        const int ik = base + k;
+        const size_t Pk = ((size_t)c0 + ik / p.n_sub + s) * p.n_sub + ik % p.n_sub;
+        const float *src = p.part_o + (Pk * p.Hq + h) * D + lane * DV;
+#pragma unroll
+        for (int e = 0; e < DV; e += 2) {
+          const float2 v = *reinterpret_cast<const float2 *>(src + e);
+          acc[e] = fmaf(fk, v.x, acc[e]);
+          acc[e + 1] = fmaf(fk, v.y, acc[e + 1]);
         }
+      }
     }
   }
   float *dst = p.out + ((size_t)s * p.Hq + h) * D + lane * DV;
   const bool any = L > 0.f;
+  const float inv = any ? 1.f / L : 0.f;
 #pragma unroll
   for (int e = 0; e < DV; e += 2)
-    *reinterpret_cast<float2 *>(dst + e) =
-        any ? make_float2(acc[e] / L, acc[e + 1] / L) : make_float2(0.f, 0.f);
+    *reinterpret_cast<float2 *>(dst + e) = make_float2(acc[e] * inv, acc[e + 1] * inv);
   if (p.lse && lane == 0)
     p.lse[(size_t)s * p.Hq + h] = any ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
 }
@@ -1105,13 +1128,15 @@ mt_status launch_decode(const Params &prm, const Plan &pl, cudaStream_t s) {
     configured_dev = dev;
     configured_smem = pl.smem;
   }
-  kern<<<pl.n_ctas, 32 * (pl.n_cw + 1), pl.smem, s>>>(prm);
-  mt_status st = cuda_check(cudaGetLastError(), "paged decode launch");
+  mt_status st = cuda_check(
+      launch_pdl(kern, dim3(pl.n_ctas), dim3(32 * (pl.n_cw + 1)), pl.smem, s, prm),
+      "paged decode launch");
   if (st != MT_OK) return st;
   const int warps = prm.B * prm.Hq;
   if (warps > 0) {
-    splitk_combine_kernel<D><<<(warps + 7) / 8, 256, 0, s>>>(prm);
-    st = cuda_check(cudaGetLastError(), "split-K combine launch");
+    st = cuda_check(launch_pdl(splitk_combine_kernel<D>, dim3((warps + 7) / 8), dim3(256), 0, s,
+                               prm),
+                    "split-K combine launch");
   }
   return st;
 }

@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(256) kv_store_kernel(uint8_t *__restrict__ k_p
                                                        const float *__restrict__ v_new,
                                                        const int64_t *__restrict__ cells,
                                                        int n_rows, uint32_t *status) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int groups = row_elems >> 5;
   const long long warp = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -96,20 +97,21 @@ extern "C" mt_status mt_kv_store(mt_kv_format fmt, void *k_pool, void *v_pool, i
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   auto *kp = static_cast<uint8_t *>(k_pool);
   auto *vp = static_cast<uint8_t *>(v_pool);
+  cudaError_t e;
   switch (fmt) {
     case MT_KV_F32:
-      kv_store_kernel<MT_KV_F32><<<grid, 256, 0, s>>>(kp, vp, n_cells, row_elems, (int)rb, k_new,
-                                                      v_new, cells, n_rows, status);
+      e = launch_pdl(kv_store_kernel<MT_KV_F32>, grid, dim3(256), 0, s, kp, vp, n_cells, row_elems,
+                     (int)rb, k_new, v_new, cells, n_rows, status);
       break;
     case MT_KV_F16:
-      kv_store_kernel<MT_KV_F16><<<grid, 256, 0, s>>>(kp, vp, n_cells, row_elems, (int)rb, k_new,
-                                                      v_new, cells, n_rows, status);
+      e = launch_pdl(kv_store_kernel<MT_KV_F16>, grid, dim3(256), 0, s, kp, vp, n_cells, row_elems,
+                     (int)rb, k_new, v_new, cells, n_rows, status);
       break;
     default:
-      kv_store_kernel<MT_KV_Q8_0><<<grid, 256, 0, s>>>(kp, vp, n_cells, row_elems, (int)rb,
-                                                       k_new, v_new, cells, n_rows, status);
+      e = launch_pdl(kv_store_kernel<MT_KV_Q8_0>, grid, dim3(256), 0, s, kp, vp, n_cells, row_elems,
+                     (int)rb, k_new, v_new, cells, n_rows, status);
       break;
   }
-  mt_status st = cuda_check(cudaGetLastError(), "mt_kv_store launch");
+  mt_status st = cuda_check(e, "mt_kv_store launch");
   return st == MT_OK ? ok() : st;
 }
