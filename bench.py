@@ -399,6 +399,221 @@ def run_gpu(args, rank, world, local_rank):
     return line
 
 
+# ----------------------------------------------------------------- other workloads
+#
+# `--workload` selects one of the other synthetic configurations to measure the
+# remaining kernels on GB300; the default line is the Llama-3 f16 step above.
+
+def _gpu_time(fn, steps, warmup, stream):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def _decode_setup(mtkv, w, n_pools, dev, g, table=None):
+    """n_pools K/V pool pairs filled through mt_kv_store from N(0,1) rows."""
+    hkv, d, bs = w.n_kv_heads, w.head_dim, w.block_size
+    rb = mtkv.mt_kv_row_bytes(w.fmt, hkv, d)
+    table = torch.from_numpy(w.block_table if table is None else table).to(dev)
+    ctx = torch.from_numpy(w.context_lens).to(dev)
+    spans = None if w.spans is None else torch.from_numpy(w.spans).to(dev)
+    cells_all = torch.arange(w.n_cells, device=dev, dtype=torch.int64)
+    layers = []
+    for _ in range(n_pools):
+        kp = torch.empty(w.n_cells, rb, dtype=torch.uint8, device=dev)
+        vp = torch.empty_like(kp)
+        for c0 in range(0, w.n_cells, 1 << 16):
+            cells = cells_all[c0:c0 + (1 << 16)]
+            rows = torch.randn(cells.numel(), hkv * d, generator=g, device=dev)
+            mtkv.mt_kv_store(w.fmt, kp, vp, hkv, d, rows, -rows, cells)
+        q = torch.randn(w.n_seqs, w.n_heads, d, generator=g, device=dev)
+        out = torch.empty_like(q)
+        args = mtkv.paged_attn_args(w.fmt, q, kp, vp, table, ctx, out, n_kv_heads=hkv,
+                                    block_size=bs, n_phys_blocks=w.n_phys_blocks, scale=w.scale,
+                                    spans=spans)
+        k_new = torch.randn(w.n_seqs, hkv * d, generator=g, device=dev)
+        layers.append((kp, vp, args, k_new))
+    ws = torch.zeros(mtkv.mt_paged_attn_workspace_bytes(layers[0][2]), dtype=torch.uint8,
+                     device=dev)
+    return layers, ws, rb
+
+
+def _window_bytes(w, rb_seg, table=None):
+    """(unique-cell bytes, per-sequence logical bytes, attended positions) of
+    one decode call: K+V head segments of attended positions (distinct
+    physical cells counted once for the unique figure), table entries, Q, out."""
+    table = w.block_table if table is None else table
+    bs = w.block_size
+    uniq, toks, blocks = set(), 0, 0
+    for s in range(w.n_seqs):
+        lo, hi = 0, int(w.context_lens[s])
+        if w.spans is not None:
+            lo, hi = max(int(w.spans[s, 0]), 0), min(int(w.spans[s, 1]), hi)
+        for lb in range(lo // bs, (hi - 1) // bs + 1 if hi > lo else lo // bs):
+            b = int(table[s, lb])
+            blocks += 1
+            if b < 0:
+                continue
+            a, z = max(lo, lb * bs), min(hi, lb * bs + bs)
+            toks += z - a
+            uniq.update(b * bs + p - lb * bs for p in range(a, z))
+    fixed = blocks * 4 + w.n_seqs * 4 + 2 * w.n_seqs * w.n_heads * w.head_dim * 4
+    per = w.n_kv_heads * rb_seg * 2
+    return len(uniq) * per + fixed, toks * per + fixed, toks
+
+
+def run_extra(args, rank, world, local_rank):
+    from paged_kv_cache_gqa_gb300 import mtkv
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(SEED + 7)
+    peak, peak_kind = _peak()
+    steps, warmup = args.steps, args.warmup
+    clocks = Clocks(local_rank)
+    res = {}
+    if args.workload == "smollm2_f32":
+        w = workloads.smollm2_f32(hist=False)
+        layers, ws, rb = _decode_setup(mtkv, w, w.n_layers, dev, g)
+        cells = torch.from_numpy(w.new_cells).to(dev)
+
+        def step():
+            for kp, vp, a, kn in layers:
+                mtkv.mt_kv_store("f32", kp, vp, w.n_kv_heads, w.head_dim, kn, kn, cells)
+                mtkv.mt_paged_attn_decode(a, ws)
+
+        clocks.start()
+        ms = _gpu_time(step, steps, warmup, stream)
+        ub, lb_, toks = _window_bytes(w, w.head_dim * 4)
+        step_bytes = w.n_layers * (ub + store_bytes(w))
+        value = step_bytes / (ms * 1e-3) / 1e9
+        # grow-on-demand re-layout: 30 layers x kv_dim 192 f32, K and V, 64 -> 8192
+        row = 192 * 4
+        caps = [64]
+        while caps[-1] < 8192:
+            caps.append(mtkv.mt_kv_grow_capacity(caps[-1], caps[-1] + 1, 8192))
+        bufs = [(torch.empty(30 * c * row, dtype=torch.uint8, device=dev),
+                 torch.empty(30 * c * row, dtype=torch.uint8, device=dev)) for c in caps]
+
+        def grow():
+            for i in range(len(caps) - 1):
+                for kv in range(2):
+                    mtkv.mt_kv_relayout(bufs[i][kv], bufs[i + 1][kv], 30, caps[i], caps[i + 1], row)
+
+        g_ms = _gpu_time(grow, steps, warmup, stream)
+        g_bytes = sum(2 * 2 * 30 * c * row for c in caps[:-1])
+        # copy_cells: 1000 overlapping run moves on the 60 pools (30 layers x K, V)
+        moves, n_cells = workloads.compaction_moves(seed=SEED)
+        ordered = mtkv.mt_order_moves(moves)
+        pools = [torch.empty(n_cells, row, dtype=torch.uint8, device=dev) for _ in range(60)]
+        c_ms = _gpu_time(lambda: mtkv.mt_copy_cells(pools, row, n_cells, ordered), steps, warmup,
+                         stream)
+        c_bytes = sum(m[2] for m in ordered) * row * 60 * 2
+        clk = clocks.stop()
+        res = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s",
+               "ms_per_step": round(ms, 4), "frac_of_peak": round(value / peak, 4),
+               "attended_tokens_per_s": round(w.n_layers * toks / (ms * 1e-3), 1),
+               "config": {"workload": "smollm2-135m-shaped f32 paged decode: 30 layers, 8 seqs, "
+                                      "ctx U[2048,8192], 9/3 heads, head_dim 64, bs 16"},
+               "relayout": {"what": "grow 64->8192, 30 layers x kv_dim 192 f32, K and V",
+                            "ms": round(g_ms, 4), "bytes": g_bytes,
+                            "GB/s": round(g_bytes / (g_ms * 1e-3) / 1e9, 1),
+                            "frac": round(g_bytes / (g_ms * 1e-3) / 1e9 / peak, 4)},
+               "copy_cells": {"what": "1000 ordered overlapping run moves x 60 pools, 768 B rows",
+                              "ms": round(c_ms, 4), "bytes": c_bytes,
+                              "GB/s": round(c_bytes / (c_ms * 1e-3) / 1e9, 1),
+                              "frac": round(c_bytes / (c_ms * 1e-3) / 1e9 / peak, 4)},
+               "clocks": clk}
+    elif args.workload == "q8_prefix":
+        w = workloads.llama3_q8_prefix(hist=False)
+        layers, ws, rb = _decode_setup(mtkv, w, 32, dev, g)
+        cells = torch.from_numpy(w.new_cells).to(dev)
+
+        def step():
+            for kp, vp, a, kn in layers:
+                mtkv.mt_kv_store("q8_0", kp, vp, w.n_kv_heads, w.head_dim, kn, kn, cells)
+                mtkv.mt_paged_attn_decode(a, ws)
+
+        clocks.start()
+        ms = _gpu_time(step, steps, warmup, stream)
+        clk = clocks.stop()
+        ub, lb_, toks = _window_bytes(w, (w.head_dim // 32) * 34)
+        value = 32 * (ub + store_bytes(w)) / (ms * 1e-3) / 1e9
+        res = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s",
+               "value_kind": "unique physical cells (shared prefix counted once)",
+               "logical_GB/s": round(32 * lb_ / (ms * 1e-3) / 1e9, 1),
+               "ms_per_step": round(ms, 4), "frac_of_peak": round(value / peak, 4),
+               "attended_tokens_per_s": round(32 * toks / (ms * 1e-3), 1),
+               "config": {"workload": "llama3-8b-shaped q8_0 paged decode: 32 layers, 32 seqs "
+                                      "sharing a 4096-token prefix + U[64,1024] suffix, random "
+                                      "windows, 32/8 heads, head_dim 128, bs 32"},
+               "clocks": clk}
+    elif args.workload == "longctx_int4":
+        w = workloads.longctx_f16_int4(hist=False)
+        table = workloads.retarget_cold(w)
+        layers, ws, rb = _decode_setup(mtkv, w, 4, dev, g, table=table)
+        src = torch.from_numpy(w.extra["cold_src"]).to(dev)
+        dst = torch.from_numpy(w.extra["cold_dst"]).to(dev)
+        n_el = w.block_size * w.n_kv_heads * w.head_dim
+        scales = torch.empty(len(src), dtype=torch.float32, device=dev)
+        nib = torch.empty(len(src), n_el // 2, dtype=torch.uint8, device=dev)
+
+        def quant():
+            for kp, vp, a, kn in layers:
+                for pool in (kp, vp):
+                    mtkv.mt_kv_quant_int4("f16", pool, w.block_size, w.n_kv_heads, w.head_dim,
+                                          w.n_phys_blocks, src, scales, nib)
+
+        def dequant():
+            for kp, vp, a, kn in layers:
+                for pool in (kp, vp):
+                    mtkv.mt_kv_dequant_int4("f16", pool, w.block_size, w.n_kv_heads, w.head_dim,
+                                            w.n_phys_blocks, dst, scales, nib)
+
+        def decode():
+            for kp, vp, a, kn in layers:
+                mtkv.mt_paged_attn_decode(a, ws)
+
+        clocks.start()
+        d_ms = _gpu_time(decode, steps, warmup, stream) / len(layers)
+        q_ms = _gpu_time(quant, steps, warmup, stream) / (2 * len(layers))
+        dq_ms = _gpu_time(dequant, steps, warmup, stream) / (2 * len(layers))
+        clk = clocks.stop()
+        ub, lb_, toks = _window_bytes(w, w.head_dim * 2, table=table)
+        value = ub / (d_ms * 1e-3) / 1e9
+        q_bytes = len(src) * (n_el * 2 + n_el // 2 + 4)
+        res = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s",
+               "ms_per_decode": round(d_ms, 4), "frac_of_peak": round(value / peak, 4),
+               "attended_tokens_per_s": round(toks / (d_ms * 1e-3), 1),
+               "int4_quant": {"blocks": len(src), "ms": round(q_ms, 4),
+                              "GB/s": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
+                              "frac": round(q_bytes / (q_ms * 1e-3) / 1e9 / peak, 4)},
+               "int4_dequant": {"blocks": len(dst), "ms": round(dq_ms, 4),
+                                "GB/s": round(q_bytes / (dq_ms * 1e-3) / 1e9, 1),
+                                "frac": round(q_bytes / (dq_ms * 1e-3) / 1e9 / peak, 4)},
+               "config": {"workload": "long-context f16 paged decode: 16 seqs x 32768, 16/4 heads, "
+                                      "head_dim 256, bs 16, 5% holes, 25% of blocks through int4 "
+                                      "into fresh ids; 4 rotated pool pairs"},
+               "clocks": clk}
+    else:
+        raise SystemExit(f"unknown workload {args.workload}")
+    res.update({"n_gpus": 1, "steps": steps, "warmup": warmup, "higher_is_better": True,
+                "peak": peak, "peak_kind": peak_kind, "data": "synthetic",
+                "workload_name": args.workload})
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -407,6 +622,9 @@ def main():
     ap.add_argument("--impl", default="mtkv", choices=["mtkv", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="oracle baseline budget; 0 skips it (profiling runs)")
+    ap.add_argument("--workload", default="llama3_f16",
+                    choices=["llama3_f16", "smollm2_f32", "q8_prefix", "longctx_int4"],
+                    help="llama3_f16 is the benchmark line; the others measure the other kernels")
     ap.add_argument("--layers", type=int, default=N_LAYERS,
                     help="layers per step; fewer than 32 only for profiling captures")
     args = ap.parse_args()
@@ -422,6 +640,8 @@ def main():
         torch.distributed.init_process_group(backend)
     if args.impl == "reference":
         line = run_reference(args, rank)
+    elif args.workload != "llama3_f16":
+        line = run_extra(args, rank, world, local_rank)
     else:
         line = run_gpu(args, rank, world, local_rank)
     if line is not None:
