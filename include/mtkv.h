@@ -234,6 +234,14 @@ mt_status mt_kv_relayout(const void *src, void *dst, int n_layers, int64_t old_c
  * positions, then cap at max_ctx. Returns -1 on invalid input. Host. */
 int64_t mt_kv_grow_capacity(int64_t cap, int64_t need, int64_t max_ctx);
 
+/* Diagnostic, no counterpart in the pages: launch one CTA that waits, with the
+ * bounded wait every pipeline wait in this library uses, on a barrier nothing
+ * will ever complete. After limit_ns (0 < limit_ns <= 2 s) the wait gives up
+ * and sets MT_STATUS_BIT_TIMEOUT in *status (device word); the kernel returns
+ * and the context stays usable. Used to test failure detection without
+ * faulting or hanging the GPU. */
+mt_status mt_selftest_bounded_wait(uint64_t limit_ns, uint32_t *status, mt_stream stream);
+
 /* Synchronise `stream`, read the device status word, clear it, and map it
  * to MT_OK, MT_ERR_TIMEOUT or MT_ERR_DEVICE_CHECK. */
 mt_status mt_check_device_status(uint32_t *status_word, mt_stream stream);

@@ -27,7 +27,7 @@ MT_ERR_TIMEOUT, MT_ERR_DEVICE_CHECK, MT_ERR_CUDA = 4, 5, 6
 EXPORTED = ("mt_kv_row_bytes", "mt_kv_store", "mt_paged_attn_workspace_bytes",
             "mt_paged_attn_decode", "mt_order_moves", "mt_check_moves", "mt_copy_cells",
             "mt_kv_quant_int4", "mt_kv_dequant_int4", "mt_kv_relayout", "mt_kv_grow_capacity",
-            "mt_check_device_status", "mt_last_error", "mt_version")
+            "mt_check_device_status", "mt_selftest_bounded_wait", "mt_last_error", "mt_version")
 
 
 class MtError(RuntimeError):
@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
         "mt_kv_relayout": (I, [P, P, I, I64, I64, SZ, P]),
         "mt_kv_grow_capacity": (I64, [I64, I64, I64]),
         "mt_check_device_status": (I, [U32P, P]),
+        "mt_selftest_bounded_wait": (I, [ctypes.c_uint64, U32P, P]),
         "mt_last_error": (ctypes.c_char_p, []),
         "mt_version": (ctypes.c_char_p, []),
     }
@@ -238,6 +239,12 @@ def mt_kv_relayout(src, dst, n_layers: int, old_cap: int, new_cap: int, row_byte
 
 def mt_kv_grow_capacity(cap: int, need: int, max_ctx: int) -> int:
     return int(lib().mt_kv_grow_capacity(cap, need, max_ctx))
+
+
+def mt_selftest_bounded_wait(limit_ns: int, status, stream=None) -> None:
+    """Run the bounded-wait self-test kernel (sets the timeout bit in `status`)."""
+    _check(lib().mt_selftest_bounded_wait(int(limit_ns), _ptr(status), _stream(stream)),
+           "mt_selftest_bounded_wait")
 
 
 def mt_check_device_status(status_word, stream=None) -> int:
