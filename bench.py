@@ -515,11 +515,11 @@ def run_extra(args, rank, world, local_rank):
         g_bytes = sum(2 * 2 * 30 * c * row for c in caps[:-1])
         # copy_cells: 1000 overlapping run moves on the 60 pools (30 layers x K, V)
         moves, n_cells = workloads.compaction_moves(seed=SEED)
-        ordered = mtkv.mt_order_moves(moves)
+        ordered = np.asarray(mtkv.mt_order_moves(moves), dtype=np.int64)
         pools = [torch.empty(n_cells, row, dtype=torch.uint8, device=dev) for _ in range(60)]
         c_ms = _gpu_time(lambda: mtkv.mt_copy_cells(pools, row, n_cells, ordered), steps, warmup,
                          stream)
-        c_bytes = sum(m[2] for m in ordered) * row * 60 * 2
+        c_bytes = int(ordered[:, 2].sum()) * row * 60 * 2
         clk = clocks.stop()
         res = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s",
                "ms_per_step": round(ms, 4), "frac_of_peak": round(value / peak, 4),
@@ -562,7 +562,7 @@ def run_extra(args, rank, world, local_rank):
     elif args.workload == "longctx_int4":
         w = workloads.longctx_f16_int4(hist=False)
         table = workloads.retarget_cold(w)
-        layers, ws, rb = _decode_setup(mtkv, w, 4, dev, g, table=table)
+        layers, ws, rb = _decode_setup(mtkv, w, min(4, args.layers), dev, g, table=table)
         src = torch.from_numpy(w.extra["cold_src"]).to(dev)
         dst = torch.from_numpy(w.extra["cold_dst"]).to(dev)
         n_el = w.block_size * w.n_kv_heads * w.head_dim

@@ -5,8 +5,10 @@
 // ascending when it slides down and descending when it slides up, with no
 // staging buffer; the moves come in order_moves order.
 //
-// GB300 design: instead of one row at a time with a barrier after each, a
-// move is cut into chunks of min(|dst - src|, len) rows. A chunk's sources and
+// GB300 design: a run that fits in shared memory (up to 48 KB per pool) moves
+// in one round through shared memory with two bulk (TMA) copies, one CTA per
+// (move, pool). Longer runs, instead of one row at a time with a barrier after
+// each, are cut into chunks of min(|dst - src|, len) rows. A chunk's sources and
 // destinations never overlap, so all of a chunk's rows, in every pool (all
 // layers, K and V), are copied in parallel with 16-byte accesses; a CTA
 // barrier separates consecutive chunks, taken in slide order. Consecutive
@@ -15,6 +17,7 @@
 // schedule travels in the kernel's parameters (up to 1024 moves per launch),
 // so nothing is allocated or copied from the host.
 #include <algorithm>
+#include <map>
 #include <vector>
 
 #include "common.cuh"
@@ -36,12 +39,16 @@ struct MoveBatch {
 
 template <typename V>
 __global__ void __launch_bounds__(256) copy_cells_kernel(const __grid_constant__ MoveBatch b) {
+  constexpr int U = 4;  // vectors each thread has in flight per round
   const mt_move mv = b.moves[blockIdx.x];
   const long long src = mv.src, dst = mv.dst, len = mv.len;
   const long long delta = dst - src;
   const long long chunk = min(delta < 0 ? -delta : delta, len);
   const long long n_chunks = (len + chunk - 1) / chunk;
   const long long vec_per_row = b.row_bytes / (long long)sizeof(V);
+  // this CTA's share of the pools (blockIdx.y of gridDim.y groups)
+  const int p0 = (int)((long long)b.n_pools * blockIdx.y / gridDim.y);
+  const int p1 = (int)((long long)b.n_pools * (blockIdx.y + 1) / gridDim.y);
   for (long long c = 0; c < n_chunks; ++c) {
     // slide order: descending chunks when moving up, ascending when down
     long long r_lo, r_hi;
@@ -52,19 +59,65 @@ __global__ void __launch_bounds__(256) copy_cells_kernel(const __grid_constant__
       r_lo = c * chunk;
       r_hi = min(r_lo + chunk, len);
     }
+    // a chunk's sources and destinations are disjoint: read U vectors, then
+    // write them, with no barrier inside the chunk
     const long long per_pool = (r_hi - r_lo) * vec_per_row;
-    const long long total = per_pool * b.n_pools;
-    for (long long i = threadIdx.x; i < total; i += blockDim.x) {
-      const int pool = (int)(i / per_pool);
-      const long long k = i % per_pool;
-      const long long row = r_lo + k / vec_per_row;
-      const long long v = k % vec_per_row;
-      V *base = reinterpret_cast<V *>(b.pools[pool]);
-      const V x = base[(src + row) * vec_per_row + v];
-      base[(dst + row) * vec_per_row + v] = x;
+    const long long total = per_pool * (p1 - p0);
+    for (long long i0 = threadIdx.x; i0 < total; i0 += (long long)blockDim.x * U) {
+      V x[U];
+      V *at[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const long long i = i0 + (long long)u * blockDim.x;
+        at[u] = nullptr;
+        if (i < total) {
+          const int pool = p0 + (int)(i / per_pool);
+          const long long k = i % per_pool;
+          V *base = reinterpret_cast<V *>(b.pools[pool]);
+          const long long off = (r_lo + k / vec_per_row) * vec_per_row + k % vec_per_row;
+          x[u] = base[src * vec_per_row + off];
+          at[u] = base + dst * vec_per_row + off;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (at[u]) *at[u] = x[u];
     }
     __syncthreads();
   }
+}
+
+// A run that fits in shared memory moves in one round: one bulk (TMA) copy
+// brings the whole source run of one pool in, and, once it has landed, one
+// bulk copy writes it to the destination. Reading everything before writing
+// anything gives memmove semantics for any overlap. One CTA per (move, pool).
+constexpr int kStagedMax = 48 * 1024;
+
+__global__ void __launch_bounds__(32) copy_cells_staged_kernel(const __grid_constant__ MoveBatch b,
+                                                               uint32_t *status) {
+  extern __shared__ __align__(128) uint8_t buf[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  const mt_move mv = b.moves[blockIdx.x];
+  uint8_t *base = b.pools[blockIdx.y];
+  const uint32_t bytes = (uint32_t)(mv.len * b.row_bytes);
+  mbar_init(&bar, 1);
+  abort_flag = 0;
+  fence_mbar_init();
+  mbar_arrive_expect_tx(&bar, bytes);
+  bulk_g2s(buf, base + mv.src * b.row_bytes, bytes, &bar, policy_evict_first());
+  if (!mbar_wait_bounded(&bar, 0, &abort_flag, 2000000000ull)) {
+    report(status, MT_STATUS_BIT_TIMEOUT);
+    return;
+  }
+  asm volatile(
+      "cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(base + mv.dst * b.row_bytes),
+      "r"(smem_u32(buf)), "r"(bytes)
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  // the shared-memory source must stay valid until the bulk store has read it
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 }  // namespace
@@ -102,28 +155,75 @@ extern "C" mt_status mt_copy_cells(void *const *pools, int n_pools, size_t row_b
   for (int i = 0; i < n_pools; ++i) batch.pools[i] = static_cast<uint8_t *>(pools[i]);
   const bool v16 = row_bytes % 16 == 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // runs that fit in shared memory (all of them, 16-byte rows) move staged
+  bool staged = v16;
+  for (const mt_move &m : live)
+    if ((long long)m.len * (long long)row_bytes > kStagedMax) staged = false;
+  long long batch_max_bytes = 0;
+  if (staged) {
+    static bool attr_set = false;
+    if (!attr_set) {
+      cudaFuncSetAttribute(copy_cells_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kStagedMax);
+      attr_set = true;
+    }
+  }
 
   // Moves in one launch run concurrently, so none may write rows another one
-  // reads or writes (reading the same source rows is fine).
+  // reads or writes (reading the same source rows is fine). The launch keeps
+  // the union of its read ranges and of its write ranges as sorted disjoint
+  // intervals, so each check and insertion is logarithmic.
+  struct Union {
+    std::map<int64_t, int64_t> iv;  // start -> end, disjoint
+    bool hits(int64_t lo, int64_t hi) const {
+      auto it = iv.upper_bound(lo);
+      if (it != iv.begin() && std::prev(it)->second > lo) return true;
+      return it != iv.end() && it->first < hi;
+    }
+    void add(int64_t lo, int64_t hi) {
+      auto it = iv.upper_bound(lo);
+      if (it != iv.begin() && std::prev(it)->second >= lo) {
+        --it;
+        lo = it->first;
+        hi = std::max(hi, it->second);
+        it = iv.erase(it);
+      }
+      while (it != iv.end() && it->first <= hi) {
+        hi = std::max(hi, it->second);
+        it = iv.erase(it);
+      }
+      iv.emplace(lo, hi);
+    }
+    void clear() { iv.clear(); }
+  };
+  Union reads, writes;
   struct Run {
     int64_t r0, r1, w0, w1;
   };
-  std::vector<Run> runs;
-  auto conflicts = [&](const Run &b) {
-    for (const Run &a : runs)
-      if ((b.w0 < a.r1 && a.r0 < b.w1) || (b.w0 < a.w1 && a.w0 < b.w1) ||
-          (a.w0 < b.r1 && b.r0 < a.w1))
-        return true;
-    return false;
+  auto conflicts = [&](const Run &r) {
+    return writes.hits(r.w0, r.w1) || reads.hits(r.w0, r.w1) || writes.hits(r.r0, r.r1);
   };
   auto flush = [&]() -> mt_status {
     if (batch.n_moves == 0) return MT_OK;
+    if (staged) {
+      const dim3 grid((unsigned)batch.n_moves, (unsigned)batch.n_pools);
+      copy_cells_staged_kernel<<<grid, 32, (size_t)batch_max_bytes, s>>>(batch, nullptr);
+      batch.n_moves = 0;
+      reads.clear();
+      writes.clear();
+      batch_max_bytes = 0;
+      return cuda_check(cudaGetLastError(), "mt_copy_cells launch");
+    }
+    // spread each move's pools over a few CTAs for more parallelism
+    const int groups = std::max(1, std::min(batch.n_pools, 2048 / std::max(1, batch.n_moves)));
+    const dim3 grid((unsigned)batch.n_moves, (unsigned)std::min(groups, 8));
     if (v16)
-      copy_cells_kernel<uint4><<<batch.n_moves, 256, 0, s>>>(batch);
+      copy_cells_kernel<uint4><<<grid, 256, 0, s>>>(batch);
     else
-      copy_cells_kernel<uint32_t><<<batch.n_moves, 256, 0, s>>>(batch);
+      copy_cells_kernel<uint32_t><<<grid, 256, 0, s>>>(batch);
     batch.n_moves = 0;
-    runs.clear();
+    reads.clear();
+    writes.clear();
     return cuda_check(cudaGetLastError(), "mt_copy_cells launch");
   };
   batch.n_moves = 0;
@@ -134,7 +234,9 @@ extern "C" mt_status mt_copy_cells(void *const *pools, int n_pools, size_t row_b
       if (st != MT_OK) return st;
     }
     batch.moves[batch.n_moves++] = m;
-    runs.push_back(r);
+    batch_max_bytes = std::max(batch_max_bytes, (long long)m.len * (long long)row_bytes);
+    reads.add(r.r0, r.r1);
+    writes.add(r.w0, r.w1);
   }
   st = flush();
   return st == MT_OK ? ok() : st;

@@ -9,14 +9,31 @@
 // then to the pool's type, into the block the caller assigned (a fresh hot
 // id). A block's elements are its cells in pool order [slot][head][dim].
 //
-// One CTA per listed block: pass 1 reduces amax over the block with 16-byte
-// loads; pass 2 re-reads the block (now in L2) and writes 8 nibbles (one
-// 32-bit word) per thread and step, so every global access is coalesced.
+// One CTA per listed block: the block (up to 48 KB) arrives in shared memory
+// by one bulk (TMA) copy, a block-wide amax reduction follows, then each thread
+// packs 8 nibbles (one 32-bit word) per step, so every global access is a bulk
+// copy or coalesced; larger blocks take two coalesced passes instead.
 #include "common.cuh"
 #include "internal.h"
 
 namespace mtkv {
 namespace {
+
+// q = clamp(rint(x / scale), -8, 7) with x / scale the IEEE quotient, given
+// inv = RN(1 / scale). |x / scale| <= 7, and x * inv is within a few ulp
+// (< 2^-19) of the quotient, so rint(x * inv) is the same integer unless the
+// product sits within 2^-16 of a half-integer; those rare values take the
+// exact division. Bit-identical to dividing every value, at one multiply.
+__device__ __forceinline__ int int4_code(float x, float scale, float inv) {
+  if (scale == 0.f) return 0;
+  const float y = x * inv;
+  const float r = rintf(y);
+  float q = r;
+  // near a half-integer, or no usable reciprocal (a subnormal scale): divide
+  if (!(fabsf(y) <= 8.f) || fabsf(fabsf(y - r) - 0.5f) < 1.52587890625e-05f)
+    q = rintf(__fdiv_rn(x, scale));
+  return max(-8, min(7, (int)q));
+}
 
 template <int FMT>
 __device__ __forceinline__ void load8(const uint8_t *p, float (&x)[8]) {
@@ -38,6 +55,109 @@ __device__ __forceinline__ void load8(const uint8_t *p, float (&x)[8]) {
   }
 }
 
+// Eight codes packed into one word of nibbles (element e in bits 4e..4e+3):
+// rint by adding 1.5 * 2^23 (the add itself rounds to nearest even), the
+// code taken from the low mantissa bits; any value within 2^-16 of a
+// half-integer (or without a usable reciprocal) is redone with the exact
+// IEEE division, so the result equals clamp(rint(x / scale), -8, 7) + 8.
+__device__ __forceinline__ uint32_t int4_pack8(const float (&x)[8], float scale, float inv) {
+  if (scale == 0.f) return 0x88888888u;
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  uint32_t word = 0;
+  bool fix = false;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float y = x[e] * inv;
+    const float t = y + kMagic;
+    const float r = t - kMagic;
+    fix |= !(fabsf(y) <= 8.f) || (0.5f - fabsf(y - r)) < 1.52587890625e-05f;
+    word |= ((__float_as_uint(t) + 8u) & 15u) << (4 * e);
+  }
+  if (fix) {
+    word = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) word |= (uint32_t)(int4_code(x[e], scale, inv) + 8) << (4 * e);
+  }
+  return word;
+}
+
+// Single read: the block arrives in shared memory by one bulk (TMA) copy,
+// then 256 threads reduce amax and pack from there. Each CTA holds one block
+// (up to 48 KB), so several blocks per SM are in flight at once.
+constexpr int kQuantSmemMax = 48 * 1024;
+
+template <int FMT>
+__global__ void __launch_bounds__(256) int4_quant_smem_kernel(
+    const uint8_t *__restrict__ pool, long long blk_bytes, long long n_elts, long long n_phys,
+    const int32_t *__restrict__ blocks, float *__restrict__ scales, uint8_t *__restrict__ nibbles,
+    uint32_t *status) {
+  constexpr int ES = FMT == MT_KV_F16 ? 2 : 4;
+  extern __shared__ __align__(128) uint8_t buf[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ float red[8];
+  __shared__ int abort_flag;
+  const int id = blocks[blockIdx.x];
+  if (id < 0 || id >= n_phys) {
+    if (threadIdx.x == 0) report(status, MT_STATUS_BIT_DEVICE_CHECK);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bar, (uint32_t)blk_bytes);
+    bulk_g2s(buf, pool + (size_t)id * blk_bytes, (uint32_t)blk_bytes, &bar, policy_evict_first());
+  }
+  // every thread waits (bounded) for the copy to land
+  if (!mbar_wait_bounded(&bar, 0, &abort_flag, 2000000000ull)) {
+    if (threadIdx.x == 0) report(status, MT_STATUS_BIT_TIMEOUT);
+    return;
+  }
+  const int n8 = (int)(n_elts / 8);
+  float amax = 0.f;
+  if constexpr (FMT == MT_KV_F16) {
+    // |x| maximum on packed pairs, converted once
+    __half2 m2 = __float2half2_rn(0.f);
+    for (int i = threadIdx.x; i < n8; i += 256) {
+      const uint4 r = *reinterpret_cast<const uint4 *>(buf + (size_t)i * 16);
+      m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __half2 *>(&r.x)));
+      m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __half2 *>(&r.y)));
+      m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __half2 *>(&r.z)));
+      m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __half2 *>(&r.w)));
+    }
+    const float2 mf = __half22float2(m2);
+    amax = fmaxf(mf.x, mf.y);
+  } else {
+    for (int i = threadIdx.x; i < n8; i += 256) {
+      float x[8];
+      load8<FMT>(buf + (size_t)i * 8 * ES, x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
+  const float scale = amax / 7.0f;
+  const float inv = scale != 0.f ? 1.0f / scale : 0.f;
+  if (threadIdx.x == 0) scales[blockIdx.x] = scale;
+  uint32_t *dst = reinterpret_cast<uint32_t *>(nibbles + (size_t)blockIdx.x * (n_elts / 2));
+  for (int i = threadIdx.x; i < n8; i += 256) {
+    float x[8];
+    load8<FMT>(buf + (size_t)i * 8 * ES, x);
+    dst[i] = int4_pack8(x, scale, inv);
+  }
+}
+
+// Two passes (amax, then quantise with a second read that hits L2), for
+// blocks too large for shared memory.
 template <int FMT>
 __global__ void __launch_bounds__(256) int4_quant_kernel(const uint8_t *__restrict__ pool,
                                                          long long blk_bytes, long long n_elts,
@@ -69,6 +189,7 @@ __global__ void __launch_bounds__(256) int4_quant_kernel(const uint8_t *__restri
   amax = red[0];
   for (int w = 1; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, red[w]);
   const float scale = amax / 7.0f;
+  const float inv = scale != 0.f ? 1.0f / scale : 0.f;
   if (threadIdx.x == 0) scales[blockIdx.x] = scale;
   uint32_t *dst = reinterpret_cast<uint32_t *>(nibbles + (size_t)blockIdx.x * (n_elts / 2));
   for (long long i = threadIdx.x; i < n8; i += blockDim.x) {
@@ -77,9 +198,7 @@ __global__ void __launch_bounds__(256) int4_quant_kernel(const uint8_t *__restri
     uint32_t word = 0;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      int q = 0;
-      if (scale != 0.f) q = max(-8, min(7, (int)rintf(x[e] / scale)));
-      word |= (uint32_t)(q + 8) << (4 * e);
+      word |= (uint32_t)(int4_code(x[e], scale, inv) + 8) << (4 * e);
     }
     dst[i] = word;
   }
@@ -160,12 +279,32 @@ extern "C" mt_status mt_kv_quant_int4(mt_kv_format fmt, const void *pool, int bl
   const long long blk_bytes = (long long)mt_kv_row_bytes(fmt, n_kv_heads, head_dim) * block_size;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const auto *pp = static_cast<const uint8_t *>(pool);
-  if (fmt == MT_KV_F16)
+  if (blk_bytes <= kQuantSmemMax && blk_bytes % 16 == 0) {
+    static bool attr_set[2] = {false, false};
+    if (fmt == MT_KV_F16) {
+      if (!attr_set[0]) {
+        cudaFuncSetAttribute(int4_quant_smem_kernel<MT_KV_F16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemMax);
+        attr_set[0] = true;
+      }
+      int4_quant_smem_kernel<MT_KV_F16><<<n_blocks, 256, (size_t)blk_bytes, s>>>(
+          pp, blk_bytes, n_elts, n_phys_blocks, blocks, scales, nibbles, status);
+    } else {
+      if (!attr_set[1]) {
+        cudaFuncSetAttribute(int4_quant_smem_kernel<MT_KV_F32>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemMax);
+        attr_set[1] = true;
+      }
+      int4_quant_smem_kernel<MT_KV_F32><<<n_blocks, 256, (size_t)blk_bytes, s>>>(
+          pp, blk_bytes, n_elts, n_phys_blocks, blocks, scales, nibbles, status);
+    }
+  } else if (fmt == MT_KV_F16) {
     int4_quant_kernel<MT_KV_F16><<<n_blocks, 256, 0, s>>>(pp, blk_bytes, n_elts, n_phys_blocks,
                                                           blocks, scales, nibbles, status);
-  else
+  } else {
     int4_quant_kernel<MT_KV_F32><<<n_blocks, 256, 0, s>>>(pp, blk_bytes, n_elts, n_phys_blocks,
                                                           blocks, scales, nibbles, status);
+  }
   st = cuda_check(cudaGetLastError(), "mt_kv_quant_int4 launch");
   return st == MT_OK ? ok() : st;
 }

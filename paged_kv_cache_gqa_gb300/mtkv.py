@@ -187,17 +187,22 @@ def mt_paged_attn_decode_static(args: mt_paged_attn_args, status=None, stream=No
 
 
 def _moves_array(moves):
-    arr = (mt_move * max(1, len(moves)))()
-    for i, (s, d, n) in enumerate(moves):
-        arr[i].src, arr[i].dst, arr[i].len = int(s), int(d), int(n)
-    return arr
+    """mt_move array for `moves`: (src, dst, len) triples, or an int64 numpy
+    array of shape (n, 3), which is passed without copying."""
+    import numpy as np
+    a = np.ascontiguousarray(np.asarray(moves, dtype=np.int64).reshape(-1, 3))
+    if a.shape[0] == 0:
+        a = np.zeros((1, 3), dtype=np.int64)
+    ptr = a.ctypes.data_as(ctypes.POINTER(mt_move))
+    ptr._keep = a  # the array must outlive the call
+    return ptr
 
 
 def mt_order_moves(moves):
     arr = _moves_array(moves)
     n_out = ctypes.c_int(0)
     _check(lib().mt_order_moves(arr, len(moves), ctypes.byref(n_out)), "mt_order_moves")
-    return [(arr[i].src, arr[i].dst, arr[i].len) for i in range(n_out.value)]
+    return [tuple(int(v) for v in r) for r in arr._keep[:n_out.value]]
 
 
 def mt_check_moves(moves, n_cells: int):
