@@ -63,6 +63,26 @@ def _peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks (x itself when running alone)."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def whole_job_rate(bytes_per_rank: float, seconds: float, world: int) -> float:
+    """Aggregate GB/s of `world` independent replicas that each moved
+    bytes_per_rank in (at most) `seconds`."""
+    return world * bytes_per_rank / seconds / 1e9
+
+
 def _structure():
     return workloads.llama3_f16(seed=SEED, hist=False)
 
@@ -285,8 +305,7 @@ def run_gpu(args, rank, world, local_rank):
     assert mtkv.mt_check_device_status(ws) == 0, mtkv.mt_last_error()
 
     clocks = Clocks(local_rank)
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
@@ -303,19 +322,14 @@ def run_gpu(args, rank, world, local_rank):
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    if world > 1:
-        torch.distributed.barrier()
-    total_ms = t0.elapsed_time(t1)
+    barrier(world)
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     dec_times = [a.elapsed_time(b) for st in dec_ms for (a, b) in st]
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
 
     dbytes, toks = decode_bytes(w)
     step_bytes = n_layers * (dbytes + store_bytes(w))
     ms_per_step = total_ms / args.steps
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_rate(step_bytes, ms_per_step * 1e-3, world)
     peak, peak_kind = _peak()
     dec_avg_ms = statistics.mean(dec_times)
     achieved = dbytes / (dec_avg_ms * 1e-3) / 1e9
@@ -348,17 +362,12 @@ def run_gpu(args, rank, world, local_rank):
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
     e0 = time.perf_counter()
     for _ in range(e2e_steps):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_s = (time.perf_counter() - e0) / e2e_steps
-    if world > 1:
-        tt = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(tt.item())
+    e2e_s = max_over_ranks((time.perf_counter() - e0) / e2e_steps, world, dev)
     assert mtkv.mt_check_device_status(status) == 0, mtkv.mt_last_error()
     assert mtkv.mt_check_device_status(ws) == 0, mtkv.mt_last_error()
 
@@ -389,7 +398,7 @@ def run_gpu(args, rank, world, local_rank):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "bytes_per_launch": dbytes, "avg_launch_ms": round(dec_avg_ms, 5),
                      "traffic": _traffic_from_profile()},
-        "e2e": {"value": round(world * step_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(whole_job_rate(step_bytes, e2e_s, world), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_s * 1e3, 4)},
         "gpu_launches": args.steps * n_layers * 3,
