@@ -40,6 +40,7 @@
 
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 #include <string>
 
@@ -83,6 +84,7 @@ struct Params {
   int rows;      // block rows per stage (block_size, or a divisor of it for wide rows)
   int pitch;     // shared-memory bytes between consecutive staged rows
   int use_tmap;  // 1: stage blocks with swizzled tensor copies (f16 tensor-core path)
+  int scratch_bytes;  // shared-memory bytes between the header and the stage ring
   int ncb;       // 128-byte chunks per staged row (odd), tensor path
   int n_sub;     // partial records per (CTA, sequence) slot
   int stages;
@@ -463,6 +465,263 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
   }
 }
 
+// ----------------------------------------------------------- q8_0 on MMA
+//
+// q8_0 rows hold 34-byte blocks ({f16 d; int8 q[32]}), so the codes are never
+// 16-byte aligned and ldmatrix cannot read them in place. Each consumer warp
+// instead converts its head's codes, 16 tokens at a time, into a private f16
+// tile in shared memory (exactly: int8 -> f16 by the 1024-bias trick), then
+// runs the tensor-core consumer on the tile:
+//   S += d[tok][grp] * (Qhl . q^T) per 32-dim group: one accumulator per group
+//        and 8-token tile, scaled in f32 by the token's group scale;
+//   O^T += q^T . (P * d)^T: the group scale folds into the probability operand
+//        (one B fragment per group, hi/lo f16 split), so dequantisation stays
+//        exact up to the f16 split of p*d.
+// Tile rows are 2*D+16 bytes apart (an odd number of 16-byte units), which
+// keeps every ldmatrix phase conflict-free.
+template <int D>
+__device__ __forceinline__ void q8_tile(const uint8_t *st, int row_bytes, int seg, int t0,
+                                        int r0, int r1, uint8_t *tile, int lane) {
+  constexpr int GPR = D / 4;      // 4-value groups per head row
+  constexpr int TP = 2 * D + 16;  // tile pitch in bytes
+  for (int idx = lane; idx < 16 * GPR; idx += 32) {
+    const int tr = idx / GPR, grp = idx % GPR;
+    const int tok = t0 + tr;
+    uint2 out = make_uint2(0u, 0u);
+    if (tok >= r0 && tok < r1) {
+      const uint8_t *a = st + (size_t)tok * row_bytes + seg + (grp >> 3) * 34 + 2 + (grp & 7) * 4;
+      const uint32_t w = ((uint32_t)*reinterpret_cast<const uint16_t *>(a) |
+                          ((uint32_t)*reinterpret_cast<const uint16_t *>(a + 2) << 16)) ^
+                         0x80808080u;
+      const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+      uint32_t lo = __byte_perm(w, 0x64646464u, 0x4140);
+      uint32_t hi = __byte_perm(w, 0x64646464u, 0x4342);
+      lo = h2_bits(__hsub2(*reinterpret_cast<__half2 *>(&lo), bias));
+      hi = h2_bits(__hsub2(*reinterpret_cast<__half2 *>(&hi), bias));
+      out = make_uint2(lo, hi);
+    }
+    *reinterpret_cast<uint2 *>(tile + tr * TP + grp * 8) = out;
+  }
+}
+
+__device__ __forceinline__ float q8_scale(const uint8_t *st, int row_bytes, int seg, int tok,
+                                          int grp) {
+  return __half2float(*reinterpret_cast<const __half *>(st + (size_t)tok * row_bytes + seg +
+                                                        grp * 34));
+}
+
+template <int D, int GP>
+__device__ __forceinline__ void consume_mma_q8(const Params &p, uint64_t *full, uint64_t *empty,
+                                               StageInfo *infos, volatile int *abort_flag,
+                                               uint8_t *ring, uint8_t *tiles, int warp,
+                                               int lane) {
+  using M = MmaCfg<D, GP>;
+  static_assert(M::WPH == 1, "q8_0 tensor-core consumers take one warp per KV head");
+  constexpr int NG = D / 32;      // q8_0 groups per head
+  constexpr int TP = 2 * D + 16;
+  const int kvh = warp;
+  const int g = lane >> 2, c = lane & 3;
+  const int G = p.G;
+  const int S = p.stages;
+  const int hrow = M::HILO ? (g >> 1) : g;
+  const bool row_ok = hrow < G;
+  const bool lo_col = M::HILO && (g & 1);
+  const int src0 = 8 * c;
+  const int src1 = M::HILO ? 8 * c : 8 * c + 4;
+  const int seg = kvh * NG * 34;  // byte offset of this head in a row
+  uint8_t *tk = tiles + (size_t)warp * 2 * 16 * TP;
+  uint8_t *tv = tk + 16 * TP;
+
+  uint32_t qa[M::KS][4];
+  float oacc[M::MTW][4];
+  float m_run = -INFINITY, l_run = 0.f;
+
+  for (uint32_t it = 0;; ++it) {
+    const int slot = (int)(it % (uint32_t)S);
+    int okv = 1;
+    if (lane == 0)
+      okv = mbar_wait_bounded(&full[slot], (it / (uint32_t)S) & 1u, abort_flag, p.wait_ns) ? 1 : 0;
+    okv = __shfl_sync(kFull, okv, 0);
+    if (!okv) {
+      if (lane == 0) {
+        *abort_flag = 1;
+        report(p.status, MT_STATUS_BIT_TIMEOUT);
+      }
+      return;
+    }
+    int seq, r0, r1, flags, base;
+    {
+      const volatile int *vi = reinterpret_cast<const volatile int *>(&infos[slot]);
+      seq = vi[0];
+      r0 = vi[1];
+      r1 = vi[2];
+      flags = vi[3] & 0xff;
+      base = vi[3] >> 8;
+    }
+    if (flags & F_EXIT) return;
+
+    if (flags & F_NEW) {
+      const float *qh = p.q + ((size_t)seq * p.Hq + (size_t)kvh * G + hrow) * D;
+#pragma unroll
+      for (int ks = 0; ks < M::KS; ++ks) {
+        float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
+        if (row_ok) {
+          x0 = *reinterpret_cast<const float2 *>(qh + 16 * ks + 2 * c);
+          x1 = *reinterpret_cast<const float2 *>(qh + 16 * ks + 2 * c + 8);
+        }
+        split_h2(x0.x * p.qscale, x0.y * p.qscale, qa[ks][0], qa[ks][1]);
+        split_h2(x1.x * p.qscale, x1.y * p.qscale, qa[ks][2], qa[ks][3]);
+      }
+#pragma unroll
+      for (int mt = 0; mt < M::MTW; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) oacc[mt][e] = 0.f;
+      m_run = -INFINITY;
+      l_run = 0.f;
+    }
+
+    if (flags & F_DATA) {
+      // block-relative rows: stage row r holds block row base + r
+      const uint8_t *kst = ring + (size_t)slot * 2 * p.blk_pad - (ptrdiff_t)base * p.row_bytes;
+      const uint8_t *vst = kst + p.blk_pad;
+      float pr[4][2];
+      float mloc = -INFINITY;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int t0 = 16 * h;
+        pr[2 * h][0] = pr[2 * h][1] = pr[2 * h + 1][0] = pr[2 * h + 1][1] = -INFINITY;
+        if (t0 >= p.bs || t0 + 16 <= r0 || t0 >= r1) continue;
+        q8_tile<D>(kst, p.row_bytes, seg, t0, r0, r1, tk, lane);
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int tk0 = t0 + 8 * t + 2 * c;
+          float s0 = 0.f, s1 = 0.f;
+          const uint32_t kaddr = smem_u32(tk + (8 * t + (lane & 7)) * TP) +
+                                 (uint32_t)((lane >> 3) & 1) * 16 + (uint32_t)(lane >> 4) * 32;
+#pragma unroll
+          for (int grp = 0; grp < NG; ++grp) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kaddr + grp * 64, b0, b1, b2, b3);
+            mma_f16(acc, qa[2 * grp], b0, b1);
+            mma_f16(acc, qa[2 * grp + 1], b2, b3);
+            s0 = fmaf(q8_scale(kst, p.row_bytes, seg, tk0, grp), acc[0] + acc[2], s0);
+            s1 = fmaf(q8_scale(kst, p.row_bytes, seg, tk0 + 1, grp), acc[1] + acc[3], s1);
+          }
+          pr[2 * h + t][0] = (row_ok && tk0 >= r0 && tk0 < r1) ? s0 : -INFINITY;
+          pr[2 * h + t][1] = (row_ok && tk0 + 1 >= r0 && tk0 + 1 < r1) ? s1 : -INFINITY;
+          mloc = fmaxf(mloc, fmaxf(pr[2 * h + t][0], pr[2 * h + t][1]));
+        }
+        __syncwarp();
+      }
+      // ---- online softmax (base 2), as on the f16 path
+      mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, 1));
+      mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, 2));
+      const float m_new = fmaxf(m_run, mloc);
+      const bool none = m_new == -INFINITY;
+      const float alpha = none ? 1.f : exp2f(m_run - m_new);
+      m_run = m_new;
+      float lsum = 0.f;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        pr[t][0] = none ? 0.f : exp2f(pr[t][0] - m_new);
+        pr[t][1] = none ? 0.f : exp2f(pr[t][1] - m_new);
+        lsum += pr[t][0] + pr[t][1];
+      }
+      l_run = l_run * alpha + lsum;
+      const float a0 = __shfl_sync(kFull, alpha, src0);
+      const float a1 = __shfl_sync(kFull, alpha, src1);
+      if (!__all_sync(kFull, a0 == 1.f && a1 == 1.f)) {
+#pragma unroll
+        for (int mt = 0; mt < M::MTW; ++mt) {
+          oacc[mt][0] *= a0;
+          oacc[mt][1] *= a1;
+          oacc[mt][2] *= a0;
+          oacc[mt][3] *= a1;
+        }
+      }
+      // ---- O^T += q^T . (P * d)^T per 16-token half
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int t0 = 16 * h;
+        if (t0 >= p.bs || t0 + 16 <= r0 || t0 >= r1) continue;
+        q8_tile<D>(vst, p.row_bytes, seg, t0, r0, r1, tv, lane);
+        __syncwarp();
+        const uint32_t vaddr = smem_u32(tv + (((lane >> 4) & 1) * 8 + (lane & 7)) * TP) +
+                               (uint32_t)((lane >> 3) & 1) * 16;
+        const int ta = t0 + 2 * c, tb = t0 + 8 + 2 * c;  // this thread's B rows (tokens)
+        const bool va0 = ta >= r0 && ta < r1, va1 = ta + 1 >= r0 && ta + 1 < r1;
+        const bool vb0 = tb >= r0 && tb < r1, vb1 = tb + 1 >= r0 && tb + 1 < r1;
+#pragma unroll
+        for (int grp = 0; grp < NG; ++grp) {
+          const float pa0 = va0 ? pr[2 * h][0] * q8_scale(vst, p.row_bytes, seg, ta, grp) : 0.f;
+          const float pa1 = va1 ? pr[2 * h][1] * q8_scale(vst, p.row_bytes, seg, ta + 1, grp) : 0.f;
+          const float pb0 = vb0 ? pr[2 * h + 1][0] * q8_scale(vst, p.row_bytes, seg, tb, grp) : 0.f;
+          const float pb1 =
+              vb1 ? pr[2 * h + 1][1] * q8_scale(vst, p.row_bytes, seg, tb + 1, grp) : 0.f;
+          uint32_t bq0, bq1;
+          if (M::HILO) {
+            uint32_t h0, l0, h1, l1;
+            split_h2(pa0, pa1, h0, l0);
+            split_h2(pb0, pb1, h1, l1);
+            bq0 = lo_col ? l0 : h0;
+            bq1 = lo_col ? l1 : h1;
+          } else {
+            bq0 = h2_bits(__floats2half2_rn(pa0, pa1));
+            bq1 = h2_bits(__floats2half2_rn(pb0, pb1));
+          }
+          if (!row_ok) bq0 = bq1 = 0u;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int mt = 2 * grp + j;
+            uint32_t a[4];
+            ldsm_x4_t(vaddr + mt * 32, a[0], a[1], a[2], a[3]);
+            mma_f16(oacc[mt], a, bq0, bq1);
+          }
+        }
+        __syncwarp();
+      }
+    }
+
+    if (flags & F_END) {
+      float l = l_run;
+      l += __shfl_xor_sync(kFull, l, 1);
+      l += __shfl_xor_sync(kFull, l, 2);
+      const size_t P = (size_t)blockIdx.x + seq;
+      const size_t hq0 = P * p.Hq + (size_t)kvh * G;
+      if (c == 0 && row_ok && !lo_col) {
+        p.part_ml[(hq0 + hrow) * 2 + 0] = m_run;
+        p.part_ml[(hq0 + hrow) * 2 + 1] = l;
+      }
+#pragma unroll
+      for (int mt = 0; mt < M::MTW; ++mt) {
+        const int dm = mt * 16 + g;
+        if (M::HILO) {
+          if (c < G) {
+            float *dst = p.part_o + (hq0 + c) * D;
+            dst[dm] = oacc[mt][0] + oacc[mt][1];
+            dst[dm + 8] = oacc[mt][2] + oacc[mt][3];
+          }
+        } else {
+          if (2 * c < G) {
+            float *dst = p.part_o + (hq0 + 2 * c) * D;
+            dst[dm] = oacc[mt][0];
+            dst[dm + 8] = oacc[mt][2];
+          }
+          if (2 * c + 1 < G) {
+            float *dst = p.part_o + (hq0 + 2 * c + 1) * D;
+            dst[dm] = oacc[mt][1];
+            dst[dm + 8] = oacc[mt][3];
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+  }
+}
+
 template <int FMT, int D, int GP, bool MMA>
 __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_constant__ Params p) {
   using C = Cfg<FMT, D, GP>;
@@ -473,8 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 128);
   float *scratch = reinterpret_cast<float *>(smem + kHdrBytes);
   // the ring starts on a 1024-byte boundary (the 128-byte swizzle's period)
-  uint8_t *ring = smem + kHdrBytes +
-                  ((kMaxConsumerWarps * scratch_floats_per_warp<GP>() * 4 + 127) & ~127);
+  uint8_t *ring = smem + kHdrBytes + p.scratch_bytes;
   ring += (1024u - (smem_u32(ring) & 1023u)) & 1023u;
 
   const int warp = threadIdx.x >> 5;
@@ -634,7 +892,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
   }
 
   if (warp >= p.n_cw) return;
-  if constexpr (MMA) {
+  if constexpr (MMA && FMT == MT_KV_Q8_0 && D <= 128) {
+    consume_mma_q8<D, GP>(p, full, empty, infos, abort_flag, ring, smem + kHdrBytes, warp, lane);
+  } else if constexpr (MMA) {
     consume_mma<D, GP>(p, full, empty, infos, abort_flag, ring, warp, lane);
   } else {
   // ------------------------------------------------------- consumer warps
@@ -1013,7 +1273,7 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(const Params p) {
 struct Plan {
   int D, GP, wph, n_cw, stages, n_ctas, blk_pad, rows, smem;
   bool mma;
-  int pitch, n_sub, ncb;
+  int pitch, n_sub, ncb, scratch;
   size_t ws_status, ws_seq, ws_ml, ws_o, ws_total;
 };
 
@@ -1048,8 +1308,13 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
     return fail(MT_ERR_UNSUPPORTED, "paged decode: max_blocks * block_size overflows int32");
   pl->D = a->head_dim;
   pl->GP = GP;
-  // header, softmax scratch, 1024 bytes to align the ring, 16 bytes of tail
-  const int fixed = kHdrBytes + ((kMaxConsumerWarps * (32 * GP + GP) * 4 + 127) & ~127) + 1024 + 16;
+  // header, scratch (softmax rows, or the q8_0 conversion tiles), 1024 bytes
+  // to align the ring, 16 bytes of tail
+  const bool q8_mma = a->fmt == MT_KV_Q8_0 && (a->head_dim == 64 || a->head_dim == 128);
+  const int simt_scratch = (kMaxConsumerWarps * (32 * GP + GP) * 4 + 127) & ~127;
+  const int tile_scratch = kMaxConsumerWarps * 2 * 16 * (2 * a->head_dim + 16);
+  pl->scratch = q8_mma ? std::max(simt_scratch, tile_scratch) : simt_scratch;
+  const int fixed = kHdrBytes + pl->scratch + 1024 + 16;
   int n_ctas = a->n_ctas;
   int smem_cap = 232448;
   if (need_device || n_ctas == 0) {
@@ -1080,7 +1345,13 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
   pl->ncb = nc | 1;  // odd number of 128-byte lines per staged row
   pl->mma = a->fmt == MT_KV_F16 && rb % 128 == 0 && pl->ncb <= 255 &&
             a->n_kv_heads * mma_wph <= kMaxConsumerWarps && fit(128 * pl->ncb, 16, rows, pad, stages);
-  if (pl->mma) {
+  // q8_0 pools: tensor-core consumers on per-warp converted tiles (d <= 128)
+  if (!pl->mma && q8_mma && fit((int)rb, 16, rows, pad, stages)) {
+    pl->mma = true;
+    wph = 1;
+    pl->pitch = (int)rb;
+    pl->n_sub = 1;
+  } else if (pl->mma) {
     wph = mma_wph;
     pl->pitch = 128 * pl->ncb;
     pl->n_sub = 1;
@@ -1226,7 +1497,8 @@ mt_status fill_params(Params &prm, const mt_paged_attn_args *a, const Plan &pl, 
   prm.blk_pad = pl.blk_pad;
   prm.rows = pl.rows;
   prm.pitch = pl.pitch;
-  prm.use_tmap = pl.mma ? 1 : 0;
+  prm.use_tmap = (pl.mma && a->fmt == MT_KV_F16) ? 1 : 0;
+  prm.scratch_bytes = pl.scratch;
   prm.ncb = pl.ncb;
   prm.n_sub = pl.n_sub;
   prm.stages = pl.stages;
@@ -1235,7 +1507,7 @@ mt_status fill_params(Params &prm, const mt_paged_attn_args *a, const Plan &pl, 
   prm.n_ctas = pl.n_ctas;
   prm.qscale = a->scale * 1.4426950408889634f;
   prm.wait_ns = kWaitLimitNs;
-  if (pl.mma) {
+  if (prm.use_tmap) {
     const long long n_cells = (long long)a->n_phys_blocks * a->block_size;
     const size_t rb = (size_t)prm.row_bytes;
     mt_status st = encode_pool_map(&prm.tmap_k, a->k_pool, n_cells, rb, pl);
@@ -1252,7 +1524,9 @@ mt_status dispatch(const Params &prm, const Plan &pl, mt_kv_format fmt, cudaStre
     case MT_KV_F16:
       return pl.mma ? dispatch_d<MT_KV_F16, true>(prm, pl, s)
                     : dispatch_d<MT_KV_F16, false>(prm, pl, s);
-    default: return dispatch_d<MT_KV_Q8_0, false>(prm, pl, s);
+    default:
+      return pl.mma ? dispatch_d<MT_KV_Q8_0, true>(prm, pl, s)
+                    : dispatch_d<MT_KV_Q8_0, false>(prm, pl, s);
   }
 }
 
