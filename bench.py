@@ -288,15 +288,32 @@ def run_gpu(args, rank, world, local_rank):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(n_layers)]
 
-    def step(record=False):
-        for l in range(n_layers):
+    fused = args.store == "fused"
+
+    def layer(l):
+        if fused:
+            mtkv.mt_paged_attn_decode_append(args_l[l], k_news[l], v_news[l], ws)
+        else:
             mtkv.mt_kv_store("f16", k_pools[l], v_pools[l], hkv, d, k_news[l], v_news[l], cells,
                              status=status)
-            if record:
-                ev[l][0].record(stream)
             mtkv.mt_paged_attn_decode(args_l[l], ws)
-            if record:
-                ev[l][1].record(stream)
+
+    def step(record=False):
+        for l in range(n_layers):
+            if fused:
+                if record:
+                    ev[l][0].record(stream)
+                mtkv.mt_paged_attn_decode_append(args_l[l], k_news[l], v_news[l], ws)
+                if record:
+                    ev[l][1].record(stream)
+            else:
+                mtkv.mt_kv_store("f16", k_pools[l], v_pools[l], hkv, d, k_news[l], v_news[l],
+                                 cells, status=status)
+                if record:
+                    ev[l][0].record(stream)
+                mtkv.mt_paged_attn_decode(args_l[l], ws)
+                if record:
+                    ev[l][1].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -332,7 +349,9 @@ def run_gpu(args, rank, world, local_rank):
     value = whole_job_rate(step_bytes, ms_per_step * 1e-3, world)
     peak, peak_kind = _peak()
     dec_avg_ms = statistics.mean(dec_times)
-    achieved = dbytes / (dec_avg_ms * 1e-3) / 1e9
+    # the timed call: decode + combine, with the row store when it is fused
+    call_bytes = dbytes + (store_bytes(w) if fused else 0)
+    achieved = call_bytes / (dec_avg_ms * 1e-3) / 1e9
 
     # ---- end to end: inputs from pinned host memory, outputs back to host
     h_q = [q.cpu().pin_memory() for q in qs]
@@ -342,20 +361,20 @@ def run_gpu(args, rank, world, local_rank):
     h_ctx = torch.from_numpy(w.context_lens).pin_memory()
     h_cells = torch.from_numpy(w.new_cells).pin_memory()
     h_out = [torch.empty(B, hq, d, dtype=torch.float32).pin_memory() for _ in range(n_layers)]
-    h2d = sum(t.numel() * t.element_size() for t in h_q + h_k + h_v + [h_table, h_ctx, h_cells])
+    h_meta = [h_table, h_ctx] + ([] if fused else [h_cells])
+    h2d = sum(t.numel() * t.element_size() for t in h_q + h_k + h_v + h_meta)
     d2h = sum(t.numel() * t.element_size() for t in h_out)
 
     def e2e_step():
         table.copy_(h_table, non_blocking=True)
         ctx.copy_(h_ctx, non_blocking=True)
-        cells.copy_(h_cells, non_blocking=True)
+        if not fused:
+            cells.copy_(h_cells, non_blocking=True)
         for l in range(n_layers):
             qs[l].copy_(h_q[l], non_blocking=True)
             k_news[l].copy_(h_k[l], non_blocking=True)
             v_news[l].copy_(h_v[l], non_blocking=True)
-            mtkv.mt_kv_store("f16", k_pools[l], v_pools[l], hkv, d, k_news[l], v_news[l], cells,
-                             status=status)
-            mtkv.mt_paged_attn_decode(args_l[l], ws)
+            layer(l)
             h_out[l].copy_(outs[l], non_blocking=True)
 
     e2e_steps = max(3, args.steps // 4)
@@ -389,19 +408,24 @@ def run_gpu(args, rank, world, local_rank):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "kv_format": "f16", "n_layers": n_layers,
                    "n_seqs": B, "attended_tokens_per_layer": toks,
+                   "store": ("fused into the decode launch" if fused else
+                             "separate mt_kv_store launch"),
                    "l2": "inputs larger than L2 (1.3 GB of K/V per layer, 42 GB per step)",
                    "parallelism": f"replicas x{world}"},
         "frac_of_peak": round(value / peak, 4),
         "attended_tokens_per_s": round(world * n_layers * toks / (ms_per_step * 1e-3), 1),
-        "roofline": {"bound": "hbm", "kernel": "mt_paged_attn_decode (split-K decode + combine)",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("mt_paged_attn_decode_append (decode with the row store fused, "
+                                "+ combine)" if fused else
+                                "mt_paged_attn_decode (split-K decode + combine)"),
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "bytes_per_launch": dbytes, "avg_launch_ms": round(dec_avg_ms, 5),
+                     "bytes_per_launch": call_bytes, "avg_launch_ms": round(dec_avg_ms, 5),
                      "traffic": _traffic_from_profile()},
         "e2e": {"value": round(whole_job_rate(step_bytes, e2e_s, world), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_s * 1e3, 4)},
-        "gpu_launches": args.steps * n_layers * 3,
+        "gpu_launches": args.steps * n_layers * (2 if fused else 3),
         "clocks": clk,
         "cpu_baseline": cpu,
     }
@@ -634,6 +658,9 @@ def main():
     ap.add_argument("--workload", default="llama3_f16",
                     choices=["llama3_f16", "smollm2_f32", "q8_prefix", "longctx_int4"],
                     help="llama3_f16 is the benchmark line; the others measure the other kernels")
+    ap.add_argument("--store", default="fused", choices=["fused", "separate"],
+                    help="store each layer's new row inside the decode launch "
+                         "(mt_paged_attn_decode_append) or with its own mt_kv_store launch")
     ap.add_argument("--layers", type=int, default=N_LAYERS,
                     help="layers per step; fewer than 32 only for profiling captures")
     args = ap.parse_args()

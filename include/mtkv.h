@@ -141,6 +141,28 @@ size_t mt_paged_attn_workspace_bytes(const mt_paged_attn_args *args);
 mt_status mt_paged_attn_decode(const mt_paged_attn_args *args, void *workspace,
                                size_t workspace_bytes, mt_stream stream);
 
+/* Paged decode attention with the new token's K/V store fused in.
+ * "KV Cache Design — cells, format, sessions", section 1 (the store writes
+ * the cell the allocator resolved; the paged model resolves position p of
+ * sequence s to cell block_table[s][p/bs]*bs + p%bs) and section 2 (the
+ * fused decode family stores the new row into its cell in the same pass
+ * that reads the cache). Equivalent to mt_kv_store of row s of k_new/v_new
+ * into the cell of position context_lens[s]-1 of every sequence with a
+ * positive context length, followed by mt_paged_attn_decode(args): the
+ * attention sees the new row when its position is inside the window.
+ *   k_new, v_new  device float32 [n_seqs][n_kv_heads*head_dim], 16-byte
+ *                 aligned; converted exactly as mt_kv_store converts.
+ * The CTA whose share of the work loads the block of position ctx-1 writes
+ * that row just before it copies the block, so no separate store launch is
+ * needed. The appended block must belong to its sequence alone (copy on
+ * write before a store into a shared block, as the pages' sharing rule
+ * says); a sequence whose appended block is a hole or out of range stores
+ * nothing and is flagged in the workspace status word. Other arguments,
+ * workspace and errors as mt_paged_attn_decode. */
+mt_status mt_paged_attn_decode_append(const mt_paged_attn_args *args, const float *k_new,
+                                      const float *v_new, void *workspace,
+                                      size_t workspace_bytes, mt_stream stream);
+
 /* Bytes of the scratch array built into the library for
  * mt_paged_attn_decode_static (8 MiB per device that loads the library). */
 #define MT_STATIC_SCRATCH_BYTES ((size_t)8 << 20)

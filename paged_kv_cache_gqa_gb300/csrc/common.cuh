@@ -139,7 +139,35 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Order this thread's earlier generic-proxy global writes before later
+// async-proxy (bulk copy / TMA) accesses issued after a barrier.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ------------------------------------------------------------ numerics --
+
+// q8_0 quantisation of one 32-value group, value `x` held by lane `lane` of
+// the calling warp (all 32 lanes take part). "KV Cache Design — cells,
+// format, sessions", section 3: scale amax/127 in float32, stored as f16;
+// code = round-ties-even(x / (amax/127)) clamped to +-127; an all-zero
+// group stores scale 0 and codes 0. `blk` is the group's 34-byte block
+// {f16 d; int8 q[32]}. The division is IEEE (no fast-math), so any correct
+// float32 implementation of the rule gives the same bytes.
+__device__ __forceinline__ void q8_quant_group(uint8_t *blk, float x, int lane) {
+  float amax = fabsf(x);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float d32 = amax / 127.0f;
+  int q = 0;
+  if (d32 != 0.0f) {
+    q = (int)rintf(x / d32);
+    q = max(-127, min(127, q));
+  }
+  blk[2 + lane] = (uint8_t)(int8_t)q;
+  if (lane == 0) *reinterpret_cast<__half *>(blk) = __float2half_rn(d32);
+}
+
 
 __device__ __forceinline__ float2 h2_to_f2(uint32_t w) {
   __half2 h = *reinterpret_cast<__half2 *>(&w);

@@ -77,6 +77,8 @@ struct Params {
   float *part_ml;      // [P][Hq][2] partial (max, sum) in base-2 logits
   int32_t *seq_start;  // [B+1] stream offset of each sequence's first block
   uint32_t *status;
+  const float *k_new;  // [B][Hkv*D] rows appended at position ctx-1, or null
+  const float *v_new;
   int B, Hq, Hkv, G, bs, max_blocks;
   long long n_phys;
   int row_bytes;
@@ -722,6 +724,70 @@ __device__ __forceinline__ void consume_mma_q8(const Params &p, uint64_t *full, 
   }
 }
 
+// Fused store of one sequence's new row (decode with append): convert
+// k_new[s] and v_new[s] to the pool format and write them into `cell` of
+// both pools, by the 32 lanes of the calling warp, with the arithmetic of
+// kv_store_kernel (so the bytes are the same). Loads go out in batches of 8
+// per lane before any store. Ends with each lane's proxy fence and a warp
+// barrier: a bulk copy issued afterwards by any lane reads the new bytes.
+template <int FMT, int D>
+__device__ __noinline__ void append_row(const Params &p, int s, long long cell, int lane) {
+  const int n = p.Hkv * D;
+#pragma unroll 1
+  for (int kv = 0; kv < 2; ++kv) {
+    const float *src = (kv ? p.v_new : p.k_new) + (size_t)s * n;
+    uint8_t *dst = const_cast<uint8_t *>(kv ? p.v_pool : p.k_pool) + (size_t)cell * p.row_bytes;
+    if constexpr (FMT == MT_KV_Q8_0) {
+      const int groups = n / 32;
+#pragma unroll 1
+      for (int g0 = 0; g0 < groups; g0 += 8) {
+        float x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = g0 + j < groups ? src[(g0 + j) * 32 + lane] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (g0 + j < groups) q8_quant_group(dst + (size_t)(g0 + j) * 34, x[j], lane);
+      }
+      const int pad = p.row_bytes - groups * 34;
+      if (lane < pad) dst[groups * 34 + lane] = 0;
+    } else {
+#pragma unroll 1
+      for (int i0 = 4 * lane; i0 < n; i0 += 128 * 8) {
+        float4 x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + 128 * j;
+          x[j] = i < n ? *reinterpret_cast<const float4 *>(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + 128 * j;
+          if (i >= n) break;
+          if constexpr (FMT == MT_KV_F32) {
+            *reinterpret_cast<float4 *>(dst + (size_t)i * 4) = x[j];
+          } else {
+            const __half2 a = __floats2half2_rn(x[j].x, x[j].y);
+            const __half2 b = __floats2half2_rn(x[j].z, x[j].w);
+            *reinterpret_cast<uint2 *>(dst + (size_t)i * 2) =
+                make_uint2(*reinterpret_cast<const uint32_t *>(&a),
+                           *reinterpret_cast<const uint32_t *>(&b));
+          }
+        }
+      }
+    }
+  }
+  fence_proxy_async_global();
+  __syncwarp();
+}
+
+// Position ctx-1 of sequence s, for decode with append: its logical block,
+// or -1 when the context length is out of range (flagged) or zero.
+__device__ __forceinline__ int append_block(const Params &p, int s) {
+  const int c = p.ctx[s];
+  if (c <= 0 || c > p.max_blocks * p.bs) return -1;
+  return (c - 1) / p.bs;
+}
+
 template <int FMT, int D, int GP, bool MMA>
 __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_constant__ Params p) {
   using C = Cfg<FMT, D, GP>;
@@ -767,6 +833,25 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
     const int per = total > 0 ? (total + (int)gridDim.x - 1) / (int)gridDim.x : 0;
     const long long b0 = (long long)blockIdx.x * per;
     const long long b1 = min((long long)total, b0 + per);
+
+    if (p.k_new) {
+      // Appended rows outside every window are read by no CTA: CTA s mod
+      // grid writes them now. The others are written below, by the CTA whose
+      // range loads their block, just before it issues that block's copy.
+      for (int s = blockIdx.x; s < p.B; s += gridDim.x) {
+        const int lb = append_block(p, s);
+        if (lb < 0) continue;
+        int lo, hi;
+        const int nb = seq_window(p, s, lo, hi);
+        if (nb > 0 && lb >= lo / p.bs && lb < lo / p.bs + nb) continue;
+        const int phys = p.table[(size_t)s * p.max_blocks + lb];
+        if (phys < 0 || (long long)phys >= p.n_phys) {
+          if (lane == 0) report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
+          continue;
+        }
+        append_row<FMT, D>(p, s, (long long)phys * p.bs + (p.ctx[s] - 1) % p.bs, lane);
+      }
+    }
 
     uint32_t it = 0;
     bool alive = true;
@@ -839,6 +924,20 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
             bulk_prefetch_l2(p.q + (size_t)s * p.Hq * D, (uint32_t)(p.Hq * D * sizeof(float)));
           bool first = true;
           const int lb0 = lo / p.bs;
+          // decode with append: the logical block of position ctx-1 when this
+          // segment loads it (its new row is written just before the copy)
+          int lb_app = -1;
+          if (p.k_new) {
+            const int lb = append_block(p, s);
+            if (lb >= lb0 + (int)(seg_lo - start) && lb < lb0 + (int)(seg_hi - start)) {
+              lb_app = lb;
+              if (lane == 0) {
+                const uint32_t row = (uint32_t)(p.Hkv * D * sizeof(float));
+                bulk_prefetch_l2(p.k_new + (size_t)s * p.Hkv * D, row);
+                bulk_prefetch_l2(p.v_new + (size_t)s * p.Hkv * D, row);
+              }
+            }
+          }
           const int32_t *trow = p.table + (size_t)s * p.max_blocks;
           for (long long y0 = seg_lo; alive && y0 < seg_hi; y0 += 32) {
             const long long y = y0 + lane;
@@ -847,12 +946,19 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
             const int cnt = (int)min(32LL, seg_hi - y0);
             for (int i = 0; i < cnt; ++i) {
               const int phys = __shfl_sync(kFull, ent, i);
+              const int lb = lb0 + (int)(y0 + i - start);
+              if (lb == lb_app) {
+                if (phys < 0 || (long long)phys >= p.n_phys) {
+                  if (lane == 0) report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
+                } else {
+                  append_row<FMT, D>(p, s, (long long)phys * p.bs + (p.ctx[s] - 1) % p.bs, lane);
+                }
+              }
               if (phys == MT_INVALID_BLOCK_ID) continue;
               if (phys < 0 || (long long)phys >= p.n_phys) {
                 if (lane == 0) report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
                 continue;
               }
-              const int lb = lb0 + (int)(y0 + i - start);
               const int r0 = max(lo - lb * p.bs, 0);
               const int r1 = min(hi - lb * p.bs, p.bs);
               for (int c0 = (r0 / p.rows) * p.rows; c0 < r1; c0 += p.rows) {
@@ -1242,19 +1348,46 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(const Params p) {
       M = m_new;
 #pragma unroll
       for (int e = 0; e < DV; ++e) acc[e] *= f_old;
-#pragma unroll 4
-      for (int k = 0; k < cnt; ++k) {
-        const float fk = __shfl_sync(kFull, f, k);
-        if (fk == 0.f) continue;
-        const int ik = base + k;
-        const size_t Pk = ((size_t)c0 + ik / p.n_sub + s) * p.n_sub + ik % p.n_sub;
-        const float *src = p.part_o + (Pk * p.Hq + h) * D + lane * DV;
+      // All loads of a batch of partials are issued before any is used, so
+      // a long list costs one L2 round trip per batch, not one per partial.
+      constexpr int KB = DV >= 8 ? 4 : 8;
+      for (int k0 = 0; k0 < cnt; k0 += KB) {
+        float v[KB][DV];
+        float fk[KB];
 #pragma unroll
-        for (int e = 0; e < DV; e += 2) {
-          const float2 v = *reinterpret_cast<const float2 *>(src + e);
-          acc[e] = fmaf(fk, v.x, acc[e]);
-          acc[e + 1] = fmaf(fk, v.y, acc[e + 1]);
+        for (int j = 0; j < KB; ++j) {
+          fk[j] = __shfl_sync(kFull, f, (k0 + j) & 31);
+          const int ik = base + k0 + j;
+          if (k0 + j < cnt && fk[j] != 0.f) {
+            const size_t Pk = ((size_t)c0 + ik / p.n_sub + s) * p.n_sub + ik % p.n_sub;
+            const float *src = p.part_o + (Pk * p.Hq + h) * D + lane * DV;
+            if constexpr (DV % 4 == 0) {
+#pragma unroll
+              for (int e = 0; e < DV; e += 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(src + e);
+                v[j][e] = x.x;
+                v[j][e + 1] = x.y;
+                v[j][e + 2] = x.z;
+                v[j][e + 3] = x.w;
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < DV; e += 2) {
+                const float2 x = *reinterpret_cast<const float2 *>(src + e);
+                v[j][e] = x.x;
+                v[j][e + 1] = x.y;
+              }
+            }
+          } else {
+            fk[j] = 0.f;
+#pragma unroll
+            for (int e = 0; e < DV; ++e) v[j][e] = 0.f;
+          }
         }
+#pragma unroll
+        for (int j = 0; j < KB; ++j)
+#pragma unroll
+          for (int e = 0; e < DV; ++e) acc[e] = fmaf(fk[j], v[j][e], acc[e]);
       }
     }
   }
@@ -1483,6 +1616,8 @@ mt_status fill_params(Params &prm, const mt_paged_attn_args *a, const Plan &pl, 
   prm.out = a->out;
   prm.lse = a->lse;
   prm.status = status;
+  prm.k_new = nullptr;
+  prm.v_new = nullptr;
   prm.seq_start = reinterpret_cast<int32_t *>(ws + pl.ws_seq);
   prm.part_ml = reinterpret_cast<float *>(ws + pl.ws_ml);
   prm.part_o = reinterpret_cast<float *>(ws + pl.ws_o);
@@ -1559,6 +1694,35 @@ extern "C" mt_status mt_paged_attn_decode(const mt_paged_attn_args *a, void *wor
   Params prm;
   st = fill_params(prm, a, pl, ws, reinterpret_cast<uint32_t *>(ws + pl.ws_status));
   if (st != MT_OK) return st;
+  st = dispatch(prm, pl, a->fmt, reinterpret_cast<cudaStream_t>(stream));
+  return st == MT_OK ? ok() : st;
+}
+
+extern "C" mt_status mt_paged_attn_decode_append(const mt_paged_attn_args *a, const float *k_new,
+                                                 const float *v_new, void *workspace,
+                                                 size_t workspace_bytes, mt_stream stream) {
+  Plan pl;
+  mt_status st = make_plan(a, &pl, true);
+  if (st != MT_OK) return st;
+  if (a->n_seqs == 0) return ok();
+  if (!a->q || !a->k_pool || !a->v_pool || !a->block_table || !a->context_lens || !a->out ||
+      !k_new || !v_new)
+    return fail(MT_ERR_INVALID_ARG, "paged decode with append: null pointer");
+  if (!workspace || workspace_bytes < pl.ws_total)
+    return fail(MT_ERR_INVALID_ARG,
+                "paged decode with append: workspace missing or too small (need " +
+                    std::to_string(pl.ws_total) + " bytes)");
+  if (!aligned16(a->k_pool) || !aligned16(a->v_pool) || !aligned16(a->q) || !aligned16(a->out) ||
+      !aligned16(workspace) || !aligned16(k_new) || !aligned16(v_new))
+    return fail(MT_ERR_INVALID_ARG,
+                "paged decode with append: q, pools, out, new rows and workspace must be 16-byte "
+                "aligned");
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  Params prm;
+  st = fill_params(prm, a, pl, ws, reinterpret_cast<uint32_t *>(ws + pl.ws_status));
+  if (st != MT_OK) return st;
+  prm.k_new = k_new;
+  prm.v_new = v_new;
   st = dispatch(prm, pl, a->fmt, reinterpret_cast<cudaStream_t>(stream));
   return st == MT_OK ? ok() : st;
 }

@@ -8,9 +8,7 @@
 //
 // One warp handles one 32-value group of one row of K or V: lane i loads
 // value i (coalesced 128-byte loads), the q8_0 amax is a 5-step shuffle
-// reduction, and each lane writes its own output element. Division is IEEE
-// (the library is built without fast-math), so the codes match any correct
-// float32 implementation bit for bit.
+// reduction (q8_quant_group), and each lane writes its own output element.
 #include "common.cuh"
 #include "internal.h"
 
@@ -48,21 +46,7 @@ __global__ void __launch_bounds__(256) kv_store_kernel(uint8_t *__restrict__ k_p
   } else if (FMT == MT_KV_F16) {
     reinterpret_cast<__half *>(dst)[g * 32 + lane] = __float2half_rn(x);
   } else {
-    float amax = fabsf(x);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float d32 = amax / 127.0f;
-    int q = 0;
-    if (d32 != 0.0f) {
-      q = (int)rintf(x / d32);
-      q = max(-127, min(127, q));
-    }
-    uint8_t *blk = dst + (size_t)g * 34;
-    blk[2 + lane] = (uint8_t)(int8_t)q;
-    if (lane == 0) {
-      const __half d16 = __float2half_rn(d32);
-      *reinterpret_cast<__half *>(blk) = d16;
-    }
+    q8_quant_group(dst + (size_t)g * 34, x, lane);
     // the row is padded to whole 4-byte words: keep the pad bytes zero
     const int pad = row_bytes - groups * 34;
     if (g == groups - 1 && lane < pad) dst[groups * 34 + lane] = 0;

@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
         "mt_kv_store": (I, [I, P, P, I64, I, I, P, P, P, I, U32P, P]),
         "mt_paged_attn_workspace_bytes": (SZ, [ctypes.POINTER(mt_paged_attn_args)]),
         "mt_paged_attn_decode": (I, [ctypes.POINTER(mt_paged_attn_args), P, SZ, P]),
+        "mt_paged_attn_decode_append": (I, [ctypes.POINTER(mt_paged_attn_args), P, P, P, SZ, P]),
         "mt_paged_attn_decode_static": (I, [ctypes.POINTER(mt_paged_attn_args), U32P, P]),
         "mt_order_moves": (I, [ctypes.POINTER(mt_move), I, ctypes.POINTER(I)]),
         "mt_check_moves": (I, [ctypes.POINTER(mt_move), I, I64, ctypes.POINTER(I)]),
@@ -174,6 +175,16 @@ def mt_paged_attn_decode(args: mt_paged_attn_args, workspace, stream=None) -> No
     nbytes = workspace.numel() * workspace.element_size()
     _check(lib().mt_paged_attn_decode(ctypes.byref(args), _ptr(workspace), nbytes,
                                       _stream(stream)), "mt_paged_attn_decode")
+
+
+def mt_paged_attn_decode_append(args: mt_paged_attn_args, k_new, v_new, workspace,
+                                stream=None) -> None:
+    """Decode with each sequence's new K/V row (float32 [n_seqs][Hkv*d])
+    stored into the cell of position context_lens[s]-1 in the same launch."""
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().mt_paged_attn_decode_append(ctypes.byref(args), _ptr(k_new), _ptr(v_new),
+                                             _ptr(workspace), nbytes, _stream(stream)),
+           "mt_paged_attn_decode_append")
 
 
 MT_STATIC_SCRATCH_BYTES = 8 << 20
