@@ -572,11 +572,19 @@ def run_extra(args, rank, world, local_rank):
         w = workloads.llama3_q8_prefix(hist=False)
         layers, ws, rb = _decode_setup(mtkv, w, 32, dev, g)
         cells = torch.from_numpy(w.new_cells).to(dev)
+        groups = [(0, w.n_seqs, w.extra["prefix"] // w.block_size)]
+        cascade = args.prefix == "cascade"
+        if cascade:
+            ws = torch.zeros(mtkv.mt_paged_attn_cascade_workspace_bytes(layers[0][2], groups),
+                             dtype=torch.uint8, device=dev)
 
         def step():
             for kp, vp, a, kn in layers:
                 mtkv.mt_kv_store("q8_0", kp, vp, w.n_kv_heads, w.head_dim, kn, kn, cells)
-                mtkv.mt_paged_attn_decode(a, ws)
+                if cascade:
+                    mtkv.mt_paged_attn_decode_cascade(a, groups, ws)
+                else:
+                    mtkv.mt_paged_attn_decode(a, ws)
 
         clocks.start()
         ms = _gpu_time(step, steps, warmup, stream)
@@ -590,7 +598,10 @@ def run_extra(args, rank, world, local_rank):
                "attended_tokens_per_s": round(32 * toks / (ms * 1e-3), 1),
                "config": {"workload": "llama3-8b-shaped q8_0 paged decode: 32 layers, 32 seqs "
                                       "sharing a 4096-token prefix + U[64,1024] suffix, random "
-                                      "windows, 32/8 heads, head_dim 128, bs 32"},
+                                      "windows, 32/8 heads, head_dim 128, bs 32",
+                          "prefix": ("cascade: shared blocks read once per group "
+                                     "(mt_paged_attn_decode_cascade)" if cascade else
+                                     "per-sequence decode (mt_paged_attn_decode)")},
                "clocks": clk}
     elif args.workload == "longctx_int4":
         w = workloads.longctx_f16_int4(hist=False)
@@ -661,6 +672,9 @@ def main():
     ap.add_argument("--store", default="fused", choices=["fused", "separate"],
                     help="store each layer's new row inside the decode launch "
                          "(mt_paged_attn_decode_append) or with its own mt_kv_store launch")
+    ap.add_argument("--prefix", default="cascade", choices=["cascade", "plain"],
+                    help="q8_prefix workload: decode the shared prefix once per group "
+                         "(mt_paged_attn_decode_cascade) or per sequence")
     ap.add_argument("--layers", type=int, default=N_LAYERS,
                     help="layers per step; fewer than 32 only for profiling captures")
     args = ap.parse_args()

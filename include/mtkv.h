@@ -163,6 +163,44 @@ mt_status mt_paged_attn_decode_append(const mt_paged_attn_args *args, const floa
                                       const float *v_new, void *workspace,
                                       size_t workspace_bytes, mt_stream stream);
 
+/* A group of consecutive sequences whose block tables start with the same
+ * n_prefix_blocks physical block ids: a prompt prefix shared through
+ * refcounted blocks ("Tiered KV cache — architecture", section "The
+ * paged-attention block model", point 2: forks share blocks by refcount,
+ * copy on write). */
+typedef struct {
+  int32_t seq_begin;       /* first sequence of the group                   */
+  int32_t seq_end;         /* one past the last                             */
+  int32_t n_prefix_blocks; /* leading block-table entries all of them share */
+} mt_prefix_group;
+
+/* Workspace bytes mt_paged_attn_decode_cascade needs (0 on invalid
+ * arguments). Like mt_paged_attn_workspace_bytes, its first 4 bytes are the
+ * device status word. Queries the current device. */
+size_t mt_paged_attn_cascade_workspace_bytes(const mt_paged_attn_args *args,
+                                             const mt_prefix_group *groups, int n_groups);
+
+/* Shared-prefix (cascade) paged decode: computes exactly what
+ * mt_paged_attn_decode(args) computes (same outputs, same tolerances), for
+ * batches whose sequences share prefix blocks. Each shared block is read once
+ * per KV head for all sequences of its group (their queries form one
+ * tensor-core tile), instead of once per sequence; each sequence's private
+ * suffix goes through the ordinary decode; the two partial results merge by
+ * log-sum-exp ("KV Cache Design — cells, format, sessions", section 1: a
+ * sequence reads another's prefix in place, within its window).
+ *   groups    host array of n_groups (<= 64) disjoint groups; sequences in no
+ *             group are decoded as usual. Each group's sequences must hold
+ *             identical first n_prefix_blocks table entries (holes included):
+ *             the kernel checks this and flags a mismatch in the workspace
+ *             status word (MT_ERR_DEVICE_CHECK), the affected outputs then
+ *             being undefined.
+ * Shapes the prefix kernel is not built for (head_dim 256) run the ordinary
+ * decode. Errors as mt_paged_attn_decode, plus MT_ERR_INVALID_ARG for bad or
+ * overlapping groups. */
+mt_status mt_paged_attn_decode_cascade(const mt_paged_attn_args *args,
+                                       const mt_prefix_group *groups, int n_groups,
+                                       void *workspace, size_t workspace_bytes, mt_stream stream);
+
 /* Bytes of the scratch array built into the library for
  * mt_paged_attn_decode_static (8 MiB per device that loads the library). */
 #define MT_STATIC_SCRATCH_BYTES ((size_t)8 << 20)

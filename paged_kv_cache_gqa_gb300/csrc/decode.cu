@@ -35,14 +35,18 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include "cascade.h"
 #include "common.cuh"
+#include "mma.cuh"
 #include "internal.h"
+#include "prefix.h"
 
 #include <math.h>
 
 #include <algorithm>
 #include <mutex>
 #include <string>
+#include <vector>
 
 namespace mtkv {
 namespace {
@@ -95,6 +99,7 @@ struct Params {
   int n_ctas;
   float qscale;  // softmax scale * log2(e)
   uint64_t wait_ns;
+  Cascade casc;  // shared-prefix groups (n_groups == 0: plain decode)
 };
 
 // Shared memory: [barriers | stage infos | abort] header, per-warp softmax
@@ -119,6 +124,8 @@ __device__ __forceinline__ int seq_window(const Params &p, int s, int &lo, int &
     lo = max(p.spans[2 * s], 0);
     hi = min(p.spans[2 * s + 1], c);
   }
+  // cascade: the shared prefix is read by the prefix kernel, not here
+  if (p.casc.n_groups) lo = max(lo, cascade_skip(p.casc, s, p.bs));
   if (hi <= lo) {
     lo = hi = 0;
     return 0;
@@ -228,38 +235,6 @@ struct MmaCfg {
   static constexpr bool HILO = GP <= 4;          // p split into two f16 columns
 };
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                        uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                          uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                        uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
-
-// high and low f16 halves of a float pair: x ~= hi + lo to ~2^-22 relative
-__device__ __forceinline__ void split_h2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
-  const __half2 h = __floats2half2_rn(x0, x1);
-  const float2 hf = __half22float2(h);
-  hi = h2_bits(h);
-  lo = h2_bits(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
-}
 
 template <int D, int GP>
 __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uint64_t *empty,
@@ -1320,75 +1295,98 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(const Params p) {
 #pragma unroll
   for (int e = 0; e < DV; ++e) acc[e] = 0.f;
   float M = -INFINITY, L = 0.f;
-  if (end > beg) {
-    const int c0 = beg / per;
-    const int NP = ((end - 1) / per - c0 + 1) * p.n_sub;  // partials, CTA-major
-    for (int base = 0; base < NP; base += 32) {
-      const int cnt = min(32, NP - base);
-      const int i = base + lane;
-      float m = -INFINITY, l = 0.f;
-      if (lane < cnt) {
-        const size_t P = ((size_t)c0 + i / p.n_sub + s) * p.n_sub + i % p.n_sub;
-        const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + (P * p.Hq + h) * 2);
-        m = ml.x;
-        l = ml.y;
-      }
-      if (!(l > 0.f)) m = -INFINITY;
-      float mc = m;
+  // The partials of (s, h): the decode's (CTA-major, n_sub per CTA), then,
+  // for a sequence of a shared-prefix group, the prefix kernel's records of
+  // its tile (one per prefix CTA whose range meets the tile).
+  const int c0 = end > beg ? beg / per : 0;
+  const int NPd = end > beg ? ((end - 1) / per - c0 + 1) * p.n_sub : 0;
+  int NPc = 0, Tc = 0, Rc = 0, cc0 = 0;
+  if (p.casc.n_groups) {
+    long long u0 = 0;
+    const int gi = cascade_find(p.casc, p.Hkv, p.G, s, h, Tc, Rc, u0);
+    if (gi >= 0 && p.casc.g[gi].nblk > 0) {
+      cc0 = (int)(u0 / p.casc.per);
+      NPc = (int)((u0 + p.casc.g[gi].nblk - 1) / p.casc.per) - cc0 + 1;
+    }
+  }
+  const int NP = NPd + NPc;
+  auto part = [&](int i, const float *&ml, const float *&o) {
+    if (i < NPd) {
+      const size_t P = ((size_t)c0 + i / p.n_sub + s) * p.n_sub + i % p.n_sub;
+      ml = p.part_ml + (P * p.Hq + h) * 2;
+      o = p.part_o + (P * p.Hq + h) * D;
+    } else {
+      const size_t slot = (size_t)cc0 + (i - NPd) + Tc;
+      ml = p.casc.rec_ml + (slot * kPrefixRows + Rc) * 2;
+      o = p.casc.rec_o + (slot * kPrefixRows + Rc) * D;
+    }
+  };
+  for (int base = 0; base < NP; base += 32) {
+    const int cnt = min(32, NP - base);
+    const int i = base + lane;
+    float m = -INFINITY, l = 0.f;
+    if (lane < cnt) {
+      const float *mlp, *op;
+      part(i, mlp, op);
+      const float2 ml = *reinterpret_cast<const float2 *>(mlp);
+      m = ml.x;
+      l = ml.y;
+    }
+    if (!(l > 0.f)) m = -INFINITY;
+    float mc = m;
 #pragma unroll
-      for (int o = 16; o; o >>= 1) mc = fmaxf(mc, __shfl_xor_sync(kFull, mc, o));
-      const float m_new = fmaxf(M, mc);
-      if (m_new == -INFINITY) continue;  // nothing valid yet
-      const float f_old = exp2f(M - m_new);
-      const float f = m == -INFINITY ? 0.f : exp2f(m - m_new);
-      float lc = l * f;
+    for (int o = 16; o; o >>= 1) mc = fmaxf(mc, __shfl_xor_sync(kFull, mc, o));
+    const float m_new = fmaxf(M, mc);
+    if (m_new == -INFINITY) continue;  // nothing valid yet
+    const float f_old = exp2f(M - m_new);
+    const float f = m == -INFINITY ? 0.f : exp2f(m - m_new);
+    float lc = l * f;
 #pragma unroll
-      for (int o = 16; o; o >>= 1) lc += __shfl_xor_sync(kFull, lc, o);
-      L = L * f_old + lc;
-      M = m_new;
+    for (int o = 16; o; o >>= 1) lc += __shfl_xor_sync(kFull, lc, o);
+    L = L * f_old + lc;
+    M = m_new;
 #pragma unroll
-      for (int e = 0; e < DV; ++e) acc[e] *= f_old;
-      // All loads of a batch of partials are issued before any is used, so
-      // a long list costs one L2 round trip per batch, not one per partial.
-      constexpr int KB = DV >= 8 ? 4 : 8;
-      for (int k0 = 0; k0 < cnt; k0 += KB) {
-        float v[KB][DV];
-        float fk[KB];
+    for (int e = 0; e < DV; ++e) acc[e] *= f_old;
+    // All loads of a batch of partials are issued before any is used, so
+    // a long list costs one L2 round trip per batch, not one per partial.
+    constexpr int KB = DV >= 8 ? 4 : 8;
+    for (int k0 = 0; k0 < cnt; k0 += KB) {
+      float v[KB][DV];
+      float fk[KB];
 #pragma unroll
-        for (int j = 0; j < KB; ++j) {
-          fk[j] = __shfl_sync(kFull, f, (k0 + j) & 31);
-          const int ik = base + k0 + j;
-          if (k0 + j < cnt && fk[j] != 0.f) {
-            const size_t Pk = ((size_t)c0 + ik / p.n_sub + s) * p.n_sub + ik % p.n_sub;
-            const float *src = p.part_o + (Pk * p.Hq + h) * D + lane * DV;
-            if constexpr (DV % 4 == 0) {
+      for (int j = 0; j < KB; ++j) {
+        fk[j] = __shfl_sync(kFull, f, (k0 + j) & 31);
+        if (k0 + j < cnt && fk[j] != 0.f) {
+          const float *mlp, *op;
+          part(base + k0 + j, mlp, op);
+          const float *src = op + lane * DV;
+          if constexpr (DV % 4 == 0) {
 #pragma unroll
-              for (int e = 0; e < DV; e += 4) {
-                const float4 x = *reinterpret_cast<const float4 *>(src + e);
-                v[j][e] = x.x;
-                v[j][e + 1] = x.y;
-                v[j][e + 2] = x.z;
-                v[j][e + 3] = x.w;
-              }
-            } else {
-#pragma unroll
-              for (int e = 0; e < DV; e += 2) {
-                const float2 x = *reinterpret_cast<const float2 *>(src + e);
-                v[j][e] = x.x;
-                v[j][e + 1] = x.y;
-              }
+            for (int e = 0; e < DV; e += 4) {
+              const float4 x = *reinterpret_cast<const float4 *>(src + e);
+              v[j][e] = x.x;
+              v[j][e + 1] = x.y;
+              v[j][e + 2] = x.z;
+              v[j][e + 3] = x.w;
             }
           } else {
-            fk[j] = 0.f;
 #pragma unroll
-            for (int e = 0; e < DV; ++e) v[j][e] = 0.f;
+            for (int e = 0; e < DV; e += 2) {
+              const float2 x = *reinterpret_cast<const float2 *>(src + e);
+              v[j][e] = x.x;
+              v[j][e + 1] = x.y;
+            }
           }
+        } else {
+          fk[j] = 0.f;
+#pragma unroll
+          for (int e = 0; e < DV; ++e) v[j][e] = 0.f;
         }
-#pragma unroll
-        for (int j = 0; j < KB; ++j)
-#pragma unroll
-          for (int e = 0; e < DV; ++e) acc[e] = fmaf(fk[j], v[j][e], acc[e]);
       }
+#pragma unroll
+      for (int j = 0; j < KB; ++j)
+#pragma unroll
+        for (int e = 0; e < DV; ++e) acc[e] = fmaf(fk[j], v[j][e], acc[e]);
     }
   }
   float *dst = p.out + ((size_t)s * p.Hq + h) * D + lane * DV;
@@ -1618,6 +1616,7 @@ mt_status fill_params(Params &prm, const mt_paged_attn_args *a, const Plan &pl, 
   prm.status = status;
   prm.k_new = nullptr;
   prm.v_new = nullptr;
+  prm.casc.n_groups = 0;
   prm.seq_start = reinterpret_cast<int32_t *>(ws + pl.ws_seq);
   prm.part_ml = reinterpret_cast<float *>(ws + pl.ws_ml);
   prm.part_o = reinterpret_cast<float *>(ws + pl.ws_o);
@@ -1695,6 +1694,142 @@ extern "C" mt_status mt_paged_attn_decode(const mt_paged_attn_args *a, void *wor
   st = fill_params(prm, a, pl, ws, reinterpret_cast<uint32_t *>(ws + pl.ws_status));
   if (st != MT_OK) return st;
   st = dispatch(prm, pl, a->fmt, reinterpret_cast<cudaStream_t>(stream));
+  return st == MT_OK ? ok() : st;
+}
+
+// ------------------------------------------------- shared-prefix (cascade)
+
+namespace mtkv {
+namespace {
+
+struct CascadePlan {
+  bool use;          // the prefix kernel covers the shape (else: plain decode)
+  Cascade c;
+  size_t rec_off;    // records start (bytes into the workspace)
+  size_t total;      // workspace bytes
+};
+
+mt_status cascade_plan(const mt_paged_attn_args *a, const Plan &pl,
+                       const mt_prefix_group *groups, int n_groups, CascadePlan *cp) {
+  if (n_groups < 0) return fail(MT_ERR_INVALID_ARG, "cascade decode: negative group count");
+  if (n_groups > kMaxPrefixGroups)
+    return fail(MT_ERR_UNSUPPORTED, "cascade decode: at most 64 prefix groups");
+  if (n_groups > 0 && !groups) return fail(MT_ERR_INVALID_ARG, "cascade decode: null groups");
+  std::vector<std::pair<int, int>> spans;
+  for (int i = 0; i < n_groups; ++i) {
+    const mt_prefix_group &g = groups[i];
+    if (g.seq_begin < 0 || g.seq_end > a->n_seqs || g.seq_begin >= g.seq_end)
+      return fail(MT_ERR_INVALID_ARG, "cascade decode: group " + std::to_string(i) +
+                                          " has an empty or out-of-range sequence range");
+    if (g.n_prefix_blocks < 0 || g.n_prefix_blocks > a->max_blocks)
+      return fail(MT_ERR_INVALID_ARG,
+                  "cascade decode: group " + std::to_string(i) + " prefix outside the table");
+    spans.emplace_back(g.seq_begin, g.seq_end);
+  }
+  std::sort(spans.begin(), spans.end());
+  for (size_t i = 1; i < spans.size(); ++i)
+    if (spans[i].first < spans[i - 1].second)
+      return fail(MT_ERR_INVALID_ARG, "cascade decode: prefix groups overlap");
+  cp->total = pl.ws_total;
+  cp->rec_off = pl.ws_total;
+  Cascade &c = cp->c;
+  c = Cascade{};
+  cp->use = n_groups > 0 && prefix_supported(a->head_dim, a->block_size, pl.GP);
+  if (!cp->use) return MT_OK;
+  c.n_groups = n_groups;
+  c.gp = pl.GP;
+  c.tq = kPrefixRows / pl.GP;
+  long long tiles = 0, units = 0;
+  for (int i = 0; i < n_groups; ++i) {
+    c.g[i] = PrefixGroup{groups[i].seq_begin, groups[i].seq_end, groups[i].n_prefix_blocks};
+    const long long t = (long long)cascade_qtiles(c, i) * a->n_kv_heads;
+    tiles += t;
+    units += t * groups[i].n_prefix_blocks;
+  }
+  DeviceInfo di;
+  mt_status st = device_info(&di);
+  if (st != MT_OK) return st;
+  const long long ctas = std::min<long long>((long long)di.n_sm * prefix_ctas_per_sm(), units);
+  c.n_tiles = (int)tiles;
+  c.n_units = units;
+  c.n_ctas = ctas > 0 ? (int)ctas : 0;
+  c.per = ctas > 0 ? (int)((units + ctas - 1) / ctas) : 1;
+  const size_t slots = (size_t)c.n_ctas + (size_t)c.n_tiles;
+  const size_t ml_bytes = (slots * kPrefixRows * 2 * 4 + 255) & ~(size_t)255;
+  const size_t o_bytes = slots * kPrefixRows * (size_t)a->head_dim * 4;
+  cp->total = cp->rec_off + ml_bytes + o_bytes;
+  return MT_OK;
+}
+
+}  // namespace
+}  // namespace mtkv
+
+extern "C" size_t mt_paged_attn_cascade_workspace_bytes(const mt_paged_attn_args *a,
+                                                        const mt_prefix_group *groups,
+                                                        int n_groups) {
+  Plan pl;
+  if (make_plan(a, &pl, false) != MT_OK) return 0;
+  CascadePlan cp;
+  if (cascade_plan(a, pl, groups, n_groups, &cp) != MT_OK) return 0;
+  return cp.total;
+}
+
+extern "C" mt_status mt_paged_attn_decode_cascade(const mt_paged_attn_args *a,
+                                                  const mt_prefix_group *groups, int n_groups,
+                                                  void *workspace, size_t workspace_bytes,
+                                                  mt_stream stream) {
+  Plan pl;
+  mt_status st = make_plan(a, &pl, true);
+  if (st != MT_OK) return st;
+  CascadePlan cp;
+  st = cascade_plan(a, pl, groups, n_groups, &cp);
+  if (st != MT_OK) return st;
+  if (a->n_seqs == 0) return ok();
+  if (!a->q || !a->k_pool || !a->v_pool || !a->block_table || !a->context_lens || !a->out)
+    return fail(MT_ERR_INVALID_ARG, "cascade decode: null pointer");
+  if (!workspace || workspace_bytes < cp.total)
+    return fail(MT_ERR_INVALID_ARG, "cascade decode: workspace missing or too small (need " +
+                                        std::to_string(cp.total) + " bytes)");
+  if (!aligned16(a->k_pool) || !aligned16(a->v_pool) || !aligned16(a->q) || !aligned16(a->out) ||
+      !aligned16(workspace))
+    return fail(MT_ERR_INVALID_ARG,
+                "cascade decode: q, pools, out and workspace must be 16-byte aligned");
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  Params prm;
+  st = fill_params(prm, a, pl, ws, reinterpret_cast<uint32_t *>(ws + pl.ws_status));
+  if (st != MT_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cp.use) {
+    Cascade &c = cp.c;
+    c.rec_ml = reinterpret_cast<float *>(ws + cp.rec_off);
+    const size_t slots = (size_t)c.n_ctas + (size_t)c.n_tiles;
+    c.rec_o = reinterpret_cast<float *>(ws + cp.rec_off +
+                                        ((slots * kPrefixRows * 2 * 4 + 255) & ~(size_t)255));
+    prm.casc = c;
+    if (c.n_units > 0) {
+      PrefixParams pp;
+      pp.q = a->q;
+      pp.k_pool = static_cast<const uint8_t *>(a->k_pool);
+      pp.v_pool = static_cast<const uint8_t *>(a->v_pool);
+      pp.table = a->block_table;
+      pp.ctx = a->context_lens;
+      pp.spans = a->spans;
+      pp.status = prm.status;
+      pp.B = prm.B;
+      pp.Hq = prm.Hq;
+      pp.Hkv = prm.Hkv;
+      pp.G = prm.G;
+      pp.bs = prm.bs;
+      pp.max_blocks = prm.max_blocks;
+      pp.n_phys = prm.n_phys;
+      pp.row_bytes = prm.row_bytes;
+      pp.qscale = prm.qscale;
+      pp.c = c;
+      st = launch_prefix(a->fmt, a->head_dim, pl.GP, pp, c.n_ctas, s);
+      if (st != MT_OK) return st;
+    }
+  }
+  st = dispatch(prm, pl, a->fmt, s);
   return st == MT_OK ? ok() : st;
 }
 

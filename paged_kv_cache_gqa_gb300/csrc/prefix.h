@@ -1,0 +1,37 @@
+// Host interface of the prefix kernel of the shared-prefix (cascade) decode.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mtkv.h"
+#include "cascade.h"
+
+namespace mtkv {
+
+struct PrefixParams {
+  const float *q;
+  const uint8_t *k_pool;
+  const uint8_t *v_pool;
+  const int32_t *table;
+  const int32_t *ctx;
+  const int32_t *spans;
+  uint32_t *status;
+  int B, Hq, Hkv, G, bs, max_blocks;
+  long long n_phys;
+  int row_bytes;
+  float qscale;  // softmax scale * log2(e)
+  Cascade c;
+};
+
+// Whether the prefix kernel is built for this shape (head_dim 64 or 128,
+// block_size 16 or 32, padded query group <= 8).
+bool prefix_supported(int head_dim, int block_size, int gp);
+// Dynamic shared memory of the prefix kernel for (format, head_dim).
+int prefix_smem_bytes(mt_kv_format fmt, int head_dim);
+// CTAs of the prefix kernel that can be resident on the device at once.
+int prefix_ctas_per_sm();
+mt_status launch_prefix(mt_kv_format fmt, int head_dim, int gp, const PrefixParams &p, int n_ctas,
+                        cudaStream_t stream);
+
+}  // namespace mtkv

@@ -40,6 +40,11 @@ class mt_move(ctypes.Structure):
     _fields_ = [("src", ctypes.c_int64), ("dst", ctypes.c_int64), ("len", ctypes.c_int64)]
 
 
+class mt_prefix_group(ctypes.Structure):
+    _fields_ = [("seq_begin", ctypes.c_int32), ("seq_end", ctypes.c_int32),
+                ("n_prefix_blocks", ctypes.c_int32)]
+
+
 class mt_paged_attn_args(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int), ("q", ctypes.c_void_p), ("k_pool", ctypes.c_void_p),
                 ("v_pool", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
@@ -71,6 +76,10 @@ def lib() -> ctypes.CDLL:
         "mt_paged_attn_decode": (I, [ctypes.POINTER(mt_paged_attn_args), P, SZ, P]),
         "mt_paged_attn_decode_append": (I, [ctypes.POINTER(mt_paged_attn_args), P, P, P, SZ, P]),
         "mt_paged_attn_decode_static": (I, [ctypes.POINTER(mt_paged_attn_args), U32P, P]),
+        "mt_paged_attn_cascade_workspace_bytes": (SZ, [ctypes.POINTER(mt_paged_attn_args),
+                                                       ctypes.POINTER(mt_prefix_group), I]),
+        "mt_paged_attn_decode_cascade": (I, [ctypes.POINTER(mt_paged_attn_args),
+                                             ctypes.POINTER(mt_prefix_group), I, P, SZ, P]),
         "mt_order_moves": (I, [ctypes.POINTER(mt_move), I, ctypes.POINTER(I)]),
         "mt_check_moves": (I, [ctypes.POINTER(mt_move), I, I64, ctypes.POINTER(I)]),
         "mt_copy_cells": (I, [ctypes.POINTER(P), I, SZ, I64, ctypes.POINTER(mt_move), I, P]),
@@ -185,6 +194,32 @@ def mt_paged_attn_decode_append(args: mt_paged_attn_args, k_new, v_new, workspac
     _check(lib().mt_paged_attn_decode_append(ctypes.byref(args), _ptr(k_new), _ptr(v_new),
                                              _ptr(workspace), nbytes, _stream(stream)),
            "mt_paged_attn_decode_append")
+
+
+def _groups_array(groups):
+    """mt_prefix_group array for (seq_begin, seq_end, n_prefix_blocks) triples."""
+    n = len(groups)
+    arr = (mt_prefix_group * max(n, 1))()
+    for i, (b, e, nb) in enumerate(groups):
+        arr[i].seq_begin, arr[i].seq_end, arr[i].n_prefix_blocks = int(b), int(e), int(nb)
+    return arr, n
+
+
+def mt_paged_attn_cascade_workspace_bytes(args: mt_paged_attn_args, groups) -> int:
+    arr, n = _groups_array(groups)
+    return int(lib().mt_paged_attn_cascade_workspace_bytes(ctypes.byref(args), arr, n))
+
+
+def mt_paged_attn_decode_cascade(args: mt_paged_attn_args, groups, workspace,
+                                 stream=None) -> None:
+    """Decode where the sequences of each group (seq_begin, seq_end,
+    n_prefix_blocks) share their first n_prefix_blocks block-table entries:
+    each shared block is read once per KV head for the whole group."""
+    arr, n = _groups_array(groups)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().mt_paged_attn_decode_cascade(ctypes.byref(args), arr, n, _ptr(workspace),
+                                              nbytes, _stream(stream)),
+           "mt_paged_attn_decode_cascade")
 
 
 MT_STATIC_SCRATCH_BYTES = 8 << 20

@@ -1,0 +1,159 @@
+"""GPU parity of the shared-prefix (cascade) decode against the oracle.
+
+The cascade is an execution strategy: for any batch whose groups really
+share their leading block-table entries, mt_paged_attn_decode_cascade must
+give what the oracle's plain decode gives (f32 1e-4, f16 and q8_0 2e-3).
+Groups are made by pointing the first k table entries of a run of sequences
+at the same physical blocks, which is exactly what a refcounted fork does.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moves as om
+from oracle import formats as ofmt
+from paged_kv_cache_gqa_gb300 import workloads
+from tests.gpu_util import (TOL, assert_close, assert_lse, oracle_decode, oracle_pools,
+                            to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mt():
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_cache_gqa_gb300 import mtkv
+    return mtkv
+
+
+def share(table, groups):
+    """Table in which each group's sequences use the first sequence's first
+    n_prefix_blocks entries."""
+    t = table.copy()
+    for b, e, nb in groups:
+        for s in range(b + 1, e):
+            t[s, :nb] = t[b, :nb]
+    return t
+
+
+def cascade(mt, w, k_dev, v_dev, table, groups, spans="w"):
+    q = to_dev(w.q)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((w.n_seqs, w.n_heads), float("nan"), device="cuda")
+    sp = (None if w.spans is None else to_dev(w.spans)) if isinstance(spans, str) else \
+        (None if spans is None else to_dev(spans))
+    args = mt.paged_attn_args(w.fmt, q, k_dev, v_dev, to_dev(table), to_dev(w.context_lens), out,
+                              n_kv_heads=w.n_kv_heads, block_size=w.block_size,
+                              n_phys_blocks=w.n_phys_blocks, scale=w.scale, spans=sp, lse=lse)
+    nbytes = mt.mt_paged_attn_cascade_workspace_bytes(args, groups)
+    assert nbytes > 0, mt.mt_last_error()
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    mt.mt_paged_attn_decode_cascade(args, groups, ws)
+    st = mt.mt_check_device_status(ws)
+    return out.cpu().numpy(), lse.cpu().numpy(), st
+
+
+def check(mt, w, groups, table=None, expect_status=0):
+    table = share(w.block_table if table is None else table, groups)
+    kp, vp = oracle_pools(w)
+    k_dev, v_dev = to_dev(kp), to_dev(vp)
+    want, want_lse = oracle_decode(w, kp, vp, table=table)
+    got, got_lse, st = cascade(mt, w, k_dev, v_dev, table, groups)
+    assert st == expect_status, mt.mt_last_error()
+    if expect_status == 0:
+        assert_close(got, want, TOL[w.fmt], f"{w.name} cascade")
+        assert_lse(got_lse, want_lse, TOL[w.fmt], f"{w.name} cascade")
+    return got, want
+
+
+@pytest.mark.parametrize("groups", [[(0, 6, 3)], [(0, 6, 3), (7, 10, 5)], [(2, 3, 4)],
+                                    [(0, 10, 0)], [(0, 10, 6)]])
+def test_cascade_llama3_f16(mt, groups):
+    w = workloads.llama3_f16(seed=21, n_seqs=10, ctx_lo=30, ctx_hi=400)
+    check(mt, w, groups)
+
+
+def test_cascade_many_sequences_per_tile(mt):
+    # 40 sequences with G = 4: tiles of 16 sequences, a ragged third tile
+    w = workloads.llama3_f16(seed=22, n_seqs=40, ctx_lo=100, ctx_hi=300)
+    check(mt, w, [(0, 40, 5)])
+    check(mt, w, [(0, 17, 6), (20, 39, 2)])
+
+
+def test_cascade_smollm2_f32(mt):
+    # f32 (1e-4) through the three-product split, d = 64, G = 3 (padded to 4)
+    w = workloads.smollm2_f32(seed=23, n_seqs=9, ctx_lo=60, ctx_hi=300)
+    check(mt, w, [(0, 9, 3)])
+    check(mt, w, [(1, 4, 2), (5, 9, 4)])
+
+
+def test_cascade_q8_prefix_windows(mt):
+    # the q8_0 shared-prefix configuration, small: windows cut the prefix
+    w = workloads.llama3_q8_prefix(seed=24, n_seqs=20, prefix=320, suffix_lo=10, suffix_hi=90)
+    kp, vp = oracle_pools(w)
+    cow = om.order_moves(w.extra["cow_moves"])
+    om.copy_cells([kp, vp], cow)  # no partial block here: prefix % 32 == 0
+    assert not cow
+    groups = [(0, w.n_seqs, w.extra["prefix"] // w.block_size)]
+    # the generator's own tables already share the prefix blocks
+    t = w.block_table
+    assert (t[1:, :groups[0][2]] == t[0, :groups[0][2]]).all()
+    k_dev, v_dev = to_dev(kp), to_dev(vp)
+    want, want_lse = oracle_decode(w, kp, vp)
+    got, got_lse, st = cascade(mt, w, k_dev, v_dev, t, groups)
+    assert st == 0
+    assert_close(got, want, TOL["q8_0"], "q8_0 cascade")
+    assert_lse(got_lse, want_lse, TOL["q8_0"], "q8_0 cascade")
+    # and without windows
+    got, got_lse, st = cascade(mt, w, k_dev, v_dev, t, groups, spans=None)
+    assert st == 0
+    import dataclasses
+    want, want_lse = oracle_decode(dataclasses.replace(w, spans=None), kp, vp)
+    assert_close(got, want, TOL["q8_0"], "q8_0 cascade, no windows")
+
+
+@pytest.mark.parametrize("fmt,d,bs,hq,hkv", [("q8_0", 64, 16, 2, 2), ("q8_0", 128, 16, 16, 2),
+                                             ("f16", 64, 32, 8, 1), ("f32", 128, 32, 4, 4),
+                                             ("f16", 128, 16, 6, 2)])
+def test_cascade_shape_grid(mt, fmt, d, bs, hq, hkv):
+    w = workloads.llama3_f16(seed=25 + d + bs + hq, n_seqs=7, ctx_lo=20, ctx_hi=150, fmt=fmt,
+                             block_size=bs, n_heads=hq, n_kv_heads=hkv, head_dim=d)
+    check(mt, w, [(0, 7, 2)])
+
+
+def test_cascade_holes_in_prefix_and_fallback_shape(mt):
+    w = workloads.llama3_f16(seed=26, n_seqs=6, ctx_lo=120, ctx_hi=300)
+    t = w.block_table.copy()
+    t[:, 1] = -1  # a hole inside the shared prefix, in every sequence
+    check(mt, w, [(0, 6, 4)], table=t)
+    # head_dim 256 has no prefix kernel: the call runs the plain decode
+    w2 = workloads.longctx_f16_int4(seed=27, n_seqs=3, ctx=400)
+    check(mt, w2, [(0, 3, 5)])
+
+
+def test_cascade_broken_promise_is_flagged(mt):
+    w = workloads.llama3_f16(seed=28, n_seqs=5, ctx_lo=100, ctx_hi=200)
+    groups = [(0, 5, 3)]
+    t = share(w.block_table, groups)
+    t[3, 1] = w.block_table[3, 1] if w.block_table[3, 1] != t[0, 1] else t[0, 2]
+    kp, vp = oracle_pools(w)
+    _, _, st = cascade(mt, w, to_dev(kp), to_dev(vp), t, groups)
+    assert st == mt.MT_ERR_DEVICE_CHECK
+
+
+def test_cascade_rejects_bad_groups(mt):
+    w = workloads.llama3_f16(seed=29, n_seqs=4, ctx_lo=40, ctx_hi=60)
+    kp, vp = oracle_pools(w)
+    q = to_dev(w.q)
+    out = torch.zeros_like(q)
+    args = mt.paged_attn_args(w.fmt, q, to_dev(kp), to_dev(vp), to_dev(w.block_table),
+                              to_dev(w.context_lens), out, n_kv_heads=w.n_kv_heads,
+                              block_size=w.block_size, n_phys_blocks=w.n_phys_blocks,
+                              scale=w.scale)
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    for bad in ([(0, 3, 1), (2, 4, 1)], [(3, 2, 1)], [(0, 5, 1)], [(0, 2, -1)],
+                [(0, 1, 1)] * 65):
+        assert mt.mt_paged_attn_cascade_workspace_bytes(args, bad) == 0
+        with pytest.raises(mt.MtError):
+            mt.mt_paged_attn_decode_cascade(args, bad, ws)
