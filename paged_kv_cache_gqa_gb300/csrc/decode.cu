@@ -1321,16 +1321,50 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(const Params p) {
       o = p.casc.rec_o + (slot * kPrefixRows + Rc) * D;
     }
   };
+  // Per round of up to 32 partials: the (m, l) pairs (a lane each) and the
+  // output rows of the first KB partials are all requested before any is
+  // used, so a list of up to KB partials costs one L2 round trip. Every
+  // listed partial was written by its kernel (zeros where it saw nothing),
+  // so the loads need no validity test; weights of empty partials are 0.
+  constexpr int KB = DV >= 8 ? 8 : 16;
   for (int base = 0; base < NP; base += 32) {
     const int cnt = min(32, NP - base);
-    const int i = base + lane;
     float m = -INFINITY, l = 0.f;
     if (lane < cnt) {
       const float *mlp, *op;
-      part(i, mlp, op);
+      part(base + lane, mlp, op);
       const float2 ml = *reinterpret_cast<const float2 *>(mlp);
       m = ml.x;
       l = ml.y;
+    }
+    float v[KB][DV];
+#pragma unroll
+    for (int j = 0; j < KB; ++j) {
+      if (j < cnt) {
+        const float *mlp, *op;
+        part(base + j, mlp, op);
+        const float *src = op + lane * DV;
+        if constexpr (DV % 4 == 0) {
+#pragma unroll
+          for (int e = 0; e < DV; e += 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(src + e);
+            v[j][e] = x.x;
+            v[j][e + 1] = x.y;
+            v[j][e + 2] = x.z;
+            v[j][e + 3] = x.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < DV; e += 2) {
+            const float2 x = *reinterpret_cast<const float2 *>(src + e);
+            v[j][e] = x.x;
+            v[j][e + 1] = x.y;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < DV; ++e) v[j][e] = 0.f;
+      }
     }
     if (!(l > 0.f)) m = -INFINITY;
     float mc = m;
@@ -1347,35 +1381,27 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(const Params p) {
     M = m_new;
 #pragma unroll
     for (int e = 0; e < DV; ++e) acc[e] *= f_old;
-    // All loads of a batch of partials are issued before any is used, so
-    // a long list costs one L2 round trip per batch, not one per partial.
-    constexpr int KB = DV >= 8 ? 4 : 8;
-    for (int k0 = 0; k0 < cnt; k0 += KB) {
-      float v[KB][DV];
+#pragma unroll
+    for (int j = 0; j < KB; ++j) {
+      const float fk = __shfl_sync(kFull, f, j);
+#pragma unroll
+      for (int e = 0; e < DV; ++e) acc[e] = fmaf(fk, v[j][e], acc[e]);
+    }
+    // partials beyond the first KB of the round, KB at a time
+    for (int k0 = KB; k0 < cnt; k0 += KB) {
       float fk[KB];
 #pragma unroll
       for (int j = 0; j < KB; ++j) {
         fk[j] = __shfl_sync(kFull, f, (k0 + j) & 31);
-        if (k0 + j < cnt && fk[j] != 0.f) {
+        if (k0 + j < cnt) {
           const float *mlp, *op;
           part(base + k0 + j, mlp, op);
           const float *src = op + lane * DV;
-          if constexpr (DV % 4 == 0) {
 #pragma unroll
-            for (int e = 0; e < DV; e += 4) {
-              const float4 x = *reinterpret_cast<const float4 *>(src + e);
-              v[j][e] = x.x;
-              v[j][e + 1] = x.y;
-              v[j][e + 2] = x.z;
-              v[j][e + 3] = x.w;
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < DV; e += 2) {
-              const float2 x = *reinterpret_cast<const float2 *>(src + e);
-              v[j][e] = x.x;
-              v[j][e + 1] = x.y;
-            }
+          for (int e = 0; e < DV; e += 2) {
+            const float2 x = *reinterpret_cast<const float2 *>(src + e);
+            v[j][e] = x.x;
+            v[j][e + 1] = x.y;
           }
         } else {
           fk[j] = 0.f;

@@ -25,8 +25,11 @@
 //     the probability operand of that group;
 //   * f32 pools (1e-4): K and V become high/low f16 tile pairs and both
 //     products use three MMAs (hi.hi + lo.hi + hi.lo).
-// The block ring has three stages; every block is fetched once per tile, i.e.
-// once for all the sequences of the tile instead of once per sequence.
+// The block ring holds about 64 KB of staged blocks (6 q8_0, 4 f16, 3 f32
+// stages); each CTA reads its units' block ids into shared memory once, so
+// no global load sits between a stage's release and its next copy. Every
+// block is fetched once per tile, i.e. once for all the sequences of the tile
+// instead of once per sequence.
 #include <limits.h>
 #include <math.h>
 
@@ -45,8 +48,8 @@ namespace {
 constexpr unsigned kAll = 0xffffffffu;
 constexpr int kPWarps = kPrefixRows / 16;  // 4 consumer warps, 16 rows each
 constexpr int kPThreads = 32 * kPWarps;
-constexpr int kPStages = 3;
 constexpr int kMaxBs = 32;
+constexpr int kUnitChunk = 256;  // units whose block ids sit in shared memory at once
 
 template <int FMT, int D>
 struct PCfg {
@@ -59,10 +62,12 @@ struct PCfg {
   // d = 128 (136-byte slices) and 4-byte aligned when d = 64 (68 bytes)
   static constexpr int CH = FMT == MT_KV_Q8_0 ? (HB % 8 == 0 ? 8 : 4) : 16;
   static constexpr int RAW_STAGE = 2 * kMaxBs * RP;       // K and V
+  // ring depth: about 64 KB of staged blocks (f32 blocks are 32 KB)
+  static constexpr int STAGES = FMT == MT_KV_F32 ? 3 : FMT == MT_KV_F16 ? 4 : 6;
   static constexpr int N_TILES = FMT == MT_KV_F32 ? 4 : FMT == MT_KV_Q8_0 ? 2 : 0;
   static constexpr int TILE_BYTES = N_TILES * kMaxBs * TP;
   static constexpr int SCALE_BYTES = FMT == MT_KV_Q8_0 ? 2 * NG * kMaxBs * 4 : 0;
-  static constexpr int SMEM = kPStages * RAW_STAGE + TILE_BYTES + SCALE_BYTES;
+  static constexpr int SMEM = STAGES * RAW_STAGE + TILE_BYTES + SCALE_BYTES;
 };
 
 template <int CH>
@@ -82,47 +87,80 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // Physical block of unit u (its tile's leading sequence's table entry), or
-// -1 for a hole, an id out of range (flagged) or a unit past the end.
-__device__ __forceinline__ int unit_block(const PrefixParams &p, long long u, int &T, int &grp,
-                                          int &qt, int &kvh, int &b) {
+// -1 for a hole, an id out of range (flagged) or a unit past the end. Also
+// checks the group's promise for the sequence of the tile at `lane_seq`
+// (identical table entry), flagging a mismatch.
+__device__ __forceinline__ int unit_block(const PrefixParams &p, long long u, int lane_seq) {
+  int T, grp, qt, kvh, b;
   cascade_unit(p.c, p.Hkv, u, T, grp, qt, kvh, b);
   if (T < 0) return -1;
-  const int phys = p.table[(size_t)p.c.g[grp].s0 * p.max_blocks + b];
+  const PrefixGroup g = p.c.g[grp];
+  const int phys = p.table[(size_t)g.s0 * p.max_blocks + b];
+  const int s = g.s0 + qt * p.c.tq + lane_seq;
+  if (lane_seq > 0 && lane_seq < p.c.tq && s < g.s1 &&
+      p.table[(size_t)s * p.max_blocks + b] != phys)
+    report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
   if (phys == MT_INVALID_BLOCK_ID) return -1;
   if (phys < 0 || (long long)phys >= p.n_phys) {
-    if (threadIdx.x == 0) report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
+    report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
     return -1;
   }
   return phys;
 }
 
-// Issue the copies of unit u's K and V head slices into ring slot `slot`
-// (one commit group per call, empty for holes and units past the range).
-// Threads below the tile's sequence count also check that their sequence's
-// table holds the same block (the group's promise); mismatches are flagged.
+// Walks consecutive units without divisions: (tile, group, query tile, KV
+// head, block) of the current unit.
+struct UnitIter {
+  int T, grp, qt, kvh, b;
+  __device__ __forceinline__ void init(const PrefixParams &p, long long u) {
+    cascade_unit(p.c, p.Hkv, u, T, grp, qt, kvh, b);
+  }
+  __device__ __forceinline__ void next(const PrefixParams &p) {
+    if (++b < p.c.g[grp].nblk) return;
+    b = 0;
+    ++T;
+    if (++kvh < p.Hkv) return;
+    kvh = 0;
+    if (++qt < cascade_qtiles(p.c, grp)) return;
+    qt = 0;
+    // groups without a prefix have no units, but their tiles count in T
+    for (++grp; grp < p.c.n_groups && p.c.g[grp].nblk == 0; ++grp)
+      T += cascade_qtiles(p.c, grp) * p.Hkv;
+    if (grp >= p.c.n_groups) T = -1;
+  }
+};
+
+// Block ids of units [u0, u0 + n) into phys_s (n <= kUnitChunk + STAGES),
+// with the group checks spread over the CTA's threads.
+__device__ __forceinline__ void load_unit_blocks(const PrefixParams &p, long long u0, int n,
+                                                 long long u_end, int *phys_s) {
+  const int tq = p.c.tq;
+  for (int i = threadIdx.x; i < n * tq; i += blockDim.x) {
+    const int k = i / tq, j = i % tq;
+    const long long u = u0 + k;
+    const int ph = u < u_end ? unit_block(p, u, j) : -1;
+    if (j == 0) phys_s[k] = ph;
+  }
+}
+
+// Issue the copies of unit u's K and V head slices (block `phys`, -1: none)
+// into ring slot `slot`; one commit group per call, empty for holes and
+// units past the range.
 template <int FMT, int D>
-__device__ __forceinline__ void issue_unit(const PrefixParams &p, long long u, long long u_end,
+__device__ __forceinline__ void issue_unit(const PrefixParams &p, int kvh, int phys,
                                            uint8_t *ring, int slot) {
   using C = PCfg<FMT, D>;
-  if (u < u_end) {
-    int T, grp, qt, kvh, b;
-    const int phys = unit_block(p, u, T, grp, qt, kvh, b);
-    if (phys >= 0) {
-      const int s = p.c.g[grp].s0 + qt * p.c.tq + (int)threadIdx.x;
-      if ((int)threadIdx.x < p.c.tq && s < p.c.g[grp].s1 &&
-          p.table[(size_t)s * p.max_blocks + b] != phys)
-        report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
-      constexpr int PER_ROW = C::HB / C::CH;
-      const int n = p.bs * PER_ROW;
-      const uint32_t base = smem_u32(ring + (size_t)slot * C::RAW_STAGE);
-      const size_t cell0 = (size_t)phys * p.bs;
-      for (int i = threadIdx.x; i < n; i += kPThreads) {
-        const int r = i / PER_ROW, off = (i % PER_ROW) * C::CH;
-        const size_t g = (cell0 + r) * (size_t)p.row_bytes + (size_t)kvh * C::HB + off;
-        const uint32_t d = base + (uint32_t)(r * C::RP + off);
-        cp_async<C::CH>(d, p.k_pool + g);
-        cp_async<C::CH>(d + kMaxBs * C::RP, p.v_pool + g);
-      }
+  if (phys >= 0) {
+    constexpr int PER_ROW = C::HB / C::CH;
+    const int n = p.bs * PER_ROW;
+    const uint32_t base = smem_u32(ring + (size_t)slot * C::RAW_STAGE);
+    const size_t cell0 = (size_t)phys * p.bs;
+    for (int i = threadIdx.x; i < n; i += kPThreads) {
+      const int r = i / PER_ROW, off = (i % PER_ROW) * C::CH;
+      const size_t g = (cell0 + r) * (size_t)p.row_bytes + (size_t)kvh * C::HB + off;
+      const uint32_t d = base + (uint32_t)(r * C::RP + off);
+      cp_async<C::CH>(d, p.k_pool + g);
+      cp_async<C::CH>(d + kMaxBs * C::RP, p.v_pool + g);
     }
   }
   cp_async_commit();
@@ -182,10 +220,11 @@ __device__ __forceinline__ void convert_unit(const uint8_t *raw, uint8_t *tiles,
   using C = PCfg<FMT, D>;
   if constexpr (FMT == MT_KV_Q8_0) {
     // tiles: K codes, V codes; scales: [K|V][group][token]
-    const int n = 2 * bs * C::NG;
-    for (int i = threadIdx.x; i < n; i += kPThreads) {
-      const int kv = i / (bs * C::NG);
-      const int r = (i / C::NG) % bs;
+    const int n = bs * C::NG;  // (token, group) items of K, then of V
+    for (int i2 = threadIdx.x; i2 < 2 * n; i2 += kPThreads) {
+      const int kv = i2 >= n;
+      const int i = i2 - kv * n;
+      const int r = i / C::NG;  // NG is a power of two
       const int grp = i % C::NG;
       float *sc = scales + (kv * C::NG + grp) * kMaxBs + r;
       q8_convert_group(raw + kv * kMaxBs * C::RP + r * C::RP,
@@ -196,10 +235,11 @@ __device__ __forceinline__ void convert_unit(const uint8_t *raw, uint8_t *tiles,
   } else if constexpr (FMT == MT_KV_F32) {
     // tiles: K hi, K lo, V hi, V lo
     constexpr int Q4 = D / 4;
-    const int n = 2 * bs * Q4;
-    for (int i = threadIdx.x; i < n; i += kPThreads) {
-      const int kv = i / (bs * Q4);
-      const int r = (i / Q4) % bs;
+    const int n = bs * Q4;
+    for (int i2 = threadIdx.x; i2 < 2 * n; i2 += kPThreads) {
+      const int kv = i2 >= n;
+      const int i = i2 - kv * n;
+      const int r = i / Q4;
       const int e = (i % Q4) * 4;
       const float4 x =
           *reinterpret_cast<const float4 *>(raw + kv * kMaxBs * C::RP + r * C::RP + e * 4);
@@ -240,7 +280,7 @@ __global__ void __launch_bounds__(kPThreads, 2) prefix_kernel(const __grid_const
   constexpr int TQ = kPrefixRows / GP;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t *ring = smem;
-  uint8_t *tiles = smem + kPStages * C::RAW_STAGE;
+  uint8_t *tiles = smem + C::STAGES * C::RAW_STAGE;
   float *scales = reinterpret_cast<float *>(tiles + C::TILE_BYTES);
   pdl_enter();
 
@@ -251,8 +291,22 @@ __global__ void __launch_bounds__(kPThreads, 2) prefix_kernel(const __grid_const
   if (u_beg >= u_end) return;
   const int bs = p.bs;
 
+  constexpr int S = C::STAGES;
+  // block ids of units [chunk0, chunk0 + kUnitChunk + S), refilled as the
+  // loop walks the range (the copies run S-1 units ahead)
+  __shared__ int phys_s[kUnitChunk + S];
+  long long chunk0 = u_beg;
+  load_unit_blocks(p, chunk0, (int)min((long long)kUnitChunk + S, u_end - chunk0), u_end, phys_s);
+  __syncthreads();
+  auto phys_of = [&](long long u) { return u < u_end ? phys_s[u - chunk0] : -1; };
+  UnitIter cur, ahead;  // the unit being computed, the next one to copy
+  cur.init(p, u_beg);
+  ahead = cur;
 #pragma unroll
-  for (int i = 0; i < kPStages - 1; ++i) issue_unit<FMT, D>(p, u_beg + i, u_end, ring, i);
+  for (int i = 0; i < S - 1; ++i) {
+    issue_unit<FMT, D>(p, ahead.kvh, phys_of(u_beg + i), ring, i);
+    if (u_beg + i + 1 < u_end) ahead.next(p);
+  }
 
   uint32_t qh[KS][4], ql[KS][4];
   float o[ND][4];
@@ -288,13 +342,21 @@ __global__ void __launch_bounds__(kPThreads, 2) prefix_kernel(const __grid_const
   };
 
   for (long long u = u_beg; u < u_end; ++u) {
-    const int slot = (int)((u - u_beg) % kPStages);
-    cp_async_wait<kPStages - 2>();
+    const int slot = (int)((u - u_beg) % S);
+    cp_async_wait<S - 2>();
     __syncthreads();  // unit u staged by every thread; unit u-1 finished by every warp
-    issue_unit<FMT, D>(p, u + kPStages - 1, u_end, ring, (slot + kPStages - 1) % kPStages);
+    if (u - chunk0 == kUnitChunk) {
+      // the next chunk of block ids (units already issued are re-read: same values)
+      chunk0 = u;
+      load_unit_blocks(p, chunk0, (int)min((long long)kUnitChunk + S, u_end - chunk0), u_end,
+                       phys_s);
+      __syncthreads();
+    }
+    issue_unit<FMT, D>(p, ahead.kvh, phys_of(u + S - 1), ring, (slot + S - 1) % S);
+    if (u + S < u_end) ahead.next(p);
 
-    int T, grp, qt, kvh, b;
-    cascade_unit(p.c, p.Hkv, u, T, grp, qt, kvh, b);
+    if (u > u_beg) cur.next(p);
+    const int T = cur.T, grp = cur.grp, qt = cur.qt, kvh = cur.kvh, b = cur.b;
     if (T != cur_T) {
       if (cur_T >= 0) flush();
       cur_T = rec_T = T;
@@ -356,8 +418,7 @@ __global__ void __launch_bounds__(kPThreads, 2) prefix_kernel(const __grid_const
       }
     }
 
-    const int phys = p.table[(size_t)p.c.g[grp].s0 * p.max_blocks + b];
-    if (phys < 0 || (long long)phys >= p.n_phys) continue;  // hole (or flagged id)
+    if (phys_s[u - chunk0] < 0) continue;  // hole (or flagged id)
     const int pos0 = b * bs;
     // rows of this warp with no position in the block skip the math
     const bool any = __any_sync(kAll, (lo_r[0] < pos0 + bs && hi_r[0] > pos0) ||
@@ -385,45 +446,72 @@ __global__ void __launch_bounds__(kPThreads, 2) prefix_kernel(const __grid_const
                                             : tiles + 2 * kMaxBs * C::TP;
     const int NT = bs / 8;
 
-    // ---- S = Q.K^T (base-2 logits), 8 tokens per n-tile
+    // ---- S = Q.K^T (base-2 logits), 8 tokens per n-tile; per 32 dims the
+    // B fragments of all n-tiles are fetched first, then the MMAs of the
+    // n-tiles interleave (independent accumulators)
     float sc[4][4];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-      if (nt >= NT) continue;
-      const uint32_t ka = smem_u32(kt + (nt * 8 + (lane & 7)) * C::TP) + (lane >> 3) * 16;
+    for (int nt = 0; nt < 4; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+    const uint32_t ka = smem_u32(kt + (lane & 7) * C::TP) + (lane >> 3) * 16;
 #pragma unroll
-      for (int k2 = 0; k2 < D / 32; ++k2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(ka + k2 * 64, b0, b1, b2, b3);
-        if constexpr (FMT == MT_KV_F16) {
-          mma_f16(sc[nt], qh[2 * k2], b0, b1);
-          mma_f16(sc[nt], ql[2 * k2], b0, b1);
-          mma_f16(sc[nt], qh[2 * k2 + 1], b2, b3);
-          mma_f16(sc[nt], ql[2 * k2 + 1], b2, b3);
-        } else if constexpr (FMT == MT_KV_Q8_0) {
-          // one 32-dim group: its own accumulator, then times the scale
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_f16(acc, qh[2 * k2], b0, b1);
-          mma_f16(acc, ql[2 * k2], b0, b1);
-          mma_f16(acc, qh[2 * k2 + 1], b2, b3);
-          mma_f16(acc, ql[2 * k2 + 1], b2, b3);
-          const float2 d =
-              *reinterpret_cast<const float2 *>(scales + k2 * kMaxBs + nt * 8 + 2 * c4);
-          sc[nt][0] = fmaf(d.x, acc[0], sc[nt][0]);
-          sc[nt][1] = fmaf(d.y, acc[1], sc[nt][1]);
-          sc[nt][2] = fmaf(d.x, acc[2], sc[nt][2]);
-          sc[nt][3] = fmaf(d.y, acc[3], sc[nt][3]);
-        } else {
-          uint32_t l0, l1, l2, l3;
-          ldsm_x4(ka + k2 * 64 + kMaxBs * C::TP, l0, l1, l2, l3);
-          mma_f16(sc[nt], qh[2 * k2], b0, b1);
-          mma_f16(sc[nt], ql[2 * k2], b0, b1);
-          mma_f16(sc[nt], qh[2 * k2], l0, l1);
-          mma_f16(sc[nt], qh[2 * k2 + 1], b2, b3);
-          mma_f16(sc[nt], ql[2 * k2 + 1], b2, b3);
-          mma_f16(sc[nt], qh[2 * k2 + 1], l2, l3);
+    for (int k2 = 0; k2 < D / 32; ++k2) {
+      uint32_t bf[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+        if (nt < NT) ldsm_x4(ka + nt * 8 * C::TP + k2 * 64, bf[nt][0], bf[nt][1], bf[nt][2], bf[nt][3]);
+      if constexpr (FMT == MT_KV_F16) {
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+          if (nt < NT) {
+            mma_f16(sc[nt], qh[2 * k2], bf[nt][0], bf[nt][1]);
+            mma_f16(sc[nt], qh[2 * k2 + 1], bf[nt][2], bf[nt][3]);
+          }
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+          if (nt < NT) {
+            mma_f16(sc[nt], ql[2 * k2], bf[nt][0], bf[nt][1]);
+            mma_f16(sc[nt], ql[2 * k2 + 1], bf[nt][2], bf[nt][3]);
+          }
+      } else if constexpr (FMT == MT_KV_Q8_0) {
+        // one 32-dim group: its own accumulators, then times the scales
+        float acc[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+          if (nt < NT) {
+            mma_f16(acc[nt], qh[2 * k2], bf[nt][0], bf[nt][1]);
+            mma_f16(acc[nt], qh[2 * k2 + 1], bf[nt][2], bf[nt][3]);
+          }
         }
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+          if (nt < NT) {
+            mma_f16(acc[nt], ql[2 * k2], bf[nt][0], bf[nt][1]);
+            mma_f16(acc[nt], ql[2 * k2 + 1], bf[nt][2], bf[nt][3]);
+          }
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+          if (nt < NT) {
+            const float2 d =
+                *reinterpret_cast<const float2 *>(scales + k2 * kMaxBs + nt * 8 + 2 * c4);
+            sc[nt][0] = fmaf(d.x, acc[nt][0], sc[nt][0]);
+            sc[nt][1] = fmaf(d.y, acc[nt][1], sc[nt][1]);
+            sc[nt][2] = fmaf(d.x, acc[nt][2], sc[nt][2]);
+            sc[nt][3] = fmaf(d.y, acc[nt][3], sc[nt][3]);
+          }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+          if (nt < NT) {
+            uint32_t l0, l1, l2, l3;
+            ldsm_x4(ka + nt * 8 * C::TP + k2 * 64 + kMaxBs * C::TP, l0, l1, l2, l3);
+            mma_f16(sc[nt], qh[2 * k2], bf[nt][0], bf[nt][1]);
+            mma_f16(sc[nt], qh[2 * k2 + 1], bf[nt][2], bf[nt][3]);
+            mma_f16(sc[nt], ql[2 * k2], bf[nt][0], bf[nt][1]);
+            mma_f16(sc[nt], ql[2 * k2 + 1], bf[nt][2], bf[nt][3]);
+            mma_f16(sc[nt], qh[2 * k2], l0, l1);
+            mma_f16(sc[nt], qh[2 * k2 + 1], l2, l3);
+          }
       }
     }
 
