@@ -163,6 +163,62 @@ mt_status mt_paged_attn_decode_append(const mt_paged_attn_args *args, const floa
                                       const float *v_new, void *workspace,
                                       size_t workspace_bytes, mt_stream stream);
 
+/* Runs per query of a set-valued (kv_map) window. The pages name the limit
+ * KV_MAP_MAX_SPANS without a value; this library fixes 8. */
+#define MT_KV_MAP_MAX_SPANS 8
+
+/* Arguments of multi-query (prefill) paged attention. Device pointers unless
+ * stated; all arrays dense, row-major. */
+typedef struct {
+  mt_kv_format fmt;
+  const float *q;               /* [n_tokens][n_heads][head_dim] float32, the
+                                   queries of all sequences, sequence-major      */
+  const void *k_pool;           /* as mt_paged_attn_args (the queries' own K/V
+                                   rows already stored)                          */
+  const void *v_pool;
+  const int32_t *block_table;   /* [n_seqs][max_blocks]                          */
+  const int32_t *context_lens;  /* [n_seqs], the queries' positions included     */
+  const int32_t *q_start;       /* [n_seqs + 1]: sequence s owns query rows
+                                   q_start[s] .. q_start[s+1]-1; its n queries sit
+                                   at positions ctx - n .. ctx - 1               */
+  const int32_t *spans;         /* [n_tokens][2] per-query [lo, hi), or NULL     */
+  const int32_t *kv_map;        /* [n_tokens][MT_KV_MAP_MAX_SPANS][2] per-query
+                                   (start, len) runs (len <= 0: unused), or NULL;
+                                   at most one of spans / kv_map                 */
+  float *out;                   /* [n_tokens][n_heads][head_dim] float32         */
+  float *lse;                   /* [n_tokens][n_heads] natural log, or NULL      */
+  int n_seqs;
+  int n_tokens;                 /* rows of q / out                               */
+  int n_heads;
+  int n_kv_heads;
+  int head_dim;
+  int block_size;
+  int max_blocks;
+  int64_t n_phys_blocks;
+  float scale;
+} mt_paged_prefill_args;
+
+/* Workspace bytes mt_paged_attn_prefill needs (its first 4 bytes are the
+ * device status word; zero them once after allocating). */
+size_t mt_paged_prefill_workspace_bytes(const mt_paged_prefill_args *args);
+
+/* Multi-query (prefill, or chunked prefill) attention through the paged
+ * cache. "Tiered KV cache — architecture", section "Kernel dispatch"
+ * (per-sequence context and query lengths) and "The paged-attention block
+ * model" (holes read as -infinity); "KV Cache Design — cells, format,
+ * sessions", section 1 (causal positions, one [lo, hi) window or kv_map runs
+ * per query, read as logical positions). For query row i of sequence s,
+ * j = i - q_start[s], position p = ctx - n + j:
+ *   out[i][h] = sum_t softmax_t(scale * q[i][h] . k_t) v_t over the positions
+ *   t <= p, t < ctx, not in a hole, inside the query's window;
+ *   lse[i][h] = log sum_t exp(scale * q . k_t). No valid t: out 0, lse -inf.
+ * Shapes built: head_dim 64 or 128, block_size 16 or 32, n_heads/n_kv_heads
+ * <= 8, n_kv_heads <= 8 (others MT_ERR_UNSUPPORTED). Out-of-range block ids,
+ * query counts above the context length and query rows outside
+ * [0, n_tokens) are skipped and flagged in the workspace status word. */
+mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *args, void *workspace,
+                                size_t workspace_bytes, mt_stream stream);
+
 /* A group of consecutive sequences whose block tables start with the same
  * n_prefix_blocks physical block ids: a prompt prefix shared through
  * refcounted blocks ("Tiered KV cache — architecture", section "The

@@ -40,6 +40,21 @@ class mt_move(ctypes.Structure):
     _fields_ = [("src", ctypes.c_int64), ("dst", ctypes.c_int64), ("len", ctypes.c_int64)]
 
 
+MT_KV_MAP_MAX_SPANS = 8
+
+
+class mt_paged_prefill_args(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int), ("q", ctypes.c_void_p), ("k_pool", ctypes.c_void_p),
+                ("v_pool", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+                ("context_lens", ctypes.c_void_p), ("q_start", ctypes.c_void_p),
+                ("spans", ctypes.c_void_p), ("kv_map", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("n_seqs", ctypes.c_int),
+                ("n_tokens", ctypes.c_int), ("n_heads", ctypes.c_int),
+                ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("block_size", ctypes.c_int), ("max_blocks", ctypes.c_int),
+                ("n_phys_blocks", ctypes.c_int64), ("scale", ctypes.c_float)]
+
+
 class mt_prefix_group(ctypes.Structure):
     _fields_ = [("seq_begin", ctypes.c_int32), ("seq_end", ctypes.c_int32),
                 ("n_prefix_blocks", ctypes.c_int32)]
@@ -76,6 +91,8 @@ def lib() -> ctypes.CDLL:
         "mt_paged_attn_decode": (I, [ctypes.POINTER(mt_paged_attn_args), P, SZ, P]),
         "mt_paged_attn_decode_append": (I, [ctypes.POINTER(mt_paged_attn_args), P, P, P, SZ, P]),
         "mt_paged_attn_decode_static": (I, [ctypes.POINTER(mt_paged_attn_args), U32P, P]),
+        "mt_paged_prefill_workspace_bytes": (SZ, [ctypes.POINTER(mt_paged_prefill_args)]),
+        "mt_paged_attn_prefill": (I, [ctypes.POINTER(mt_paged_prefill_args), P, SZ, P]),
         "mt_paged_attn_cascade_workspace_bytes": (SZ, [ctypes.POINTER(mt_paged_attn_args),
                                                        ctypes.POINTER(mt_prefix_group), I]),
         "mt_paged_attn_decode_cascade": (I, [ctypes.POINTER(mt_paged_attn_args),
@@ -194,6 +211,40 @@ def mt_paged_attn_decode_append(args: mt_paged_attn_args, k_new, v_new, workspac
     _check(lib().mt_paged_attn_decode_append(ctypes.byref(args), _ptr(k_new), _ptr(v_new),
                                              _ptr(workspace), nbytes, _stream(stream)),
            "mt_paged_attn_decode_append")
+
+
+def prefill_args(fmt, q, k_pool, v_pool, block_table, context_lens, q_start, out, *,
+                 n_kv_heads, block_size, n_phys_blocks, scale, spans=None, kv_map=None,
+                 lse=None):
+    """Arguments of mt_paged_attn_prefill from device tensors: q [n_tokens][Hq][d],
+    q_start int32 [n_seqs + 1], spans [n_tokens][2] or kv_map
+    [n_tokens][MT_KV_MAP_MAX_SPANS][2] (optional)."""
+    n_tok, Hq, D = q.shape
+    a = mt_paged_prefill_args()
+    a.fmt = _fmt(fmt)
+    a.q, a.k_pool, a.v_pool = _ptr(q), _ptr(k_pool), _ptr(v_pool)
+    a.block_table, a.context_lens, a.q_start = _ptr(block_table), _ptr(context_lens), _ptr(q_start)
+    a.spans, a.kv_map = _ptr(spans), _ptr(kv_map)
+    a.out, a.lse = _ptr(out), _ptr(lse)
+    a.n_seqs = int(context_lens.numel())
+    a.n_tokens, a.n_heads, a.n_kv_heads, a.head_dim = n_tok, Hq, n_kv_heads, D
+    a.block_size = block_size
+    a.max_blocks = int(block_table.shape[1]) if block_table.dim() == 2 else 0
+    a.n_phys_blocks = int(n_phys_blocks)
+    a.scale = float(scale)
+    a._tensors = (q, k_pool, v_pool, block_table, context_lens, q_start, spans, kv_map, out, lse)
+    return a
+
+
+def mt_paged_prefill_workspace_bytes(args: mt_paged_prefill_args) -> int:
+    return int(lib().mt_paged_prefill_workspace_bytes(ctypes.byref(args)))
+
+
+def mt_paged_attn_prefill(args: mt_paged_prefill_args, workspace, stream=None) -> None:
+    """Multi-query (prefill) attention through the paged cache."""
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().mt_paged_attn_prefill(ctypes.byref(args), _ptr(workspace), nbytes,
+                                       _stream(stream)), "mt_paged_attn_prefill")
 
 
 def _groups_array(groups):
