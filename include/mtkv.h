@@ -93,6 +93,10 @@ mt_status mt_kv_store(mt_kv_format fmt, void *k_pool, void *v_pool, int64_t n_ce
                       const int64_t *cells, int n_rows, uint32_t *status, mt_stream stream);
 
 /* Arguments of paged decode attention (one query token per sequence). */
+/* Runs per query of a set-valued (kv_map) window. The pages name the limit
+ * KV_MAP_MAX_SPANS without a value; this library fixes 8. */
+#define MT_KV_MAP_MAX_SPANS 8
+
 typedef struct {
   mt_kv_format fmt;
   const float *q;              /* device float32 [n_seqs][n_heads][head_dim]        */
@@ -113,6 +117,10 @@ typedef struct {
   int64_t n_phys_blocks;
   float scale;                 /* softmax scale applied to q.k                        */
   int n_ctas;                  /* 0 = one persistent CTA per SM; >0 forces the split  */
+  const int32_t *kv_map;       /* [n_seqs][MT_KV_MAP_MAX_SPANS][2] set-valued window:
+                                  (start, len) runs of logical positions per query
+                                  (len <= 0: unused run), or NULL. The third window
+                                  mode: at most one of spans / kv_map.                */
 } mt_paged_attn_args;
 
 /* Workspace bytes mt_paged_attn_decode needs for `args` (0 on invalid args).
@@ -128,8 +136,10 @@ size_t mt_paged_attn_workspace_bytes(const mt_paged_attn_args *args);
  * block_table[s][p/bs]*bs + p%bs of each pool) and "Kernel dispatch"
  * (block table, context lengths; MT_INVALID_BLOCK_ID positions get logit
  * -infinity, so zero weight). "KV Cache Design — cells, format, sessions",
- * section 1: the optional window [lo, hi) of each query, read as logical
- * positions intersected with [0, context_len).
+ * section 1: the optional window of each query — one [lo, hi) pair
+ * (spans) or a set of (start, len) runs (kv_map) — read as logical
+ * positions intersected with [0, context_len). spans and kv_map together
+ * are MT_ERR_INVALID_ARG.
  * For each sequence s and query head h (KV head h / (n_heads/n_kv_heads)):
  *   out[s][h] = sum_p softmax_p(scale * q[s][h] . k_p) v_p over the valid
  *   positions p; lse[s][h] = log sum_p exp(scale * q . k_p) (natural log).
@@ -162,10 +172,6 @@ mt_status mt_paged_attn_decode(const mt_paged_attn_args *args, void *workspace,
 mt_status mt_paged_attn_decode_append(const mt_paged_attn_args *args, const float *k_new,
                                       const float *v_new, void *workspace,
                                       size_t workspace_bytes, mt_stream stream);
-
-/* Runs per query of a set-valued (kv_map) window. The pages name the limit
- * KV_MAP_MAX_SPANS without a value; this library fixes 8. */
-#define MT_KV_MAP_MAX_SPANS 8
 
 /* Arguments of multi-query (prefill) paged attention. Device pointers unless
  * stated; all arrays dense, row-major. */
@@ -252,7 +258,7 @@ size_t mt_paged_attn_cascade_workspace_bytes(const mt_paged_attn_args *args,
  *             being undefined.
  * Shapes the prefix kernel is not built for (head_dim 256) run the ordinary
  * decode. Errors as mt_paged_attn_decode, plus MT_ERR_INVALID_ARG for bad or
- * overlapping groups. */
+ * overlapping groups and MT_ERR_UNSUPPORTED for kv_map windows. */
 mt_status mt_paged_attn_decode_cascade(const mt_paged_attn_args *args,
                                        const mt_prefix_group *groups, int n_groups,
                                        void *workspace, size_t workspace_bytes, mt_stream stream);

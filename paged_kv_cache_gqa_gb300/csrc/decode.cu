@@ -41,6 +41,7 @@
 #include "internal.h"
 #include "prefix.h"
 
+#include <limits.h>
 #include <math.h>
 
 #include <algorithm>
@@ -64,6 +65,7 @@ struct StageInfo {
   int r0;     // first valid row of the block (relative to the block)
   int r1;     // one past the last valid row
   int flags;  // F_* bits | (first block row held by the stage) << 8
+  int mask;   // valid rows of the block as bits (bit t: block row t), within [r0, r1)
 };
 
 struct Params {
@@ -75,6 +77,7 @@ struct Params {
   const int32_t *table;
   const int32_t *ctx;
   const int32_t *spans;
+  const int32_t *kv_map;  // [B][MT_KV_MAP_MAX_SPANS][2] (start, len) runs, or null
   float *out;
   float *lse;
   float *part_o;       // [P][Hq][D] unnormalised partial outputs
@@ -111,6 +114,15 @@ __host__ __device__ constexpr int scratch_floats_per_warp() {
   return 32 * GP + GP;  // p[32 tokens][GP] and alpha[GP]
 }
 
+// Block rows [a, b) as bits (0 <= a, b <= 32; empty when b <= a).
+__device__ __forceinline__ uint32_t row_bits(int a, int b) {
+  a = max(a, 0);
+  b = min(b, 32);
+  if (b <= a) return 0u;
+  const uint32_t upto = b >= 32 ? 0xffffffffu : ((1u << b) - 1u);
+  return upto & ~((1u << a) - 1u);
+}
+
 __device__ __forceinline__ int seq_window(const Params &p, int s, int &lo, int &hi) {
   int c = p.ctx[s];
   const int cmax = p.max_blocks * p.bs;
@@ -123,6 +135,23 @@ __device__ __forceinline__ int seq_window(const Params &p, int s, int &lo, int &
   if (p.spans) {
     lo = max(p.spans[2 * s], 0);
     hi = min(p.spans[2 * s + 1], c);
+  } else if (p.kv_map) {
+    // set-valued window: stream the span of its runs; the producer masks
+    // the positions between them
+    int rl = INT_MAX, rh = INT_MIN;
+#pragma unroll
+    for (int r = 0; r < MT_KV_MAP_MAX_SPANS; ++r) {
+      const int a = max(p.kv_map[((size_t)s * MT_KV_MAP_MAX_SPANS + r) * 2], 0);
+      const int e = min(p.kv_map[((size_t)s * MT_KV_MAP_MAX_SPANS + r) * 2] +
+                            p.kv_map[((size_t)s * MT_KV_MAP_MAX_SPANS + r) * 2 + 1],
+                        c);
+      if (e > a) {
+        rl = min(rl, a);
+        rh = max(rh, e);
+      }
+    }
+    lo = rl;
+    hi = rh;
   }
   // cascade: the shared prefix is read by the prefix kernel, not here
   if (p.casc.n_groups) lo = max(lo, cascade_skip(p.casc, s, p.bs));
@@ -273,6 +302,7 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
       return;
     }
     int seq, r0, r1, flags, base;
+    uint32_t mask;
     {
       const volatile int *vi = reinterpret_cast<const volatile int *>(&infos[slot]);
       seq = vi[0];
@@ -280,6 +310,7 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
       r1 = vi[2];
       flags = vi[3] & 0xff;
       base = vi[3] >> 8;
+      mask = (uint32_t)vi[4];
     }
     if (flags & F_EXIT) return;
 
@@ -308,16 +339,17 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
       const uint32_t vst = kst + p.blk_pad;
       uint8_t *vst_ptr = ring + (size_t)slot * 2 * p.blk_pad + p.blk_pad;
       const int row_end = base + p.rows;
-      // Rows of the stage outside [r0, r1) hold bytes of other positions: P
+      // Rows of the stage outside its mask hold bytes of other positions: P
       // is 0 there but 0 * NaN would not be, so clear this head's V chunks of
       // those rows (all 8 units of a chunk, so the swizzle does not matter).
       bool wrote = false;
-      if (r0 > base || r1 < row_end) {
+      const uint32_t bad = row_bits(base, row_end) & ~mask;
+      if (bad) {
         constexpr int V16 = D * 2 / 16;  // 16-byte pieces of one head row
-        const int n_bad = (r0 - base) + (row_end - r1);
+        const int n_bad = __popc(bad);
         for (int i = lane; i < n_bad * V16; i += 32) {
           const int k = i / V16;
-          const int row = k < r0 - base ? k : r1 - base + (k - (r0 - base));
+          const int row = (int)__fns(bad, 0, k + 1) - base;  // stage row of the k-th bad row
           const int line = row * p.ncb + (head_e >> 6) + (i % V16) / 8;
           *reinterpret_cast<uint4 *>(vst_ptr + (size_t)line * 128 + (i % 8) * 16) =
               make_uint4(0, 0, 0, 0);
@@ -345,8 +377,8 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
         }
         const int tk = t0 + 2 * c;
         const float s0 = acc[0] + acc[2], s1 = acc[1] + acc[3];
-        pr[t][0] = (row_ok && tk >= r0 && tk < r1) ? s0 : -INFINITY;
-        pr[t][1] = (row_ok && tk + 1 >= r0 && tk + 1 < r1) ? s1 : -INFINITY;
+        pr[t][0] = (row_ok && ((mask >> tk) & 1u)) ? s0 : -INFINITY;
+        pr[t][1] = (row_ok && ((mask >> (tk + 1)) & 1u)) ? s1 : -INFINITY;
         mloc = fmaxf(mloc, fmaxf(pr[t][0], pr[t][1]));
       }
       // ---- online softmax (base 2) per head: the 4 lanes of group g agree
@@ -458,14 +490,14 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
 // keeps every ldmatrix phase conflict-free.
 template <int D>
 __device__ __forceinline__ void q8_tile(const uint8_t *st, int row_bytes, int seg, int t0,
-                                        int r0, int r1, uint8_t *tile, int lane) {
+                                        uint32_t mask, uint8_t *tile, int lane) {
   constexpr int GPR = D / 4;      // 4-value groups per head row
   constexpr int TP = 2 * D + 16;  // tile pitch in bytes
   for (int idx = lane; idx < 16 * GPR; idx += 32) {
     const int tr = idx / GPR, grp = idx % GPR;
     const int tok = t0 + tr;
     uint2 out = make_uint2(0u, 0u);
-    if (tok >= r0 && tok < r1) {
+    if ((mask >> tok) & 1u) {
       const uint8_t *a = st + (size_t)tok * row_bytes + seg + (grp >> 3) * 34 + 2 + (grp & 7) * 4;
       const uint32_t w = ((uint32_t)*reinterpret_cast<const uint16_t *>(a) |
                           ((uint32_t)*reinterpret_cast<const uint16_t *>(a + 2) << 16)) ^
@@ -527,6 +559,7 @@ __device__ __forceinline__ void consume_mma_q8(const Params &p, uint64_t *full, 
       return;
     }
     int seq, r0, r1, flags, base;
+    uint32_t mask;
     {
       const volatile int *vi = reinterpret_cast<const volatile int *>(&infos[slot]);
       seq = vi[0];
@@ -534,6 +567,7 @@ __device__ __forceinline__ void consume_mma_q8(const Params &p, uint64_t *full, 
       r1 = vi[2];
       flags = vi[3] & 0xff;
       base = vi[3] >> 8;
+      mask = (uint32_t)vi[4];
     }
     if (flags & F_EXIT) return;
 
@@ -568,7 +602,7 @@ __device__ __forceinline__ void consume_mma_q8(const Params &p, uint64_t *full, 
         const int t0 = 16 * h;
         pr[2 * h][0] = pr[2 * h][1] = pr[2 * h + 1][0] = pr[2 * h + 1][1] = -INFINITY;
         if (t0 >= p.bs || t0 + 16 <= r0 || t0 >= r1) continue;
-        q8_tile<D>(kst, p.row_bytes, seg, t0, r0, r1, tk, lane);
+        q8_tile<D>(kst, p.row_bytes, seg, t0, mask, tk, lane);
         __syncwarp();
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -586,8 +620,8 @@ __device__ __forceinline__ void consume_mma_q8(const Params &p, uint64_t *full, 
             s0 = fmaf(q8_scale(kst, p.row_bytes, seg, tk0, grp), acc[0] + acc[2], s0);
             s1 = fmaf(q8_scale(kst, p.row_bytes, seg, tk0 + 1, grp), acc[1] + acc[3], s1);
           }
-          pr[2 * h + t][0] = (row_ok && tk0 >= r0 && tk0 < r1) ? s0 : -INFINITY;
-          pr[2 * h + t][1] = (row_ok && tk0 + 1 >= r0 && tk0 + 1 < r1) ? s1 : -INFINITY;
+          pr[2 * h + t][0] = (row_ok && ((mask >> tk0) & 1u)) ? s0 : -INFINITY;
+          pr[2 * h + t][1] = (row_ok && ((mask >> (tk0 + 1)) & 1u)) ? s1 : -INFINITY;
           mloc = fmaxf(mloc, fmaxf(pr[2 * h + t][0], pr[2 * h + t][1]));
         }
         __syncwarp();
@@ -623,13 +657,13 @@ __device__ __forceinline__ void consume_mma_q8(const Params &p, uint64_t *full, 
       for (int h = 0; h < 2; ++h) {
         const int t0 = 16 * h;
         if (t0 >= p.bs || t0 + 16 <= r0 || t0 >= r1) continue;
-        q8_tile<D>(vst, p.row_bytes, seg, t0, r0, r1, tv, lane);
+        q8_tile<D>(vst, p.row_bytes, seg, t0, mask, tv, lane);
         __syncwarp();
         const uint32_t vaddr = smem_u32(tv + (((lane >> 4) & 1) * 8 + (lane & 7)) * TP) +
                                (uint32_t)((lane >> 3) & 1) * 16;
         const int ta = t0 + 2 * c, tb = t0 + 8 + 2 * c;  // this thread's B rows (tokens)
-        const bool va0 = ta >= r0 && ta < r1, va1 = ta + 1 >= r0 && ta + 1 < r1;
-        const bool vb0 = tb >= r0 && tb < r1, vb1 = tb + 1 >= r0 && tb + 1 < r1;
+        const bool va0 = (mask >> ta) & 1u, va1 = (mask >> (ta + 1)) & 1u;
+        const bool vb0 = (mask >> tb) & 1u, vb1 = (mask >> (tb + 1)) & 1u;
 #pragma unroll
         for (int grp = 0; grp < NG; ++grp) {
           const float pa0 = va0 ? pr[2 * h][0] * q8_scale(vst, p.row_bytes, seg, ta, grp) : 0.f;
@@ -755,6 +789,20 @@ __device__ __noinline__ void append_row(const Params &p, int s, long long cell, 
   __syncwarp();
 }
 
+// Set-valued window: the rows of logical block lb of sequence s that one of
+// its (start, len) runs covers, within the sequence's window [lo, hi); lane r
+// of the calling warp takes run r. Kept out of line: only kv_map calls pay.
+__device__ __noinline__ uint32_t kv_map_block_mask(const Params &p, int s, int lb, int lo, int hi,
+                                                   int lane) {
+  uint32_t m = 0u;
+  if (lane < MT_KV_MAP_MAX_SPANS) {
+    const int32_t *rp = p.kv_map + ((size_t)s * MT_KV_MAP_MAX_SPANS + lane) * 2;
+    const int a = max(rp[0], lo), e = min(rp[0] + rp[1], hi);
+    m = row_bits(a - lb * p.bs, e - lb * p.bs);
+  }
+  return __reduce_or_sync(kFull, m);
+}
+
 // Position ctx-1 of sequence s, for decode with append: its logical block,
 // or -1 when the context length is out of range (flagged) or zero.
 __device__ __forceinline__ int append_block(const Params &p, int s) {
@@ -770,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
   uint64_t *empty = full + kMaxStages;
   StageInfo *infos = reinterpret_cast<StageInfo *>(smem + 64);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 128);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 192);
   float *scratch = reinterpret_cast<float *>(smem + kHdrBytes);
   // the ring starts on a 1024-byte boundary (the 128-byte swizzle's period)
   uint8_t *ring = smem + kHdrBytes + p.scratch_bytes;
@@ -832,7 +880,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
     bool alive = true;
     // Publish one stage. Lane 0 waits for the slot and issues; the others
     // learn the outcome through the shuffle.
-    auto emit = [&](int flags, int s, int r0, int r1, int phys, int base) -> bool {
+    auto emit = [&](int flags, int s, int r0, int r1, int phys, int base,
+                    uint32_t mask) -> bool {
       const int slot = (int)(it % (uint32_t)S);
       const uint32_t round = it / (uint32_t)S;
       int okv = 1;
@@ -841,7 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
                                                     p.wait_ns))
           okv = 0;
         if (okv) {
-          infos[slot] = StageInfo{s, r0, r1, flags | (base << 8)};
+          infos[slot] = StageInfo{s, r0, r1, flags | (base << 8), (int)mask};
           if ((flags & F_DATA) && p.use_tmap) {
             // the whole stage (rows [base, base + rows)) in two tensor copies
             uint8_t *dk = ring + (size_t)slot * 2 * p.blk_pad;
@@ -936,9 +985,21 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
               }
               const int r0 = max(lo - lb * p.bs, 0);
               const int r1 = min(hi - lb * p.bs, p.bs);
+              uint32_t bmask = row_bits(r0, r1);
+              if (p.kv_map) {
+                bmask &= kv_map_block_mask(p, s, lb, lo, hi, lane);
+                if (!bmask) continue;  // no run reaches into this block
+              }
               for (int c0 = (r0 / p.rows) * p.rows; c0 < r1; c0 += p.rows) {
+                // consumers read only the stage's rows, so a whole-block stage
+                // carries the block mask as it is
+                uint32_t cmask = bmask;
+                if (p.rows < p.bs) {
+                  cmask &= row_bits(c0, c0 + p.rows);
+                  if (!cmask) continue;
+                }
                 if (!emit(F_DATA | (first ? F_NEW : 0), s, max(r0, c0), min(r1, c0 + p.rows),
-                          phys, c0)) {
+                          phys, c0, cmask)) {
                   alive = false;
                   break;
                 }
@@ -947,13 +1008,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
               if (!alive) break;
             }
           }
-          if (alive && !emit(F_END | (first ? F_NEW : 0), s, 0, 0, -1, 0)) alive = false;
+          if (alive && !emit(F_END | (first ? F_NEW : 0), s, 0, 0, -1, 0, 0u)) alive = false;
           x = seg_hi;
         }
         start += nb;
       }
     }
-    if (alive) alive = emit(F_EXIT, 0, 0, 0, -1, 0);
+    if (alive) alive = emit(F_EXIT, 0, 0, 0, -1, 0, 0u);
     if (!alive) {
       // Stop: flag the others, then let every copy already issued land in
       // shared memory before this warp (and so the CTA) can retire.
@@ -1019,6 +1080,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
     }
     struct {
       int seq, r0, r1, flags, base;
+      uint32_t mask;
     } inf;
     {
       const volatile int *vi = reinterpret_cast<const volatile int *>(&infos[slot]);
@@ -1027,6 +1089,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
       inf.r1 = vi[2];
       inf.flags = vi[3] & 0xff;
       inf.base = vi[3] >> 8;
+      inf.mask = (uint32_t)vi[4];
     }
     if (inf.flags & F_EXIT) break;
     const int seq = inf.seq;
@@ -1124,7 +1187,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
           }
         }
         halve<GP, C::LPT / 2>(acc, j);
-        const bool valid = tok >= r0 && tok < r1 && hidx < G;
+        const bool valid = ((inf.mask >> tok) & 1u) && hidx < G;
         const float sc = valid ? acc[0] : -INFINITY;
         if (rep0) p_s[tok * GP + hidx] = sc;
         mloc = fmaxf(mloc, sc);
@@ -1162,6 +1225,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
         if (st >= nsteps) break;
         const int ta = max(st * C::TPS, r0), tb = min(st * C::TPS + C::TPS, r1);
         for (int tok = ta; tok < tb; ++tok) {
+          if (!((inf.mask >> tok) & 1u)) continue;  // between kv_map runs
           float pg[GP];
           if constexpr (GP == 1) {
             pg[0] = p_s[tok];
@@ -1451,6 +1515,9 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
     return fail(MT_ERR_INVALID_ARG, "paged decode: negative or zero size");
   if (a->n_heads % a->n_kv_heads)
     return fail(MT_ERR_INVALID_ARG, "paged decode: n_heads must be a multiple of n_kv_heads");
+  if (a->spans && a->kv_map)
+    return fail(MT_ERR_INVALID_ARG,
+                "paged decode: spans and kv_map are two window modes: pass at most one");
   if (a->head_dim != 64 && a->head_dim != 128 && a->head_dim != 256)
     return fail(MT_ERR_UNSUPPORTED, "paged decode: head_dim must be 64, 128 or 256");
   if (a->block_size != 16 && a->block_size != 32)
@@ -1637,6 +1704,7 @@ mt_status fill_params(Params &prm, const mt_paged_attn_args *a, const Plan &pl, 
   prm.table = a->block_table;
   prm.ctx = a->context_lens;
   prm.spans = a->spans;
+  prm.kv_map = a->kv_map;
   prm.out = a->out;
   prm.lse = a->lse;
   prm.status = status;
@@ -1741,6 +1809,8 @@ mt_status cascade_plan(const mt_paged_attn_args *a, const Plan &pl,
   if (n_groups > kMaxPrefixGroups)
     return fail(MT_ERR_UNSUPPORTED, "cascade decode: at most 64 prefix groups");
   if (n_groups > 0 && !groups) return fail(MT_ERR_INVALID_ARG, "cascade decode: null groups");
+  if (n_groups > 0 && a->kv_map)
+    return fail(MT_ERR_UNSUPPORTED, "cascade decode: kv_map windows are not supported");
   std::vector<std::pair<int, int>> spans;
   for (int i = 0; i < n_groups; ++i) {
     const mt_prefix_group &g = groups[i];

@@ -68,7 +68,8 @@ class mt_paged_attn_args(ctypes.Structure):
                 ("n_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("block_size", ctypes.c_int),
                 ("max_blocks", ctypes.c_int), ("n_phys_blocks", ctypes.c_int64),
-                ("scale", ctypes.c_float), ("n_ctas", ctypes.c_int)]
+                ("scale", ctypes.c_float), ("n_ctas", ctypes.c_int),
+                ("kv_map", ctypes.c_void_p)]
 
 
 _lib = None
@@ -174,7 +175,8 @@ def mt_kv_store(fmt, k_pool, v_pool, n_kv_heads, head_dim, k_new, v_new, cells,
 
 
 def paged_attn_args(fmt, q, k_pool, v_pool, block_table, context_lens, out, *, n_kv_heads,
-                    block_size, n_phys_blocks, scale, spans=None, lse=None, n_ctas=0):
+                    block_size, n_phys_blocks, scale, spans=None, lse=None, n_ctas=0,
+                    kv_map=None):
     B, Hq, D = q.shape
     a = mt_paged_attn_args()
     a.fmt = _fmt(fmt)
@@ -189,7 +191,8 @@ def paged_attn_args(fmt, q, k_pool, v_pool, block_table, context_lens, out, *, n
     a.scale = float(scale)
     a.n_ctas = int(n_ctas)
     # the struct holds raw addresses: keep the tensors alive as long as it is
-    a._tensors = (q, k_pool, v_pool, block_table, context_lens, out, spans, lse)
+    a.kv_map = _ptr(kv_map)
+    a._tensors = (q, k_pool, v_pool, block_table, context_lens, out, spans, lse, kv_map)
     return a
 
 
