@@ -63,6 +63,16 @@ def _peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _tensor_peak():
+    """Dense f16/bf16 tensor peak (same rate on this part): the measured
+    burst figure for kernels timed alone."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (bf16 burst; f16 same rate)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def max_over_ranks(x: float, world: int, device=None) -> float:
     """The largest value of x over all ranks (x itself when running alone)."""
     if world <= 1:
@@ -321,6 +331,18 @@ def run_gpu(args, rank, world, local_rank):
     assert mtkv.mt_check_device_status(status) == 0, mtkv.mt_last_error()
     assert mtkv.mt_check_device_status(ws) == 0, mtkv.mt_last_error()
 
+    graph = None
+    if args.graph:
+        # the whole L-layer step as one CUDA graph (every kernel was
+        # configured by the warm-up steps; the calls neither allocate nor
+        # synchronise)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert mtkv.mt_check_device_status(ws) == 0, mtkv.mt_last_error()
+
     clocks = Clocks(local_rank)
     barrier(world)
     torch.cuda.synchronize()
@@ -331,6 +353,9 @@ def run_gpu(args, rank, world, local_rank):
     dec_ms = []
     t0.record(stream)
     for _ in range(args.steps):
+        if graph is not None:
+            graph.replay()
+            continue
         step(record=True)
         # per-call decode durations of this step (read back after the run)
         dec_ms.append([e for e in ev])
@@ -341,6 +366,14 @@ def run_gpu(args, rank, world, local_rank):
     clk = clocks.stop()
     barrier(world)
     total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    if graph is not None:
+        # per-call durations for the roofline from a few eager steps
+        for _ in range(3):
+            step(record=True)
+            dec_ms.append([e for e in ev])
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(n_layers)]
+        torch.cuda.synchronize()
     dec_times = [a.elapsed_time(b) for st in dec_ms for (a, b) in st]
 
     dbytes, toks = decode_bytes(w)
@@ -381,10 +414,19 @@ def run_gpu(args, rank, world, local_rank):
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
+    run_e2e = e2e_step
+    if args.graph:
+        # the copies from and to pinned host memory are captured with the step
+        g_e2e = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_e2e):
+            e2e_step()
+        run_e2e = g_e2e.replay
+        run_e2e()
+        torch.cuda.synchronize()
     barrier(world)
     e0 = time.perf_counter()
     for _ in range(e2e_steps):
-        e2e_step()
+        run_e2e()
     torch.cuda.synchronize()
     e2e_s = max_over_ranks((time.perf_counter() - e0) / e2e_steps, world, dev)
     assert mtkv.mt_check_device_status(status) == 0, mtkv.mt_last_error()
@@ -410,6 +452,8 @@ def run_gpu(args, rank, world, local_rank):
                    "n_seqs": B, "attended_tokens_per_layer": toks,
                    "store": ("fused into the decode launch" if fused else
                              "separate mt_kv_store launch"),
+                   "launch": ("one CUDA graph per 32-layer step" if args.graph else
+                              "eager launches (programmatic dependent launch)"),
                    "l2": "inputs larger than L2 (1.3 GB of K/V per layer, 42 GB per step)",
                    "parallelism": f"replicas x{world}"},
         "frac_of_peak": round(value / peak, 4),
@@ -603,6 +647,58 @@ def run_extra(args, rank, world, local_rank):
                                      "(mt_paged_attn_decode_cascade)" if cascade else
                                      "per-sequence decode (mt_paged_attn_decode)")},
                "clocks": clk}
+    elif args.workload == "prefill_f16":
+        # chunked prefill through the paged cache: 16 sequences at context
+        # 2048 whose last 512 positions are the queries (their K/V rows
+        # already stored), Llama-3-8B-shaped heads, f16 pools; 8 layers with
+        # their own pools, so successive calls do not hit in L2
+        w = workloads.llama3_f16(seed=SEED + 9, n_seqs=16, ctx_lo=2048, ctx_hi=2048, hist=False)
+        n_q = 512
+        layers, _, rb = _decode_setup(mtkv, w, 8, dev, g)
+        table = torch.from_numpy(w.block_table).to(dev)
+        ctx_d = torch.from_numpy(w.context_lens).to(dev)
+        q_start = torch.arange(0, n_q * w.n_seqs + 1, n_q, dtype=torch.int32, device=dev)
+        calls = []
+        for kp, vp, _a, _kn in layers:
+            q = torch.randn(n_q * w.n_seqs, w.n_heads, w.head_dim, generator=g, device=dev)
+            out = torch.empty_like(q)
+            a = mtkv.prefill_args("f16", q, kp, vp, table, ctx_d, q_start, out,
+                                  n_kv_heads=w.n_kv_heads, block_size=w.block_size,
+                                  n_phys_blocks=w.n_phys_blocks, scale=w.scale)
+            calls.append(a)
+        ws = torch.zeros(mtkv.mt_paged_prefill_workspace_bytes(calls[0]), dtype=torch.uint8,
+                         device=dev)
+
+        def step():
+            for a in calls:
+                mtkv.mt_paged_attn_prefill(a, ws)
+
+        clocks.start()
+        ms = _gpu_time(step, steps, warmup, stream)
+        clk = clocks.stop()
+        assert mtkv.mt_check_device_status(ws) == 0, mtkv.mt_last_error()
+        # each query j (position ctx - n + j) reads j + ctx - n + 1 positions;
+        # per (query, head, position): q.k and p.v, 2 * head_dim MACs
+        ctx0 = int(w.context_lens[0])
+        pairs = w.n_seqs * sum(ctx0 - n_q + j + 1 for j in range(n_q))
+        flop = 4.0 * pairs * w.n_heads * w.head_dim
+        kv_bytes = 2 * int(w.context_lens.sum()) * w.n_kv_heads * w.head_dim * 2
+        tflops = len(calls) * flop / (ms * 1e-3) / 1e12
+        tpeak = _tensor_peak()
+        res = {"metric": "paged prefill attention TFLOP/s (f16 operands, f32 accumulate)",
+               "value": round(tflops, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+               "ms_per_call": round(ms / len(calls), 5),
+               "query_tokens_per_s": round(len(calls) * n_q * w.n_seqs / (ms * 1e-3), 1),
+               "roofline": {"bound": "tensor", "achieved": round(tflops, 2),
+                            "peak": tpeak[0], "peak_kind": tpeak[1], "unit": "TFLOP/s",
+                            "frac": round(tflops / tpeak[0], 4),
+                            "note": "useful FLOPs (4 * pairs * heads * head_dim); the kernel "
+                                    "also multiplies the low half of q and padding rows"},
+               "kv_GB_per_s": round(len(calls) * kv_bytes / (ms * 1e-3) / 1e9, 1),
+               "config": {"workload": "llama3-8b-shaped f16 chunked prefill: 16 seqs x ctx "
+                                      "2048, last 512 positions as queries, 32/8 heads, "
+                                      "head_dim 128, bs 16, 8 layers"},
+               "clocks": clk}
     elif args.workload == "longctx_int4":
         w = workloads.longctx_f16_int4(hist=False)
         table = workloads.retarget_cold(w)
@@ -667,7 +763,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="oracle baseline budget; 0 skips it (profiling runs)")
     ap.add_argument("--workload", default="llama3_f16",
-                    choices=["llama3_f16", "smollm2_f32", "q8_prefix", "longctx_int4"],
+                    choices=["llama3_f16", "smollm2_f32", "q8_prefix", "longctx_int4",
+                             "prefill_f16"],
                     help="llama3_f16 is the benchmark line; the others measure the other kernels")
     ap.add_argument("--store", default="fused", choices=["fused", "separate"],
                     help="store each layer's new row inside the decode launch "
@@ -675,6 +772,8 @@ def main():
     ap.add_argument("--prefix", default="cascade", choices=["cascade", "plain"],
                     help="q8_prefix workload: decode the shared prefix once per group "
                          "(mt_paged_attn_decode_cascade) or per sequence")
+    ap.add_argument("--graph", action=argparse.BooleanOptionalAction, default=True,
+                    help="replay the L-layer step as one captured CUDA graph")
     ap.add_argument("--layers", type=int, default=N_LAYERS,
                     help="layers per step; fewer than 32 only for profiling captures")
     args = ap.parse_args()
