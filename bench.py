@@ -481,10 +481,18 @@ def run_gpu(args, rank, world, local_rank):
 # `--workload` selects one of the other synthetic configurations to measure the
 # remaining kernels on GB300; the default line is the Llama-3 f16 step above.
 
-def _gpu_time(fn, steps, warmup, stream):
+def _gpu_time(fn, steps, warmup, stream, graph=False):
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
+    if graph:
+        # time replays of `fn` captured as one CUDA graph
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        g.replay()
+        torch.cuda.synchronize()
+        fn = g.replay
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
@@ -567,11 +575,14 @@ def run_extra(args, rank, world, local_rank):
 
         def step():
             for kp, vp, a, kn in layers:
-                mtkv.mt_kv_store("f32", kp, vp, w.n_kv_heads, w.head_dim, kn, kn, cells)
-                mtkv.mt_paged_attn_decode(a, ws)
+                if args.store == "fused":
+                    mtkv.mt_paged_attn_decode_append(a, kn, kn, ws)
+                else:
+                    mtkv.mt_kv_store("f32", kp, vp, w.n_kv_heads, w.head_dim, kn, kn, cells)
+                    mtkv.mt_paged_attn_decode(a, ws)
 
         clocks.start()
-        ms = _gpu_time(step, steps, warmup, stream)
+        ms = _gpu_time(step, steps, warmup, stream, graph=args.graph)
         ub, lb_, toks = _window_bytes(w, w.head_dim * 4)
         step_bytes = w.n_layers * (ub + store_bytes(w))
         value = step_bytes / (ms * 1e-3) / 1e9
@@ -602,7 +613,8 @@ def run_extra(args, rank, world, local_rank):
                "ms_per_step": round(ms, 4), "frac_of_peak": round(value / peak, 4),
                "attended_tokens_per_s": round(w.n_layers * toks / (ms * 1e-3), 1),
                "config": {"workload": "smollm2-135m-shaped f32 paged decode: 30 layers, 8 seqs, "
-                                      "ctx U[2048,8192], 9/3 heads, head_dim 64, bs 16"},
+                                      "ctx U[2048,8192], 9/3 heads, head_dim 64, bs 16",
+                          "store": args.store, "graph": bool(args.graph)},
                "relayout": {"what": "grow 64->8192, 30 layers x kv_dim 192 f32, K and V",
                             "ms": round(g_ms, 4), "bytes": g_bytes,
                             "GB/s": round(g_bytes / (g_ms * 1e-3) / 1e9, 1),
@@ -631,7 +643,7 @@ def run_extra(args, rank, world, local_rank):
                     mtkv.mt_paged_attn_decode(a, ws)
 
         clocks.start()
-        ms = _gpu_time(step, steps, warmup, stream)
+        ms = _gpu_time(step, steps, warmup, stream, graph=args.graph)
         clk = clocks.stop()
         ub, lb_, toks = _window_bytes(w, (w.head_dim // 32) * 34)
         value = 32 * (ub + store_bytes(w)) / (ms * 1e-3) / 1e9

@@ -101,6 +101,7 @@ struct Params {
   int n_cw;      // consumer warps = Hkv * wph
   int n_ctas;
   float qscale;  // softmax scale * log2(e)
+  int combine_wps;  // combine warps per (sequence, query head): 1, 2, 4 or 8
   uint64_t wait_ns;
   Cascade casc;  // shared-prefix groups (n_groups == 0: plain decode)
 };
@@ -1348,10 +1349,15 @@ template <int D>
 __global__ void __launch_bounds__(256) splitk_combine_kernel(const Params p) {
   constexpr int DV = D / 32;
   pdl_enter();
-  const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (w >= p.B * p.Hq) return;
-  const int s = w / p.Hq, h = w % p.Hq;
+  // With few (s, h) pairs, wps warps share one pair's partial list (each a
+  // contiguous share) and merge their results through shared memory.
+  __shared__ float red_s[8][2 + D];
+  const int wps = p.combine_wps;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = blockIdx.x * (8 / wps) + warp / wps;
+  const int kw = warp % wps;
+  const bool live = w < p.B * p.Hq;
+  const int s = live ? w / p.Hq : 0, h = live ? w % p.Hq : 0;
   const int T = p.seq_start[p.B];
   const int beg = p.seq_start[s], end = p.seq_start[s + 1];
   const int per = T > 0 ? (T + p.n_ctas - 1) / p.n_ctas : 1;
@@ -1373,8 +1379,11 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(const Params p) {
       NPc = (int)((u0 + p.casc.g[gi].nblk - 1) / p.casc.per) - cc0 + 1;
     }
   }
-  const int NP = NPd + NPc;
+  const int NP_all = live ? NPd + NPc : 0;
+  const int i_beg = kw * NP_all / wps, i_end = (kw + 1) * NP_all / wps;
+  const int NP = i_end - i_beg;
   auto part = [&](int i, const float *&ml, const float *&o) {
+    i += i_beg;
     if (i < NPd) {
       const size_t P = ((size_t)c0 + i / p.n_sub + s) * p.n_sub + i % p.n_sub;
       ml = p.part_ml + (P * p.Hq + h) * 2;
@@ -1479,6 +1488,35 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(const Params p) {
         for (int e = 0; e < DV; ++e) acc[e] = fmaf(fk[j], v[j][e], acc[e]);
     }
   }
+  if (wps > 1) {
+    if (lane == 0) {
+      red_s[warp][0] = M;
+      red_s[warp][1] = L;
+    }
+#pragma unroll
+    for (int e = 0; e < DV; ++e) red_s[warp][2 + lane * DV + e] = acc[e];
+    __syncthreads();
+    if (kw == 0) {
+      float Mx = -INFINITY;
+      for (int i = 0; i < wps; ++i)
+        if (red_s[warp + i][1] > 0.f) Mx = fmaxf(Mx, red_s[warp + i][0]);
+      L = 0.f;
+#pragma unroll
+      for (int e = 0; e < DV; ++e) acc[e] = 0.f;
+      if (Mx != -INFINITY) {
+        for (int i = 0; i < wps; ++i) {
+          const float li = red_s[warp + i][1];
+          if (!(li > 0.f)) continue;
+          const float f = exp2f(red_s[warp + i][0] - Mx);
+          L = fmaf(f, li, L);
+#pragma unroll
+          for (int e = 0; e < DV; ++e) acc[e] = fmaf(f, red_s[warp + i][2 + lane * DV + e], acc[e]);
+        }
+      }
+      M = Mx;
+    }
+  }
+  if (!live || kw != 0) return;
   float *dst = p.out + ((size_t)s * p.Hq + h) * D + lane * DV;
   const bool any = L > 0.f;
   const float inv = any ? 1.f / L : 0.f;
@@ -1596,8 +1634,8 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
   pl->rows = rows;
   pl->blk_pad = pad;
   pl->stages = stages;
-  pl->n_ctas = n_ctas;
   pl->smem = fixed + stages * 2 * pl->blk_pad;
+  pl->n_ctas = n_ctas;
   const size_t P = ((size_t)n_ctas + (size_t)a->n_seqs) * pl->n_sub;
   auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
   pl->ws_status = 0;
@@ -1620,6 +1658,10 @@ mt_status launch_decode(const Params &prm, const Plan &pl, cudaStream_t s) {
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem),
         "cudaFuncSetAttribute(decode smem)");
     if (st != MT_OK) return st;
+    st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared),
+                    "cudaFuncSetAttribute(decode carveout)");
+    if (st != MT_OK) return st;
     configured_dev = dev;
     configured_smem = pl.smem;
   }
@@ -1627,7 +1669,7 @@ mt_status launch_decode(const Params &prm, const Plan &pl, cudaStream_t s) {
       launch_pdl(kern, dim3(pl.n_ctas), dim3(32 * (pl.n_cw + 1)), pl.smem, s, prm),
       "paged decode launch");
   if (st != MT_OK) return st;
-  const int warps = prm.B * prm.Hq;
+  const int warps = prm.B * prm.Hq * prm.combine_wps;
   if (warps > 0) {
     st = cuda_check(launch_pdl(splitk_combine_kernel<D>, dim3((warps + 7) / 8), dim3(256), 0, s,
                                prm),
@@ -1735,6 +1777,13 @@ mt_status fill_params(Params &prm, const mt_paged_attn_args *a, const Plan &pl, 
   prm.n_ctas = pl.n_ctas;
   prm.qscale = a->scale * 1.4426950408889634f;
   prm.wait_ns = kWaitLimitNs;
+  // about 2048 combine warps: small batches split each pair's partial list
+  {
+    const long long pairs = (long long)a->n_seqs * a->n_heads;
+    int wps = 1;
+    while (wps < 8 && pairs * wps < 2048) wps *= 2;
+    prm.combine_wps = wps;
+  }
   if (prm.use_tmap) {
     const long long n_cells = (long long)a->n_phys_blocks * a->block_size;
     const size_t rb = (size_t)prm.row_bytes;
