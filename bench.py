@@ -634,13 +634,20 @@ def run_extra(args, rank, world, local_rank):
             ws = torch.zeros(mtkv.mt_paged_attn_cascade_workspace_bytes(layers[0][2], groups),
                              dtype=torch.uint8, device=dev)
 
+        fused = args.store == "fused"
+
         def step():
             for kp, vp, a, kn in layers:
-                mtkv.mt_kv_store("q8_0", kp, vp, w.n_kv_heads, w.head_dim, kn, kn, cells)
-                if cascade:
-                    mtkv.mt_paged_attn_decode_cascade(a, groups, ws)
+                if fused and cascade:
+                    mtkv.mt_paged_attn_decode_cascade_append(a, groups, kn, kn, ws)
+                elif fused:
+                    mtkv.mt_paged_attn_decode_append(a, kn, kn, ws)
                 else:
-                    mtkv.mt_paged_attn_decode(a, ws)
+                    mtkv.mt_kv_store("q8_0", kp, vp, w.n_kv_heads, w.head_dim, kn, kn, cells)
+                    if cascade:
+                        mtkv.mt_paged_attn_decode_cascade(a, groups, ws)
+                    else:
+                        mtkv.mt_paged_attn_decode(a, ws)
 
         clocks.start()
         ms = _gpu_time(step, steps, warmup, stream, graph=args.graph)
@@ -657,7 +664,8 @@ def run_extra(args, rank, world, local_rank):
                                       "windows, 32/8 heads, head_dim 128, bs 32",
                           "prefix": ("cascade: shared blocks read once per group "
                                      "(mt_paged_attn_decode_cascade)" if cascade else
-                                     "per-sequence decode (mt_paged_attn_decode)")},
+                                     "per-sequence decode (mt_paged_attn_decode)"),
+                          "store": args.store, "graph": bool(args.graph)},
                "clocks": clk}
     elif args.workload == "prefill_f16":
         # chunked prefill through the paged cache: 16 sequences at context
@@ -778,9 +786,11 @@ def main():
                     choices=["llama3_f16", "smollm2_f32", "q8_prefix", "longctx_int4",
                              "prefill_f16"],
                     help="llama3_f16 is the benchmark line; the others measure the other kernels")
-    ap.add_argument("--store", default="fused", choices=["fused", "separate"],
+    ap.add_argument("--store", default=None, choices=["fused", "separate"],
                     help="store each layer's new row inside the decode launch "
-                         "(mt_paged_attn_decode_append) or with its own mt_kv_store launch")
+                         "(mt_paged_attn_decode_append) or with its own mt_kv_store launch; "
+                         "default: fused for f32/f16 pools, separate for q8_0 (whose "
+                         "quantiser would run on the copy-issuing warp)")
     ap.add_argument("--prefix", default="cascade", choices=["cascade", "plain"],
                     help="q8_prefix workload: decode the shared prefix once per group "
                          "(mt_paged_attn_decode_cascade) or per sequence")
@@ -789,6 +799,8 @@ def main():
     ap.add_argument("--layers", type=int, default=N_LAYERS,
                     help="layers per step; fewer than 32 only for profiling captures")
     args = ap.parse_args()
+    if args.store is None:
+        args.store = "separate" if args.workload == "q8_prefix" else "fused"
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))

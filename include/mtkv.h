@@ -263,6 +263,17 @@ mt_status mt_paged_attn_decode_cascade(const mt_paged_attn_args *args,
                                        const mt_prefix_group *groups, int n_groups,
                                        void *workspace, size_t workspace_bytes, mt_stream stream);
 
+/* mt_paged_attn_decode_cascade with each sequence's new K/V row stored
+ * into the cell of position context_lens[s]-1 in the same call, exactly as
+ * mt_paged_attn_decode_append does it (see there). The appended block must
+ * lie outside the group's shared prefix (copy on write first), so only the
+ * suffix decode reads it. */
+mt_status mt_paged_attn_decode_cascade_append(const mt_paged_attn_args *args,
+                                              const mt_prefix_group *groups, int n_groups,
+                                              const float *k_new, const float *v_new,
+                                              void *workspace, size_t workspace_bytes,
+                                              mt_stream stream);
+
 /* Bytes of the scratch array built into the library for
  * mt_paged_attn_decode_static (8 MiB per device that loads the library). */
 #define MT_STATIC_SCRATCH_BYTES ((size_t)8 << 20)

@@ -804,6 +804,42 @@ __device__ __noinline__ uint32_t kv_map_block_mask(const Params &p, int s, int l
   return __reduce_or_sync(kFull, m);
 }
 
+// Part `part` of `n_parts` of the work of append_row (q8_0: 32-value groups
+// part, part + n_parts, ...; f16/f32: 4-value chunks likewise), for rows that
+// no CTA reads in this launch, so no ordering with any copy is needed.
+template <int FMT, int D>
+__device__ __noinline__ void append_row_part(const Params &p, int s, long long cell, int lane,
+                                             int part, int n_parts) {
+  const int n = p.Hkv * D;
+#pragma unroll 1
+  for (int kv = 0; kv < 2; ++kv) {
+    const float *src = (kv ? p.v_new : p.k_new) + (size_t)s * n;
+    uint8_t *dst = const_cast<uint8_t *>(kv ? p.v_pool : p.k_pool) + (size_t)cell * p.row_bytes;
+    if constexpr (FMT == MT_KV_Q8_0) {
+      const int groups = n / 32;
+#pragma unroll 1
+      for (int g = part; g < groups; g += n_parts)
+        q8_quant_group(dst + (size_t)g * 34, src[g * 32 + lane], lane);
+      const int pad = p.row_bytes - groups * 34;
+      if (part == 0 && lane < pad) dst[groups * 34 + lane] = 0;
+    } else {
+#pragma unroll 1
+      for (int i = 4 * lane + 128 * part; i < n; i += 128 * n_parts) {
+        const float4 x = *reinterpret_cast<const float4 *>(src + i);
+        if constexpr (FMT == MT_KV_F32) {
+          *reinterpret_cast<float4 *>(dst + (size_t)i * 4) = x;
+        } else {
+          const __half2 a = __floats2half2_rn(x.x, x.y);
+          const __half2 b = __floats2half2_rn(x.z, x.w);
+          *reinterpret_cast<uint2 *>(dst + (size_t)i * 2) =
+              make_uint2(*reinterpret_cast<const uint32_t *>(&a),
+                         *reinterpret_cast<const uint32_t *>(&b));
+        }
+      }
+    }
+  }
+}
+
 // Position ctx-1 of sequence s, for decode with append: its logical block,
 // or -1 when the context length is out of range (flagged) or zero.
 __device__ __forceinline__ int append_block(const Params &p, int s) {
@@ -857,25 +893,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
     const int per = total > 0 ? (total + (int)gridDim.x - 1) / (int)gridDim.x : 0;
     const long long b0 = (long long)blockIdx.x * per;
     const long long b1 = min((long long)total, b0 + per);
-
-    if (p.k_new) {
-      // Appended rows outside every window are read by no CTA: CTA s mod
-      // grid writes them now. The others are written below, by the CTA whose
-      // range loads their block, just before it issues that block's copy.
-      for (int s = blockIdx.x; s < p.B; s += gridDim.x) {
-        const int lb = append_block(p, s);
-        if (lb < 0) continue;
-        int lo, hi;
-        const int nb = seq_window(p, s, lo, hi);
-        if (nb > 0 && lb >= lo / p.bs && lb < lo / p.bs + nb) continue;
-        const int phys = p.table[(size_t)s * p.max_blocks + lb];
-        if (phys < 0 || (long long)phys >= p.n_phys) {
-          if (lane == 0) report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
-          continue;
-        }
-        append_row<FMT, D>(p, s, (long long)phys * p.bs + (p.ctx[s] - 1) % p.bs, lane);
-      }
-    }
 
     uint32_t it = 0;
     bool alive = true;
@@ -1035,6 +1052,26 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
   }
 
   if (warp >= p.n_cw) return;
+  if (p.k_new) {
+    // Appended rows outside every window are read by no CTA: the consumer
+    // warps of CTA s mod grid write them while the first stages load. The
+    // others are written by the producer of the CTA whose range loads their
+    // block, just before it issues that block's copy.
+    for (int s = blockIdx.x; s < p.B; s += gridDim.x) {
+      const int lb = append_block(p, s);
+      if (lb < 0) continue;
+      int lo, hi;
+      const int nb = seq_window(p, s, lo, hi);
+      if (nb > 0 && lb >= lo / p.bs && lb < lo / p.bs + nb) continue;
+      const int phys = p.table[(size_t)s * p.max_blocks + lb];
+      if (phys < 0 || (long long)phys >= p.n_phys) {
+        if (warp == 0 && lane == 0) report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
+        continue;
+      }
+      append_row_part<FMT, D>(p, s, (long long)phys * p.bs + (p.ctx[s] - 1) % p.bs, lane, warp,
+                              p.n_cw);
+    }
+  }
   if constexpr (MMA && FMT == MT_KV_Q8_0 && D <= 128) {
     consume_mma_q8<D, GP>(p, full, empty, infos, abort_flag, ring, smem + kHdrBytes, warp, lane);
   } else if constexpr (MMA) {
@@ -1919,10 +1956,37 @@ extern "C" size_t mt_paged_attn_cascade_workspace_bytes(const mt_paged_attn_args
   return cp.total;
 }
 
+namespace mtkv {
+namespace {
+mt_status cascade_decode(const mt_paged_attn_args *a, const mt_prefix_group *groups, int n_groups,
+                         const float *k_new, const float *v_new, void *workspace,
+                         size_t workspace_bytes, mt_stream stream);
+}  // namespace
+}  // namespace mtkv
+
 extern "C" mt_status mt_paged_attn_decode_cascade(const mt_paged_attn_args *a,
                                                   const mt_prefix_group *groups, int n_groups,
                                                   void *workspace, size_t workspace_bytes,
                                                   mt_stream stream) {
+  return cascade_decode(a, groups, n_groups, nullptr, nullptr, workspace, workspace_bytes, stream);
+}
+
+extern "C" mt_status mt_paged_attn_decode_cascade_append(const mt_paged_attn_args *a,
+                                                         const mt_prefix_group *groups,
+                                                         int n_groups, const float *k_new,
+                                                         const float *v_new, void *workspace,
+                                                         size_t workspace_bytes,
+                                                         mt_stream stream) {
+  if (!k_new || !v_new)
+    return fail(MT_ERR_INVALID_ARG, "cascade decode with append: null new rows");
+  return cascade_decode(a, groups, n_groups, k_new, v_new, workspace, workspace_bytes, stream);
+}
+
+namespace mtkv {
+namespace {
+mt_status cascade_decode(const mt_paged_attn_args *a, const mt_prefix_group *groups, int n_groups,
+                         const float *k_new, const float *v_new, void *workspace,
+                         size_t workspace_bytes, mt_stream stream) {
   Plan pl;
   mt_status st = make_plan(a, &pl, true);
   if (st != MT_OK) return st;
@@ -1939,10 +2003,16 @@ extern "C" mt_status mt_paged_attn_decode_cascade(const mt_paged_attn_args *a,
       !aligned16(workspace))
     return fail(MT_ERR_INVALID_ARG,
                 "cascade decode: q, pools, out and workspace must be 16-byte aligned");
+  if ((k_new && !aligned16(k_new)) || (v_new && !aligned16(v_new)))
+    return fail(MT_ERR_INVALID_ARG, "cascade decode with append: new rows must be 16-byte aligned");
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   Params prm;
   st = fill_params(prm, a, pl, ws, reinterpret_cast<uint32_t *>(ws + pl.ws_status));
   if (st != MT_OK) return st;
+  // the new rows land in private suffix blocks, which only the suffix decode
+  // reads (the prefix kernel reads shared blocks only)
+  prm.k_new = k_new;
+  prm.v_new = v_new;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cp.use) {
     Cascade &c = cp.c;
@@ -1977,6 +2047,8 @@ extern "C" mt_status mt_paged_attn_decode_cascade(const mt_paged_attn_args *a,
   st = dispatch(prm, pl, a->fmt, s);
   return st == MT_OK ? ok() : st;
 }
+}  // namespace
+}  // namespace mtkv
 
 extern "C" mt_status mt_paged_attn_decode_append(const mt_paged_attn_args *a, const float *k_new,
                                                  const float *v_new, void *workspace,

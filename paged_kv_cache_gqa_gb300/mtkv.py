@@ -98,6 +98,9 @@ def lib() -> ctypes.CDLL:
                                                        ctypes.POINTER(mt_prefix_group), I]),
         "mt_paged_attn_decode_cascade": (I, [ctypes.POINTER(mt_paged_attn_args),
                                              ctypes.POINTER(mt_prefix_group), I, P, SZ, P]),
+        "mt_paged_attn_decode_cascade_append": (I, [ctypes.POINTER(mt_paged_attn_args),
+                                                    ctypes.POINTER(mt_prefix_group), I, P, P, P,
+                                                    SZ, P]),
         "mt_order_moves": (I, [ctypes.POINTER(mt_move), I, ctypes.POINTER(I)]),
         "mt_check_moves": (I, [ctypes.POINTER(mt_move), I, I64, ctypes.POINTER(I)]),
         "mt_copy_cells": (I, [ctypes.POINTER(P), I, SZ, I64, ctypes.POINTER(mt_move), I, P]),
@@ -274,6 +277,18 @@ def mt_paged_attn_decode_cascade(args: mt_paged_attn_args, groups, workspace,
     _check(lib().mt_paged_attn_decode_cascade(ctypes.byref(args), arr, n, _ptr(workspace),
                                               nbytes, _stream(stream)),
            "mt_paged_attn_decode_cascade")
+
+
+def mt_paged_attn_decode_cascade_append(args: mt_paged_attn_args, groups, k_new, v_new,
+                                        workspace, stream=None) -> None:
+    """Cascade decode with each sequence's new K/V row stored at position
+    context_lens[s]-1 in the same call."""
+    arr, n = _groups_array(groups)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().mt_paged_attn_decode_cascade_append(ctypes.byref(args), arr, n, _ptr(k_new),
+                                                     _ptr(v_new), _ptr(workspace), nbytes,
+                                                     _stream(stream)),
+           "mt_paged_attn_decode_cascade_append")
 
 
 MT_STATIC_SCRATCH_BYTES = 8 << 20

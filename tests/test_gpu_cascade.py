@@ -157,3 +157,33 @@ def test_cascade_rejects_bad_groups(mt):
         assert mt.mt_paged_attn_cascade_workspace_bytes(args, bad) == 0
         with pytest.raises(mt.MtError):
             mt.mt_paged_attn_decode_cascade(args, bad, ws)
+
+
+def test_cascade_with_fused_store(mt):
+    # the q8_0 shared-prefix configuration with a partly filled shared block:
+    # copy on write first, then one call stores every new row and decodes
+    w = workloads.llama3_q8_prefix(seed=30, n_seqs=9, prefix=100, suffix_lo=10, suffix_hi=90)
+    kp, vp = oracle_pools(w)
+    k_dev, v_dev = to_dev(kp), to_dev(vp)
+    cow = om.order_moves(w.extra["cow_moves"])
+    om.copy_cells([kp, vp], cow)
+    rb = ofmt.row_bytes("q8_0", w.n_kv_heads, w.head_dim)
+    mt.mt_copy_cells([k_dev, v_dev], rb, w.n_cells, cow)
+    groups = [(0, w.n_seqs, w.extra["prefix"] // w.block_size)]
+    from oracle import attention as oatt
+    oatt.kv_store(w.fmt, kp, vp, w.k_new, w.v_new, w.new_cells, w.n_kv_heads, w.head_dim)
+    want, want_lse = oracle_decode(w, kp, vp)
+    q = to_dev(w.q)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((w.n_seqs, w.n_heads), float("nan"), device="cuda")
+    args = mt.paged_attn_args(w.fmt, q, k_dev, v_dev, to_dev(w.block_table),
+                              to_dev(w.context_lens), out, n_kv_heads=w.n_kv_heads,
+                              block_size=w.block_size, n_phys_blocks=w.n_phys_blocks,
+                              scale=w.scale, spans=to_dev(w.spans), lse=lse)
+    ws = torch.zeros(mt.mt_paged_attn_cascade_workspace_bytes(args, groups), dtype=torch.uint8,
+                     device="cuda")
+    mt.mt_paged_attn_decode_cascade_append(args, groups, to_dev(w.k_new), to_dev(w.v_new), ws)
+    assert mt.mt_check_device_status(ws) == 0
+    assert np.array_equal(k_dev.cpu().numpy(), kp) and np.array_equal(v_dev.cpu().numpy(), vp)
+    assert_close(out.cpu().numpy(), want, TOL["q8_0"], "cascade + fused store")
+    assert_lse(lse.cpu().numpy(), want_lse, TOL["q8_0"], "cascade + fused store")
