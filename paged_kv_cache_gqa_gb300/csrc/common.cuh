@@ -164,10 +164,12 @@ __device__ __forceinline__ void q8_quant_group(uint8_t *blk, float x, int lane) 
     // x / d32 through the (IEEE) reciprocal: |t - x/d32| <= |t| 2^-22 <=
     // 3.1e-5 for |t| <= 127, so rounding t gives rint(x / d32) unless t lies
     // within 2^-13 of a half-integer; there the exact division decides
-    const float t = x * (1.0f / d32);
+    // (a reciprocal that overflows, for d32 below ~2^-128, takes the exact path)
+    const float inv = 1.0f / d32;
+    const float t = x * inv;
     const float r = rintf(t);
     q = (int)r;
-    if (fabsf(fabsf(t - r) - 0.5f) < 1.220703125e-4f) q = (int)rintf(x / d32);
+    if (!isfinite(inv) || fabsf(fabsf(t - r) - 0.5f) < 1.220703125e-4f) q = (int)rintf(x / d32);
     q = max(-127, min(127, q));
   }
   blk[2 + lane] = (uint8_t)(int8_t)q;

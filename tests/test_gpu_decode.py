@@ -216,6 +216,12 @@ def test_store_formats_bit_exact(mt):
             rows = (rng.standard_normal((20, hkv * d)) * rng.uniform(0.01, 100)).astype(np.float32)
             rows[3, :32] = 0.0                    # an all-zero q8_0 group
             rows[4, :32] = np.float32(2.5)        # ties after division
+            # scale 3: x / d = k + 1/2 exactly, while x * fl(1/3) misses the tie
+            ks = rng.integers(-127, 127, 32)
+            rows[6, :32] = (3.0 * (ks + 0.5)).astype(np.float32)
+            rows[6, 0] = np.float32(381.0)        # amax = 3 * 127
+            # a group whose scale is subnormal (its reciprocal overflows)
+            rows[7, :32] = (rng.standard_normal(32) * 1e-38).astype(np.float32)
             cells = rng.permutation(n_cells)[:20].astype(np.int64)
             cells[5] = -1                         # skipped row
             k_dev, v_dev = to_dev(kp), to_dev(vp)
