@@ -599,7 +599,7 @@ def run_extra(args, rank, world, local_rank):
                 for kv in range(2):
                     mtkv.mt_kv_relayout(bufs[i][kv], bufs[i + 1][kv], 30, caps[i], caps[i + 1], row)
 
-        g_ms = _gpu_time(grow, steps, warmup, stream)
+        g_ms = _gpu_time(grow, steps, warmup, stream, graph=args.graph)
         g_bytes = sum(2 * 2 * 30 * c * row for c in caps[:-1])
         # copy_cells: 1000 overlapping run moves on the 60 pools (30 layers x K, V)
         moves, n_cells = workloads.compaction_moves(seed=SEED)

@@ -55,25 +55,29 @@ __device__ __forceinline__ void load8(const uint8_t *p, float (&x)[8]) {
   }
 }
 
-// Eight codes packed into one word of nibbles (element e in bits 4e..4e+3):
-// rint by adding 1.5 * 2^23 (the add itself rounds to nearest even), the
-// code taken from the low mantissa bits; any value within 2^-16 of a
-// half-integer (or without a usable reciprocal) is redone with the exact
-// IEEE division, so the result equals clamp(rint(x / scale), -8, 7) + 8.
-__device__ __forceinline__ uint32_t int4_pack8(const float (&x)[8], float scale, float inv) {
+// Eight codes packed into one word of nibbles (element e in bits 4e..4e+3).
+// t = y + (1.5 * 2^23 + 8) rounds y = x * inv to the nearest integer, ties to
+// even (the constant is even and its ulp is 1), and leaves rint(y) + 8 in
+// the low 4 bits of t, which is the nibble (|y| <= 7 because |x| <= amax).
+// One running maximum of |y - rint(y)| per word catches any value within
+// 2^-16 of a half-integer; that word is redone with the exact IEEE division,
+// so the result equals clamp(rint(x / scale), -8, 7) + 8 for every element.
+// `fast` is false when the reciprocal is not usable (a scale so small that
+// 1 / scale overflows), and then every element takes the exact path.
+__device__ __forceinline__ uint32_t int4_pack8(const float (&x)[8], float scale, float inv,
+                                               bool fast) {
   if (scale == 0.f) return 0x88888888u;
-  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  constexpr float kMagic8 = 12582920.0f;  // 1.5 * 2^23 + 8
   uint32_t word = 0;
-  bool fix = false;
+  float dev = 0.f;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const float y = x[e] * inv;
-    const float t = y + kMagic;
-    const float r = t - kMagic;
-    fix |= !(fabsf(y) <= 8.f) || (0.5f - fabsf(y - r)) < 1.52587890625e-05f;
-    word |= ((__float_as_uint(t) + 8u) & 15u) << (4 * e);
+    const float t = y + kMagic8;
+    dev = fmaxf(dev, fabsf(y - (t - kMagic8)));
+    word |= (__float_as_uint(t) & 15u) << (4 * e);
   }
-  if (fix) {
+  if (!fast || dev > 0.5f - 1.52587890625e-05f) {
     word = 0;
 #pragma unroll
     for (int e = 0; e < 8; ++e) word |= (uint32_t)(int4_code(x[e], scale, inv) + 8) << (4 * e);
@@ -147,12 +151,13 @@ __global__ void __launch_bounds__(256) int4_quant_smem_kernel(
   for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
   const float scale = amax / 7.0f;
   const float inv = scale != 0.f ? 1.0f / scale : 0.f;
+  const bool fast = isfinite(inv);
   if (threadIdx.x == 0) scales[blockIdx.x] = scale;
   uint32_t *dst = reinterpret_cast<uint32_t *>(nibbles + (size_t)blockIdx.x * (n_elts / 2));
   for (int i = threadIdx.x; i < n8; i += 256) {
     float x[8];
     load8<FMT>(buf + (size_t)i * 8 * ES, x);
-    dst[i] = int4_pack8(x, scale, inv);
+    dst[i] = int4_pack8(x, scale, inv, fast);
   }
 }
 

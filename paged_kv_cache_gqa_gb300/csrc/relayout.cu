@@ -7,7 +7,8 @@
 // preallocated at full size.
 //
 // One 2-D grid: blockIdx.y is the layer, x walks that layer's old_cap rows as
-// one contiguous span with 16-byte (or 4-byte) vector copies.
+// one contiguous span with 16-byte (or 4-byte) vector copies, four in flight
+// per thread.
 #include <algorithm>
 
 #include "common.cuh"
@@ -16,17 +17,27 @@
 namespace mtkv {
 namespace {
 
-template <typename V>
+// Each thread keeps U vector loads in flight (all issued before any store):
+// with one load per thread the device held too few bytes in flight to cover
+// HBM latency (0.67 of the copy peak).
+template <typename V, int U>
 __global__ void __launch_bounds__(256) relayout_kernel(const uint8_t *__restrict__ src,
                                                        uint8_t *__restrict__ dst,
                                                        long long old_bytes, long long new_bytes) {
   const size_t layer = blockIdx.y;
-  const V *s = reinterpret_cast<const V *>(src + layer * old_bytes);
-  V *d = reinterpret_cast<V *>(dst + layer * new_bytes);
+  const V *__restrict__ s = reinterpret_cast<const V *>(src + layer * old_bytes);
+  V *__restrict__ d = reinterpret_cast<V *>(dst + layer * new_bytes);
   const long long n = old_bytes / (long long)sizeof(V);
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x)
-    d[i] = s[i];
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride * U) {
+    V v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i + u * stride < n) v[u] = s[i + u * stride];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i + u * stride < n) d[i + u * stride] = v[u];
+  }
 }
 
 }  // namespace
@@ -52,18 +63,19 @@ extern "C" mt_status mt_kv_relayout(const void *src, void *dst, int n_layers, in
   DeviceInfo di;
   mt_status st = device_info(&di);
   if (st != MT_OK) return st;
-  // enough CTAs to cover the device a few times, spread over the layers
+  // enough CTAs to cover the device a few times, spread over the layers;
+  // each thread copies 4 vectors per round
   long long want = (long long)di.n_sm * 8 / n_layers + 1;
-  long long need = (n + 255) / 256;
+  long long need = (n + 1023) / 1024;
   const unsigned gx = (unsigned)std::max(1LL, std::min(want, need));
   dim3 grid(gx, (unsigned)n_layers);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const auto *sp = static_cast<const uint8_t *>(src);
   auto *dp = static_cast<uint8_t *>(dst);
   if (v16)
-    relayout_kernel<uint4><<<grid, 256, 0, s>>>(sp, dp, old_bytes, new_bytes);
+    relayout_kernel<uint4, 4><<<grid, 256, 0, s>>>(sp, dp, old_bytes, new_bytes);
   else
-    relayout_kernel<uint32_t><<<grid, 256, 0, s>>>(sp, dp, old_bytes, new_bytes);
+    relayout_kernel<uint32_t, 4><<<grid, 256, 0, s>>>(sp, dp, old_bytes, new_bytes);
   st = cuda_check(cudaGetLastError(), "mt_kv_relayout launch");
   return st == MT_OK ? ok() : st;
 }
