@@ -28,31 +28,12 @@
 #include "common.cuh"
 #include "internal.h"
 #include "mq.cuh"
+#include "prefill.h"
 
 namespace mtkv {
 namespace {
 
-constexpr int kMaxPrefillSeqs = 1024;  // sequences per launch (tile offsets in shared memory)
 constexpr uint64_t kPrefillWsBytes = 256;
-
-struct PrefillParams {
-  const float *q;
-  const uint8_t *k_pool;
-  const uint8_t *v_pool;
-  const int32_t *table;
-  const int32_t *ctx;
-  const int32_t *q_start;
-  const int32_t *spans;
-  const int32_t *kv_map;
-  float *out;
-  float *lse;
-  uint32_t *status;
-  int B, Hq, Hkv, G, bs, max_blocks;
-  int n_tok;  // query rows in q / out (rows outside [0, n_tok) are flagged, not read)
-  long long n_phys;
-  int row_bytes;
-  float qscale;
-};
 
 // The CTA's walk over its tiles (blockIdx.x, + gridDim.x, ...) and their
 // blocks [0, nb). A tile whose rows read nothing still has one (empty) unit,
@@ -411,6 +392,13 @@ extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void 
     p.table = a->block_table + (size_t)s0 * a->max_blocks;
     p.ctx = a->context_lens + s0;
     p.q_start = a->q_start + s0;
+    if (prefill_tc_supported(a->fmt, a->head_dim, a->block_size)) {
+      // f16 pools: the tcgen05 kernel, one CTA (256 tensor-memory columns,
+      // ~210 KB of shared memory for head_dim 128) per SM
+      st = launch_prefill_tc(p, a->head_dim, GP, di.n_sm, s);
+      if (st != MT_OK) return st;
+      continue;
+    }
     const int n_ctas = di.n_sm * 2;
     switch (a->fmt) {
       case MT_KV_F32: st = launch_f<MT_KV_F32>(a->head_dim, GP, p, n_ctas, s); break;

@@ -1,0 +1,38 @@
+// Shared parameters of the multi-query (prefill) kernels: the mma.sync
+// kernel (prefill.cu) and the tcgen05 kernel (prefill_tc.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mtkv.h"
+
+namespace mtkv {
+
+constexpr int kMaxPrefillSeqs = 1024;  // sequences per launch (tile offsets in shared memory)
+
+struct PrefillParams {
+  const float *q;
+  const uint8_t *k_pool;
+  const uint8_t *v_pool;
+  const int32_t *table;
+  const int32_t *ctx;
+  const int32_t *q_start;
+  const int32_t *spans;
+  const int32_t *kv_map;
+  float *out;
+  float *lse;
+  uint32_t *status;
+  int B, Hq, Hkv, G, bs, max_blocks;
+  int n_tok;  // query rows in q / out (rows outside [0, n_tok) are flagged, not read)
+  long long n_phys;
+  int row_bytes;
+  float qscale;
+};
+
+// tcgen05 prefill kernel (f16 pools, head_dim 64 or 128, block_size 16 or 32).
+bool prefill_tc_supported(mt_kv_format fmt, int head_dim, int block_size);
+mt_status launch_prefill_tc(const PrefillParams &p, int head_dim, int gp, int n_ctas,
+                            cudaStream_t stream);
+
+}  // namespace mtkv
