@@ -39,6 +39,7 @@
 #include "common.cuh"
 #include "mma.cuh"
 #include "internal.h"
+#include "tmap.h"
 #include "prefix.h"
 
 #include <limits.h>
@@ -1734,44 +1735,11 @@ mt_status dispatch_d(const Params &prm, const Plan &pl, cudaStream_t s) {
   }
 }
 
-// cuTensorMapEncodeTiled from the driver, looked up once.
-mt_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000 *out) {
-  static std::mutex mu;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!fn) {
-    void *f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    mt_status st = cuda_check(
-        cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q),
-        "cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)");
-    if (st != MT_OK) return st;
-    if (q != cudaDriverEntryPointSuccess || !f)
-      return fail(MT_ERR_CUDA, "driver has no cuTensorMapEncodeTiled");
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
-  *out = fn;
-  return MT_OK;
-}
-
 // 3-D tensor map of a pool for the tensor-core path: [cells][row chunks of
 // 128 bytes][64 f16], box = (64, ncb, rows), 128-byte swizzle, zero fill.
 mt_status encode_pool_map(CUtensorMap *map, const void *pool, long long n_cells, size_t rb,
                           const Plan &pl) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn;
-  mt_status st = encode_fn(&fn);
-  if (st != MT_OK) return st;
-  const cuuint64_t dims[3] = {64, (cuuint64_t)(rb / 128), (cuuint64_t)n_cells};
-  const cuuint64_t strides[2] = {128, (cuuint64_t)rb};
-  const cuuint32_t box[3] = {64, (cuuint32_t)pl.ncb, (cuuint32_t)pl.rows};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(pool), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return fail(MT_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string((int)r) + ")");
-  return MT_OK;
+  return encode_pool_map_3d(map, pool, n_cells, rb, pl.ncb, pl.rows);
 }
 
 // Fill the kernel parameters shared by both decode entry points.

@@ -7,24 +7,31 @@
 // KV cache — architecture", sections "The paged-attention block model" and
 // "Kernel dispatch"; "KV Cache Design — cells, format, sessions", section 1).
 //
-// How (GB300): a tile is 128 (query, head) rows of one KV head — one row per
-// thread of a 4-warp CTA, which is also that row's tensor-memory lane — and
-// the sequence's positions up to the tile's last query, in chunks of 64
-// tokens. Per chunk:
-//   1. the chunk's K and V head slices are copied (cp.async, 16 B) into
-//      128-byte-swizzled shared tiles, [token][64 dims] per half head; holes
-//      and rows past the context are zero-filled (no read);
-//   2. one thread issues S = Q_hi K^T + Q_lo K^T (M = 128, N = 64, f16 in,
-//      f32 accumulated in tensor memory; q = Q_hi + Q_lo to ~2^-22, so scores
-//      keep float32 accuracy) and commits to an mbarrier;
-//   3. every thread loads its row of S, masks it, and runs its own online
-//      softmax in registers (no cross-thread reduction); the output row in
-//      tensor memory is rescaled only when the running maximum grows by more
-//      than 2^8 (probabilities then stay below 256, exact in f16);
-//   4. the probabilities go to a swizzled P tile (f16) and one thread issues
-//      O += P V (N = head_dim; V read MN-major straight from its tile).
-// Chunks are staged three ahead; a tile's output is normalised once at the
-// end. CTAs take whole tiles round-robin (no split-K combine).
+// How (GB300): a tile is 128 (query, head) rows of one KV head (one
+// tensor-memory lane per row) and the sequence's positions up to the tile's
+// last query, in chunks of 64 tokens. A CTA takes whole tiles round-robin
+// (no split-K combine) and runs three roles that hand work to each other
+// through mbarriers only — no CTA-wide barrier inside the chunk loop:
+//   * a load warp reads the chunk's block ids from the table and stages the
+//     chunk's K and V head slices with one tensor copy (TMA, 128-byte
+//     swizzle) per block and 64-dim half into a ring of stages; holes are not
+//     read at all;
+//   * an MMA warp (one thread issues) computes S(c+1) = Q_hi K^T + Q_lo K^T
+//     (M = 128, N = 64, f16 in, f32 accumulated in tensor memory; q = Q_hi +
+//     Q_lo to ~2^-22, so scores keep float32 accuracy) ahead of the softmax,
+//     then O += P(c) V(c) once the probabilities of chunk c are written (V
+//     read MN-major straight from its stage). V rows of holes and past the
+//     context are zeroed first: P is 0 there but 0 * NaN would not be;
+//   * eight softmax warps, two threads per row (warps w and w + 4 share the
+//     tensor-memory lanes 32 (w % 4) .. + 31; each takes 32 of the 64 score
+//     columns and half of O): load S, mask it, exchange the row maximum with
+//     the partner through shared memory and a two-warp named barrier, run the
+//     online softmax, and write f16 probabilities to one of two swizzled P
+//     tiles. The output row in tensor memory is rescaled only when the
+//     running maximum grows by more than 2^8 (probabilities then stay below
+//     256, exact in f16); a tile's output is normalised once at the end.
+// The next tile's Q is written as soon as the last S of a tile is read, so
+// its first scores are computed while the previous tile's output is stored.
 #include <limits.h>
 #include <math.h>
 
@@ -35,36 +42,33 @@
 #include "mma.cuh"
 #include "prefill.h"
 #include "tc.cuh"
+#include "tmap.h"
 
 namespace mtkv {
 namespace {
 
 constexpr unsigned kAll = 0xffffffffu;
-constexpr int kTcRows = 128;    // rows per tile = threads per CTA
-constexpr int kChunk = 64;      // tokens per chunk
-constexpr int kTcStages = 4;
-constexpr int kOCol = 2 * 64;        // S double buffer: columns [0, 64), [64, 128); O: [128, 128 + d)
+constexpr int kTcRows = 128;       // rows per tile = tensor-memory lanes
+constexpr int kSoftWarps = 8;      // two threads per row
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kTcThreads = 320;
+constexpr int kChunk = 64;         // tokens per chunk
+constexpr int kOCol = 2 * 64;      // S double buffer: columns [0, 64), [64, 128); O: [128, 128 + d)
 constexpr uint32_t kTmemCols = 256;
 
 template <int D>
 struct TcCfg {
   static constexpr int HALVES = D / 64;                 // 64-dim halves of a head
   static constexpr int QB = HALVES * kTcRows * 128;     // one Q tile (hi or lo)
-  static constexpr int PB = kTcRows * 128;              // P tile: 128 rows x 64 tokens
+  static constexpr int PB = kTcRows * 128;              // one P tile: 128 rows x 64 tokens
   static constexpr int KVB = HALVES * kChunk * 128;     // K (or V) of one chunk
   static constexpr int STAGE = 2 * KVB;
-  static constexpr int SMEM = 1024 + 2 * QB + PB + kTcStages * STAGE;
+  static constexpr int STAGES = D == 64 ? 6 : 3;
+  static constexpr int SMEM = 1024 + 2 * QB + 2 * PB + STAGES * STAGE;
 };
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t n) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
-               : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+static_assert(TcCfg<128>::SMEM + 8 * 1024 <= 227 * 1024, "shared memory");
+static_assert(TcCfg<64>::SMEM + 8 * 1024 <= 227 * 1024, "shared memory");
 
 // 2^x by the hardware approximation (relative error ~2^-22, 2^-inf = 0):
 // far below the f16 rounding the probabilities get right after.
@@ -72,6 +76,29 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// One swizzled tensor copy of box (64, 1, rows): 128-byte chunk `chunk` of
+// the rows of cells [cell, cell + rows), completing on `bar`.
+__device__ __forceinline__ void tma_rows(uint32_t dst, const CUtensorMap *map, int chunk, int cell,
+                                         uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(chunk), "r"(cell), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Two-warp named barrier (ids 1..4: warps w and w + 4) that also ANDs a flag.
+__device__ __forceinline__ bool pair_sync_and(int id, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; barrier.red.and.pred q, %2, 64, p; "
+      "selp.u32 %0, 1, 0, q; }"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(id)
+      : "memory");
+  return r != 0;
 }
 
 struct Tile {
@@ -96,87 +123,90 @@ __device__ __forceinline__ bool tile_of(const PrefillParams &p, const int *ts, i
   constexpr int TQ = kTcRows / GP;
   const int last = tl.c - tl.n + min(tl.n, (tl.qt + 1) * TQ) - 1;
   const int reach = min(last + 1, tl.c);
-  tl.nch = reach > 0 ? (reach + kChunk - 1) / kChunk : 0;
+  // at least one chunk, so every tile takes the same hand-offs through all
+  // roles (a tile that reaches no position reads nothing and stores zeros)
+  tl.nch = reach > 0 ? (reach + kChunk - 1) / kChunk : 1;
   return true;
 }
 
-// Block ids of chunk `ch` (block k of the chunk -> ids[k]; -1: a hole, a
-// flagged id or past the context), loaded by the first 64 / bs threads.
-__device__ __forceinline__ void load_chunk_ids(const PrefillParams &p, const Tile &tl, int ch,
-                                               int *ids) {
-  const int nb = kChunk / p.bs;
-  if ((int)threadIdx.x < nb) {
-    const int pos = ch * kChunk + (int)threadIdx.x * p.bs;
-    int phys = -1;
-    if (ch < tl.nch && pos < tl.c) {
-      phys = p.table[(size_t)tl.s * p.max_blocks + pos / p.bs];
-      if (phys < -1 || (phys >= 0 && (long long)phys >= p.n_phys)) {
-        report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
-        phys = -1;
-      }
+// Bits [a, b) of a 64-bit chunk mask (0 <= a, b <= 64).
+__device__ __forceinline__ uint64_t bit_range(int a, int b) {
+  if (b <= a) return 0ull;
+  return (b >= 64 ? ~0ull : ((1ull << b) - 1ull)) & ~((1ull << a) - 1ull);
+}
+
+// The (query, head) row a softmax thread owns in tile `tl`.
+template <int GP>
+struct RowOf {
+  int j, hg, i;
+  bool in, ok;  // in: a query row of this launch; ok: and it has a position
+  __device__ __forceinline__ RowOf(const PrefillParams &p, const Tile &tl, int row) {
+    constexpr int TQ = kTcRows / GP;
+    j = tl.qt * TQ + row / GP;
+    hg = row % GP;
+    i = p.q_start[tl.s] + j;
+    in = j < tl.n && hg < p.G && i >= 0 && i < p.n_tok;
+    ok = in && tl.c - tl.n + j >= 0;
+  }
+};
+
+// Write the row's query as a high / low f16 pair into the two Q tiles (this
+// thread's half of the head dims; zeros for rows that hold no query).
+template <int D, int GP>
+__device__ __forceinline__ void write_q(const PrefillParams &p, const Tile &tl, int row, int hc,
+                                        uint8_t *qhi, uint8_t *qlo) {
+  const RowOf<GP> r(p, tl, row);
+  const float *qrow = p.q + ((size_t)(r.ok ? r.i : 0) * p.Hq + (size_t)tl.kvh * p.G + r.hg) * D;
+#pragma unroll 4
+  for (int e = hc * (D / 2); e < (hc + 1) * (D / 2); e += 8) {
+    float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+    if (r.ok) {
+      x0 = *reinterpret_cast<const float4 *>(qrow + e);
+      x1 = *reinterpret_cast<const float4 *>(qrow + e + 4);
     }
-    ids[threadIdx.x] = phys;
+    uint32_t h[4], l[4];
+    const float qs = p.qscale;
+    split_h2(x0.x * qs, x0.y * qs, h[0], l[0]);
+    split_h2(x0.z * qs, x0.w * qs, h[1], l[1]);
+    split_h2(x1.x * qs, x1.y * qs, h[2], l[2]);
+    split_h2(x1.z * qs, x1.w * qs, h[3], l[3]);
+    const uint32_t off = (uint32_t)((e >> 6) * kTcRows * 128) + tc::sw128(row, (e & 63) >> 3);
+    *reinterpret_cast<uint4 *>(qhi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4 *>(qlo + off) = make_uint4(l[0], l[1], l[2], l[3]);
   }
 }
 
-// Copy chunk `ch` of the tile's KV head into ring slot `slot` (every thread
-// issues its share; one commit group per call, empty past the last chunk).
-// Rows of holes and past the context are zero-filled without a read. Thread
-// t always moves 16-byte column t % CPR of rows t / CPR + (128 / CPR) k, so
-// its shared-memory column and swizzle are fixed.
-template <int D>
-__device__ __forceinline__ void issue_chunk(const PrefillParams &p, const Tile &tl, int ch,
-                                            const int *ids, uint8_t *ring, int slot,
-                                            int bs_shift) {
-  using C = TcCfg<D>;
-  constexpr int CPR = D * 2 / 16;        // 16-byte columns per head row
-  constexpr int RSTEP = kTcRows / CPR;   // rows between a thread's items
-  constexpr int ITEMS = kChunk / RSTEP;
-  if (ch < tl.nch) {
-    const int cc = threadIdx.x % CPR, t0 = threadIdx.x / CPR;
-    const uint32_t base = smem_u32(ring + (size_t)slot * C::STAGE) +
-                          (uint32_t)((cc >> 3) * kChunk * 128) + (uint32_t)t0 * 128 +
-                          (uint32_t)(((cc & 7) ^ (t0 & 7)) << 4);
-    const size_t col = (size_t)tl.kvh * D * 2 + (size_t)cc * 16;
-    const int pos0 = ch * kChunk, bmask = (1 << bs_shift) - 1;
-#pragma unroll
-    for (int k = 0; k < ITEMS; ++k) {
-      const int t = t0 + RSTEP * k;  // RSTEP is a multiple of 8: the swizzle is unchanged
-      const int pos = pos0 + t;
-      const int phys = ids[t >> bs_shift];
-      const bool ok = phys >= 0 && pos < tl.c;
-      const size_t g =
-          ok ? (((size_t)phys << bs_shift) + (pos & bmask)) * (size_t)p.row_bytes + col : 0;
-      const uint32_t dst = base + (uint32_t)(RSTEP * k * 128);
-      cp_async16(dst, p.k_pool + g, ok ? 16u : 0u);
-      cp_async16(dst + C::KVB, p.v_pool + g, ok ? 16u : 0u);
-    }
-  }
-  cp_commit();
-}
+// Tensor maps of the two pools: [cell][128-byte chunk][64 f16], box (64, 1, bs).
+struct TcMaps {
+  CUtensorMap k, v;
+};
 
 template <int D, int GP>
-__global__ void __launch_bounds__(kTcRows, 1)
-    prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ TcMaps maps) {
   using C = TcCfg<D>;
-  constexpr int TQ = kTcRows / GP;
+  constexpr int ST = C::STAGES;
   constexpr int R_RUNS = MT_KV_MAP_MAX_SPANS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ int ts[kMaxPrefillSeqs + 1];
   __shared__ uint32_t tmem_slot;
-  __shared__ __align__(8) uint64_t bar_s[2], bar_pv;
-  __shared__ int ids_s[kTcStages][4];  // block ids of the staged chunks, by slot
+  __shared__ __align__(8) uint64_t kv_full[ST], kv_free[ST], s_full[2], s_free[2], p_full[2],
+      pv_done[2], q_full, o_free, drain;
+  __shared__ uint64_t vmask_s[ST];       // staged rows that hold data (not a hole, < ctx)
+  __shared__ float pm_s[2][2][kTcRows];  // partial row maxima: [chunk parity][half][row]
+  __shared__ float pl_s[2][kTcRows];     // partial row sums at the tile end
   __shared__ int abort_s;
   uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *qhi = base;
   uint8_t *qlo = base + C::QB;
-  uint8_t *pt = base + 2 * C::QB;
-  uint8_t *ring = pt + C::PB;
+  uint8_t *pt = base + 2 * C::QB;  // two P tiles
+  uint8_t *ring = pt + 2 * C::PB;
   pdl_enter();
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // tile offsets: ceil(n_s / TQ) query tiles per sequence, times Hkv
+  constexpr int TQ = kTcRows / GP;
   if (warp == 0) {
     int run = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
@@ -199,9 +229,19 @@ __global__ void __launch_bounds__(kTcRows, 1)
     if (lane == 0) ts[p.B] = run;
   }
   if (tid == 0) {
-    mbar_init(&bar_s[0], 1);
-    mbar_init(&bar_s[1], 1);
-    mbar_init(&bar_pv, 1);
+    for (int k = 0; k < ST; ++k) {
+      mbar_init(&kv_full[k], 1);
+      mbar_init(&kv_free[k], 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&s_full[k], 1);
+      mbar_init(&s_free[k], kSoftWarps);
+      mbar_init(&p_full[k], kSoftWarps);
+      mbar_init(&pv_done[k], 1);
+    }
+    mbar_init(&q_full, kSoftWarps);
+    mbar_init(&o_free, kSoftWarps);
+    mbar_init(&drain, 1);
     abort_s = 0;
     fence_mbar_init();
   }
@@ -213,263 +253,350 @@ __global__ void __launch_bounds__(kTcRows, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
-  constexpr uint32_t idesc_s = tc::idesc_f16(kTcRows, kChunk, false);
-  constexpr uint32_t idesc_o = tc::idesc_f16(kTcRows, D, true);
-  uint32_t ph_pv = 0;
-  const int bs_shift = p.bs == 32 ? 5 : 4;
-  uint32_t n_s0 = 0, n_s1 = 0;  // completions consumed per S buffer (their wait parity)
-  bool ok_run = true;
   const uint64_t wait_ns = 2000000000ull;
+  const int bs_shift = p.bs == 32 ? 5 : 4;
+  bool fine = true;  // false once a bounded wait ran out (or another role gave up)
 
-  for (int t = blockIdx.x; ok_run; t += gridDim.x) {
-    Tile tl;
-    if (!tile_of<GP>(p, ts, n_tiles, t, tl)) break;
-    // ---- this thread's row: (query j, head hg)
-    const int j = tl.qt * TQ + tid / GP, hg = tid % GP;
-    const int i = p.q_start[tl.s] + j;
-    const int pos_q = tl.c - tl.n + j;
-    const bool row_in = j < tl.n && hg < p.G && i >= 0 && i < p.n_tok;
-    if (j < tl.n && hg < p.G && !row_in) report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
-    const bool row_ok = row_in && pos_q >= 0;
-    int lo = 0, hi = row_ok ? min(pos_q + 1, tl.c) : 0;
-    if (row_ok && p.spans) {
-      lo = max(p.spans[2 * i], 0);
-      hi = min(hi, p.spans[2 * i + 1]);
-    }
-    int ra[R_RUNS], re[R_RUNS];
-    if (p.kv_map) {
-#pragma unroll
-      for (int r = 0; r < R_RUNS; ++r) {
-        ra[r] = re[r] = 0;
-        if (row_ok) {
-          const int32_t *rp = p.kv_map + ((size_t)i * R_RUNS + r) * 2;
-          ra[r] = max(rp[0], 0);
-          re[r] = min(rp[0] + rp[1], hi);
+  if (warp == kLoadWarp) {
+    // ================================================================ load
+    int g = 0;  // chunks staged by this CTA so far (all tiles)
+    for (int t = blockIdx.x; fine; t += gridDim.x) {
+      Tile tl;
+      if (!tile_of<GP>(p, ts, n_tiles, t, tl)) break;
+      for (int c = 0; c < tl.nch; ++c, ++g) {
+        const int st = g % ST;
+        if (g >= ST && !mbar_wait_bounded(&kv_free[st], (uint32_t)((g / ST) - 1) & 1u, &abort_s,
+                                          wait_ns)) {
+          fine = false;
+          break;
+        }
+        // lane k < 64 / bs: block k of the chunk
+        const int nb = kChunk >> bs_shift;
+        const int pos = c * kChunk + (lane << bs_shift);
+        int phys = -1;
+        if (lane < nb && pos < tl.c) {
+          phys = p.table[(size_t)tl.s * p.max_blocks + (pos >> bs_shift)];
+          if (phys < -1 || (phys >= 0 && (long long)phys >= p.n_phys)) {
+            report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
+            phys = -1;
+          }
+        }
+        const uint64_t mine =
+            phys >= 0 ? bit_range(lane << bs_shift, (lane << bs_shift) + min(p.bs, tl.c - pos))
+                      : 0ull;
+        const uint32_t m_lo = __reduce_or_sync(kAll, (uint32_t)mine);
+        const uint32_t m_hi = __reduce_or_sync(kAll, (uint32_t)(mine >> 32));
+        const int n_valid = __popc(__ballot_sync(kAll, phys >= 0));
+        if (lane == 0) {
+          vmask_s[st] = ((uint64_t)m_hi << 32) | m_lo;
+          mbar_arrive_expect_tx(&kv_full[st], (uint32_t)(n_valid * 2 * C::HALVES * 128) << bs_shift);
+        }
+        __syncwarp();
+        // one copy per (block, K / V, 64-dim half): lane = (k * 2 + kv) * HALVES + h
+        constexpr int PER = 2 * C::HALVES;
+        const int k = lane / PER, r = lane % PER;
+        const int pk = __shfl_sync(kAll, phys, k & 31);
+        if (k < nb && pk >= 0) {
+          const int kv = r / C::HALVES, h = r % C::HALVES;
+          const uint32_t dst = smem_u32(ring) + (uint32_t)(st * C::STAGE + kv * C::KVB +
+                                                           h * (kChunk * 128) + (k << bs_shift) * 128);
+          tma_rows(dst, kv ? &maps.v : &maps.k, tl.kvh * C::HALVES + h, pk << bs_shift,
+                   &kv_full[st]);
         }
       }
     }
-    // ---- the row's query as a high / low f16 pair in the two Q tiles
-    {
-      const float *qrow = p.q + ((size_t)(row_ok ? i : 0) * p.Hq + (size_t)tl.kvh * p.G + hg) * D;
-#pragma unroll 4
-      for (int e = 0; e < D; e += 8) {
-        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-        if (row_ok) {
-          x0 = *reinterpret_cast<const float4 *>(qrow + e);
-          x1 = *reinterpret_cast<const float4 *>(qrow + e + 4);
-        }
-        uint32_t h[4], l[4];
-        const float qs = p.qscale;
-        split_h2(x0.x * qs, x0.y * qs, h[0], l[0]);
-        split_h2(x0.z * qs, x0.w * qs, h[1], l[1]);
-        split_h2(x1.x * qs, x1.y * qs, h[2], l[2]);
-        split_h2(x1.z * qs, x1.w * qs, h[3], l[3]);
-        const uint32_t off = (uint32_t)((e >> 6) * kTcRows * 128) + tc::sw128(tid, (e & 63) >> 3);
-        *reinterpret_cast<uint4 *>(qhi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4 *>(qlo + off) = make_uint4(l[0], l[1], l[2], l[3]);
-      }
+    // copies still in flight land before the CTA leaves (the last fill of each stage)
+    for (int k = 0; k < ST; ++k) {
+      if (g <= k) continue;
+      const int gl = g - 1 - ((g - 1 - k) % ST);
+      if (!mbar_wait_bounded(&kv_full[k], (uint32_t)(gl / ST) & 1u, &abort_s, wait_ns)) fine = false;
     }
-    float m_run = -INFINITY, l_run = 0.f;
-
-    // ---- chunks: S(ch+1) is computed by the tensor cores while the threads
-    // run the softmax of chunk ch (two S buffers, one mbarrier each)
-    load_chunk_ids(p, tl, 0, ids_s[0]);
-    load_chunk_ids(p, tl, 1, ids_s[1]);
-    load_chunk_ids(p, tl, 2, ids_s[2]);
-    load_chunk_ids(p, tl, 3, ids_s[3]);
-    __syncthreads();
+  } else if (warp == kMmaWarp) {
+    // ================================================================= MMA
+    constexpr uint32_t idesc_s = tc::idesc_f16(kTcRows, kChunk, false);
+    constexpr uint32_t idesc_o = tc::idesc_f16(kTcRows, D, true);
+    // S(x) = Q_hi K^T + Q_lo K^T into S buffer x % 2, once chunk x is staged
+    // and the softmax has read S(x - 2) from that buffer
+    auto issue_s = [&](int x) -> bool {
+      const int st = x % ST;
+      if (!mbar_wait_bounded(&kv_full[st], (uint32_t)(x / ST) & 1u, &abort_s, wait_ns)) return false;
+      if (x >= 2 &&
+          !mbar_wait_bounded(&s_free[x & 1], (uint32_t)((x - 2) >> 1) & 1u, &abort_s, wait_ns))
+        return false;
+      tc::fence_after();
+      if (lane == 0) {
+        const uint32_t kt = smem_u32(ring) + (uint32_t)(st * C::STAGE);
+        const uint32_t dcol = tmem + (uint32_t)((x & 1) * 64);
 #pragma unroll
-    for (int k = 0; k < kTcStages - 1; ++k) issue_chunk<D>(p, tl, k, ids_s[k], ring, k, bs_shift);
-    auto issue_s = [&](int x) {
-      // S(x) = Q_hi K^T + Q_lo K^T into S buffer x % 2 (one thread)
-      const uint8_t *kt = ring + (size_t)(x % kTcStages) * C::STAGE;
-      const uint32_t dcol = tmem + (uint32_t)((x & 1) * 64);
+        for (int hf = 0; hf < C::HALVES; ++hf)
 #pragma unroll
-      for (int hf = 0; hf < C::HALVES; ++hf)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t qo = (uint32_t)(hf * kTcRows * 128 + kk * 32);
-          const uint64_t bd = tc::desc_sw128(smem_u32(kt) + hf * kChunk * 128 + kk * 32, 16, 1024);
-          tc::mma_f16(dcol, tc::desc_sw128(smem_u32(qhi) + qo, 16, 1024), bd, idesc_s,
-                      hf + kk > 0);
-          tc::mma_f16(dcol, tc::desc_sw128(smem_u32(qlo) + qo, 16, 1024), bd, idesc_s, true);
-        }
-      tc::commit(&bar_s[x & 1]);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t qo = (uint32_t)(hf * kTcRows * 128 + kk * 32);
+            const uint64_t bd = tc::desc_sw128(kt + hf * kChunk * 128 + kk * 32, 16, 1024);
+            tc::mma_f16(dcol, tc::desc_sw128(smem_u32(qhi) + qo, 16, 1024), bd, idesc_s,
+                        hf + kk > 0);
+            tc::mma_f16(dcol, tc::desc_sw128(smem_u32(qlo) + qo, 16, 1024), bd, idesc_s, true);
+          }
+        tc::commit(&s_full[x & 1]);
+      }
+      __syncwarp();
+      return true;
     };
-    for (int ch = 0; ch < tl.nch; ++ch) {
-      // chunks ch and ch+1 staged (groups: S-1 in the prologue, one per iteration)
-      cp_wait<kTcStages - 3>();
-      tc::fence_proxy_shared();  // this thread's copies (and Q / P writes) -> async proxy
-      tc::fence_before();
-      __syncthreads();
-      tc::fence_after();
-      if (tid == 0) {
-        if (ch == 0) issue_s(0);
-        if (ch + 1 < tl.nch) issue_s(ch + 1);
+    int g = 0;
+    for (int t = blockIdx.x, k = 0; fine; t += gridDim.x, ++k) {
+      Tile tl;
+      if (!tile_of<GP>(p, ts, n_tiles, t, tl)) break;
+      // this tile's Q is in place
+      if (!mbar_wait_bounded(&q_full, (uint32_t)k & 1u, &abort_s, wait_ns) || !issue_s(g)) {
+        fine = false;
+        break;
       }
-      // a wait that runs out is carried to the next CTA barrier, where every
-      // thread leaves together (no thread may skip a barrier the others reach)
-      bool fine = mbar_wait_bounded(&bar_s[ch & 1], ((ch & 1) ? n_s1 : n_s0) & 1u, &abort_s,
-                                    wait_ns);
-      if (ch & 1) ++n_s1; else ++n_s0;
-      tc::fence_after();
-      float sv[kChunk];
+      for (int c = 0; c < tl.nch; ++c) {
+        const int x = g + c, st = x % ST;
+        if (c + 1 < tl.nch && !issue_s(x + 1)) {
+          fine = false;
+          break;
+        }
+        // V rows without data (holes, past the context) -> 0
+        const uint64_t vm = vmask_s[st];
+        if (vm != ~0ull) {
+          uint8_t *vt = ring + (size_t)st * C::STAGE + C::KVB;
+          for (int u = lane; u < kChunk * C::HALVES * 8; u += 32) {
+            const int line = u >> 3;  // half * 64 + row
+            if (!((vm >> (line & 63)) & 1ull))
+              *reinterpret_cast<uint4 *>(vt + (size_t)line * 128 + (u & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
+          }
+          tc::fence_proxy_shared();
+          __syncwarp();
+        }
+        // P(x) written; before the tile's first P.V, the previous output read out
+        if (!mbar_wait_bounded(&p_full[x & 1], (uint32_t)(x >> 1) & 1u, &abort_s, wait_ns) ||
+            (c == 0 && k > 0 &&
+             !mbar_wait_bounded(&o_free, (uint32_t)(k - 1) & 1u, &abort_s, wait_ns))) {
+          fine = false;
+          break;
+        }
+        tc::fence_after();
+        if (lane == 0) {
+          // O += P V (V MN-major: LBO = the distance between its 64-dim halves)
+          const uint32_t vt = smem_u32(ring) + (uint32_t)(st * C::STAGE + C::KVB);
+          const uint32_t pb = smem_u32(pt) + (uint32_t)((x & 1) * C::PB);
 #pragma unroll
-      for (int c16 = 0; c16 < kChunk; c16 += 16) {
-        float v[16];
-        tc::ld16(t_row + (uint32_t)((ch & 1) * 64) + c16, v);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) sv[c16 + e] = v[e];
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_f16(tmem + kOCol, tc::desc_sw128(pb + kk * 32, 16, 1024),
+                        tc::desc_sw128(vt + kk * 2048, kChunk * 128, 1024), idesc_o,
+                        c > 0 || kk > 0);
+          tc::commit(&pv_done[x & 1]);
+          tc::commit(&kv_free[st]);
+        }
+        __syncwarp();
       }
-      tc::wait_ld();
-      // ---- mask: positions of this chunk the row may read
-      const int pos0 = ch * kChunk;
-      uint64_t mk = 0;
+      g += tl.nch;
+    }
+    // every MMA issued here has completed before tensor memory is released
+    if (lane == 0) tc::commit(&drain);
+    __syncwarp();
+    if (!mbar_wait_bounded(&drain, 0, &abort_s, wait_ns)) fine = false;
+  } else {
+    // ============================================================= softmax
+    const int row = tid & (kTcRows - 1), hc = tid >> 7, pair = 1 + (warp & 3);
+    const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // lanes of this row
+    constexpr int HC = kChunk / 2;  // score columns per thread
+    Tile tl;
+    bool have = tile_of<GP>(p, ts, n_tiles, blockIdx.x, tl);
+    if (have) {
+      write_q<D, GP>(p, tl, row, hc, qhi, qlo);
+      tc::fence_proxy_shared();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_full);
+    }
+    int g = 0;
+    for (int t = blockIdx.x; have; t += gridDim.x) {
+      const RowOf<GP> rw(p, tl, row);
+      if (hc == 0 && rw.j < tl.n && rw.hg < p.G && !rw.in)
+        report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
+      int lo = 0, hi = rw.ok ? min(tl.c - tl.n + rw.j + 1, tl.c) : 0;
+      if (rw.ok && p.spans) {
+        lo = max(p.spans[2 * rw.i], 0);
+        hi = min(hi, p.spans[2 * rw.i + 1]);
+      }
+      int ra[R_RUNS], re[R_RUNS];
       if (p.kv_map) {
 #pragma unroll
         for (int r = 0; r < R_RUNS; ++r) {
-          const int a = max(ra[r] - pos0, 0), b = min(re[r] - pos0, kChunk);
-          if (b > a) mk |= (b >= 64 ? ~0ull : ((1ull << b) - 1ull)) & ~((1ull << a) - 1ull);
-        }
-      } else {
-        const int a = max(lo - pos0, 0), b = min(hi - pos0, kChunk);
-        if (b > a) mk = (b >= 64 ? ~0ull : ((1ull << b) - 1ull)) & ~((1ull << a) - 1ull);
-      }
-      // holes (and flagged ids) read as -infinity
-      {
-        const int *ids = ids_s[ch % kTcStages];
-        const uint64_t bmask = p.bs >= 64 ? ~0ull : ((1ull << p.bs) - 1ull);
-        for (int k = 0; k * p.bs < kChunk; ++k)
-          if (ids[k] < 0) mk &= ~(bmask << (k * p.bs));
-      }
-      // most chunks are wholly readable: only partial ones pay for the mask
-      if (mk != ~0ull) {
-        const uint32_t m0 = (uint32_t)mk, m1 = (uint32_t)(mk >> 32);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          sv[e] = (m0 & (1u << e)) ? sv[e] : -INFINITY;
-          sv[e + 32] = (m1 & (1u << e)) ? sv[e + 32] : -INFINITY;
+          ra[r] = re[r] = 0;
+          if (rw.ok) {
+            const int32_t *rp = p.kv_map + ((size_t)rw.i * R_RUNS + r) * 2;
+            ra[r] = max(rp[0], 0);
+            re[r] = min(rp[0] + rp[1], hi);
+          }
         }
       }
-      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // 4 independent chains
-#pragma unroll
-      for (int e = 0; e < kChunk; ++e) mq[e & 3] = fmaxf(mq[e & 3], sv[e]);
-      const float mloc = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-      // ---- the previous P.V has finished: O, the P tile and the previous slot are free
-      if (ch > 0) {
-        fine = mbar_wait_bounded(&bar_pv, ph_pv, &abort_s, wait_ns) && fine;
-        ph_pv ^= 1u;
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int c = 0; c < tl.nch; ++c) {
+        const int x = g + c, st = x % ST;
+        // ---- S(x): load this thread's 32 columns, then hand the buffer back
+        fine = mbar_wait_bounded(&s_full[x & 1], (uint32_t)(x >> 1) & 1u, &abort_s, wait_ns) &&
+               fine;
         tc::fence_after();
-      }
-      issue_chunk<D>(p, tl, ch + kTcStages - 1, ids_s[(ch + kTcStages - 1) % kTcStages], ring,
-                     (ch + kTcStages - 1) % kTcStages, bs_shift);
-      // ---- online softmax, rescaling O only when the maximum grows past 2^8
-      const float m_new = fmaxf(m_run, mloc);
-      float scale_o = 1.f;
-      if (m_new != -INFINITY && (m_run == -INFINITY || m_new > m_run + 8.f)) {
-        scale_o = m_run == -INFINITY ? 1.f : exp2f(m_run - m_new);
-        l_run *= scale_o;
-        m_run = m_new;
-      }
-      if (ch > 0 && __any_sync(kAll, scale_o != 1.f)) {
-#pragma unroll 1
-        for (int c16 = 0; c16 < D; c16 += 16) {
+        float sv[HC];
+#pragma unroll
+        for (int c16 = 0; c16 < HC; c16 += 16) {
           float v[16];
-          tc::ld16(t_row + kOCol + c16, v);
-          tc::wait_ld();
+          tc::ld16(t_row + (uint32_t)((x & 1) * 64 + hc * HC + c16), v);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] *= scale_o;
-          tc::st16(t_row + kOCol + c16, v);
+          for (int e = 0; e < 16; ++e) sv[c16 + e] = v[e];
         }
-        tc::wait_st();
-      }
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-      const float mr = m_run == -INFINITY ? 0.f : m_run;  // all sv are -inf then: p = 0
+        tc::wait_ld();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[x & 1]);
+        // ---- mask: the row's window, then the staged rows that hold data
+        fine = mbar_wait_bounded(&kv_full[st], (uint32_t)(x / ST) & 1u, &abort_s, wait_ns) && fine;
+        const int pos0 = c * kChunk;
+        uint64_t mk = 0;
+        if (p.kv_map) {
 #pragma unroll
-      for (int e = 0; e < kChunk; e += 8) {
-        uint32_t h[4];
-#pragma unroll
-        for (int k2 = 0; k2 < 4; ++k2) {
-          const float a = ex2(sv[e + 2 * k2] - mr);
-          const float b = ex2(sv[e + 2 * k2 + 1] - mr);
-          ls[k2] += a + b;
-          h[k2] = h2_bits(__floats2half2_rn(a, b));
+          for (int r = 0; r < R_RUNS; ++r)
+            mk |= bit_range(max(ra[r] - pos0, 0), min(re[r] - pos0, kChunk));
+        } else {
+          mk = bit_range(max(lo - pos0, 0), min(hi - pos0, kChunk));
         }
-        *reinterpret_cast<uint4 *>(pt + tc::sw128(tid, e >> 3)) = make_uint4(h[0], h[1], h[2], h[3]);
+        mk &= vmask_s[st];
+        // most chunks are wholly readable: only partial ones pay for the mask
+        const uint32_t mh = (uint32_t)(mk >> (hc * HC));
+        if (mh != ~0u) {
+#pragma unroll
+          for (int e = 0; e < HC; ++e) sv[e] = (mh & (1u << e)) ? sv[e] : -INFINITY;
+        }
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // 4 independent chains
+#pragma unroll
+        for (int e = 0; e < HC; ++e) mq[e & 3] = fmaxf(mq[e & 3], sv[e]);
+        pm_s[x & 1][hc][row] = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        // both halves of the row (and their waits) meet here; a wait that ran
+        // out on either side ends the pair's loop at the same point
+        if (!pair_sync_and(pair, fine)) {
+          fine = false;
+          break;
+        }
+        const float mloc = fmaxf(pm_s[x & 1][0][row], pm_s[x & 1][1][row]);
+        // ---- online softmax, rescaling O only when the maximum grows past 2^8
+        const float m_new = fmaxf(m_run, mloc);
+        float scale_o = 1.f;
+        if (m_new != -INFINITY && (m_run == -INFINITY || m_new > m_run + 8.f)) {
+          scale_o = m_run == -INFINITY ? 1.f : exp2f(m_run - m_new);
+          l_run *= scale_o;
+          m_run = m_new;
+        }
+        if (c > 0 && __any_sync(kAll, scale_o != 1.f)) {
+          // P(x-1) V has been added to O
+          fine = mbar_wait_bounded(&pv_done[(x - 1) & 1], (uint32_t)((x - 1) >> 1) & 1u, &abort_s,
+                                   wait_ns) &&
+                 fine;
+          tc::fence_after();
+#pragma unroll 1
+          for (int c16 = hc * (D / 2); c16 < (hc + 1) * (D / 2); c16 += 16) {
+            float v[16];
+            tc::ld16(t_row + kOCol + c16, v);
+            tc::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] *= scale_o;
+            tc::st16(t_row + kOCol + c16, v);
+          }
+          tc::wait_st();
+        }
+        // ---- probabilities into P tile x % 2 (free once P(x-2) V has run)
+        if (x >= 2)
+          fine = mbar_wait_bounded(&pv_done[x & 1], (uint32_t)((x - 2) >> 1) & 1u, &abort_s,
+                                   wait_ns) &&
+                 fine;
+        uint8_t *pb = pt + (size_t)(x & 1) * C::PB;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        const float mr = m_run == -INFINITY ? 0.f : m_run;  // all sv are -inf then: p = 0
+#pragma unroll
+        for (int e = 0; e < HC; e += 8) {
+          uint32_t h[4];
+#pragma unroll
+          for (int k2 = 0; k2 < 4; ++k2) {
+            const float a = ex2(sv[e + 2 * k2] - mr);
+            const float b = ex2(sv[e + 2 * k2 + 1] - mr);
+            ls[k2] += a + b;
+            h[k2] = h2_bits(__floats2half2_rn(a, b));
+          }
+          *reinterpret_cast<uint4 *>(pb + tc::sw128(row, (hc * HC + e) >> 3)) =
+              make_uint4(h[0], h[1], h[2], h[3]);
+        }
+        l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        tc::fence_proxy_shared();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[x & 1]);
       }
-      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      tc::fence_proxy_shared();
-      tc::fence_before();
-      if (!__syncthreads_and(fine)) {
-        ok_run = false;
+      if (!fine) break;
+      const int x_last = g + tl.nch - 1;
+      g += tl.nch;
+      // ---- every S of this tile has been read: the next tile's Q goes in
+      Tile nx;
+      const bool have_next = tile_of<GP>(p, ts, n_tiles, t + (int)gridDim.x, nx);
+      if (have_next) {
+        write_q<D, GP>(p, nx, row, hc, qhi, qlo);
+        tc::fence_proxy_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_full);
+      }
+      // ---- the last P.V, then the normalised row
+      fine = mbar_wait_bounded(&pv_done[x_last & 1], (uint32_t)(x_last >> 1) & 1u, &abort_s,
+                               wait_ns) &&
+             fine;
+      tc::fence_after();
+      pl_s[hc][row] = l_run;
+      if (!pair_sync_and(pair, fine)) {
+        fine = false;
         break;
       }
-      // every thread has read this chunk's block ids: the slot takes those of
-      // chunk ch + S (copied in the next iteration)
-      load_chunk_ids(p, tl, ch + kTcStages, ids_s[ch % kTcStages]);
-      if (tid == 0) {
-        tc::fence_after();
-        // O += P V (V MN-major: LBO = the distance between its 64-dim halves)
-        const uint8_t *vt = ring + (size_t)(ch % kTcStages) * C::STAGE + C::KVB;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc::mma_f16(tmem + kOCol, tc::desc_sw128(smem_u32(pt) + kk * 32, 16, 1024),
-                      tc::desc_sw128(smem_u32(vt) + kk * 2048, kChunk * 128, 1024), idesc_o,
-                      ch > 0 || kk > 0);
-        tc::commit(&bar_pv);
-      }
-    }
-    cp_wait<0>();
-    if (!ok_run) break;
-    // ---- the last P.V, then the normalised row
-    bool fine = true;
-    if (tl.nch > 0) {
-      fine = mbar_wait_bounded(&bar_pv, ph_pv, &abort_s, wait_ns);
-      ph_pv ^= 1u;
-      tc::fence_after();
-    }
-    if (!__syncthreads_and(fine)) {
-      ok_run = false;
-      break;
-    }
-    const bool any = l_run > 0.f;
-    const float inv = any ? 1.f / l_run : 0.f;
-    float *dst = row_in ? p.out + ((size_t)i * p.Hq + (size_t)tl.kvh * p.G + hg) * D : nullptr;
+      const float l_row = pl_s[0][row] + pl_s[1][row];
+      const bool any = l_row > 0.f;
+      const float inv = any ? 1.f / l_row : 0.f;
+      float *dst = rw.in ? p.out + ((size_t)rw.i * p.Hq + (size_t)tl.kvh * p.G + rw.hg) * D : nullptr;
 #pragma unroll 1
-    for (int c16 = 0; c16 < D; c16 += 16) {
-      float v[16];
-      if (tl.nch > 0) {
+      for (int c16 = hc * (D / 2); c16 < (hc + 1) * (D / 2); c16 += 16) {
+        float v[16];
         tc::ld16(t_row + kOCol + c16, v);
         tc::wait_ld();
-      }
-      if (dst) {
+        if (dst) {
 #pragma unroll
-        for (int e = 0; e < 16; e += 4)
-          *reinterpret_cast<float4 *>(dst + c16 + e) =
-              tl.nch > 0 && any
-                  ? make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv)
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4 *>(dst + c16 + e) =
+                any ? make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
+      if (rw.in && p.lse && hc == 0)
+        p.lse[(size_t)rw.i * p.Hq + (size_t)tl.kvh * p.G + rw.hg] =
+            any ? (m_run + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
+      // the output has been read out of tensor memory
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free);
+      tl = nx;
+      have = have_next;
     }
-    if (row_in && p.lse)
-      p.lse[(size_t)i * p.Hq + (size_t)tl.kvh * p.G + hg] =
-          any ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
-    // every thread is done with tensor memory and the shared tiles of this
-    // tile before the next one overwrites them
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
   }
-  if (!ok_run && tid == 0) report(p.status, MT_STATUS_BIT_TIMEOUT);
-  cp_wait<0>();
+  if (!fine) {
+    abort_s = 1;  // the other roles stop waiting within a few polls
+    if (lane == 0) report(p.status, MT_STATUS_BIT_TIMEOUT);
+  }
   tc::fence_before();
   __syncthreads();
-  if (warp == 0) tc::dealloc(tmem, kTmemCols);
+  if (warp == 0) {
+    tc::fence_after();
+    tc::dealloc(tmem, kTmemCols);
+  }
 }
 
 template <int D, int GP>
-mt_status launch_t(const PrefillParams &p, int n_ctas, cudaStream_t s) {
+mt_status launch_t(const PrefillParams &p, const TcMaps &m, int n_ctas, cudaStream_t s) {
   static int configured_dev = -1;
   auto kern = prefill_tc_kernel<D, GP>;
   constexpr int smem = TcCfg<D>::SMEM;
@@ -482,17 +609,17 @@ mt_status launch_t(const PrefillParams &p, int n_ctas, cudaStream_t s) {
     if (st != MT_OK) return st;
     configured_dev = dev;
   }
-  return cuda_check(launch_pdl(kern, dim3(n_ctas), dim3(kTcRows), smem, s, p),
+  return cuda_check(launch_pdl(kern, dim3(n_ctas), dim3(kTcThreads), smem, s, p, m),
                     "prefill tc kernel launch");
 }
 
 template <int D>
-mt_status launch_d(int gp, const PrefillParams &p, int n_ctas, cudaStream_t s) {
+mt_status launch_d(int gp, const PrefillParams &p, const TcMaps &m, int n_ctas, cudaStream_t s) {
   switch (gp) {
-    case 1: return launch_t<D, 1>(p, n_ctas, s);
-    case 2: return launch_t<D, 2>(p, n_ctas, s);
-    case 4: return launch_t<D, 4>(p, n_ctas, s);
-    default: return launch_t<D, 8>(p, n_ctas, s);
+    case 1: return launch_t<D, 1>(p, m, n_ctas, s);
+    case 2: return launch_t<D, 2>(p, m, n_ctas, s);
+    case 4: return launch_t<D, 4>(p, m, n_ctas, s);
+    default: return launch_t<D, 8>(p, m, n_ctas, s);
   }
 }
 
@@ -505,8 +632,15 @@ bool prefill_tc_supported(mt_kv_format fmt, int head_dim, int block_size) {
 
 mt_status launch_prefill_tc(const PrefillParams &p, int head_dim, int gp, int n_ctas,
                             cudaStream_t stream) {
-  return head_dim == 64 ? launch_d<64>(gp, p, n_ctas, stream)
-                        : launch_d<128>(gp, p, n_ctas, stream);
+  // the pools as [cell][128-byte chunk][64 f16]; one copy = bs cells of one chunk
+  const long long n_cells = p.n_phys * p.bs;
+  TcMaps m;
+  mt_status st = encode_pool_map_3d(&m.k, p.k_pool, n_cells, (size_t)p.row_bytes, 1, p.bs);
+  if (st != MT_OK) return st;
+  st = encode_pool_map_3d(&m.v, p.v_pool, n_cells, (size_t)p.row_bytes, 1, p.bs);
+  if (st != MT_OK) return st;
+  return head_dim == 64 ? launch_d<64>(gp, p, m, n_ctas, stream)
+                        : launch_d<128>(gp, p, m, n_ctas, stream);
 }
 
 }  // namespace mtkv
