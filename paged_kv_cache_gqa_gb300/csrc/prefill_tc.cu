@@ -50,9 +50,11 @@ namespace {
 constexpr unsigned kAll = 0xffffffffu;
 constexpr int kTcRows = 128;       // rows per tile = tensor-memory lanes
 constexpr int kSoftWarps = 8;      // two threads per row
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kTcThreads = 320;
+constexpr int kLoadWarpK = 8;
+constexpr int kLoadWarpV = 9;
+constexpr int kMmaWarpS = 10;   // issues S = Q K^T
+constexpr int kMmaWarpO = 11;   // issues O += P V
+constexpr int kTcThreads = 384;
 constexpr int kChunk = 64;         // tokens per chunk
 constexpr int kOCol = 2 * 64;      // S double buffer: columns [0, 64), [64, 128); O: [128, 128 + d)
 constexpr uint32_t kTmemCols = 256;
@@ -190,9 +192,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ int ts[kMaxPrefillSeqs + 1];
   __shared__ uint32_t tmem_slot;
-  __shared__ __align__(8) uint64_t kv_full[ST], kv_free[ST], s_full[2], s_free[2], p_full[2],
-      pv_done[2], q_full, o_free, drain;
-  __shared__ uint64_t vmask_s[ST];       // staged rows that hold data (not a hole, < ctx)
+  __shared__ __align__(8) uint64_t k_full[ST], k_free[ST], v_full[ST], v_free[ST], s_full[2],
+      s_free[2], p_full[2], pv_done[2], q_full, o_free, drain[2];
+  __shared__ uint64_t mask_s[2][ST];     // [K / V] staged rows that hold data (not a hole, < ctx)
+  __shared__ uint64_t smask_s[2];        // the same for the chunk in S buffer x % 2
   __shared__ float pm_s[2][2][kTcRows];  // partial row maxima: [chunk parity][half][row]
   __shared__ float pl_s[2][kTcRows];     // partial row sums at the tile end
   __shared__ int abort_s;
@@ -230,18 +233,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (tid == 0) {
     for (int k = 0; k < ST; ++k) {
-      mbar_init(&kv_full[k], 1);
-      mbar_init(&kv_free[k], 1);
+      mbar_init(&k_full[k], 1);
+      mbar_init(&k_free[k], 1);
+      mbar_init(&v_full[k], 1);
+      mbar_init(&v_free[k], 1);
     }
     for (int k = 0; k < 2; ++k) {
-      mbar_init(&s_full[k], 1);
+      mbar_init(&s_full[k], 2);  // the MMAs' commit + the issuing thread (smask_s written)
       mbar_init(&s_free[k], kSoftWarps);
       mbar_init(&p_full[k], kSoftWarps);
       mbar_init(&pv_done[k], 1);
     }
     mbar_init(&q_full, kSoftWarps);
     mbar_init(&o_free, kSoftWarps);
-    mbar_init(&drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     abort_s = 0;
     fence_mbar_init();
   }
@@ -257,30 +263,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int bs_shift = p.bs == 32 ? 5 : 4;
   bool fine = true;  // false once a bounded wait ran out (or another role gave up)
 
-  if (warp == kLoadWarp) {
+  if (warp == kLoadWarpK || warp == kLoadWarpV) {
     // ================================================================ load
+    // one warp stages K, one V: a K stage is refilled as soon as its S has
+    // been computed, a V stage once its P.V has run
+    const int kv = warp == kLoadWarpV;
+    uint64_t *full = kv ? v_full : k_full;
+    uint64_t *empty = kv ? v_free : k_free;
+    const CUtensorMap *map = kv ? &maps.v : &maps.k;
+    const int nb = kChunk >> bs_shift;
+    // lane k < 64 / bs reads the table entry of block k of a chunk, one chunk
+    // ahead of its use (checked when used)
+    auto fetch = [&](const Tile &u, int c) -> int {
+      const int pos = c * kChunk + (lane << bs_shift);
+      return (lane < nb && pos < u.c) ? p.table[(size_t)u.s * p.max_blocks + (pos >> bs_shift)]
+                                      : -1;
+    };
     int g = 0;  // chunks staged by this CTA so far (all tiles)
-    for (int t = blockIdx.x; fine; t += gridDim.x) {
-      Tile tl;
-      if (!tile_of<GP>(p, ts, n_tiles, t, tl)) break;
+    Tile tl;
+    bool have = tile_of<GP>(p, ts, n_tiles, blockIdx.x, tl);
+    int raw_next = have ? fetch(tl, 0) : -1;
+    for (int t = blockIdx.x; have && fine; t += gridDim.x) {
+      Tile nx;
+      const bool have_next = tile_of<GP>(p, ts, n_tiles, t + (int)gridDim.x, nx);
       for (int c = 0; c < tl.nch; ++c, ++g) {
+        int phys = raw_next;
+        raw_next = c + 1 < tl.nch ? fetch(tl, c + 1) : (have_next ? fetch(nx, 0) : -1);
         const int st = g % ST;
-        if (g >= ST && !mbar_wait_bounded(&kv_free[st], (uint32_t)((g / ST) - 1) & 1u, &abort_s,
-                                          wait_ns)) {
+        if (g >= ST &&
+            !mbar_wait_bounded(&empty[st], (uint32_t)((g / ST) - 1) & 1u, &abort_s, wait_ns)) {
           fine = false;
           break;
         }
-        // lane k < 64 / bs: block k of the chunk
-        const int nb = kChunk >> bs_shift;
-        const int pos = c * kChunk + (lane << bs_shift);
-        int phys = -1;
-        if (lane < nb && pos < tl.c) {
-          phys = p.table[(size_t)tl.s * p.max_blocks + (pos >> bs_shift)];
-          if (phys < -1 || (phys >= 0 && (long long)phys >= p.n_phys)) {
-            report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
-            phys = -1;
-          }
+        if (phys < -1 || (phys >= 0 && (long long)phys >= p.n_phys)) {
+          report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
+          phys = -1;
         }
+        const int pos = c * kChunk + (lane << bs_shift);
         const uint64_t mine =
             phys >= 0 ? bit_range(lane << bs_shift, (lane << bs_shift) + min(p.bs, tl.c - pos))
                       : 0ull;
@@ -288,77 +307,90 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t m_hi = __reduce_or_sync(kAll, (uint32_t)(mine >> 32));
         const int n_valid = __popc(__ballot_sync(kAll, phys >= 0));
         if (lane == 0) {
-          vmask_s[st] = ((uint64_t)m_hi << 32) | m_lo;
-          mbar_arrive_expect_tx(&kv_full[st], (uint32_t)(n_valid * 2 * C::HALVES * 128) << bs_shift);
+          mask_s[kv][st] = ((uint64_t)m_hi << 32) | m_lo;
+          mbar_arrive_expect_tx(&full[st], (uint32_t)(n_valid * C::HALVES * 128) << bs_shift);
         }
         __syncwarp();
-        // one copy per (block, K / V, 64-dim half): lane = (k * 2 + kv) * HALVES + h
-        constexpr int PER = 2 * C::HALVES;
-        const int k = lane / PER, r = lane % PER;
+        // one copy per (block, 64-dim half): lane = k * HALVES + h
+        const int k = lane / C::HALVES, h = lane % C::HALVES;
         const int pk = __shfl_sync(kAll, phys, k & 31);
         if (k < nb && pk >= 0) {
-          const int kv = r / C::HALVES, h = r % C::HALVES;
           const uint32_t dst = smem_u32(ring) + (uint32_t)(st * C::STAGE + kv * C::KVB +
                                                            h * (kChunk * 128) + (k << bs_shift) * 128);
-          tma_rows(dst, kv ? &maps.v : &maps.k, tl.kvh * C::HALVES + h, pk << bs_shift,
-                   &kv_full[st]);
+          tma_rows(dst, map, tl.kvh * C::HALVES + h, pk << bs_shift, &full[st]);
         }
       }
+      tl = nx;
+      have = have_next;
     }
     // copies still in flight land before the CTA leaves (the last fill of each stage)
     for (int k = 0; k < ST; ++k) {
       if (g <= k) continue;
       const int gl = g - 1 - ((g - 1 - k) % ST);
-      if (!mbar_wait_bounded(&kv_full[k], (uint32_t)(gl / ST) & 1u, &abort_s, wait_ns)) fine = false;
+      if (!mbar_wait_bounded(&full[k], (uint32_t)(gl / ST) & 1u, &abort_s, wait_ns)) fine = false;
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarpS || warp == kMmaWarpO) {
     // ================================================================= MMA
+    // two issuing warps share the tensor pipe: while one waits or commits,
+    // the other's MMAs keep it busy (one MMA is accepted every ~50 cycles)
+    const int role = warp - kMmaWarpS;  // 0: S, 1: P.V
     constexpr uint32_t idesc_s = tc::idesc_f16(kTcRows, kChunk, false);
     constexpr uint32_t idesc_o = tc::idesc_f16(kTcRows, D, true);
-    // S(x) = Q_hi K^T + Q_lo K^T into S buffer x % 2, once chunk x is staged
-    // and the softmax has read S(x - 2) from that buffer
-    auto issue_s = [&](int x) -> bool {
-      const int st = x % ST;
-      if (!mbar_wait_bounded(&kv_full[st], (uint32_t)(x / ST) & 1u, &abort_s, wait_ns)) return false;
-      if (x >= 2 &&
-          !mbar_wait_bounded(&s_free[x & 1], (uint32_t)((x - 2) >> 1) & 1u, &abort_s, wait_ns))
-        return false;
-      tc::fence_after();
-      if (lane == 0) {
-        const uint32_t kt = smem_u32(ring) + (uint32_t)(st * C::STAGE);
-        const uint32_t dcol = tmem + (uint32_t)((x & 1) * 64);
-#pragma unroll
-        for (int hf = 0; hf < C::HALVES; ++hf)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t qo = (uint32_t)(hf * kTcRows * 128 + kk * 32);
-            const uint64_t bd = tc::desc_sw128(kt + hf * kChunk * 128 + kk * 32, 16, 1024);
-            tc::mma_f16(dcol, tc::desc_sw128(smem_u32(qhi) + qo, 16, 1024), bd, idesc_s,
-                        hf + kk > 0);
-            tc::mma_f16(dcol, tc::desc_sw128(smem_u32(qlo) + qo, 16, 1024), bd, idesc_s, true);
-          }
-        tc::commit(&s_full[x & 1]);
-      }
-      __syncwarp();
-      return true;
-    };
+    // descriptor bases, advanced per operand by whole 16-byte units
+    const uint64_t d_qhi = tc::desc_sw128(smem_u32(qhi), 16, 1024);
+    const uint64_t d_qlo = tc::desc_sw128(smem_u32(qlo), 16, 1024);
+    const uint64_t d_k = tc::desc_sw128(smem_u32(ring), 16, 1024);
+    const uint64_t d_v = tc::desc_sw128(smem_u32(ring) + C::KVB, kChunk * 128, 1024);
+    const uint64_t d_p = tc::desc_sw128(smem_u32(pt), 16, 1024);
     int g = 0;
     for (int t = blockIdx.x, k = 0; fine; t += gridDim.x, ++k) {
       Tile tl;
       if (!tile_of<GP>(p, ts, n_tiles, t, tl)) break;
-      // this tile's Q is in place
-      if (!mbar_wait_bounded(&q_full, (uint32_t)k & 1u, &abort_s, wait_ns) || !issue_s(g)) {
+      // S: this tile's Q is in place
+      if (role == 0 && !mbar_wait_bounded(&q_full, (uint32_t)k & 1u, &abort_s, wait_ns)) {
         fine = false;
         break;
       }
       for (int c = 0; c < tl.nch; ++c) {
         const int x = g + c, st = x % ST;
-        if (c + 1 < tl.nch && !issue_s(x + 1)) {
+        if (role == 0) {
+          // S(x) = Q_hi K^T + Q_lo K^T into S buffer x % 2, once K of chunk x
+          // is staged and the softmax has read S(x - 2) (and its row mask)
+          if (!mbar_wait_bounded(&k_full[st], (uint32_t)(x / ST) & 1u, &abort_s, wait_ns) ||
+              (x >= 2 && !mbar_wait_bounded(&s_free[x & 1], (uint32_t)((x - 2) >> 1) & 1u,
+                                            &abort_s, wait_ns))) {
+            fine = false;
+            break;
+          }
+          tc::fence_after();
+          if (lane == 0) {
+            // the chunk's row mask goes with S(x) (the K stage may be refilled
+            // as soon as S(x) is done); published by this thread's arrive below
+            smask_s[x & 1] = mask_s[0][st];
+            const uint64_t kd = tc::desc_advance(d_k, (uint32_t)(st * C::STAGE));
+            const uint32_t dcol = tmem + (uint32_t)((x & 1) * 64);
+#pragma unroll
+            for (int hf = 0; hf < C::HALVES; ++hf)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t qo = (uint32_t)(hf * kTcRows * 128 + kk * 32);
+                const uint64_t bd = tc::desc_advance(kd, (uint32_t)(hf * kChunk * 128 + kk * 32));
+                tc::mma_f16(dcol, tc::desc_advance(d_qhi, qo), bd, idesc_s, hf + kk > 0);
+                tc::mma_f16(dcol, tc::desc_advance(d_qlo, qo), bd, idesc_s, true);
+              }
+            tc::commit(&s_full[x & 1]);
+            tc::commit(&k_free[st]);
+            mbar_arrive(&s_full[x & 1]);
+          }
+          __syncwarp();
+          continue;
+        }
+        // P.V: V of chunk x staged; its rows without data (holes, past the context) -> 0
+        if (!mbar_wait_bounded(&v_full[st], (uint32_t)(x / ST) & 1u, &abort_s, wait_ns)) {
           fine = false;
           break;
         }
-        // V rows without data (holes, past the context) -> 0
-        const uint64_t vm = vmask_s[st];
+        const uint64_t vm = mask_s[1][st];
         if (vm != ~0ull) {
           uint8_t *vt = ring + (size_t)st * C::STAGE + C::KVB;
           for (int u = lane; u < kChunk * C::HALVES * 8; u += 32) {
@@ -380,24 +412,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::fence_after();
         if (lane == 0) {
           // O += P V (V MN-major: LBO = the distance between its 64-dim halves)
-          const uint32_t vt = smem_u32(ring) + (uint32_t)(st * C::STAGE + C::KVB);
-          const uint32_t pb = smem_u32(pt) + (uint32_t)((x & 1) * C::PB);
+          const uint64_t vd = tc::desc_advance(d_v, (uint32_t)(st * C::STAGE));
+          const uint64_t pd = tc::desc_advance(d_p, (uint32_t)((x & 1) * C::PB));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc::mma_f16(tmem + kOCol, tc::desc_sw128(pb + kk * 32, 16, 1024),
-                        tc::desc_sw128(vt + kk * 2048, kChunk * 128, 1024), idesc_o,
-                        c > 0 || kk > 0);
+            tc::mma_f16(tmem + kOCol, tc::desc_advance(pd, kk * 32),
+                        tc::desc_advance(vd, kk * 2048), idesc_o, c > 0 || kk > 0);
           tc::commit(&pv_done[x & 1]);
-          tc::commit(&kv_free[st]);
+          tc::commit(&v_free[st]);
         }
         __syncwarp();
       }
       g += tl.nch;
     }
     // every MMA issued here has completed before tensor memory is released
-    if (lane == 0) tc::commit(&drain);
+    if (lane == 0) tc::commit(&drain[role]);
     __syncwarp();
-    if (!mbar_wait_bounded(&drain, 0, &abort_s, wait_ns)) fine = false;
+    if (!mbar_wait_bounded(&drain[role], 0, &abort_s, wait_ns)) fine = false;
   } else {
     // ============================================================= softmax
     const int row = tid & (kTcRows - 1), hc = tid >> 7, pair = 1 + (warp & 3);
@@ -413,6 +444,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     int g = 0;
     for (int t = blockIdx.x; have; t += gridDim.x) {
+      // the next tile's query rows head for L2 while this tile runs
+      Tile nx;
+      const bool have_next = tile_of<GP>(p, ts, n_tiles, t + (int)gridDim.x, nx);
+      if (have_next) {
+        const RowOf<GP> rn(p, nx, row);
+        if (rn.ok) {
+          const float *qn =
+              p.q + ((size_t)rn.i * p.Hq + (size_t)nx.kvh * p.G + rn.hg) * D + hc * (D / 2);
+#pragma unroll
+          for (int e = 0; e < D / 2; e += 32)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + e));
+        }
+      }
       const RowOf<GP> rw(p, tl, row);
       if (hc == 0 && rw.j < tl.n && rw.hg < p.G && !rw.in)
         report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
@@ -435,7 +479,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       float m_run = -INFINITY, l_run = 0.f;
       for (int c = 0; c < tl.nch; ++c) {
-        const int x = g + c, st = x % ST;
+        const int x = g + c;
         // ---- S(x): load this thread's 32 columns, then hand the buffer back
         fine = mbar_wait_bounded(&s_full[x & 1], (uint32_t)(x >> 1) & 1u, &abort_s, wait_ns) &&
                fine;
@@ -448,12 +492,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) sv[c16 + e] = v[e];
         }
+        const uint64_t vm = smask_s[x & 1];
+        // P tile x % 2 is free once P(x-2) V has run: polled now, used below
+        const bool p_free = x < 2 || mbar_try_wait(&pv_done[x & 1], (uint32_t)((x - 2) >> 1) & 1u);
         tc::wait_ld();
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free[x & 1]);
         // ---- mask: the row's window, then the staged rows that hold data
-        fine = mbar_wait_bounded(&kv_full[st], (uint32_t)(x / ST) & 1u, &abort_s, wait_ns) && fine;
         const int pos0 = c * kChunk;
         uint64_t mk = 0;
         if (p.kv_map) {
@@ -463,7 +509,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         } else {
           mk = bit_range(max(lo - pos0, 0), min(hi - pos0, kChunk));
         }
-        mk &= vmask_s[st];
+        mk &= vm;
         // most chunks are wholly readable: only partial ones pay for the mask
         const uint32_t mh = (uint32_t)(mk >> (hc * HC));
         if (mh != ~0u) {
@@ -506,8 +552,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc::wait_st();
         }
-        // ---- probabilities into P tile x % 2 (free once P(x-2) V has run)
-        if (x >= 2)
+        // ---- probabilities into P tile x % 2
+        if (!p_free)
           fine = mbar_wait_bounded(&pv_done[x & 1], (uint32_t)((x - 2) >> 1) & 1u, &abort_s,
                                    wait_ns) &&
                  fine;
@@ -537,8 +583,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int x_last = g + tl.nch - 1;
       g += tl.nch;
       // ---- every S of this tile has been read: the next tile's Q goes in
-      Tile nx;
-      const bool have_next = tile_of<GP>(p, ts, n_tiles, t + (int)gridDim.x, nx);
       if (have_next) {
         write_q<D, GP>(p, nx, row, hc, qhi, qlo);
         tc::fence_proxy_shared();

@@ -65,6 +65,13 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 
+// The descriptor of the operand `bytes` further on: the start address field
+// holds address / 16 in 14 bits and every shared address is below 256 KB,
+// so the advance never carries out of the field.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t bytes) {
+  return d + (uint64_t)(bytes >> 4);
+}
+
 // Instruction descriptor of kind::f16: f16 A and B, f32 accumulator, M x N;
 // b_mn: B operand MN-major (else K-major); A is K-major.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn) {
