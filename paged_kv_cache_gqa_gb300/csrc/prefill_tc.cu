@@ -9,27 +9,31 @@
 //
 // How (GB300): a tile is 128 (query, head) rows of one KV head (one
 // tensor-memory lane per row) and the sequence's positions up to the tile's
-// last query, in chunks of 64 tokens. A CTA takes whole tiles round-robin
+// last query, in chunks of 128 tokens. A CTA takes whole tiles round-robin
 // (no split-K combine) and runs three roles that hand work to each other
 // through mbarriers only — no CTA-wide barrier inside the chunk loop:
-//   * a load warp reads the chunk's block ids from the table and stages the
-//     chunk's K and V head slices with one tensor copy (TMA, 128-byte
-//     swizzle) per block and 64-dim half into a ring of stages; holes are not
-//     read at all;
-//   * an MMA warp (one thread issues) computes S(c+1) = Q_hi K^T + Q_lo K^T
-//     (M = 128, N = 64, f16 in, f32 accumulated in tensor memory; q = Q_hi +
-//     Q_lo to ~2^-22, so scores keep float32 accuracy) ahead of the softmax,
-//     then O += P(c) V(c) once the probabilities of chunk c are written (V
-//     read MN-major straight from its stage). V rows of holes and past the
-//     context are zeroed first: P is 0 there but 0 * NaN would not be;
+//   * two load warps read the chunk's block ids from the table (a chunk
+//     ahead) and stage its K and its V head slices with one tensor copy (TMA,
+//     128-byte swizzle) per block and 64-dim half into two rings of stages; a
+//     K stage is refilled as soon as its scores are computed, a V stage once
+//     its P.V has run; holes are not read at all;
+//   * one MMA warp computes S(c) = Q_hi K^T + Q_lo K^T (M = 128, N = 128,
+//     f16 in, f32 accumulated in tensor memory; q = Q_hi + Q_lo to ~2^-22, so
+//     scores keep float32 accuracy) up to two chunks ahead of the softmax;
+//     another computes O += P(c) V(c) once the probabilities of chunk c are
+//     in tensor memory (P read from tensor memory, V MN-major straight from
+//     its stage), after zeroing the V rows of holes and past the context (P
+//     is 0 there but 0 * NaN would not be). The tensor pipe accepts one MMA
+//     every ~50 cycles whichever warp issues it, so while one warp waits or
+//     commits, the other's MMAs keep it busy;
 //   * eight softmax warps, two threads per row (warps w and w + 4 share the
-//     tensor-memory lanes 32 (w % 4) .. + 31; each takes 32 of the 64 score
+//     tensor-memory lanes 32 (w % 4) .. + 31; each takes 64 of the 128 score
 //     columns and half of O): load S, mask it, exchange the row maximum with
 //     the partner through shared memory and a two-warp named barrier, run the
-//     online softmax, and write f16 probabilities to one of two swizzled P
-//     tiles. The output row in tensor memory is rescaled only when the
-//     running maximum grows by more than 2^8 (probabilities then stay below
-//     256, exact in f16); a tile's output is normalised once at the end.
+//     online softmax, and store f16 probabilities into one of two P buffers
+//     in tensor memory. The output row is rescaled only when the running
+//     maximum grows by more than 2^8 (probabilities then stay below 256,
+//     exact in f16); a tile's output is normalised once at the end.
 // The next tile's Q is written as soon as the last S of a tile is read, so
 // its first scores are computed while the previous tile's output is stored.
 #include <limits.h>
@@ -55,19 +59,21 @@ constexpr int kLoadWarpV = 9;
 constexpr int kMmaWarpS = 10;   // issues S = Q K^T
 constexpr int kMmaWarpO = 11;   // issues O += P V
 constexpr int kTcThreads = 384;
-constexpr int kChunk = 64;         // tokens per chunk
-constexpr int kOCol = 2 * 64;      // S double buffer: columns [0, 64), [64, 128); O: [128, 128 + d)
-constexpr uint32_t kTmemCols = 256;
+constexpr int kChunk = 128;        // tokens per chunk
+// tensor-memory columns: S double buffer [0, 128), [128, 256); O [256, 256 + d);
+// P (f16 pairs) double buffer [384, 448), [448, 512)
+constexpr int kOCol = 2 * kChunk;
+constexpr int kPCol = 384;
+constexpr uint32_t kTmemCols = 512;
 
 template <int D>
 struct TcCfg {
   static constexpr int HALVES = D / 64;                 // 64-dim halves of a head
   static constexpr int QB = HALVES * kTcRows * 128;     // one Q tile (hi or lo)
-  static constexpr int PB = kTcRows * 128;              // one P tile: 128 rows x 64 tokens
   static constexpr int KVB = HALVES * kChunk * 128;     // K (or V) of one chunk
-  static constexpr int STAGE = 2 * KVB;
-  static constexpr int STAGES = D == 64 ? 6 : 3;
-  static constexpr int SMEM = 1024 + 2 * QB + 2 * PB + STAGES * STAGE;
+  static constexpr int STAGE = 2 * KVB;                 // K and V of one chunk
+  static constexpr int STAGES = D == 64 ? 4 : 2;
+  static constexpr int SMEM = 1024 + 2 * QB + STAGES * STAGE;
 };
 static_assert(TcCfg<128>::SMEM + 8 * 1024 <= 227 * 1024, "shared memory");
 static_assert(TcCfg<64>::SMEM + 8 * 1024 <= 227 * 1024, "shared memory");
@@ -194,16 +200,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(8) uint64_t k_full[ST], k_free[ST], v_full[ST], v_free[ST], s_full[2],
       s_free[2], p_full[2], pv_done[2], q_full, o_free, drain[2];
-  __shared__ uint64_t mask_s[2][ST];     // [K / V] staged rows that hold data (not a hole, < ctx)
-  __shared__ uint64_t smask_s[2];        // the same for the chunk in S buffer x % 2
+  __shared__ uint64_t mask_s[2][ST][2];  // [K / V] staged rows that hold data (not a hole, < ctx)
+  __shared__ uint64_t smask_s[2][2];     // the same for the chunk in S buffer x % 2
   __shared__ float pm_s[2][2][kTcRows];  // partial row maxima: [chunk parity][half][row]
   __shared__ float pl_s[2][kTcRows];     // partial row sums at the tile end
   __shared__ int abort_s;
   uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *qhi = base;
   uint8_t *qlo = base + C::QB;
-  uint8_t *pt = base + 2 * C::QB;  // two P tiles
-  uint8_t *ring = pt + 2 * C::PB;
+  uint8_t *ring = base + 2 * C::QB;
   pdl_enter();
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -299,15 +304,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
           phys = -1;
         }
-        const int pos = c * kChunk + (lane << bs_shift);
-        const uint64_t mine =
-            phys >= 0 ? bit_range(lane << bs_shift, (lane << bs_shift) + min(p.bs, tl.c - pos))
-                      : 0ull;
-        const uint32_t m_lo = __reduce_or_sync(kAll, (uint32_t)mine);
-        const uint32_t m_hi = __reduce_or_sync(kAll, (uint32_t)(mine >> 32));
+        // rows [a, b) of the chunk hold data (block k = lane)
+        const int a = lane << bs_shift, pos = c * kChunk + a;
+        const int b = phys >= 0 ? a + min(p.bs, tl.c - pos) : a;
+        const uint64_t m0 = bit_range(min(a, 64), min(b, 64));
+        const uint64_t m1 = bit_range(max(a - 64, 0), max(b - 64, 0));
+        const uint32_t w0 = __reduce_or_sync(kAll, (uint32_t)m0);
+        const uint32_t w1 = __reduce_or_sync(kAll, (uint32_t)(m0 >> 32));
+        const uint32_t w2 = __reduce_or_sync(kAll, (uint32_t)m1);
+        const uint32_t w3 = __reduce_or_sync(kAll, (uint32_t)(m1 >> 32));
         const int n_valid = __popc(__ballot_sync(kAll, phys >= 0));
         if (lane == 0) {
-          mask_s[kv][st] = ((uint64_t)m_hi << 32) | m_lo;
+          mask_s[kv][st][0] = ((uint64_t)w1 << 32) | w0;
+          mask_s[kv][st][1] = ((uint64_t)w3 << 32) | w2;
           mbar_arrive_expect_tx(&full[st], (uint32_t)(n_valid * C::HALVES * 128) << bs_shift);
         }
         __syncwarp();
@@ -341,7 +350,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint64_t d_qlo = tc::desc_sw128(smem_u32(qlo), 16, 1024);
     const uint64_t d_k = tc::desc_sw128(smem_u32(ring), 16, 1024);
     const uint64_t d_v = tc::desc_sw128(smem_u32(ring) + C::KVB, kChunk * 128, 1024);
-    const uint64_t d_p = tc::desc_sw128(smem_u32(pt), 16, 1024);
     int g = 0;
     for (int t = blockIdx.x, k = 0; fine; t += gridDim.x, ++k) {
       Tile tl;
@@ -366,9 +374,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (lane == 0) {
             // the chunk's row mask goes with S(x) (the K stage may be refilled
             // as soon as S(x) is done); published by this thread's arrive below
-            smask_s[x & 1] = mask_s[0][st];
+            smask_s[x & 1][0] = mask_s[0][st][0];
+            smask_s[x & 1][1] = mask_s[0][st][1];
             const uint64_t kd = tc::desc_advance(d_k, (uint32_t)(st * C::STAGE));
-            const uint32_t dcol = tmem + (uint32_t)((x & 1) * 64);
+            const uint32_t dcol = tmem + (uint32_t)((x & 1) * kChunk);
 #pragma unroll
             for (int hf = 0; hf < C::HALVES; ++hf)
 #pragma unroll
@@ -390,12 +399,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           fine = false;
           break;
         }
-        const uint64_t vm = mask_s[1][st];
-        if (vm != ~0ull) {
+        const uint64_t vm0 = mask_s[1][st][0], vm1 = mask_s[1][st][1];
+        if ((vm0 & vm1) != ~0ull) {
           uint8_t *vt = ring + (size_t)st * C::STAGE + C::KVB;
           for (int u = lane; u < kChunk * C::HALVES * 8; u += 32) {
-            const int line = u >> 3;  // half * 64 + row
-            if (!((vm >> (line & 63)) & 1ull))
+            const int line = u >> 3, r = line & (kChunk - 1);  // line = half * 128 + row
+            if (!(((r < 64 ? vm0 : vm1) >> (r & 63)) & 1ull))
               *reinterpret_cast<uint4 *>(vt + (size_t)line * 128 + (u & 7) * 16) =
                   make_uint4(0, 0, 0, 0);
           }
@@ -411,13 +420,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc::fence_after();
         if (lane == 0) {
-          // O += P V (V MN-major: LBO = the distance between its 64-dim halves)
+          // O += P V (P from tensor memory; V MN-major: LBO = the distance
+          // between its 64-dim halves)
           const uint64_t vd = tc::desc_advance(d_v, (uint32_t)(st * C::STAGE));
-          const uint64_t pd = tc::desc_advance(d_p, (uint32_t)((x & 1) * C::PB));
+          const uint32_t pa = tmem + (uint32_t)(kPCol + (x & 1) * (kChunk / 2));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc::mma_f16(tmem + kOCol, tc::desc_advance(pd, kk * 32),
-                        tc::desc_advance(vd, kk * 2048), idesc_o, c > 0 || kk > 0);
+          for (int kk = 0; kk < kChunk / 16; ++kk)
+            tc::mma_f16_ts(tmem + kOCol, pa + kk * 8, tc::desc_advance(vd, kk * 2048), idesc_o,
+                           c > 0 || kk > 0);
           tc::commit(&pv_done[x & 1]);
           tc::commit(&v_free[st]);
         }
@@ -433,7 +443,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ============================================================= softmax
     const int row = tid & (kTcRows - 1), hc = tid >> 7, pair = 1 + (warp & 3);
     const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // lanes of this row
-    constexpr int HC = kChunk / 2;  // score columns per thread
+    constexpr int HC = kChunk / 2;  // score columns per thread: [HC hc, HC hc + HC)
     Tile tl;
     bool have = tile_of<GP>(p, ts, n_tiles, blockIdx.x, tl);
     if (have) {
@@ -488,11 +498,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int c16 = 0; c16 < HC; c16 += 16) {
           float v[16];
-          tc::ld16(t_row + (uint32_t)((x & 1) * 64 + hc * HC + c16), v);
+          tc::ld16(t_row + (uint32_t)((x & 1) * kChunk + hc * HC + c16), v);
 #pragma unroll
           for (int e = 0; e < 16; ++e) sv[c16 + e] = v[e];
         }
-        const uint64_t vm = smask_s[x & 1];
+        const uint64_t vm = smask_s[x & 1][hc];
         // P tile x % 2 is free once P(x-2) V has run: polled now, used below
         const bool p_free = x < 2 || mbar_try_wait(&pv_done[x & 1], (uint32_t)((x - 2) >> 1) & 1u);
         tc::wait_ld();
@@ -500,21 +510,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free[x & 1]);
         // ---- mask: the row's window, then the staged rows that hold data
-        const int pos0 = c * kChunk;
+        const int pos0 = c * kChunk + hc * HC;  // position of this thread's first column
         uint64_t mk = 0;
         if (p.kv_map) {
 #pragma unroll
           for (int r = 0; r < R_RUNS; ++r)
-            mk |= bit_range(max(ra[r] - pos0, 0), min(re[r] - pos0, kChunk));
+            mk |= bit_range(max(ra[r] - pos0, 0), min(re[r] - pos0, HC));
         } else {
-          mk = bit_range(max(lo - pos0, 0), min(hi - pos0, kChunk));
+          mk = bit_range(max(lo - pos0, 0), min(hi - pos0, HC));
         }
         mk &= vm;
         // most chunks are wholly readable: only partial ones pay for the mask
-        const uint32_t mh = (uint32_t)(mk >> (hc * HC));
-        if (mh != ~0u) {
+        if (mk != ~0ull) {
+          const uint32_t m0 = (uint32_t)mk, m1 = (uint32_t)(mk >> 32);
 #pragma unroll
-          for (int e = 0; e < HC; ++e) sv[e] = (mh & (1u << e)) ? sv[e] : -INFINITY;
+          for (int e = 0; e < 32; ++e) {
+            sv[e] = (m0 & (1u << e)) ? sv[e] : -INFINITY;
+            sv[e + 32] = (m1 & (1u << e)) ? sv[e + 32] : -INFINITY;
+          }
         }
         float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // 4 independent chains
 #pragma unroll
@@ -557,24 +570,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           fine = mbar_wait_bounded(&pv_done[x & 1], (uint32_t)((x - 2) >> 1) & 1u, &abort_s,
                                    wait_ns) &&
                  fine;
-        uint8_t *pb = pt + (size_t)(x & 1) * C::PB;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
         const float mr = m_run == -INFINITY ? 0.f : m_run;  // all sv are -inf then: p = 0
+        const uint32_t p_row = t_row + (uint32_t)(kPCol + (x & 1) * (kChunk / 2) + hc * (HC / 2));
 #pragma unroll
-        for (int e = 0; e < HC; e += 8) {
-          uint32_t h[4];
+        for (int e = 0; e < HC; e += 32) {
+          uint32_t h[16];
 #pragma unroll
-          for (int k2 = 0; k2 < 4; ++k2) {
+          for (int k2 = 0; k2 < 16; ++k2) {
             const float a = ex2(sv[e + 2 * k2] - mr);
             const float b = ex2(sv[e + 2 * k2 + 1] - mr);
-            ls[k2] += a + b;
+            ls[k2 & 3] += a + b;
             h[k2] = h2_bits(__floats2half2_rn(a, b));
           }
-          *reinterpret_cast<uint4 *>(pb + tc::sw128(row, (hc * HC + e) >> 3)) =
-              make_uint4(h[0], h[1], h[2], h[3]);
+          tc::st16u(p_row + (uint32_t)(e / 2), h);
         }
         l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        tc::fence_proxy_shared();
+        tc::wait_st();
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[x & 1]);

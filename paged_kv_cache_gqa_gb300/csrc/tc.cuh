@@ -16,7 +16,9 @@
 //     by 2048 bytes;
 //   * the f32 accumulator of an M = 128 MMA: row i in tensor-memory lane i,
 //     column j at column (base + j); warp w of the CTA reads lanes
-//     [32 (w % 4), 32 (w % 4) + 32).
+//     [32 (w % 4), 32 (w % 4) + 32);
+//   * an A operand in tensor memory (M = 128, f16): row i in lane i, column
+//     c holding elements (2c, 2c+1), the lower one in the low half.
 #pragma once
 
 #include <stdint.h>
@@ -89,6 +91,18 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
       : "memory");
 }
 
+// D (tensor memory) = A (tensor memory) . B (+ D when acc): A row i in lane
+// i, column c holding its elements (2c, 2c+1), the lower one in the low half;
+// a K step of 16 is 8 columns.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                           uint32_t idesc, bool acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc ? 1u : 0u)
+      : "memory");
+}
+
 // Arrive on `bar` once every MMA issued so far by this thread has completed.
 __device__ __forceinline__ void commit(uint64_t *bar) {
   asm volatile(
@@ -121,6 +135,16 @@ __device__ __forceinline__ void st16(uint32_t taddr, const float (&v)[16]) {
       "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
       "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
       "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's lane from raw words.
+__device__ __forceinline__ void st16u(uint32_t taddr, const uint32_t (&w)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+      "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
       : "memory");
 }
 
