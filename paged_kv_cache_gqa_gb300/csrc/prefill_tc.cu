@@ -606,6 +606,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                wait_ns) &&
              fine;
       tc::fence_after();
+      // this thread's half of the output row out of tensor memory (every load
+      // in flight, one wait), then O is handed to the next tile's first P.V
+      constexpr int DH = D / 2;
+      float o[DH];
+#pragma unroll
+      for (int c16 = 0; c16 < DH; c16 += 16) {
+        float v[16];
+        tc::ld16(t_row + (uint32_t)(kOCol + hc * DH + c16), v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) o[c16 + e] = v[e];
+      }
+      tc::wait_ld();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free);
       pl_s[hc][row] = l_run;
       if (!pair_sync_and(pair, fine)) {
         fine = false;
@@ -614,27 +629,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float l_row = pl_s[0][row] + pl_s[1][row];
       const bool any = l_row > 0.f;
       const float inv = any ? 1.f / l_row : 0.f;
-      float *dst = rw.in ? p.out + ((size_t)rw.i * p.Hq + (size_t)tl.kvh * p.G + rw.hg) * D : nullptr;
-#pragma unroll 1
-      for (int c16 = hc * (D / 2); c16 < (hc + 1) * (D / 2); c16 += 16) {
-        float v[16];
-        tc::ld16(t_row + kOCol + c16, v);
-        tc::wait_ld();
-        if (dst) {
+      if (rw.in) {
+        float *dst = p.out + ((size_t)rw.i * p.Hq + (size_t)tl.kvh * p.G + rw.hg) * D + hc * DH;
 #pragma unroll
-          for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4 *>(dst + c16 + e) =
-                any ? make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv)
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        for (int e = 0; e < DH; e += 4)
+          *reinterpret_cast<float4 *>(dst + e) =
+              any ? make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
       }
       if (rw.in && p.lse && hc == 0)
         p.lse[(size_t)rw.i * p.Hq + (size_t)tl.kvh * p.G + rw.hg] =
             any ? (m_run + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
-      // the output has been read out of tensor memory
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&o_free);
       tl = nx;
       have = have_next;
     }
