@@ -19,7 +19,8 @@
 //     its P.V has run; holes are not read at all;
 //   * one MMA warp computes S(c) = Q_hi K^T + Q_lo K^T (M = 128, N = 128,
 //     f16 in, f32 accumulated in tensor memory; q = Q_hi + Q_lo to ~2^-22, so
-//     scores keep float32 accuracy) up to two chunks ahead of the softmax;
+//     scores keep float32 accuracy) into the S buffer as soon as the softmax
+//     has loaded the previous chunk's scores into registers;
 //     another computes O += P(c) V(c) once the probabilities of chunk c are
 //     in tensor memory (P read from tensor memory, V MN-major straight from
 //     its stage), after zeroing the V rows of holes and past the context (P
@@ -34,8 +35,12 @@
 //     in tensor memory. The output row is rescaled only when the running
 //     maximum grows by more than 2^8 (probabilities then stay below 256,
 //     exact in f16); a tile's output is normalised once at the end.
-// The next tile's Q is written as soon as the last S of a tile is read, so
-// its first scores are computed while the previous tile's output is stored.
+// The next tile's Q is built during the current tile, a slice of 8 dims per
+// chunk, as high / low f16 pairs in spare tensor-memory columns (each slice's
+// global loads issued at a chunk's start and used at its end); once the last
+// S of a tile is complete it is copied into the shared Q tiles, so the next
+// tile's first scores are computed while the last chunk's softmax and the
+// output of the current tile run.
 #include <limits.h>
 #include <math.h>
 
@@ -60,10 +65,13 @@ constexpr int kMmaWarpS = 10;   // issues S = Q K^T
 constexpr int kMmaWarpO = 11;   // issues O += P V
 constexpr int kTcThreads = 384;
 constexpr int kChunk = 128;        // tokens per chunk
-// tensor-memory columns: S double buffer [0, 128), [128, 256); O [256, 256 + d);
-// P (f16 pairs) double buffer [384, 448), [448, 512)
-constexpr int kOCol = 2 * kChunk;
-constexpr int kPCol = 384;
+// tensor-memory columns: S [0, 128); O [128, 128 + d); P (f16 pairs) double
+// buffer [256, 320), [320, 384); the next tile's Q as f16 pairs, high [384,
+// 448) and low [448, 512)
+constexpr int kOCol = kChunk;
+constexpr int kPCol = 256;
+constexpr int kQHiCol = 384;
+constexpr int kQLoCol = 448;
 constexpr uint32_t kTmemCols = 512;
 
 template <int D>
@@ -84,6 +92,29 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (a + m, b + m) by one packed f32x2 add (each lane rounded as a scalar add).
+__device__ __forceinline__ void add2(float a, float b, float m, float &x, float &y) {
+  asm("{ .reg .b64 p, q, r; mov.b64 p, {%2, %3}; mov.b64 q, {%4, %4}; add.rn.f32x2 r, p, q; "
+      "mov.b64 {%0, %1}, r; }"
+      : "=f"(x), "=f"(y)
+      : "f"(a), "f"(b), "f"(m));
+}
+
+// (s0, s1) += (a, b) by one packed f32x2 add.
+__device__ __forceinline__ void acc2(float &s0, float &s1, float a, float b) {
+  asm("{ .reg .b64 p, q; mov.b64 p, {%0, %1}; mov.b64 q, {%2, %3}; add.rn.f32x2 p, p, q; "
+      "mov.b64 {%0, %1}, p; }"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a), "f"(b));
 }
 
 // One swizzled tensor copy of box (64, 1, rows): 128-byte chunk `chunk` of
@@ -143,6 +174,15 @@ __device__ __forceinline__ uint64_t bit_range(int a, int b) {
   return (b >= 64 ? ~0ull : ((1ull << b) - 1ull)) & ~((1ull << a) - 1ull);
 }
 
+// 8 query values (scaled) as 4 high and 4 low f16 pairs.
+__device__ __forceinline__ void split8(const float4 &a, const float4 &b, float qs, uint32_t (&h)[4],
+                                       uint32_t (&l)[4]) {
+  split_h2(a.x * qs, a.y * qs, h[0], l[0]);
+  split_h2(a.z * qs, a.w * qs, h[1], l[1]);
+  split_h2(b.x * qs, b.y * qs, h[2], l[2]);
+  split_h2(b.z * qs, b.w * qs, h[3], l[3]);
+}
+
 // The (query, head) row a softmax thread owns in tile `tl`.
 template <int GP>
 struct RowOf {
@@ -198,10 +238,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ int ts[kMaxPrefillSeqs + 1];
   __shared__ uint32_t tmem_slot;
-  __shared__ __align__(8) uint64_t k_full[ST], k_free[ST], v_full[ST], v_free[ST], s_full[2],
-      s_free[2], p_full[2], pv_done[2], q_full, o_free, drain[2];
+  __shared__ __align__(8) uint64_t k_full[ST], k_free[ST], v_full[ST], v_free[ST], s_full,
+      s_free, p_full[2], pv_done[2], q_full, o_free, drain[2];
   __shared__ uint64_t mask_s[2][ST][2];  // [K / V] staged rows that hold data (not a hole, < ctx)
-  __shared__ uint64_t smask_s[2][2];     // the same for the chunk in S buffer x % 2
+  __shared__ uint64_t smask_s[2][2];     // the same for the chunk of S(x), by x % 2
   __shared__ float pm_s[2][2][kTcRows];  // partial row maxima: [chunk parity][half][row]
   __shared__ float pl_s[2][kTcRows];     // partial row sums at the tile end
   __shared__ int abort_s;
@@ -243,9 +283,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&v_full[k], 1);
       mbar_init(&v_free[k], 1);
     }
+    mbar_init(&s_full, 2);  // the MMAs' commit + the issuing thread (smask_s written)
+    mbar_init(&s_free, kSoftWarps);
     for (int k = 0; k < 2; ++k) {
-      mbar_init(&s_full[k], 2);  // the MMAs' commit + the issuing thread (smask_s written)
-      mbar_init(&s_free[k], kSoftWarps);
       mbar_init(&p_full[k], kSoftWarps);
       mbar_init(&pv_done[k], 1);
     }
@@ -362,11 +402,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int c = 0; c < tl.nch; ++c) {
         const int x = g + c, st = x % ST;
         if (role == 0) {
-          // S(x) = Q_hi K^T + Q_lo K^T into S buffer x % 2, once K of chunk x
-          // is staged and the softmax has read S(x - 2) (and its row mask)
+          // S(x) = Q_hi K^T + Q_lo K^T, once K of chunk x is staged and the
+          // softmax has loaded S(x - 1) (and read its row mask)
           if (!mbar_wait_bounded(&k_full[st], (uint32_t)(x / ST) & 1u, &abort_s, wait_ns) ||
-              (x >= 2 && !mbar_wait_bounded(&s_free[x & 1], (uint32_t)((x - 2) >> 1) & 1u,
-                                            &abort_s, wait_ns))) {
+              (x >= 1 &&
+               !mbar_wait_bounded(&s_free, (uint32_t)(x - 1) & 1u, &abort_s, wait_ns))) {
             fine = false;
             break;
           }
@@ -377,7 +417,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             smask_s[x & 1][0] = mask_s[0][st][0];
             smask_s[x & 1][1] = mask_s[0][st][1];
             const uint64_t kd = tc::desc_advance(d_k, (uint32_t)(st * C::STAGE));
-            const uint32_t dcol = tmem + (uint32_t)((x & 1) * kChunk);
+            const uint32_t dcol = tmem;
 #pragma unroll
             for (int hf = 0; hf < C::HALVES; ++hf)
 #pragma unroll
@@ -387,9 +427,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc::mma_f16(dcol, tc::desc_advance(d_qhi, qo), bd, idesc_s, hf + kk > 0);
                 tc::mma_f16(dcol, tc::desc_advance(d_qlo, qo), bd, idesc_s, true);
               }
-            tc::commit(&s_full[x & 1]);
+            tc::commit(&s_full);
             tc::commit(&k_free[st]);
-            mbar_arrive(&s_full[x & 1]);
+            mbar_arrive(&s_full);
           }
           __syncwarp();
           continue;
@@ -457,16 +497,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // the next tile's query rows head for L2 while this tile runs
       Tile nx;
       const bool have_next = tile_of<GP>(p, ts, n_tiles, t + (int)gridDim.x, nx);
+      const float *qn = nullptr;  // this thread's half of its next-tile query row (or none)
       if (have_next) {
         const RowOf<GP> rn(p, nx, row);
         if (rn.ok) {
-          const float *qn =
-              p.q + ((size_t)rn.i * p.Hq + (size_t)nx.kvh * p.G + rn.hg) * D + hc * (D / 2);
+          qn = p.q + ((size_t)rn.i * p.Hq + (size_t)nx.kvh * p.G + rn.hg) * D + hc * (D / 2);
 #pragma unroll
           for (int e = 0; e < D / 2; e += 32)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + e));
         }
       }
+      // the next tile's Q, slice k = dims [8k, 8k + 8) of this thread's half row:
+      // high / low pairs at columns kQHiCol / kQLoCol + hc * D / 4 + 4k
+      constexpr int NSL = D / 16;
+      const uint32_t q_hi_t = t_row + (uint32_t)(kQHiCol + hc * (D / 4));
+      const uint32_t q_lo_t = t_row + (uint32_t)(kQLoCol + hc * (D / 4));
+      auto load_slice = [&](int k, float4 &a, float4 &b) {
+        a = b = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (qn) {
+          a = *reinterpret_cast<const float4 *>(qn + 8 * k);
+          b = *reinterpret_cast<const float4 *>(qn + 8 * k + 4);
+        }
+      };
+      auto store_slice = [&](int k, const float4 &a, const float4 &b) {
+        uint32_t h[4], l[4];
+        split8(a, b, p.qscale, h, l);
+        tc::st4u(q_hi_t + 4 * k, h[0], h[1], h[2], h[3]);
+        tc::st4u(q_lo_t + 4 * k, l[0], l[1], l[2], l[3]);
+      };
       const RowOf<GP> rw(p, tl, row);
       if (hc == 0 && rw.j < tl.n && rw.hg < p.G && !rw.in)
         report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
@@ -490,15 +548,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float m_run = -INFINITY, l_run = 0.f;
       for (int c = 0; c < tl.nch; ++c) {
         const int x = g + c;
-        // ---- S(x): load this thread's 32 columns, then hand the buffer back
-        fine = mbar_wait_bounded(&s_full[x & 1], (uint32_t)(x >> 1) & 1u, &abort_s, wait_ns) &&
-               fine;
+        const bool last = c + 1 == tl.nch;
+        // the next tile's Q slice c: loads in flight across this chunk
+        const bool slice = have_next && c < NSL && !last;
+        float4 qa, qb;
+        if (slice) load_slice(c, qa, qb);
+        // ---- S(x) complete
+        fine = mbar_wait_bounded(&s_full, (uint32_t)x & 1u, &abort_s, wait_ns) && fine;
         tc::fence_after();
+        if (last && have_next) {
+          // every S of this tile is done: the rest of the next tile's Q is
+          // staged, then all of it moves into the shared Q tiles
+          for (int k = c; k < NSL; ++k) {
+            float4 a, b;
+            load_slice(k, a, b);
+            store_slice(k, a, b);
+          }
+          tc::wait_st();
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {  // high, then low
+            uint8_t *qt = half ? qlo : qhi;
+            const uint32_t src = half ? q_lo_t : q_hi_t;
+#pragma unroll
+            for (int w16 = 0; w16 < D / 4; w16 += 16) {
+              float v[16];
+              tc::ld16(src + w16, v);
+              tc::wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; j += 4) {
+                const int e = hc * (D / 2) + 2 * (w16 + j);  // first of the 8 dims
+                const uint32_t off =
+                    (uint32_t)((e >> 6) * kTcRows * 128) + tc::sw128(row, (e & 63) >> 3);
+                *reinterpret_cast<uint4 *>(qt + off) =
+                    make_uint4(__float_as_uint(v[j]), __float_as_uint(v[j + 1]),
+                               __float_as_uint(v[j + 2]), __float_as_uint(v[j + 3]));
+              }
+            }
+          }
+          tc::fence_proxy_shared();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&q_full);
+        }
+        // ---- S(x): load this thread's 64 columns, then hand the buffer back
         float sv[HC];
 #pragma unroll
         for (int c16 = 0; c16 < HC; c16 += 16) {
           float v[16];
-          tc::ld16(t_row + (uint32_t)((x & 1) * kChunk + hc * HC + c16), v);
+          tc::ld16(t_row + (uint32_t)(hc * HC + c16), v);
 #pragma unroll
           for (int e = 0; e < 16; ++e) sv[c16 + e] = v[e];
         }
@@ -508,7 +604,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::wait_ld();
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[x & 1]);
+        if (lane == 0) mbar_arrive(&s_free);
         // ---- mask: the row's window, then the staged rows that hold data
         const int pos0 = c * kChunk + hc * HC;  // position of this thread's first column
         uint64_t mk = 0;
@@ -529,10 +625,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             sv[e + 32] = (m1 & (1u << e)) ? sv[e + 32] : -INFINITY;
           }
         }
-        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // 4 independent chains
+        // row maximum: 4 independent chains of 3-input maxima over 16 columns each
+        float mq[4];
 #pragma unroll
-        for (int e = 0; e < HC; ++e) mq[e & 3] = fmaxf(mq[e & 3], sv[e]);
-        pm_s[x & 1][hc][row] = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        for (int j = 0; j < 4; ++j) {
+          const float *v = sv + 16 * j;
+          float m = max3f(v[0], v[1], v[2]);
+#pragma unroll
+          for (int e = 3; e < 15; e += 2) m = max3f(m, v[e], v[e + 1]);
+          mq[j] = fmaxf(m, v[15]);
+        }
+        pm_s[x & 1][hc][row] = fmaxf(max3f(mq[0], mq[1], mq[2]), mq[3]);
         // both halves of the row (and their waits) meet here; a wait that ran
         // out on either side ends the pair's loop at the same point
         if (!pair_sync_and(pair, fine)) {
@@ -570,7 +673,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           fine = mbar_wait_bounded(&pv_done[x & 1], (uint32_t)((x - 2) >> 1) & 1u, &abort_s,
                                    wait_ns) &&
                  fine;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};  // two packed pairs of partial sums
         const float mr = m_run == -INFINITY ? 0.f : m_run;  // all sv are -inf then: p = 0
         const uint32_t p_row = t_row + (uint32_t)(kPCol + (x & 1) * (kChunk / 2) + hc * (HC / 2));
 #pragma unroll
@@ -578,9 +681,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           uint32_t h[16];
 #pragma unroll
           for (int k2 = 0; k2 < 16; ++k2) {
-            const float a = ex2(sv[e + 2 * k2] - mr);
-            const float b = ex2(sv[e + 2 * k2 + 1] - mr);
-            ls[k2 & 3] += a + b;
+            float u, w;
+            add2(sv[e + 2 * k2], sv[e + 2 * k2 + 1], -mr, u, w);
+            const float a = ex2(u), b = ex2(w);
+            acc2(ls[2 * (k2 & 1)], ls[2 * (k2 & 1) + 1], a, b);
             h[k2] = h2_bits(__floats2half2_rn(a, b));
           }
           tc::st16u(p_row + (uint32_t)(e / 2), h);
@@ -590,17 +694,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[x & 1]);
+        if (slice) store_slice(c, qa, qb);
       }
       if (!fine) break;
       const int x_last = g + tl.nch - 1;
       g += tl.nch;
-      // ---- every S of this tile has been read: the next tile's Q goes in
-      if (have_next) {
-        write_q<D, GP>(p, nx, row, hc, qhi, qlo);
-        tc::fence_proxy_shared();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&q_full);
-      }
       // ---- the last P.V, then the normalised row
       fine = mbar_wait_bounded(&pv_done[x_last & 1], (uint32_t)(x_last >> 1) & 1u, &abort_s,
                                wait_ns) &&

@@ -138,6 +138,14 @@ __device__ __forceinline__ void st16(uint32_t taddr, const float (&v)[16]) {
       : "memory");
 }
 
+// 4 consecutive 32-bit columns of this thread's lane from raw words.
+__device__ __forceinline__ void st4u(uint32_t taddr, uint32_t w0, uint32_t w1, uint32_t w2,
+                                     uint32_t w3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(w0),
+               "r"(w1), "r"(w2), "r"(w3)
+               : "memory");
+}
+
 // 16 consecutive 32-bit columns of this thread's lane from raw words.
 __device__ __forceinline__ void st16u(uint32_t taddr, const uint32_t (&w)[16]) {
   asm volatile(
