@@ -55,7 +55,7 @@ namespace {
 
 constexpr int kMaxConsumerWarps = 8;
 constexpr int kThreads = 32 * (kMaxConsumerWarps + 1);
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 8;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -109,7 +109,9 @@ struct Params {
 
 // Shared memory: [barriers | stage infos | abort] header, per-warp softmax
 // scratch, then the stage ring.
-constexpr int kHdrBytes = 256;
+// shared header: full / empty mbarriers [0, 128), stage records [128, 288),
+// the abort flag at 320; scratch from kHdrBytes
+constexpr int kHdrBytes = 512;
 
 template <int GP>
 __host__ __device__ constexpr int scratch_floats_per_warp() {
@@ -255,8 +257,11 @@ __device__ __forceinline__ uint32_t swz(uint32_t stage, int row, int e, int ncb)
 //                   are (head, high/low half of p) pairs when G <= 4 and the
 //                   heads themselves when G > 4; each thread supplies column
 //                   g from its own probabilities, so P never leaves registers.
-// Rows of a stage sit `pitch` = row_bytes + 16 bytes apart, which makes every
-// ldmatrix phase hit 8 different bank groups.
+// f32 pools take the same path on the same swizzled stages (a row of f32 is
+// just more 128-byte lines): K and V values are read as floats and split into
+// high / low f16 pairs in registers, and every product runs twice, on the
+// high and on the low half (S += Qhl.Khi^T + Qhl.Klo^T, O^T += Vhi^T.P^T +
+// Vlo^T.P^T), so scores and outputs keep ~2^-22 relative accuracy.
 template <int D, int GP>
 struct MmaCfg {
   static constexpr int KS = D / 16;              // Q.K k-steps over the head dims
@@ -267,7 +272,25 @@ struct MmaCfg {
 };
 
 
-template <int D, int GP>
+// 32-bit shared-memory loads at a shared address
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float2 lds_f32x2(uint32_t a) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+  return v;
+}
+
+// Shared address of float element fe of staged f32 row `row` (same swizzled
+// line layout as the f16 rows: element fe is f16 position 2 fe).
+__device__ __forceinline__ uint32_t swz32(uint32_t stage, int row, int fe, int ncb) {
+  return swz(stage, row, 2 * fe, ncb) + (uint32_t)((fe & 3) * 4);
+}
+
+template <int FMT, int D, int GP>
 __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uint64_t *empty,
                                             StageInfo *infos, volatile int *abort_flag,
                                             uint8_t *ring, int warp, int lane) {
@@ -347,12 +370,13 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
       bool wrote = false;
       const uint32_t bad = row_bits(base, row_end) & ~mask;
       if (bad) {
-        constexpr int V16 = D * 2 / 16;  // 16-byte pieces of one head row
+        constexpr int ES = FMT == MT_KV_F32 ? 4 : 2;
+        constexpr int V16 = D * ES / 16;  // 16-byte pieces of one head row
         const int n_bad = __popc(bad);
         for (int i = lane; i < n_bad * V16; i += 32) {
           const int k = i / V16;
           const int row = (int)__fns(bad, 0, k + 1) - base;  // stage row of the k-th bad row
-          const int line = row * p.ncb + (head_e >> 6) + (i % V16) / 8;
+          const int line = row * p.ncb + head_e * ES / 128 + (i % V16) / 8;
           *reinterpret_cast<uint4 *>(vst_ptr + (size_t)line * 128 + (i % 8) * 16) =
               make_uint4(0, 0, 0, 0);
         }
@@ -368,14 +392,30 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
         const int t0 = 8 * t;
         if (t0 >= p.bs || t0 + 8 <= r0 || t0 >= r1) continue;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const int krow = t0 + (lane & 7) - base;
-        const int ke = head_e + ((lane >> 3) & 1) * 8 + (lane >> 4) * 16;
+        if constexpr (FMT == MT_KV_F32) {
+          // B fragment of k-step ks: token t0 + g, dims 16 ks + 2c (+1) and + 8
+          const int krow = t0 + g - base;
 #pragma unroll
-        for (int ks = 0; ks < M::KS; ks += 2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(swz(kst, krow, ke + ks * 16, p.ncb), b0, b1, b2, b3);
-          mma_f16(acc, qa[ks], b0, b1);
-          mma_f16(acc, qa[ks + 1], b2, b3);
+          for (int ks = 0; ks < M::KS; ++ks) {
+            const int fe = head_e + 16 * ks + 2 * c;
+            const float2 k0 = lds_f32x2(swz32(kst, krow, fe, p.ncb));
+            const float2 k1 = lds_f32x2(swz32(kst, krow, fe + 8, p.ncb));
+            uint32_t h0, l0, h1, l1;
+            split_h2(k0.x, k0.y, h0, l0);
+            split_h2(k1.x, k1.y, h1, l1);
+            mma_f16(acc, qa[ks], h0, h1);
+            mma_f16(acc, qa[ks], l0, l1);
+          }
+        } else {
+          const int krow = t0 + (lane & 7) - base;
+          const int ke = head_e + ((lane >> 3) & 1) * 8 + (lane >> 4) * 16;
+#pragma unroll
+          for (int ks = 0; ks < M::KS; ks += 2) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(swz(kst, krow, ke + ks * 16, p.ncb), b0, b1, b2, b3);
+            mma_f16(acc, qa[ks], b0, b1);
+            mma_f16(acc, qa[ks + 1], b2, b3);
+          }
         }
         const int tk = t0 + 2 * c;
         const float s0 = acc[0] + acc[2], s1 = acc[1] + acc[3];
@@ -426,13 +466,34 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
           b1 = h2_bits(__floats2half2_rn(pr[2 * kc + 1][0], pr[2 * kc + 1][1]));
         }
         if (!row_ok) b0 = b1 = 0u;
-        const int vrow = t0 + ((lane >> 4) & 1) * 8 + (lane & 7) - base;
-        const int ve = head_e + dim0 + ((lane >> 3) & 1) * 8;
+        if constexpr (FMT == MT_KV_F32) {
+          // A = V^T: element (dim g (+8), token 2c (+1) (+8)) read as floats
+          const int tr = t0 + 2 * c - base;
 #pragma unroll
-        for (int mt = 0; mt < M::MTW; ++mt) {
-          uint32_t a[4];
-          ldsm_x4_t(swz(vst, vrow, ve + mt * 16, p.ncb), a[0], a[1], a[2], a[3]);
-          mma_f16(oacc[mt], a, b0, b1);
+          for (int mt = 0; mt < M::MTW; ++mt) {
+            const int fe = head_e + dim0 + mt * 16 + g;
+            float v[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {  // (dim + 8 (q & 1), token + 8 (q >> 1))
+              const int r = tr + 8 * (q >> 1), e = fe + 8 * (q & 1);
+              v[2 * q] = lds_f32(swz32(vst, r, e, p.ncb));
+              v[2 * q + 1] = lds_f32(swz32(vst, r + 1, e, p.ncb));
+            }
+            uint32_t ah[4], al[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) split_h2(v[2 * q], v[2 * q + 1], ah[q], al[q]);
+            mma_f16(oacc[mt], ah, b0, b1);
+            mma_f16(oacc[mt], al, b0, b1);
+          }
+        } else {
+          const int vrow = t0 + ((lane >> 4) & 1) * 8 + (lane & 7) - base;
+          const int ve = head_e + dim0 + ((lane >> 3) & 1) * 8;
+#pragma unroll
+          for (int mt = 0; mt < M::MTW; ++mt) {
+            uint32_t a[4];
+            ldsm_x4_t(swz(vst, vrow, ve + mt * 16, p.ncb), a[0], a[1], a[2], a[3]);
+            mma_f16(oacc[mt], a, b0, b1);
+          }
         }
       }
       if (wrote) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -855,8 +916,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
   uint64_t *empty = full + kMaxStages;
-  StageInfo *infos = reinterpret_cast<StageInfo *>(smem + 64);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 192);
+  StageInfo *infos = reinterpret_cast<StageInfo *>(smem + 128);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 320);
   float *scratch = reinterpret_cast<float *>(smem + kHdrBytes);
   // the ring starts on a 1024-byte boundary (the 128-byte swizzle's period)
   uint8_t *ring = smem + kHdrBytes + p.scratch_bytes;
@@ -1076,7 +1137,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
   if constexpr (MMA && FMT == MT_KV_Q8_0 && D <= 128) {
     consume_mma_q8<D, GP>(p, full, empty, infos, abort_flag, ring, smem + kHdrBytes, warp, lane);
   } else if constexpr (MMA) {
-    consume_mma<D, GP>(p, full, empty, infos, abort_flag, ring, warp, lane);
+    consume_mma<FMT, D, GP>(p, full, empty, infos, abort_flag, ring, warp, lane);
   } else {
   // ------------------------------------------------------- consumer warps
   const int kvh = warp / p.wph;
@@ -1643,7 +1704,10 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
   const int mma_wph = a->head_dim == 256 ? 2 : 1;
   const int nc = (int)(rb / 128);
   pl->ncb = nc | 1;  // odd number of 128-byte lines per staged row
-  pl->mma = a->fmt == MT_KV_F16 && rb % 128 == 0 && pl->ncb <= 255 &&
+  // (f32 pools: head_dim 64 and 128; at 256 the split operands do not fit in
+  // registers and those pools stay on the FP32-core consumers)
+  pl->mma = (a->fmt == MT_KV_F16 || (a->fmt == MT_KV_F32 && a->head_dim <= 128)) &&
+            rb % 128 == 0 && pl->ncb <= 255 &&
             a->n_kv_heads * mma_wph <= kMaxConsumerWarps && fit(128 * pl->ncb, 16, rows, pad, stages);
   // q8_0 pools: tensor-core consumers on per-warp converted tiles (d <= 128)
   if (!pl->mma && q8_mma && fit((int)rb, 16, rows, pad, stages)) {
@@ -1731,7 +1795,8 @@ mt_status dispatch_d(const Params &prm, const Plan &pl, cudaStream_t s) {
   switch (pl.D) {
     case 64: return dispatch_gp<FMT, 64, MMA>(prm, pl, s);
     case 128: return dispatch_gp<FMT, 128, MMA>(prm, pl, s);
-    default: return dispatch_gp<FMT, 256, MMA>(prm, pl, s);
+    // f32 pools of head_dim 256 always take the FP32-core consumers (plan)
+    default: return dispatch_gp<FMT, 256, MMA && FMT != MT_KV_F32>(prm, pl, s);
   }
 }
 
@@ -1772,7 +1837,7 @@ mt_status fill_params(Params &prm, const mt_paged_attn_args *a, const Plan &pl, 
   prm.blk_pad = pl.blk_pad;
   prm.rows = pl.rows;
   prm.pitch = pl.pitch;
-  prm.use_tmap = (pl.mma && a->fmt == MT_KV_F16) ? 1 : 0;
+  prm.use_tmap = (pl.mma && (a->fmt == MT_KV_F16 || a->fmt == MT_KV_F32)) ? 1 : 0;
   prm.scratch_bytes = pl.scratch;
   prm.ncb = pl.ncb;
   prm.n_sub = pl.n_sub;
@@ -1802,7 +1867,9 @@ mt_status fill_params(Params &prm, const mt_paged_attn_args *a, const Plan &pl, 
 
 mt_status dispatch(const Params &prm, const Plan &pl, mt_kv_format fmt, cudaStream_t s) {
   switch (fmt) {
-    case MT_KV_F32: return dispatch_d<MT_KV_F32, false>(prm, pl, s);
+    case MT_KV_F32:
+      return pl.mma ? dispatch_d<MT_KV_F32, true>(prm, pl, s)
+                    : dispatch_d<MT_KV_F32, false>(prm, pl, s);
     case MT_KV_F16:
       return pl.mma ? dispatch_d<MT_KV_F16, true>(prm, pl, s)
                     : dispatch_d<MT_KV_F16, false>(prm, pl, s);
