@@ -1677,6 +1677,7 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
   pl->scratch = q8_mma ? std::max(simt_scratch, tile_scratch) : simt_scratch;
   const int fixed = kHdrBytes + pl->scratch + 1024 + 16;
   int n_ctas = a->n_ctas;
+  const bool auto_ctas = n_ctas == 0;
   int smem_cap = 232448;
   if (need_device || n_ctas == 0) {
     DeviceInfo di;
@@ -1733,6 +1734,23 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
   }
   pl->wph = wph;
   pl->n_cw = a->n_kv_heads * wph;
+  // Few consumer warps (pools with few KV heads, narrow rows): two CTAs per
+  // SM, each with stages sized for half of the SM's shared memory, so every
+  // scheduler runs two consumer warps. With at most 4 warps per CTA (one per
+  // scheduler) two CTAs always fit the per-scheduler register file.
+  if (auto_ctas && pl->n_cw <= 3) {
+    const int min_rows = pl->mma ? 16 : 8;
+    int rows2 = 0, pad2 = 0, stages2 = 0;
+    const int cap1 = smem_cap;
+    smem_cap = (cap1 + 1024) / 2 - 1024;
+    if (fit(pl->pitch, min_rows, rows2, pad2, stages2) && stages2 >= 3) {
+      rows = rows2;
+      pad = pad2;
+      stages = stages2;
+      n_ctas *= 2;
+    }
+    smem_cap = cap1;
+  }
   pl->rows = rows;
   pl->blk_pad = pad;
   pl->stages = stages;
