@@ -1,0 +1,80 @@
+"""GPU parity of the tcgen05 prefill kernel (f16 pools) at sizes that drive
+its pipeline: contexts of many 128-token chunks, more tiles than CTAs (tile
+changes with the next tile's query staged during the current one), running
+maxima that grow past the lazy-rescale threshold in every chunk, and more
+sequences than one launch takes. The oracle and tolerance are those of the
+other prefill tests (f16: 2e-3 on outputs and log-sum-exp).
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+from oracle import attention as oatt
+from paged_kv_cache_gqa_gb300 import workloads
+from tests.gpu_util import TOL, assert_close, assert_lse, oracle_pools
+from tests.test_gpu_prefill import make_queries, run_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mt():
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_cache_gqa_gb300 import mtkv
+    return mtkv
+
+
+def check_pools(mt, w, q, q_start, kp, vp):
+    want, want_lse = oatt.paged_attn_prefill(w.fmt, q, kp, vp, w.block_table, w.context_lens,
+                                             q_start, None, None, w.n_heads, w.n_kv_heads,
+                                             w.head_dim, w.block_size, w.scale)
+    got, got_lse, st = run_prefill(mt, w, q, q_start, kp, vp)
+    assert st == 0, mt.mt_last_error()
+    assert_close(got, want, TOL[w.fmt], f"{w.name} prefill")
+    assert_lse(got_lse, want_lse, TOL[w.fmt], f"{w.name} prefill")
+
+
+def test_prefill_tc_long_contexts_many_tiles(mt):
+    # Llama-3 heads (GP = 4: 32 queries per tile), contexts of 6-9 chunks and
+    # up to 300 queries per sequence: ~200 tiles, so CTAs take several
+    # tiles and the staging rings wrap many times
+    rng = np.random.default_rng(81)
+    w = workloads.llama3_f16(seed=81, n_seqs=3, ctx_lo=700, ctx_hi=1100)
+    q, q_start = make_queries(w, rng, 300)
+    kp, vp = oracle_pools(w)
+    check_pools(mt, w, q, q_start, kp, vp)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_tc_rescales_growing_maxima(mt, d):
+    # scores that grow by ~8.5 (base 2) per 128 tokens: every chunk raises the
+    # running maximum past the 2^8 threshold, so the output row in tensor
+    # memory is rescaled in every chunk
+    rng = np.random.default_rng(82 + d)
+    w = workloads.llama3_f16(seed=82 + d, n_seqs=2, ctx_lo=500, ctx_hi=640, n_heads=4,
+                             n_kv_heads=1, head_dim=d)
+    u = np.ones(d, dtype=np.float32) / np.sqrt(d)
+    k_hist = w.k_hist.copy()
+    for s in range(w.n_seqs):
+        for t in range(int(w.context_lens[s])):
+            cell = int(w.block_table[s, t // w.block_size]) * w.block_size + t % w.block_size
+            # q ~ sqrt(d) u, so q.k * scale * log2(e) ~ gamma * log2(e) = 8.5 t / 128
+            gamma = (8.5 / 128.0) * t / 1.4426950408889634
+            k_hist[cell] = gamma * u + 0.3 * rng.standard_normal(d).astype(np.float32)
+    w = dataclasses.replace(w, k_hist=k_hist)
+    q, q_start = make_queries(w, rng, 200)
+    q = (np.sqrt(d) * u[None, None, :] + 0.3 * q).astype(np.float32)
+    kp, vp = oracle_pools(w)
+    check_pools(mt, w, q, q_start, kp, vp)
+
+
+def test_prefill_tc_more_sequences_than_one_launch(mt):
+    # 1100 short sequences: the call runs two launches of at most 1024
+    rng = np.random.default_rng(83)
+    w = workloads.llama3_f16(seed=83, n_seqs=1100, ctx_lo=1, ctx_hi=12, n_heads=4, n_kv_heads=2,
+                             head_dim=64)
+    q, q_start = make_queries(w, rng, 6)
+    kp, vp = oracle_pools(w)
+    check_pools(mt, w, q, q_start, kp, vp)
