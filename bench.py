@@ -691,13 +691,18 @@ def run_extra(args, rank, world, local_rank):
                                      "per-sequence decode (mt_paged_attn_decode)"),
                           "store": args.store, "graph": bool(args.graph)},
                "clocks": clk}
-    elif args.workload == "prefill_f16":
-        # chunked prefill through the paged cache: 16 sequences at context
-        # 2048 whose last 512 positions are the queries (their K/V rows
-        # already stored), Llama-3-8B-shaped heads, f16 pools; 8 layers with
-        # their own pools, so successive calls do not hit in L2
-        w = workloads.llama3_f16(seed=SEED + 9, n_seqs=16, ctx_lo=2048, ctx_hi=2048, hist=False)
-        n_q = 512
+    elif args.workload in ("prefill_f16", "prefill_f16_long"):
+        # chunked prefill through the paged cache, Llama-3-8B-shaped heads, f16
+        # pools, the queries' K/V rows already stored; 8 layers with their own
+        # pools, so successive calls do not hit in L2. prefill_f16: 16
+        # sequences at context 2048 whose last 512 positions are the queries;
+        # prefill_f16_long: one sequence at context 32768 whose last 256
+        # positions are the queries (one chunk of a long prompt: 64 tiles,
+        # fewer than the SMs)
+        long_ = args.workload == "prefill_f16_long"
+        n_seqs_p, ctx_p, n_q = (1, 32768, 256) if long_ else (16, 2048, 512)
+        w = workloads.llama3_f16(seed=SEED + 9, n_seqs=n_seqs_p, ctx_lo=ctx_p, ctx_hi=ctx_p,
+                                 hist=False)
         layers, _, rb = _decode_setup(mtkv, w, 8, dev, g)
         table = torch.from_numpy(w.block_table).to(dev)
         ctx_d = torch.from_numpy(w.context_lens).to(dev)
@@ -739,9 +744,9 @@ def run_extra(args, rank, world, local_rank):
                             "note": "useful FLOPs (4 * pairs * heads * head_dim); the kernel "
                                     "also multiplies the low half of q and padding rows"},
                "kv_GB_per_s": round(len(calls) * kv_bytes / (ms * 1e-3) / 1e9, 1),
-               "config": {"workload": "llama3-8b-shaped f16 chunked prefill: 16 seqs x ctx "
-                                      "2048, last 512 positions as queries, 32/8 heads, "
-                                      "head_dim 128, bs 16, 8 layers"},
+               "config": {"workload": f"llama3-8b-shaped f16 chunked prefill: {n_seqs_p} "
+                                      f"seqs x ctx {ctx_p}, last {n_q} positions as "
+                                      "queries, 32/8 heads, head_dim 128, bs 16, 8 layers"},
                "clocks": clk}
     elif args.workload == "longctx_int4":
         w = workloads.longctx_f16_int4(hist=False)
@@ -808,7 +813,7 @@ def main():
                     help="oracle baseline budget; 0 skips it (profiling runs)")
     ap.add_argument("--workload", default="llama3_f16",
                     choices=["llama3_f16", "smollm2_f32", "q8_prefix", "longctx_int4",
-                             "prefill_f16"],
+                             "prefill_f16", "prefill_f16_long"],
                     help="llama3_f16 is the benchmark line; the others measure the other kernels")
     ap.add_argument("--store", default=None, choices=["fused", "separate"],
                     help="store each layer's new row inside the decode launch "

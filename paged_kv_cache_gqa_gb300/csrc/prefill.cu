@@ -34,6 +34,22 @@ namespace mtkv {
 namespace {
 
 constexpr uint64_t kPrefillWsBytes = 256;
+// Records for tiles split over several CTAs (tcgen05 kernel): room for
+// 2 x kSplitCtas units, enough whenever the grid has at most kSplitCtas CTAs
+// (the kernel splits only while tiles are fewer than CTAs).
+constexpr int kSplitCtas = 160;
+
+// Bytes of split records a call may need: 0 unless the f16 tensor-core kernel
+// runs and the query count leaves fewer tiles than kSplitCtas (every sequence
+// has at least ceil(n_s / TQ) tiles per KV head, so the tile count is at
+// least Hkv * ceil(n_tokens / TQ)).
+size_t prefill_rec_bytes(const mt_paged_prefill_args *a, int GP) {
+  if (!prefill_tc_supported(a->fmt, a->head_dim, a->block_size) || GP == 0) return 0;
+  const long long TQ = 128 / GP;
+  const long long min_tiles = (long long)a->n_kv_heads * ((a->n_tokens + TQ - 1) / TQ);
+  if (min_tiles >= kSplitCtas) return 0;
+  return (size_t)2 * kSplitCtas * 128 * (a->head_dim + 4) * sizeof(float);
+}
 
 // The CTA's walk over its tiles (blockIdx.x, + gridDim.x, ...) and their
 // blocks [0, nb). A tile whose rows read nothing still has one (empty) unit,
@@ -330,7 +346,9 @@ int pad_g(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : G <= 8 ? 8 : 0;
 using namespace mtkv;
 
 extern "C" size_t mt_paged_prefill_workspace_bytes(const mt_paged_prefill_args *a) {
-  return a ? kPrefillWsBytes : 0;
+  if (!a) return 0;
+  const int G = a->n_kv_heads > 0 && a->n_heads % a->n_kv_heads == 0 ? a->n_heads / a->n_kv_heads : 0;
+  return kPrefillWsBytes + prefill_rec_bytes(a, G > 0 ? pad_g(G) : 0);
 }
 
 extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void *workspace,
@@ -358,9 +376,10 @@ extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void 
   if (!a->q || !a->k_pool || !a->v_pool || !a->block_table || !a->context_lens || !a->q_start ||
       !a->out)
     return fail(MT_ERR_INVALID_ARG, "prefill: null pointer");
-  if (!workspace || workspace_bytes < kPrefillWsBytes)
+  const size_t rec_bytes = prefill_rec_bytes(a, GP);
+  if (!workspace || workspace_bytes < kPrefillWsBytes + rec_bytes)
     return fail(MT_ERR_INVALID_ARG, "prefill: workspace missing or too small (need " +
-                                        std::to_string(kPrefillWsBytes) + " bytes)");
+                                        std::to_string(kPrefillWsBytes + rec_bytes) + " bytes)");
   if (!aligned16(a->k_pool) || !aligned16(a->v_pool) || !aligned16(a->q) || !aligned16(a->out))
     return fail(MT_ERR_INVALID_ARG, "prefill: q, pools and out must be 16-byte aligned");
   DeviceInfo di;
@@ -384,6 +403,15 @@ extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void 
   p.n_phys = a->n_phys_blocks;
   p.row_bytes = (int)rb;
   p.qscale = a->scale * 1.4426950408889634f;
+  p.rec = nullptr;
+  p.rec_hdr = nullptr;
+  p.rec_units = 0;
+  if (rec_bytes && di.n_sm <= kSplitCtas) {
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    p.rec = reinterpret_cast<float *>(ws + kPrefillWsBytes);
+    p.rec_hdr = reinterpret_cast<int *>(ws + 64);
+    p.rec_units = 2 * kSplitCtas;
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // sequences are independent: launch in chunks of kMaxPrefillSeqs (query
   // rows stay absolute, so only the per-sequence arrays are offset)
@@ -396,6 +424,8 @@ extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void 
       // f16 pools: the tcgen05 kernel, one CTA (256 tensor-memory columns,
       // ~210 KB of shared memory for head_dim 128) per SM
       st = launch_prefill_tc(p, a->head_dim, GP, di.n_sm, s);
+      if (st != MT_OK) return st;
+      st = launch_prefill_tc_combine(p, a->head_dim, di.n_sm, s);
       if (st != MT_OK) return st;
       continue;
     }

@@ -28,10 +28,22 @@ struct PrefillParams {
   long long n_phys;
   int row_bytes;
   float qscale;
+  // split of each tile's chunks over several CTAs (tcgen05 kernel, when there
+  // are fewer tiles than CTAs): per (unit, row) records of D + 4 floats
+  // (max, sum, destination row as int bits, unused, unnormalised output),
+  // room for rec_units units; rec_hdr[0..1] = (tiles, pieces per tile) of the
+  // last launch, for the combine. rec == nullptr: no split.
+  float *rec;
+  int *rec_hdr;
+  int rec_units;
 };
 
 // tcgen05 prefill kernel (f16 pools, head_dim 64 or 128, block_size 16 or 32).
 bool prefill_tc_supported(mt_kv_format fmt, int head_dim, int block_size);
+// Merge the split pieces' records of the last tcgen05 launch (returns at once
+// when it did not split).
+mt_status launch_prefill_tc_combine(const PrefillParams &p, int head_dim, int n_ctas,
+                                    cudaStream_t stream);
 mt_status launch_prefill_tc(const PrefillParams &p, int head_dim, int gp, int n_ctas,
                             cudaStream_t stream);
 

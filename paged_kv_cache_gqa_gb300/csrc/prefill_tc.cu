@@ -73,6 +73,7 @@ constexpr int kPCol = 256;
 constexpr int kQHiCol = 384;
 constexpr int kQLoCol = 448;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxSplit = 16;       // pieces per tile when tiles are fewer than CTAs
 
 template <int D>
 struct TcCfg {
@@ -166,6 +167,23 @@ __device__ __forceinline__ bool tile_of(const PrefillParams &p, const int *ts, i
   // roles (a tile that reaches no position reads nothing and stores zeros)
   tl.nch = reach > 0 ? (reach + kChunk - 1) / kChunk : 1;
   return true;
+}
+
+// A unit of work: chunks [cb, ce) of a tile. With n_split pieces per tile,
+// unit u is piece u % n_split of tile u / n_split (the tile's chunks cut
+// evenly; a piece may be empty when the tile has fewer chunks than pieces).
+struct Unit {
+  Tile tl;
+  int cb, ce;
+};
+
+template <int GP>
+__device__ __forceinline__ void unit_of(const PrefillParams &p, const int *ts, int n_tiles,
+                                        int n_split, int u, Unit &un) {
+  tile_of<GP>(p, ts, n_tiles, u / n_split, un.tl);
+  const int piece = u % n_split;
+  un.cb = piece * un.tl.nch / n_split;
+  un.ce = (piece + 1) * un.tl.nch / n_split;
 }
 
 // Bits [a, b) of a 64-bit chunk mask (0 <= a, b <= 64).
@@ -298,7 +316,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   __syncthreads();
   const int n_tiles = ts[p.B];
-  if ((int)blockIdx.x >= n_tiles) return;
+  // fewer tiles than CTAs: each tile's chunks are cut into pieces that
+  // separate CTAs take, as many as fit in one wave (a second wave of pieces
+  // costs more than it saves: 3 pieces of 64 tiles on 152 CTAs ran slower
+  // than no split, 2 pieces 1.43x faster); the combine kernel merges them
+  int n_split = 1;
+  if (p.rec && n_tiles > 0 && n_tiles < (int)gridDim.x)
+    n_split = max(1, min(min((int)gridDim.x / n_tiles, kMaxSplit), p.rec_units / n_tiles));
+  const int n_units = n_tiles * n_split;
+  if (p.rec && blockIdx.x == 0 && tid == 0) {
+    p.rec_hdr[0] = n_tiles;
+    p.rec_hdr[1] = n_split;
+  }
+  if ((int)blockIdx.x >= n_units) return;
+  // the first unit at or after u (same stride as the CTA's) with chunks to run;
+  // every role walks the same sequence
+  auto live_unit = [&](int &u, Unit &un) -> bool {
+    for (; u < n_units; u += gridDim.x) {
+      unit_of<GP>(p, ts, n_tiles, n_split, u, un);
+      if (un.ce > un.cb) return true;
+    }
+    return false;
+  };
   if (warp == 0) tc::alloc(&tmem_slot, kTmemCols);
   tc::fence_before();
   __syncthreads();
@@ -324,16 +363,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       return (lane < nb && pos < u.c) ? p.table[(size_t)u.s * p.max_blocks + (pos >> bs_shift)]
                                       : -1;
     };
-    int g = 0;  // chunks staged by this CTA so far (all tiles)
-    Tile tl;
-    bool have = tile_of<GP>(p, ts, n_tiles, blockIdx.x, tl);
-    int raw_next = have ? fetch(tl, 0) : -1;
-    for (int t = blockIdx.x; have && fine; t += gridDim.x) {
-      Tile nx;
-      const bool have_next = tile_of<GP>(p, ts, n_tiles, t + (int)gridDim.x, nx);
-      for (int c = 0; c < tl.nch; ++c, ++g) {
+    int g = 0;  // chunks staged by this CTA so far (all units)
+    int u = blockIdx.x;
+    Unit un;
+    bool have = live_unit(u, un);
+    int raw_next = have ? fetch(un.tl, un.cb) : -1;
+    while (have && fine) {
+      const Tile &tl = un.tl;
+      int u2 = u + (int)gridDim.x;
+      Unit nx;
+      const bool have_next = live_unit(u2, nx);
+      for (int c = un.cb; c < un.ce; ++c, ++g) {
         int phys = raw_next;
-        raw_next = c + 1 < tl.nch ? fetch(tl, c + 1) : (have_next ? fetch(nx, 0) : -1);
+        raw_next = c + 1 < un.ce ? fetch(tl, c + 1) : (have_next ? fetch(nx.tl, nx.cb) : -1);
         const int st = g % ST;
         if (g >= ST &&
             !mbar_wait_bounded(&empty[st], (uint32_t)((g / ST) - 1) & 1u, &abort_s, wait_ns)) {
@@ -369,7 +411,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tma_rows(dst, map, tl.kvh * C::HALVES + h, pk << bs_shift, &full[st]);
         }
       }
-      tl = nx;
+      un = nx;
+      u = u2;
       have = have_next;
     }
     // copies still in flight land before the CTA leaves (the last fill of each stage)
@@ -391,16 +434,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint64_t d_k = tc::desc_sw128(smem_u32(ring), 16, 1024);
     const uint64_t d_v = tc::desc_sw128(smem_u32(ring) + C::KVB, kChunk * 128, 1024);
     int g = 0;
-    for (int t = blockIdx.x, k = 0; fine; t += gridDim.x, ++k) {
-      Tile tl;
-      if (!tile_of<GP>(p, ts, n_tiles, t, tl)) break;
-      // S: this tile's Q is in place
+    for (int u = blockIdx.x, k = 0; fine; u += gridDim.x, ++k) {
+      Unit un;
+      if (!live_unit(u, un)) break;
+      // S: this unit's Q is in place
       if (role == 0 && !mbar_wait_bounded(&q_full, (uint32_t)k & 1u, &abort_s, wait_ns)) {
         fine = false;
         break;
       }
-      for (int c = 0; c < tl.nch; ++c) {
-        const int x = g + c, st = x % ST;
+      for (int c = un.cb; c < un.ce; ++c) {
+        const int x = g + (c - un.cb), st = x % ST;
         if (role == 0) {
           // S(x) = Q_hi K^T + Q_lo K^T, once K of chunk x is staged and the
           // softmax has loaded S(x - 1) (and read its row mask)
@@ -453,7 +496,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         // P(x) written; before the tile's first P.V, the previous output read out
         if (!mbar_wait_bounded(&p_full[x & 1], (uint32_t)(x >> 1) & 1u, &abort_s, wait_ns) ||
-            (c == 0 && k > 0 &&
+            (c == un.cb && k > 0 &&
              !mbar_wait_bounded(&o_free, (uint32_t)(k - 1) & 1u, &abort_s, wait_ns))) {
           fine = false;
           break;
@@ -467,13 +510,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kChunk / 16; ++kk)
             tc::mma_f16_ts(tmem + kOCol, pa + kk * 8, tc::desc_advance(vd, kk * 2048), idesc_o,
-                           c > 0 || kk > 0);
+                           c > un.cb || kk > 0);
           tc::commit(&pv_done[x & 1]);
           tc::commit(&v_free[st]);
         }
         __syncwarp();
       }
-      g += tl.nch;
+      g += un.ce - un.cb;
     }
     // every MMA issued here has completed before tensor memory is released
     if (lane == 0) tc::commit(&drain[role]);
@@ -484,19 +527,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int row = tid & (kTcRows - 1), hc = tid >> 7, pair = 1 + (warp & 3);
     const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // lanes of this row
     constexpr int HC = kChunk / 2;  // score columns per thread: [HC hc, HC hc + HC)
-    Tile tl;
-    bool have = tile_of<GP>(p, ts, n_tiles, blockIdx.x, tl);
+    // this row's record of unit u (split tiles): max, sum, destination, O
+    auto record = [&](int u) -> float * {
+      return p.rec + ((size_t)u * kTcRows + row) * (D + 4);
+    };
+    auto dest_of = [&](const Tile &t2) -> int {
+      const RowOf<GP> r2(p, t2, row);
+      return r2.in ? r2.i * p.Hq + t2.kvh * p.G + r2.hg : -1;
+    };
+    // pieces of this CTA with no chunks: records that add nothing
+    if (n_split > 1) {
+      for (int ue = blockIdx.x; ue < n_units; ue += gridDim.x) {
+        Unit e;
+        unit_of<GP>(p, ts, n_tiles, n_split, ue, e);
+        if (e.ce > e.cb) continue;
+        float *rr = record(ue);
+        for (int d0 = hc * (D / 2); d0 < (hc + 1) * (D / 2); d0 += 4)
+          *reinterpret_cast<float4 *>(rr + 4 + d0) = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (hc == 0)
+          *reinterpret_cast<float4 *>(rr) =
+              make_float4(-INFINITY, 0.f, __int_as_float(dest_of(e.tl)), 0.f);
+      }
+    }
+    int u = blockIdx.x;
+    Unit un;
+    bool have = live_unit(u, un);
     if (have) {
-      write_q<D, GP>(p, tl, row, hc, qhi, qlo);
+      write_q<D, GP>(p, un.tl, row, hc, qhi, qlo);
       tc::fence_proxy_shared();
       __syncwarp();
       if (lane == 0) mbar_arrive(&q_full);
     }
     int g = 0;
-    for (int t = blockIdx.x; have; t += gridDim.x) {
-      // the next tile's query rows head for L2 while this tile runs
-      Tile nx;
-      const bool have_next = tile_of<GP>(p, ts, n_tiles, t + (int)gridDim.x, nx);
+    while (have) {
+      const Tile &tl = un.tl;
+      // the next unit's query rows head for L2 while this unit runs
+      int u2 = u + (int)gridDim.x;
+      Unit nxu;
+      const bool have_next = live_unit(u2, nxu);
+      const Tile &nx = nxu.tl;
       const float *qn = nullptr;  // this thread's half of its next-tile query row (or none)
       if (have_next) {
         const RowOf<GP> rn(p, nx, row);
@@ -546,20 +615,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       float m_run = -INFINITY, l_run = 0.f;
-      for (int c = 0; c < tl.nch; ++c) {
-        const int x = g + c;
-        const bool last = c + 1 == tl.nch;
-        // the next tile's Q slice c: loads in flight across this chunk
-        const bool slice = have_next && c < NSL && !last;
+      for (int c = un.cb; c < un.ce; ++c) {
+        const int lc = c - un.cb;  // chunk within the unit
+        const int x = g + lc;
+        const bool last = c + 1 == un.ce;
+        // the next unit's Q slice lc: loads in flight across this chunk
+        const bool slice = have_next && lc < NSL && !last;
         float4 qa, qb;
-        if (slice) load_slice(c, qa, qb);
+        if (slice) load_slice(lc, qa, qb);
         // ---- S(x) complete
         fine = mbar_wait_bounded(&s_full, (uint32_t)x & 1u, &abort_s, wait_ns) && fine;
         tc::fence_after();
         if (last && have_next) {
           // every S of this tile is done: the rest of the next tile's Q is
           // staged, then all of it moves into the shared Q tiles
-          for (int k = c; k < NSL; ++k) {
+          for (int k = lc; k < NSL; ++k) {
             float4 a, b;
             load_slice(k, a, b);
             store_slice(k, a, b);
@@ -651,7 +721,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           l_run *= scale_o;
           m_run = m_new;
         }
-        if (c > 0 && __any_sync(kAll, scale_o != 1.f)) {
+        if (c > un.cb && __any_sync(kAll, scale_o != 1.f)) {
           // P(x-1) V has been added to O
           fine = mbar_wait_bounded(&pv_done[(x - 1) & 1], (uint32_t)((x - 1) >> 1) & 1u, &abort_s,
                                    wait_ns) &&
@@ -694,11 +764,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[x & 1]);
-        if (slice) store_slice(c, qa, qb);
+        if (slice) store_slice(lc, qa, qb);
       }
       if (!fine) break;
-      const int x_last = g + tl.nch - 1;
-      g += tl.nch;
+      const int x_last = g + (un.ce - un.cb) - 1;
+      g += un.ce - un.cb;
       // ---- the last P.V, then the normalised row
       fine = mbar_wait_bounded(&pv_done[x_last & 1], (uint32_t)(x_last >> 1) & 1u, &abort_s,
                                wait_ns) &&
@@ -725,6 +795,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       const float l_row = pl_s[0][row] + pl_s[1][row];
+      if (n_split > 1) {
+        // a piece of a split tile: the unnormalised record, merged later
+        float *rr = record(u);
+#pragma unroll
+        for (int e = 0; e < DH; e += 4)
+          *reinterpret_cast<float4 *>(rr + 4 + hc * DH + e) =
+              make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+        if (hc == 0)
+          *reinterpret_cast<float4 *>(rr) =
+              make_float4(m_run, l_row, __int_as_float(dest_of(tl)), 0.f);
+        un = nxu;
+        u = u2;
+        have = have_next;
+        continue;
+      }
       const bool any = l_row > 0.f;
       const float inv = any ? 1.f / l_row : 0.f;
       if (rw.in) {
@@ -738,7 +823,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (rw.in && p.lse && hc == 0)
         p.lse[(size_t)rw.i * p.Hq + (size_t)tl.kvh * p.G + rw.hg] =
             any ? (m_run + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
-      tl = nx;
+      un = nxu;
+      u = u2;
       have = have_next;
     }
   }
@@ -751,6 +837,67 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) {
     tc::fence_after();
     tc::dealloc(tmem, kTmemCols);
+  }
+}
+
+// Merge the pieces of split tiles: one warp per tile row, lane l owns output
+// dims [l D/32, (l + 1) D/32); by log-sum-exp over the pieces' (max, sum)
+// records, then normalised. Rows of no query (destination -1) are skipped.
+template <int D>
+__global__ void __launch_bounds__(128) prefill_tc_combine_kernel(const __grid_constant__ PrefillParams p) {
+  constexpr int DV = D / 32;
+  pdl_enter();
+  const int n_tiles = p.rec_hdr[0], n_split = p.rec_hdr[1];
+  if (n_split <= 1) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t pstride = (size_t)kTcRows * (D + 4);  // from one piece of a tile to the next
+  for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    for (int r = warp; r < kTcRows; r += 4) {
+      const float *rr = p.rec + ((size_t)t * n_split * kTcRows + r) * (D + 4);
+      float m = -INFINITY, l = 0.f;
+      int dst = -1;
+      if (lane < n_split) {
+        const float4 h = __ldcg(reinterpret_cast<const float4 *>(rr + lane * pstride));
+        m = h.x;
+        l = h.y;
+        dst = __float_as_int(h.z);
+      }
+      if (!(l > 0.f)) m = -INFINITY;
+      float M = m;
+      int d = dst;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        M = fmaxf(M, __shfl_xor_sync(kAll, M, o));
+        d = max(d, __shfl_xor_sync(kAll, d, o));
+      }
+      if (d < 0) continue;
+      const float f = m == -INFINITY ? 0.f : exp2f(m - M);
+      float L = l * f;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(kAll, L, o);
+      float acc[DV];
+#pragma unroll
+      for (int e = 0; e < DV; ++e) acc[e] = 0.f;
+      for (int j = 0; j < n_split; ++j) {
+        const float fj = __shfl_sync(kAll, f, j);
+        if (fj == 0.f) continue;
+        const float *op = rr + j * pstride + 4 + lane * DV;
+#pragma unroll
+        for (int e = 0; e < DV; e += 2) {
+          const float2 v = __ldcg(reinterpret_cast<const float2 *>(op + e));
+          acc[e] = fmaf(fj, v.x, acc[e]);
+          acc[e + 1] = fmaf(fj, v.y, acc[e + 1]);
+        }
+      }
+      const bool any = L > 0.f;
+      const float inv = any ? 1.f / L : 0.f;
+      float *out = p.out + (size_t)d * D + lane * DV;
+#pragma unroll
+      for (int e = 0; e < DV; e += 2)
+        *reinterpret_cast<float2 *>(out + e) = make_float2(acc[e] * inv, acc[e + 1] * inv);
+      if (p.lse && lane == 0)
+        p.lse[d] = any ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+    }
   }
 }
 
@@ -787,6 +934,14 @@ mt_status launch_d(int gp, const PrefillParams &p, const TcMaps &m, int n_ctas, 
 bool prefill_tc_supported(mt_kv_format fmt, int head_dim, int block_size) {
   return fmt == MT_KV_F16 && (head_dim == 64 || head_dim == 128) &&
          (block_size == 16 || block_size == 32);
+}
+
+mt_status launch_prefill_tc_combine(const PrefillParams &p, int head_dim, int n_ctas,
+                                    cudaStream_t stream) {
+  if (!p.rec) return MT_OK;
+  auto kern = head_dim == 64 ? prefill_tc_combine_kernel<64> : prefill_tc_combine_kernel<128>;
+  return cuda_check(launch_pdl(kern, dim3(n_ctas), dim3(128), 0, stream, p),
+                    "prefill tc combine launch");
 }
 
 mt_status launch_prefill_tc(const PrefillParams &p, int head_dim, int gp, int n_ctas,
