@@ -9,9 +9,11 @@
 //
 // How (GB300): a tile is 128 (query, head) rows of one KV head (one
 // tensor-memory lane per row) and the sequence's positions up to the tile's
-// last query, in chunks of 128 tokens. A CTA takes whole tiles round-robin
-// (no split-K combine) and runs three roles that hand work to each other
-// through mbarriers only — no CTA-wide barrier inside the chunk loop:
+// last query, in chunks of 128 tokens. CTAs take units round-robin: whole
+// tiles, or, when there are fewer tiles than CTAs, pieces of each tile's
+// chunks whose unnormalised records a small combine kernel merges. A CTA runs
+// three roles that hand work to each other through mbarriers only — no
+// CTA-wide barrier inside the chunk loop:
 //   * two load warps read the chunk's block ids from the table (a chunk
 //     ahead) and stage its K and its V head slices with one tensor copy (TMA,
 //     128-byte swizzle) per block and 64-dim half into two rings of stages; a
