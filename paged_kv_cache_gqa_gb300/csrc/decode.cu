@@ -12,22 +12,25 @@
 // How (GB300-first design, not the pages' kernels):
 //  * Work is the stream of all sequences' (window-clipped) logical blocks,
 //    cut into equal contiguous ranges, one per persistent CTA (one CTA per
-//    SM). Every CTA derives its range from the context lengths itself, so
-//    long and short sequences balance without a planning launch. A CTA's
-//    range covers all KV heads of its blocks: the block's cells for all
-//    heads are one contiguous span of the pool, fetched by a single bulk
-//    (TMA) copy per K and per V.
+//    SM; two when a CTA has at most three consumer warps, so every scheduler
+//    still runs two). Every CTA derives its range from the context lengths
+//    itself, so long and short sequences balance without a planning launch.
+//    A CTA's range covers all KV heads of its blocks: the block's cells for
+//    all heads are one contiguous span of the pool.
 //  * Warp specialisation: one producer warp walks the range, reads block
-//    ids (32 at a time), skips holes, and issues bulk copies of the rows the
-//    window needs into a 2-4 stage shared-memory ring guarded by mbarriers.
-//    Consumer warps own one KV head each (several warps per head when there
-//    are fewer than 8 heads, splitting the block's tokens).
-//  * Consumer math on the FP32 pipes: lanes own 16-dim (8 when the group
-//    has more than 4 heads) slices of the head for one token; the G group
-//    heads' partial dot products are reduced across the token's lanes by
-//    recursive halving (G values cost G/2 + G/4 + ... shuffles instead of
-//    G per level); online softmax in base 2 with the max shared by the
-//    group; P.V with each lane owning head_dim/32 output dims of every head.
+//    ids (32 at a time), skips holes, and fills a shared-memory ring of up
+//    to 8 stages guarded by mbarriers: one swizzled 3-D tensor copy per K
+//    and per V block (f16, and f32 up to head_dim 128), else bulk copies of
+//    the rows the window needs.
+//  * Consumers: f16 and f32 (head_dim <= 128) pools on the tensor cores
+//    (mma.sync, one warp per KV head; f32 values split into high / low f16
+//    halves), q8_0 (head_dim <= 128) on the tensor cores from per-warp
+//    converted tiles, the rest on the FP32 pipes: lanes own 16-dim (8 when
+//    the group has more than 4 heads) slices of the head for one token; the
+//    G group heads' partial dot products are reduced across the token's
+//    lanes by recursive halving; online softmax in base 2 with the max
+//    shared by the group; P.V with each lane owning head_dim/32 output dims
+//    of every head.
 //  * Each (CTA, sequence) segment writes an unnormalised partial (o, m, l);
 //    the combine kernel merges them (log-sum-exp) and normalises.
 //  * Every mbarrier wait is bounded; a timeout sets the status word, stops
@@ -70,7 +73,7 @@ struct StageInfo {
 };
 
 struct Params {
-  CUtensorMap tmap_k;  // f16 tensor-core path: 3-D maps of the pools, see tma_block()
+  CUtensorMap tmap_k;  // tensor-copy path (f16, f32 up to d 128): 3-D maps of the pools, see tma_block()
   CUtensorMap tmap_v;
   const float *q;
   const uint8_t *k_pool;
@@ -1700,8 +1703,8 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
     return stages >= 2 && rows >= min_rows;
   };
   int rows = 0, pad = 0, stages = 0, wph = 1;
-  // f16 pools use the tensor-core consumers when a warp per KV head (two for
-  // head_dim 256) fits in the 8 consumer warps and 16-row stages fit.
+  // f16 and f32 pools use the tensor-core consumers when a warp per KV head
+  // (two for head_dim 256) fits in the 8 consumer warps and 16-row stages fit.
   const int mma_wph = a->head_dim == 256 ? 2 : 1;
   const int nc = (int)(rb / 128);
   pl->ncb = nc | 1;  // odd number of 128-byte lines per staged row

@@ -421,8 +421,9 @@ extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void 
     p.ctx = a->context_lens + s0;
     p.q_start = a->q_start + s0;
     if (prefill_tc_supported(a->fmt, a->head_dim, a->block_size)) {
-      // f16 pools: the tcgen05 kernel, one CTA (256 tensor-memory columns,
-      // ~210 KB of shared memory for head_dim 128) per SM
+      // f16 pools: the tcgen05 kernel, one CTA (all 512 tensor-memory
+      // columns, ~198 KB of shared memory for head_dim 128) per SM, then the
+      // merge of split tiles (returns at once when nothing was split)
       st = launch_prefill_tc(p, a->head_dim, GP, di.n_sm, s);
       if (st != MT_OK) return st;
       st = launch_prefill_tc_combine(p, a->head_dim, di.n_sm, s);
