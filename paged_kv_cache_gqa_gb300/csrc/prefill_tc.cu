@@ -249,7 +249,9 @@ struct TcMaps {
   CUtensorMap k, v;
 };
 
-template <int D, int GP>
+// SPLIT: the launch may cut tiles into pieces (records given); without it the
+// piece count is the constant 1 and every unit is a whole tile.
+template <int D, int GP, bool SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ TcMaps maps) {
   using C = TcCfg<D>;
@@ -323,10 +325,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // costs more than it saves: 3 pieces of 64 tiles on 152 CTAs ran slower
   // than no split, 2 pieces 1.43x faster); the combine kernel merges them
   int n_split = 1;
-  if (p.rec && n_tiles > 0 && n_tiles < (int)gridDim.x)
+  if (SPLIT && n_tiles > 0 && n_tiles < (int)gridDim.x)
     n_split = max(1, min(min((int)gridDim.x / n_tiles, kMaxSplit), p.rec_units / n_tiles));
   const int n_units = n_tiles * n_split;
-  if (p.rec && blockIdx.x == 0 && tid == 0) {
+  if (SPLIT && blockIdx.x == 0 && tid == 0) {
     p.rec_hdr[0] = n_tiles;
     p.rec_hdr[1] = n_split;
   }
@@ -903,10 +905,10 @@ __global__ void __launch_bounds__(128) prefill_tc_combine_kernel(const __grid_co
   }
 }
 
-template <int D, int GP>
+template <int D, int GP, bool SPLIT>
 mt_status launch_t(const PrefillParams &p, const TcMaps &m, int n_ctas, cudaStream_t s) {
   static int configured_dev = -1;
-  auto kern = prefill_tc_kernel<D, GP>;
+  auto kern = prefill_tc_kernel<D, GP, SPLIT>;
   constexpr int smem = TcCfg<D>::SMEM;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -921,14 +923,19 @@ mt_status launch_t(const PrefillParams &p, const TcMaps &m, int n_ctas, cudaStre
                     "prefill tc kernel launch");
 }
 
+template <int D, bool SPLIT>
+mt_status launch_g(int gp, const PrefillParams &p, const TcMaps &m, int n_ctas, cudaStream_t s) {
+  switch (gp) {
+    case 1: return launch_t<D, 1, SPLIT>(p, m, n_ctas, s);
+    case 2: return launch_t<D, 2, SPLIT>(p, m, n_ctas, s);
+    case 4: return launch_t<D, 4, SPLIT>(p, m, n_ctas, s);
+    default: return launch_t<D, 8, SPLIT>(p, m, n_ctas, s);
+  }
+}
+
 template <int D>
 mt_status launch_d(int gp, const PrefillParams &p, const TcMaps &m, int n_ctas, cudaStream_t s) {
-  switch (gp) {
-    case 1: return launch_t<D, 1>(p, m, n_ctas, s);
-    case 2: return launch_t<D, 2>(p, m, n_ctas, s);
-    case 4: return launch_t<D, 4>(p, m, n_ctas, s);
-    default: return launch_t<D, 8>(p, m, n_ctas, s);
-  }
+  return p.rec ? launch_g<D, true>(gp, p, m, n_ctas, s) : launch_g<D, false>(gp, p, m, n_ctas, s);
 }
 
 }  // namespace
