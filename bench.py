@@ -691,6 +691,43 @@ def run_extra(args, rank, world, local_rank):
                                      "per-sequence decode (mt_paged_attn_decode)"),
                           "store": args.store, "graph": bool(args.graph)},
                "clocks": clk}
+    elif args.workload == "llama3_formats":
+        # The decode call (decode + combine, no store) on the Llama-3-8B-shaped
+        # batch with each KV format in turn: 64 seqs, ctx log-uniform in
+        # [512, 16384], 32/8 heads, head_dim 128; 4 rotated pool pairs per
+        # format, so every call reads its K/V from HBM. Shows what the
+        # format's in-register dequantisation costs against the HBM roofline.
+        formats = {}
+        clocks.start()
+        for fmt, bs in (("f16", 16), ("f32", 16), ("q8_0", 16), ("q8_0", 32)):
+            w = workloads.llama3_f16(fmt=fmt, block_size=bs, hist=False)
+            layers, ws, rb = _decode_setup(mtkv, w, 4, dev, g)
+
+            def decode():
+                for kp, vp, a, kn in layers:
+                    mtkv.mt_paged_attn_decode(a, ws)
+
+            ms = _gpu_time(decode, steps, warmup, stream) / len(layers)
+            assert mtkv.mt_check_device_status(ws) == 0, mtkv.mt_last_error()
+            seg = {"f32": w.head_dim * 4, "f16": w.head_dim * 2,
+                   "q8_0": (w.head_dim // 32) * 34}[fmt]
+            ub, _lb, toks = _window_bytes(w, seg)
+            gbs = ub / (ms * 1e-3) / 1e9
+            formats[f"{fmt}_bs{bs}"] = {"row_bytes": rb, "bytes_per_call": ub,
+                                        "us_per_call": round(ms * 1e3, 2),
+                                        "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                                        "attended_tokens_per_s": round(toks / (ms * 1e-3), 1)}
+            del layers, ws
+            torch.cuda.empty_cache()
+        clk = clocks.stop()
+        q8 = formats["q8_0_bs32"]
+        res = {"metric": METRIC, "value": q8["GB/s"], "unit": "GB/s",
+               "value_kind": "q8_0 pools, block_size 32 (every format in `formats`)",
+               "frac_of_peak": q8["frac"], "formats": formats,
+               "config": {"workload": "llama3-8b-shaped paged decode call (decode + combine) per "
+                                      "KV format: 64 seqs, ctx log-uniform [512,16384], 32/8 "
+                                      "heads, head_dim 128; 4 rotated pool pairs per format"},
+               "clocks": clk}
     elif args.workload in ("prefill_f16", "prefill_f16_long"):
         # chunked prefill through the paged cache, Llama-3-8B-shaped heads, f16
         # pools, the queries' K/V rows already stored; 8 layers with their own
@@ -813,7 +850,7 @@ def main():
                     help="oracle baseline budget; 0 skips it (profiling runs)")
     ap.add_argument("--workload", default="llama3_f16",
                     choices=["llama3_f16", "smollm2_f32", "q8_prefix", "longctx_int4",
-                             "prefill_f16", "prefill_f16_long"],
+                             "llama3_formats", "prefill_f16", "prefill_f16_long"],
                     help="llama3_f16 is the benchmark line; the others measure the other kernels")
     ap.add_argument("--store", default=None, choices=["fused", "separate"],
                     help="store each layer's new row inside the decode launch "

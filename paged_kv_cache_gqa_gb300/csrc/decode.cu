@@ -554,28 +554,42 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
 //        exact up to the f16 split of p*d.
 // Tile rows are 2*D+16 bytes apart (an odd number of 16-byte units), which
 // keeps every ldmatrix phase conflict-free.
+//
+// A lane converts one 4-code unit in each of its rows: all of its loads are
+// issued first, then the conversions and stores, with no branch. Every row
+// converts, inside the window or not: q8_0 stages hold 16 or 32 rows and t0 is
+// a multiple of 16 inside the stage, so the rows t0 .. t0+15 lie in the
+// stage's buffer; int8 codes always give finite f16 values; and a row outside
+// the mask gets score -inf and probability 0, so its tile row reaches no
+// result.
 template <int D>
 __device__ __forceinline__ void q8_tile(const uint8_t *st, int row_bytes, int seg, int t0,
-                                        uint32_t mask, uint8_t *tile, int lane) {
-  constexpr int GPR = D / 4;      // 4-value groups per head row
+                                        uint8_t *tile, int lane) {
+  constexpr int GPR = D / 4;      // 4-code units per head row
+  constexpr int RPP = 32 / GPR;   // tile rows per warp pass (1 for D = 128, 2 for 64)
+  constexpr int NP = 16 / RPP;    // passes over the 16 rows
   constexpr int TP = 2 * D + 16;  // tile pitch in bytes
-  for (int idx = lane; idx < 16 * GPR; idx += 32) {
-    const int tr = idx / GPR, grp = idx % GPR;
-    const int tok = t0 + tr;
-    uint2 out = make_uint2(0u, 0u);
-    if ((mask >> tok) & 1u) {
-      const uint8_t *a = st + (size_t)tok * row_bytes + seg + (grp >> 3) * 34 + 2 + (grp & 7) * 4;
-      const uint32_t w = ((uint32_t)*reinterpret_cast<const uint16_t *>(a) |
-                          ((uint32_t)*reinterpret_cast<const uint16_t *>(a + 2) << 16)) ^
-                         0x80808080u;
-      const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-      uint32_t lo = __byte_perm(w, 0x64646464u, 0x4140);
-      uint32_t hi = __byte_perm(w, 0x64646464u, 0x4342);
-      lo = h2_bits(__hsub2(*reinterpret_cast<__half2 *>(&lo), bias));
-      hi = h2_bits(__hsub2(*reinterpret_cast<__half2 *>(&hi), bias));
-      out = make_uint2(lo, hi);
-    }
-    *reinterpret_cast<uint2 *>(tile + tr * TP + grp * 8) = out;
+  const int grp = lane % GPR;
+  const int tr = lane / GPR;
+  const uint8_t *a = st + (size_t)(t0 + tr) * row_bytes + seg + (grp >> 3) * 34 + 2 + (grp & 7) * 4;
+  uint8_t *o = tile + tr * TP + grp * 8;
+  uint32_t w[NP];
+#pragma unroll
+  for (int k = 0; k < NP; ++k) {
+    const uint8_t *ak = a + (size_t)k * RPP * row_bytes;
+    const uint32_t lo = *reinterpret_cast<const uint16_t *>(ak);
+    const uint32_t hi = *reinterpret_cast<const uint16_t *>(ak + 2);
+    w[k] = __byte_perm(lo, hi, 0x5410) ^ 0x80808080u;  // codes + 128, as bytes
+  }
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+#pragma unroll
+  for (int k = 0; k < NP; ++k) {
+    // f16 bit pattern 0x64XX is 1024 + XX; subtracting 1152 leaves the code
+    uint32_t lo = __byte_perm(w[k], 0x64646464u, 0x4140);
+    uint32_t hi = __byte_perm(w[k], 0x64646464u, 0x4342);
+    lo = h2_bits(__hsub2(*reinterpret_cast<__half2 *>(&lo), bias));
+    hi = h2_bits(__hsub2(*reinterpret_cast<__half2 *>(&hi), bias));
+    *reinterpret_cast<uint2 *>(o + k * RPP * TP) = make_uint2(lo, hi);
   }
 }
 
@@ -663,12 +677,19 @@ __device__ __forceinline__ void consume_mma_q8(const Params &p, uint64_t *full, 
       const uint8_t *vst = kst + p.blk_pad;
       float pr[4][2];
       float mloc = -INFINITY;
+      // the first 16-token half's V tile converts together with its K tile,
+      // so its loads and stores overlap the K conversion and the scores
+      int vh = -1;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int t0 = 16 * h;
         pr[2 * h][0] = pr[2 * h][1] = pr[2 * h + 1][0] = pr[2 * h + 1][1] = -INFINITY;
         if (t0 >= p.bs || t0 + 16 <= r0 || t0 >= r1) continue;
-        q8_tile<D>(kst, p.row_bytes, seg, t0, mask, tk, lane);
+        q8_tile<D>(kst, p.row_bytes, seg, t0, tk, lane);
+        if (vh < 0) {
+          q8_tile<D>(vst, p.row_bytes, seg, t0, tv, lane);
+          vh = h;
+        }
         __syncwarp();
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -723,8 +744,10 @@ __device__ __forceinline__ void consume_mma_q8(const Params &p, uint64_t *full, 
       for (int h = 0; h < 2; ++h) {
         const int t0 = 16 * h;
         if (t0 >= p.bs || t0 + 16 <= r0 || t0 >= r1) continue;
-        q8_tile<D>(vst, p.row_bytes, seg, t0, mask, tv, lane);
-        __syncwarp();
+        if (h != vh) {
+          q8_tile<D>(vst, p.row_bytes, seg, t0, tv, lane);
+          __syncwarp();
+        }
         const uint32_t vaddr = smem_u32(tv + (((lane >> 4) & 1) * 8 + (lane & 7)) * TP) +
                                (uint32_t)((lane >> 3) & 1) * 16;
         const int ta = t0 + 2 * c, tb = t0 + 8 + 2 * c;  // this thread's B rows (tokens)
