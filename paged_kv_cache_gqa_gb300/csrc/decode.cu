@@ -599,6 +599,27 @@ __device__ __forceinline__ float q8_scale(const uint8_t *st, int row_bytes, int 
                                                         grp * 34));
 }
 
+// The f32 group scales of rows t0 .. t0+15 of this head, sc[row - t0][group].
+// Staged rows sit row_bytes apart (16 banks apart for 1088-byte rows), so the
+// fragment lanes that need rows 2c and 2c+1 would all read one bank; from the
+// small row-major f32 array they read 4 (or 8) banks apart, without conflict.
+// Rows outside the mask may hold any bits here, like their codes: their scores
+// are replaced by -inf and their probabilities by 0 before any use.
+template <int D>
+__device__ __forceinline__ void q8_scales(const uint8_t *st, int row_bytes, int seg, int t0,
+                                          float *sc, int lane) {
+  constexpr int NG = D / 32;
+  constexpr int NP = 16 * NG / 32;  // 2 for D = 128, 1 for 64
+  float v[NP];
+#pragma unroll
+  for (int k = 0; k < NP; ++k) {
+    const int i = lane + 32 * k;
+    v[k] = q8_scale(st, row_bytes, seg, t0 + i / NG, i % NG);
+  }
+#pragma unroll
+  for (int k = 0; k < NP; ++k) sc[lane + 32 * k] = v[k];
+}
+
 template <int D, int GP>
 __device__ __forceinline__ void consume_mma_q8(const Params &p, uint64_t *full, uint64_t *empty,
                                                StageInfo *infos, volatile int *abort_flag,
@@ -620,6 +641,10 @@ __device__ __forceinline__ void consume_mma_q8(const Params &p, uint64_t *full, 
   const int seg = kvh * NG * 34;  // byte offset of this head in a row
   uint8_t *tk = tiles + (size_t)warp * 2 * 16 * TP;
   uint8_t *tv = tk + 16 * TP;
+  // per-warp f32 group scales of the K and V halves, after all warps' tiles
+  float *sk = reinterpret_cast<float *>(tiles + (size_t)kMaxConsumerWarps * 2 * 16 * TP) +
+              (size_t)warp * 2 * 16 * NG;
+  float *sv = sk + 16 * NG;
 
   uint32_t qa[M::KS][4];
   float oacc[M::MTW][4];
@@ -686,8 +711,10 @@ __device__ __forceinline__ void consume_mma_q8(const Params &p, uint64_t *full, 
         pr[2 * h][0] = pr[2 * h][1] = pr[2 * h + 1][0] = pr[2 * h + 1][1] = -INFINITY;
         if (t0 >= p.bs || t0 + 16 <= r0 || t0 >= r1) continue;
         q8_tile<D>(kst, p.row_bytes, seg, t0, tk, lane);
+        q8_scales<D>(kst, p.row_bytes, seg, t0, sk, lane);
         if (vh < 0) {
           q8_tile<D>(vst, p.row_bytes, seg, t0, tv, lane);
+          q8_scales<D>(vst, p.row_bytes, seg, t0, sv, lane);
           vh = h;
         }
         __syncwarp();
@@ -704,8 +731,8 @@ __device__ __forceinline__ void consume_mma_q8(const Params &p, uint64_t *full, 
             ldsm_x4(kaddr + grp * 64, b0, b1, b2, b3);
             mma_f16(acc, qa[2 * grp], b0, b1);
             mma_f16(acc, qa[2 * grp + 1], b2, b3);
-            s0 = fmaf(q8_scale(kst, p.row_bytes, seg, tk0, grp), acc[0] + acc[2], s0);
-            s1 = fmaf(q8_scale(kst, p.row_bytes, seg, tk0 + 1, grp), acc[1] + acc[3], s1);
+            s0 = fmaf(sk[(tk0 - t0) * NG + grp], acc[0] + acc[2], s0);
+            s1 = fmaf(sk[(tk0 + 1 - t0) * NG + grp], acc[1] + acc[3], s1);
           }
           pr[2 * h + t][0] = (row_ok && ((mask >> tk0) & 1u)) ? s0 : -INFINITY;
           pr[2 * h + t][1] = (row_ok && ((mask >> (tk0 + 1)) & 1u)) ? s1 : -INFINITY;
@@ -746,6 +773,7 @@ __device__ __forceinline__ void consume_mma_q8(const Params &p, uint64_t *full, 
         if (t0 >= p.bs || t0 + 16 <= r0 || t0 >= r1) continue;
         if (h != vh) {
           q8_tile<D>(vst, p.row_bytes, seg, t0, tv, lane);
+          q8_scales<D>(vst, p.row_bytes, seg, t0, sv, lane);
           __syncwarp();
         }
         const uint32_t vaddr = smem_u32(tv + (((lane >> 4) & 1) * 8 + (lane & 7)) * TP) +
@@ -755,11 +783,10 @@ __device__ __forceinline__ void consume_mma_q8(const Params &p, uint64_t *full, 
         const bool vb0 = (mask >> tb) & 1u, vb1 = (mask >> (tb + 1)) & 1u;
 #pragma unroll
         for (int grp = 0; grp < NG; ++grp) {
-          const float pa0 = va0 ? pr[2 * h][0] * q8_scale(vst, p.row_bytes, seg, ta, grp) : 0.f;
-          const float pa1 = va1 ? pr[2 * h][1] * q8_scale(vst, p.row_bytes, seg, ta + 1, grp) : 0.f;
-          const float pb0 = vb0 ? pr[2 * h + 1][0] * q8_scale(vst, p.row_bytes, seg, tb, grp) : 0.f;
-          const float pb1 =
-              vb1 ? pr[2 * h + 1][1] * q8_scale(vst, p.row_bytes, seg, tb + 1, grp) : 0.f;
+          const float pa0 = va0 ? pr[2 * h][0] * sv[(ta - t0) * NG + grp] : 0.f;
+          const float pa1 = va1 ? pr[2 * h][1] * sv[(ta + 1 - t0) * NG + grp] : 0.f;
+          const float pb0 = vb0 ? pr[2 * h + 1][0] * sv[(tb - t0) * NG + grp] : 0.f;
+          const float pb1 = vb1 ? pr[2 * h + 1][1] * sv[(tb + 1 - t0) * NG + grp] : 0.f;
           uint32_t bq0, bq1;
           if (M::HILO) {
             uint32_t h0, l0, h1, l1;
@@ -1699,7 +1726,9 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
   // to align the ring, 16 bytes of tail
   const bool q8_mma = a->fmt == MT_KV_Q8_0 && (a->head_dim == 64 || a->head_dim == 128);
   const int simt_scratch = (kMaxConsumerWarps * (32 * GP + GP) * 4 + 127) & ~127;
-  const int tile_scratch = kMaxConsumerWarps * 2 * 16 * (2 * a->head_dim + 16);
+  // (per warp: K and V tiles of 16 rows, then their f32 group scales)
+  const int tile_scratch =
+      kMaxConsumerWarps * 2 * 16 * ((2 * a->head_dim + 16) + (a->head_dim / 32) * 4);
   pl->scratch = q8_mma ? std::max(simt_scratch, tile_scratch) : simt_scratch;
   const int fixed = kHdrBytes + pl->scratch + 1024 + 16;
   int n_ctas = a->n_ctas;
