@@ -55,6 +55,27 @@ __device__ __forceinline__ void load8(const uint8_t *p, float (&x)[8]) {
   }
 }
 
+// Packed f32x2 arithmetic: each lane is rounded exactly as the scalar
+// instruction would round it (IEEE round-to-nearest-even, subnormals kept).
+__device__ __forceinline__ void mul2(float a, float b, float s, float &x, float &y) {
+  asm("{ .reg .b64 p, q, r; mov.b64 p, {%2, %3}; mov.b64 q, {%4, %4}; mul.rn.f32x2 r, p, q; "
+      "mov.b64 {%0, %1}, r; }"
+      : "=f"(x), "=f"(y)
+      : "f"(a), "f"(b), "f"(s));
+}
+__device__ __forceinline__ void add2(float a, float b, float m, float &x, float &y) {
+  asm("{ .reg .b64 p, q, r; mov.b64 p, {%2, %3}; mov.b64 q, {%4, %4}; add.rn.f32x2 r, p, q; "
+      "mov.b64 {%0, %1}, r; }"
+      : "=f"(x), "=f"(y)
+      : "f"(a), "f"(b), "f"(m));
+}
+__device__ __forceinline__ void sub2(float a, float b, float c, float d, float &x, float &y) {
+  asm("{ .reg .b64 p, q, r; mov.b64 p, {%2, %3}; mov.b64 q, {%4, %5}; sub.rn.f32x2 r, p, q; "
+      "mov.b64 {%0, %1}, r; }"
+      : "=f"(x), "=f"(y)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+}
+
 // Eight codes packed into one word of nibbles (element e in bits 4e..4e+3).
 // t = y + (1.5 * 2^23 + 8) rounds y = x * inv to the nearest integer, ties to
 // even (the constant is even and its ulp is 1), and leaves rint(y) + 8 in
@@ -63,20 +84,29 @@ __device__ __forceinline__ void load8(const uint8_t *p, float (&x)[8]) {
 // 2^-16 of a half-integer; that word is redone with the exact IEEE division,
 // so the result equals clamp(rint(x / scale), -8, 7) + 8 for every element.
 // `fast` is false when the reciprocal is not usable (a scale so small that
-// 1 / scale overflows), and then every element takes the exact path.
+// 1 / scale overflows), and then every element takes the exact path. The
+// products and sums run two elements per instruction, and each pair of
+// nibbles becomes a byte with one shift and one bit select.
 __device__ __forceinline__ uint32_t int4_pack8(const float (&x)[8], float scale, float inv,
                                                bool fast) {
   if (scale == 0.f) return 0x88888888u;
   constexpr float kMagic8 = 12582920.0f;  // 1.5 * 2^23 + 8
-  uint32_t word = 0;
+  uint32_t b[4];
   float dev = 0.f;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float y = x[e] * inv;
-    const float t = y + kMagic8;
-    dev = fmaxf(dev, fabsf(y - (t - kMagic8)));
-    word |= (__float_as_uint(t) & 15u) << (4 * e);
+  for (int e = 0; e < 8; e += 2) {
+    float y0, y1, t0, t1, r0, r1, d0, d1;
+    mul2(x[e], x[e + 1], inv, y0, y1);
+    add2(y0, y1, kMagic8, t0, t1);
+    add2(t0, t1, -kMagic8, r0, r1);  // rint(y), exactly
+    sub2(y0, y1, r0, r1, d0, d1);
+    dev = fmaxf(dev, fmaxf(fabsf(d0), fabsf(d1)));
+    // low nibble from t0, high nibble from t1 (bits above the byte are
+    // dropped by the byte permutes below)
+    b[e / 2] = (__float_as_uint(t0) & 0xFu) | ((__float_as_uint(t1) << 4) & ~0xFu);
   }
+  uint32_t word = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040),
+                              0x5410);
   if (!fast || dev > 0.5f - 1.52587890625e-05f) {
     word = 0;
 #pragma unroll
