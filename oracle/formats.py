@@ -14,7 +14,7 @@ TEST INFRASTRUCTURE: see the package docstring for who may import this.
   three-tier model": per block one f32 scale followed by ceil(n/2) packed
   int4 nibbles.
 
-Readings where the pages leave a step open (each also listed in the design doc):
+Readings where the pages leave a step open:
   - q8_0 block byte layout: {f16 d (little endian); int8 q[32]} = 34 bytes;
     head h of a row owns blocks [h*d/32, (h+1)*d/32); the row is zero-padded
     to a multiple of 4 bytes.

@@ -13,7 +13,7 @@ TEST INFRASTRUCTURE: see the package docstring for who may import this.
   grow_to doubles the capacity (capped at max_ctx) and copies each layer's
   old rows verbatim to the new stride.
 
-Readings (also in DESIGN.md): "top-down" sorts upward moves by source
+Readings: "top-down" sorts upward moves by source
 descending, "bottom-up" sorts downward moves by source ascending, and
 moves with dst == src are dropped. A move list is hazardous when some
 move writes a row that a later move still has to read; such a list has no
