@@ -241,3 +241,23 @@ def test_store_formats_bit_exact(mt):
                    torch.tensor([7], dtype=torch.int64, device="cuda"), status=status)
     assert mt.mt_check_device_status(status) == mt.MT_ERR_DEVICE_CHECK
     assert int(k_dev.sum()) == 0
+
+
+def test_store_q8_0_hand_worked_blocks(mt):
+    # The GPU quantiser against the hand-worked blocks themselves (not only
+    # against the oracle): among them, groups whose f16 scale differs from the
+    # float32 amax/127 in either direction, one subnormal, and ties.
+    from tests import golden
+    blocks = golden.q8_0_blocks()
+    rows = np.array([x for x, _ in blocks], dtype=np.float32)      # [n][32]: 1 head, d 32
+    n = rows.shape[0]
+    k_dev = torch.zeros(n, 36, dtype=torch.uint8, device="cuda")
+    v_dev = torch.zeros_like(k_dev)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cells = torch.arange(n, dtype=torch.int64, device="cuda")
+    mt.mt_kv_store("q8_0", k_dev, v_dev, 1, 32, to_dev(rows), to_dev(-rows), cells, status=status)
+    assert mt.mt_check_device_status(status) == 0
+    k = k_dev.cpu().numpy()
+    for i, (_, want) in enumerate(blocks):
+        assert list(k[i, :34]) == want, i
+        assert list(k[i, 34:]) == [0, 0]

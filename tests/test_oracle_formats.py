@@ -19,7 +19,7 @@ def test_f16_conversion_matches_ieee_encodings():
         assert int(got) == bits, (v, hex(int(got)), hex(bits))
 
 
-@pytest.mark.parametrize("case", range(4))
+@pytest.mark.parametrize("case", range(len(golden.q8_0_blocks())))
 def test_q8_0_hand_worked_blocks(case):
     x, want = golden.q8_0_blocks()[case]
     got = formats.encode_rows("q8_0", np.array([x], dtype=np.float32), 1, 32)
@@ -27,6 +27,24 @@ def test_q8_0_hand_worked_blocks(case):
     assert got.shape == (1, 36)
     assert list(got[0, :34]) == want
     assert list(got[0, 34:]) == [0, 0]
+
+
+def test_q8_0_divisor_blocks_tell_the_two_readings_apart():
+    # The fixture's last four blocks code differently when the division uses
+    # the stored f16 scale instead of the float32 amax/127: recomputing their
+    # codes that other way must disagree with the expected bytes, so the
+    # hand-worked pins above do decide which divisor the oracle uses.
+    blocks = golden.q8_0_blocks()
+    assert len(blocks) >= 8
+    for x, want in blocks[4:]:
+        x = np.array(x, dtype=np.float32)
+        d16 = np.array(want[:2], dtype=np.uint8).view("<f2")[0]
+        assert d16 != 0
+        other = np.clip(np.rint(x / np.float32(d16)), -127, 127).astype(np.int8)
+        assert list(other.view(np.uint8)) != want[2:]
+        # and the stored scale is the f16 rounding of the float32 amax/127
+        d32 = np.float32(np.abs(x).max()) / np.float32(127)
+        assert np.float16(d32) == d16 and np.float32(d16) != d32
 
 
 def test_q8_0_row_width_whole_blocks_in_whole_words():
