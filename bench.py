@@ -24,7 +24,8 @@ from __future__ import annotations
 
 import os
 
-# the CPU oracle runs single-threaded; fix the BLAS pools before numpy loads
+# each CPU oracle worker runs single-threaded (the workers spread over the
+# host's cores); fix the BLAS pools before numpy loads
 for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -32,14 +33,17 @@ import argparse
 import hashlib
 import json
 import math
-import re
+import multiprocessing as mp
 import statistics
 import subprocess
 import sys
 import time
 
 import numpy as np
-import torch
+
+if __name__ != "__mp_main__":
+    # the oracle workers (spawned children that import this file) need numpy only
+    import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -172,93 +176,143 @@ class Clocks:
 
 
 def _traffic_from_profile():
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current decode kernel source (else None)."""
-    prof = os.path.join(ROOT, "profiles", "paged_decode_llama3_f16.md")
+    """DRAM bytes (read + write) per decode launch from the committed ncu
+    counters in profiles/decode_traffic.json, if they were taken on the
+    current decode kernel source (else None)."""
+    data = os.path.join(ROOT, "profiles", "decode_traffic.json")
     src = os.path.join(ROOT, "paged_kv_cache_gqa_gb300", "csrc", "decode.cu")
     try:
-        txt = open(prof).read()
+        with open(data) as f:
+            rec = json.load(f)
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        m_sha = re.search(r"decode\.cu sha256\[:16\]:\s*([0-9a-f]{16})", txt)
-        m_tr = re.search(r"traffic_bytes_per_launch_full:\s*([0-9.eE+]+)", txt)
-        if m_sha and m_tr and m_sha.group(1) == sha:
-            return float(m_tr.group(1))
-    except OSError:
+        if rec.get("source_sha256_16") == sha:
+            return float(rec["traffic_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
         pass
     return None
 
 
 class OracleSample:
-    """The CPU oracle (store + decode of one layer) on the first `n`
-    sequences of the workload, on pool rows generated for those sequences."""
+    """The CPU oracle (store + decode of one layer) on the sequences `seqs`
+    of the workload, on pool rows generated for those sequences (each
+    sequence's rows from its own seeded generator, so a sequence's data do
+    not depend on how the batch is split over workers). The sample's blocks
+    are renumbered into a compact pool (same shapes and lengths; only the
+    physical ids differ), so a worker holds only its own rows."""
 
-    def __init__(self, w, n):
+    def __init__(self, w, seqs):
         from oracle import formats as ofmt
-        self.w, self.n = w, n
-        rng = np.random.default_rng(SEED + 7)
+        self.w, self.seqs = w, list(seqs)
         hkv, d, bs = w.n_kv_heads, w.head_dim, w.block_size
         rb = ofmt.row_bytes("f16", hkv, d)
-        self.kp = np.zeros((w.n_cells, rb), np.uint8)
-        self.vp = np.zeros((w.n_cells, rb), np.uint8)
-        for s in range(n):
-            nb = -(-int(w.context_lens[s]) // bs)
-            for b in w.block_table[s, :nb]:
-                rows = rng.standard_normal((2, bs, hkv * d), dtype=np.float32)
-                self.kp[b * bs:(b + 1) * bs] = ofmt.encode_rows("f16", rows[0], hkv, d)
-                self.vp[b * bs:(b + 1) * bs] = ofmt.encode_rows("f16", rows[1], hkv, d)
-        db, self.toks = decode_bytes(w, range(n))
-        self.bytes = db + store_bytes(w) * n // w.n_seqs
+        nbs = [-(-int(w.context_lens[s]) // bs) for s in self.seqs]
+        self.table = np.full_like(w.block_table, -1)
+        self.cells = np.full(w.n_seqs, -1, dtype=np.int64)
+        self.kp = np.empty((sum(nbs) * bs, rb), np.uint8)
+        self.vp = np.empty_like(self.kp)
+        nxt = 0
+        for s, nb in zip(self.seqs, nbs):
+            self.table[s, :nb] = np.arange(nxt, nxt + nb, dtype=self.table.dtype)
+            c = int(w.context_lens[s]) - 1
+            self.cells[s] = (nxt + c // bs) * bs + c % bs
+            rng = np.random.default_rng((SEED + 7, s))
+            rows = rng.standard_normal((2, nb * bs, hkv * d), dtype=np.float32)
+            self.kp[nxt * bs:(nxt + nb) * bs] = ofmt.encode_rows("f16", rows[0], hkv, d)
+            self.vp[nxt * bs:(nxt + nb) * bs] = ofmt.encode_rows("f16", rows[1], hkv, d)
+            nxt += nb
+        db, self.toks = decode_bytes(w, self.seqs)
+        self.bytes = db + store_bytes(w) * len(self.seqs) // w.n_seqs
 
     def run(self) -> float:
         from oracle import attention as oatt
-        w, n = self.w, self.n
+        w, sq = self.w, self.seqs
         t0 = time.perf_counter()
-        oatt.kv_store("f16", self.kp, self.vp, w.k_new[:n], w.v_new[:n], w.new_cells[:n],
+        oatt.kv_store("f16", self.kp, self.vp, w.k_new[sq], w.v_new[sq], self.cells[sq],
                       w.n_kv_heads, w.head_dim)
-        oatt.paged_attn_decode("f16", w.q, self.kp, self.vp, w.block_table, w.context_lens, None,
+        oatt.paged_attn_decode("f16", w.q, self.kp, self.vp, self.table, w.context_lens, None,
                                w.n_heads, w.n_kv_heads, w.head_dim, w.block_size, w.scale,
-                               seqs=range(n))
+                               seqs=sq)
         return time.perf_counter() - t0
 
-    @classmethod
-    def calibrated(cls, w, budget_s: float):
-        """Smallest prefix of sequences whose oracle run takes >= budget_s
-        (estimated from a one-sequence run)."""
-        one = cls(w, 1)
-        t1 = max(one.run(), 1e-4) / max(1, one.toks)
-        toks, n = 0, 0
-        while n < w.n_seqs and toks * t1 < budget_s:
-            toks += int(w.context_lens[n])
-            n += 1
-        return cls(w, max(1, n))
+
+def _oracle_worker(seqs, reps, bar):
+    """One CPU core's share of the oracle layer: build its sequences' pools,
+    then run store + decode once per repetition between two barriers."""
+    smp = OracleSample(_structure(), seqs)
+    bar.wait()                      # data ready
+    for _ in range(reps):
+        bar.wait()                  # start together
+        smp.run()
+        bar.wait()                  # all done
+
+
+def _balanced_split(lengths, n):
+    """Sequences dealt to n workers, longest first to the least loaded."""
+    load = [0] * n
+    parts = [[] for _ in range(n)]
+    for s in sorted(range(len(lengths)), key=lambda i: -int(lengths[i])):
+        j = min(range(n), key=lambda k: load[k])
+        parts[j].append(s)
+        load[j] += int(lengths[s])
+    return [sorted(p) for p in parts if p]
+
+
+def oracle_layer_times(reps: int, max_workers: int | None = None):
+    """Wall-clock seconds of the CPU oracle's store + decode of one whole
+    layer (all sequences), spread over the host's cores by sequence: one
+    spawned single-threaded worker per core (each runs the oracle as it
+    stands on its share). Returns (times, cores, sample)."""
+    w = _structure()
+    cores = len(os.sched_getaffinity(0))
+    n = max(1, min(cores, w.n_seqs, max_workers or cores))
+    parts = _balanced_split(w.context_lens, n)
+    ctx = mp.get_context("spawn")
+    bar = ctx.Barrier(len(parts) + 1)
+    procs = [ctx.Process(target=_oracle_worker, args=(p, reps, bar), daemon=True) for p in parts]
+    for pr in procs:
+        pr.start()
+    times = []
+    try:
+        bar.wait(timeout=600)
+        for _ in range(reps):
+            bar.wait(timeout=600)
+            t0 = time.perf_counter()
+            bar.wait(timeout=600)
+            times.append(time.perf_counter() - t0)
+    finally:
+        for pr in procs:
+            pr.join(timeout=60)
+            if pr.is_alive():
+                pr.terminate()
+    db, toks = decode_bytes(w)
+    layer_bytes = db + store_bytes(w)
+    sample = (f"store+decode of all {w.n_seqs} sequences of one layer ({toks} attended "
+              f"positions), float64 numpy oracle, sequences split over {len(parts)} "
+              f"single-threaded worker processes")
+    return times, len(parts), sample, layer_bytes, toks
 
 
 def run_reference(args, rank):
-    """The reference arm: the CPU oracle, as it stands, on the host cores."""
+    """The reference arm: the CPU oracle, as it stands, on the host cores
+    (one step = store + decode of one whole layer)."""
     if rank != 0:
         return None
-    w = _structure()
-    # size one step's sample so that all steps fit in about two minutes
-    per_step = max(0.02, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
-    smp = OracleSample.calibrated(w, per_step)
-    times = []
-    for i in range(args.warmup + args.steps):
-        t = smp.run()
-        if i >= args.warmup:
-            times.append(t)
+    times, cores, sample, layer_bytes, toks = oracle_layer_times(args.warmup + args.steps)
+    times = times[args.warmup:]
     sec = statistics.median(times)
-    val = smp.bytes / sec / 1e9
+    val = layer_bytes / sec / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(val, 5), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "kv_format": "f16",
-                   "sample": f"first {smp.n} of 64 sequences, one layer per step"},
-        "attended_tokens_per_s": round(smp.toks / sec, 1),
-        "cpu_baseline": {"value": round(val, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"store+decode of the first {smp.n} sequences of one layer "
-                                   f"({smp.toks} attended positions), float64 numpy oracle"},
+                   "sample": "all 64 sequences of one layer per step"},
+        "step_ms": {"median": round(sec * 1e3, 3), "min": round(min(times) * 1e3, 3),
+                    "max": round(max(times) * 1e3, 3), "n": len(times)},
+        "attended_tokens_per_s": round(toks / sec, 1),
+        "cpu_baseline": {"value": round(val, 5), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": round(val, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -348,24 +402,25 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
+    # one event between consecutive steps: the total and each step's time
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     dec_ms = []
-    t0.record(stream)
-    for _ in range(args.steps):
+    marks[0].record(stream)
+    for i in range(args.steps):
         if graph is not None:
             graph.replay()
-            continue
-        step(record=True)
-        # per-call decode durations of this step (read back after the run)
-        dec_ms.append([e for e in ev])
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(n_layers)]
-    t1.record(stream)
+        else:
+            step(record=True)
+            # per-call decode durations of this step (read back after the run)
+            dec_ms.append([e for e in ev])
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(n_layers)]
+        marks[i + 1].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     barrier(world)
-    total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    total_ms = max_over_ranks(marks[0].elapsed_time(marks[-1]), world, dev)
+    per_step = [marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps)]
     if graph is not None:
         # per-call durations for the roofline from a few eager steps
         for _ in range(3):
@@ -457,13 +512,11 @@ def run_gpu(args, rank, world, local_rank):
         return None
     cpu = None
     if args.cpu_seconds > 0:
-        smp = OracleSample.calibrated(w, args.cpu_seconds / 3)
-        cpu_t = statistics.median([smp.run() for _ in range(3)])
-        cpu = {"value": round(smp.bytes / cpu_t / 1e9, 5), "unit": "GB/s", "cores": 1,
-               "kind": "oracle", "attended_tokens_per_s": round(smp.toks / cpu_t, 1),
-               "sample": f"store+decode of the first {smp.n} of 64 sequences of one layer "
-                         f"({smp.toks} attended positions), float64 numpy oracle, median of "
-                         f"3 runs of {cpu_t:.2f} s"}
+        times, cores, sample, layer_bytes, ltoks = oracle_layer_times(3)
+        cpu_t = statistics.median(times)
+        cpu = {"value": round(layer_bytes / cpu_t / 1e9, 5), "unit": "GB/s", "cores": cores,
+               "kind": "oracle", "attended_tokens_per_s": round(ltoks / cpu_t, 1),
+               "sample": sample + f", median of 3 runs ({cpu_t:.2f} s wall each)"}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -478,6 +531,7 @@ def run_gpu(args, rank, world, local_rank):
                    "l2": "inputs larger than L2 (1.3 GB of K/V per layer, 42 GB per step)",
                    "parallelism": f"replicas x{world}"},
         "frac_of_peak": round(value / peak, 4),
+        "step_ms": _spread(per_step),
         "attended_tokens_per_s": round(world * n_layers * toks / (ms_per_step * 1e-3), 1),
         "roofline": {"bound": "hbm",
                      "kernel": ("mt_paged_attn_decode_append (decode with the row store fused, "
@@ -505,7 +559,15 @@ def run_gpu(args, rank, world, local_rank):
 # `--workload` selects one of the other synthetic configurations to measure the
 # remaining kernels on GB300; the default line is the Llama-3 f16 step above.
 
-def _gpu_time(fn, steps, warmup, stream, graph=False):
+def _spread(ms):
+    """Median, min and max of per-step times (ms) from CUDA events."""
+    return {"median": round(statistics.median(ms), 4), "min": round(min(ms), 4),
+            "max": round(max(ms), 4), "n": len(ms)}
+
+
+def _gpu_time(fn, steps, warmup, stream, graph=False, spread=None):
+    """Mean ms per call of `fn` over `steps` timed calls after `warmup`;
+    `spread`, if given, receives the per-call median / min / max."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
@@ -517,14 +579,15 @@ def _gpu_time(fn, steps, warmup, stream, graph=False):
         g.replay()
         torch.cuda.synchronize()
         fn = g.replay
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    marks[0].record(stream)
+    for i in range(steps):
         fn()
-    b.record(stream)
+        marks[i + 1].record(stream)
     torch.cuda.synchronize()
-    return a.elapsed_time(b) / steps
+    if spread is not None:
+        spread.update(_spread([marks[i].elapsed_time(marks[i + 1]) for i in range(steps)]))
+    return marks[0].elapsed_time(marks[-1]) / steps
 
 
 def _decode_setup(mtkv, w, n_pools, dev, g, table=None):
@@ -606,7 +669,8 @@ def run_extra(args, rank, world, local_rank):
                     mtkv.mt_paged_attn_decode(a, ws)
 
         clocks.start()
-        ms = _gpu_time(step, steps, warmup, stream, graph=args.graph)
+        sp = {}
+        ms = _gpu_time(step, steps, warmup, stream, graph=args.graph, spread=sp)
         ub, lb_, toks = _window_bytes(w, w.head_dim * 4)
         step_bytes = w.n_layers * (ub + store_bytes(w))
         value = step_bytes / (ms * 1e-3) / 1e9
@@ -634,7 +698,7 @@ def run_extra(args, rank, world, local_rank):
         c_bytes = int(ordered[:, 2].sum()) * row * 60 * 2
         clk = clocks.stop()
         res = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s",
-               "ms_per_step": round(ms, 4), "frac_of_peak": round(value / peak, 4),
+               "ms_per_step": round(ms, 4), "step_ms": sp, "frac_of_peak": round(value / peak, 4),
                "attended_tokens_per_s": round(w.n_layers * toks / (ms * 1e-3), 1),
                "config": {"workload": "smollm2-135m-shaped f32 paged decode: 30 layers, 8 seqs, "
                                       "ctx U[2048,8192], 9/3 heads, head_dim 64, bs 16",
@@ -674,14 +738,15 @@ def run_extra(args, rank, world, local_rank):
                         mtkv.mt_paged_attn_decode(a, ws)
 
         clocks.start()
-        ms = _gpu_time(step, steps, warmup, stream, graph=args.graph)
+        sp = {}
+        ms = _gpu_time(step, steps, warmup, stream, graph=args.graph, spread=sp)
         clk = clocks.stop()
         ub, lb_, toks = _window_bytes(w, (w.head_dim // 32) * 34)
         value = 32 * (ub + store_bytes(w)) / (ms * 1e-3) / 1e9
         res = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s",
                "value_kind": "unique physical cells (shared prefix counted once)",
                "logical_GB/s": round(32 * lb_ / (ms * 1e-3) / 1e9, 1),
-               "ms_per_step": round(ms, 4), "frac_of_peak": round(value / peak, 4),
+               "ms_per_step": round(ms, 4), "step_ms": sp, "frac_of_peak": round(value / peak, 4),
                "attended_tokens_per_s": round(32 * toks / (ms * 1e-3), 1),
                "config": {"workload": "llama3-8b-shaped q8_0 paged decode: 32 layers, 32 seqs "
                                       "sharing a 4096-token prefix + U[64,1024] suffix, random "
@@ -760,7 +825,8 @@ def run_extra(args, rank, world, local_rank):
                 mtkv.mt_paged_attn_prefill(a, ws)
 
         clocks.start()
-        ms = _gpu_time(step, steps, warmup, stream)
+        sp = {}
+        ms = _gpu_time(step, steps, warmup, stream, spread=sp)
         clk = clocks.stop()
         assert mtkv.mt_check_device_status(ws) == 0, mtkv.mt_last_error()
         # each query j (position ctx - n + j) reads j + ctx - n + 1 positions;
@@ -773,6 +839,7 @@ def run_extra(args, rank, world, local_rank):
         tpeak = _tensor_peak()
         res = {"metric": "paged prefill attention TFLOP/s (f16 operands, f32 accumulate)",
                "value": round(tflops, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+               "step_ms": sp,
                "ms_per_call": round(ms / len(calls), 5),
                "query_tokens_per_s": round(len(calls) * n_q * w.n_seqs / (ms * 1e-3), 1),
                "roofline": {"bound": "tensor", "achieved": round(tflops, 2),
@@ -847,7 +914,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mtkv", choices=["mtkv", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
-                    help="oracle baseline budget; 0 skips it (profiling runs)")
+                    help="0 skips the CPU oracle baseline (profiling runs); any other value "
+                         "runs it: one whole layer over all host cores, three times")
     ap.add_argument("--workload", default="llama3_f16",
                     choices=["llama3_f16", "smollm2_f32", "q8_prefix", "longctx_int4",
                              "llama3_formats", "prefill_f16", "prefill_f16_long"],
