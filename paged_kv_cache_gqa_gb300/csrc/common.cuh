@@ -56,6 +56,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a warp whose phase is not complete yet is suspended
+// (it takes no issue slots) until the phase completes or about `hint_ns`
+// nanoseconds have passed.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; "
+      "selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -64,14 +79,17 @@ __device__ __forceinline__ uint64_t global_ns() {
 
 // Wait for the phase with `parity` to complete. Gives up (returns false)
 // when *abort becomes non-zero or after `limit_ns` nanoseconds (checked
-// every 64 polls, and never more than 2^31 polls), so no wait can hang.
+// every 8 polls, and never more than 2^31 polls), so no wait can hang.
+// After one plain test the waiting warp sleeps in suspended polls of at
+// most 20 us each, so a producer or consumer that waits long does not take
+// issue slots from the warps it shares a scheduler with.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   volatile int *abort, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 1; it < 0x80000000u; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
+    if ((it & 7u) == 0) {
       if (*abort) return false;
       if (global_ns() - t0 > limit_ns) return false;
     }

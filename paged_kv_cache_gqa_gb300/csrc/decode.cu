@@ -849,6 +849,356 @@ __device__ __forceinline__ void consume_mma_q8(const Params &p, uint64_t *full, 
   }
 }
 
+// ------------------------------------ q8_0 on MMA, operands from the rows
+//
+// For head_dim 128 the q8_0 consumer builds its tensor-core operands
+// straight from the staged rows instead of converting whole code tiles
+// through shared memory (no tile stores, no ldmatrix, no warp barrier
+// between conversion and use):
+//   * S = Q.K^T per 32-dim group: inside a group, the k-slots (2c, 2c+1,
+//     2c+8, 2c+9) of k-step j stand for dims 8c + 4j + (0, 1, 2, 3). Lane
+//     (g, c) of the B operand then needs the 8 consecutive codes [8c, 8c+8)
+//     of its token: one or two loads from the staged row, because a group's
+//     codes start 2 bytes after its f16 scale at an offset whose residue
+//     mod 8 is fixed (rows and head segments are whole 8-byte units for
+//     head_dim 128). Q's A fragments are built in the same dim order.
+//   * O^T += V^T.(P*d)^T: the A-operand rows of a group's two 16-dim m-tiles
+//     stand for dims 4g + (0, 1) and 4g + (2, 3), so lane (g, c) loads one
+//     4-code word per token and pairs two tokens' words with byte permutes
+//     (a register of the A operand holds two k-slots, i.e. two tokens, of
+//     one dim).
+//   * The score columns of a 16-row half take its tokens in the order
+//     0 4 1 5 2 6 3 7 | 8 12 9 13 10 14 11 15, so the four tokens a lane holds
+//     probabilities for (c, 4+c, 8+c, 12+c) are exactly the four k-slots it
+//     supplies to P.V: P never leaves registers.
+// int8 -> f16 is exact (the 1024-bias byte permute); each half's group
+// scales are read once into two small f32 arrays in score-column order.
+// Every row of a half converts, valid or not: codes always give finite
+// values, and an invalid row gets score -inf and a zero P.V operand (its
+// scale, which may be stale bits, is never multiplied in).
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void lds_u32x2(uint32_t a, uint32_t &x, uint32_t &y) {
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "r"(a));
+}
+__device__ __forceinline__ float lds_f16f(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return __half2float(__ushort_as_half(v));
+}
+
+// The 8 bytes at shared address a, where a % 8 == MIS (even): x = bytes
+// [a, a+4), y = bytes [a+4, a+8), with aligned loads only.
+template <int MIS>
+__device__ __forceinline__ void lds_code8(uint32_t a, uint32_t &x, uint32_t &y) {
+  static_assert(MIS == 0 || MIS == 2 || MIS == 4 || MIS == 6, "even offset");
+  if constexpr (MIS == 0) {
+    lds_u32x2(a, x, y);
+  } else if constexpr (MIS == 4) {
+    x = lds_u32(a);
+    y = lds_u32(a + 4);
+  } else if constexpr (MIS == 2) {
+    uint32_t w0, w1;
+    lds_u32x2(a - 2, w0, w1);
+    const uint32_t w2 = lds_u32(a + 6);
+    x = __byte_perm(w0, w1, 0x5432);
+    y = __byte_perm(w1, w2, 0x5432);
+  } else {
+    const uint32_t w0 = lds_u32(a - 2);
+    uint32_t w1, w2;
+    lds_u32x2(a + 2, w1, w2);
+    x = __byte_perm(w0, w1, 0x5432);
+    y = __byte_perm(w1, w2, 0x5432);
+  }
+}
+
+// The 4 bytes at shared address a, a % 4 == MIS (0 or 2).
+template <int MIS>
+__device__ __forceinline__ uint32_t lds_code4(uint32_t a) {
+  if constexpr (MIS == 0) {
+    return lds_u32(a);
+  } else {
+    return __byte_perm(lds_u32(a - 2), lds_u32(a + 2), 0x5432);
+  }
+}
+
+// f16 bit patterns 0x64XX are 1024 + XX: codes + 128 as bytes, then minus 1152
+__device__ __forceinline__ uint32_t biased_to_h2(uint32_t b, uint32_t sel) {
+  uint32_t h = __byte_perm(b, 0x64646464u, sel);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  return h2_bits(__hsub2(*reinterpret_cast<__half2 *>(&h), bias));
+}
+
+// int8 codes of word w (bytes 0..3) -> f16 pairs (code0, code1), (code2, code3)
+__device__ __forceinline__ void codes_to_h2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t b = w ^ 0x80808080u;
+  lo = biased_to_h2(b, 0x4140);
+  hi = biased_to_h2(b, 0x4342);
+}
+
+// words x (one token's codes of dims k..k+3) and y (another token's, same
+// dims) -> f16 pairs (x_i, y_i) for i = 0..3
+__device__ __forceinline__ void code_pairs_to_h2(uint32_t x, uint32_t y, uint32_t (&o)[4]) {
+  const uint32_t lo = __byte_perm(x, y, 0x5140) ^ 0x80808080u;  // x0 y0 x1 y1
+  const uint32_t hi = __byte_perm(x, y, 0x7362) ^ 0x80808080u;  // x2 y2 x3 y3
+  o[0] = biased_to_h2(lo, 0x4140);
+  o[1] = biased_to_h2(lo, 0x4342);
+  o[2] = biased_to_h2(hi, 0x4140);
+  o[3] = biased_to_h2(hi, 0x4342);
+}
+
+// Token (row within a 16-row half) of score column position pos = 8t + n.
+__host__ __device__ constexpr int q8d_col_token(int pos) {
+  return 8 * (pos >> 3) + ((pos & 7) >> 1) + 4 * (pos & 1);
+}
+
+// mma with a zero accumulator input: d = a.b
+__device__ __forceinline__ void mma_f16_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// Per-warp f32 scale arrays of the direct q8_0 consumer: K and V, for each
+// 16-row half of a stage, [group][score-column position].
+constexpr int kQ8dScaleFloats = 2 * 2 * 4 * 16;
+
+template <int GP, int NH>
+__device__ __forceinline__ void consume_q8_direct(const Params &p, uint64_t *full,
+                                                  uint64_t *empty, StageInfo *infos,
+                                                  volatile int *abort_flag, uint8_t *ring,
+                                                  float *scr, int warp, int lane) {
+  constexpr int D = 128;
+  constexpr int NG = 4;                 // q8_0 groups per head
+  constexpr bool HILO = GP <= 4;        // p split into two f16 columns
+  const int kvh = warp;
+  const int g = lane >> 2, c = lane & 3;
+  const int G = p.G;
+  const int S = p.stages;
+  const int hrow = HILO ? (g >> 1) : g;
+  const bool row_ok = hrow < G;
+  const bool lo_col = HILO && (g & 1);
+  const int src0 = 8 * c;
+  const int src1 = HILO ? 8 * c : 8 * c + 4;
+  const uint32_t seg = (uint32_t)kvh * (NG * 34);  // this head's bytes in a row
+  const uint32_t pitch = (uint32_t)p.pitch;
+  float *sK = scr + (size_t)warp * kQ8dScaleFloats;  // [h][grp][16]
+  float *sV = sK + 2 * NG * 16;
+  // this lane's K row within a 16-row half (tile t adds 8): score column g
+  const int krow = (g >> 1) + 4 * (g & 1);
+
+  uint32_t qa[NG][2][4];
+  float oacc[2 * NG][4];
+  float m_run = -INFINITY, l_run = 0.f;
+
+  for (uint32_t it = 0;; ++it) {
+    const int slot = (int)(it % (uint32_t)S);
+    int okv = 1;
+    if (lane == 0)
+      okv = mbar_wait_bounded(&full[slot], (it / (uint32_t)S) & 1u, abort_flag, p.wait_ns) ? 1 : 0;
+    okv = __shfl_sync(kFull, okv, 0);
+    if (!okv) {
+      if (lane == 0) {
+        *abort_flag = 1;
+        report(p.status, MT_STATUS_BIT_TIMEOUT);
+      }
+      return;
+    }
+    int seq, flags, base;
+    uint32_t mask;
+    {
+      const volatile int *vi = reinterpret_cast<const volatile int *>(&infos[slot]);
+      seq = vi[0];
+      flags = vi[3] & 0xff;
+      base = vi[3] >> 8;
+      mask = (uint32_t)vi[4];
+    }
+    if (flags & F_EXIT) return;
+
+    if (flags & F_NEW) {
+      const float *qh = p.q + ((size_t)seq * p.Hq + (size_t)kvh * G + hrow) * D;
+#pragma unroll
+      for (int grp = 0; grp < NG; ++grp)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (row_ok) x = *reinterpret_cast<const float4 *>(qh + 32 * grp + 8 * c + 4 * j);
+          split_h2(x.x * p.qscale, x.y * p.qscale, qa[grp][j][0], qa[grp][j][1]);
+          split_h2(x.z * p.qscale, x.w * p.qscale, qa[grp][j][2], qa[grp][j][3]);
+        }
+#pragma unroll
+      for (int mt = 0; mt < 2 * NG; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) oacc[mt][e] = 0.f;
+      m_run = -INFINITY;
+      l_run = 0.f;
+    }
+
+    if (flags & F_DATA) {
+      const uint32_t kst = smem_u32(ring + (size_t)slot * 2 * p.blk_pad);
+      const uint32_t vst = kst + (uint32_t)p.blk_pad;
+      // ---- group scales of both pools, per half, in score-column order
+#pragma unroll
+      for (int h = 0; h < NH; ++h)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int i = lane + 32 * k;          // [grp][pos]
+          const int grp = i >> 4, pos = i & 15;
+          const uint32_t off = (uint32_t)(16 * h + q8d_col_token(pos)) * pitch + seg + 34u * grp;
+          sK[h * NG * 16 + i] = lds_f16f(kst + off);
+          sV[h * NG * 16 + i] = lds_f16f(vst + off);
+        }
+      __syncwarp();
+      // ---- scores: two 8-column tiles per half
+      float pr[NH][2][2];
+      float mloc = -INFINITY;
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const uint32_t mh = (mask >> (base + 16 * h)) & 0xffffu;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const uint32_t ka = kst + (uint32_t)(16 * h + 8 * t + krow) * pitch + seg + 2u + 8u * c;
+          uint32_t w[NG][2];
+          lds_code8<2>(ka, w[0][0], w[0][1]);
+          lds_code8<4>(ka + 34, w[1][0], w[1][1]);
+          lds_code8<6>(ka + 68, w[2][0], w[2][1]);
+          lds_code8<0>(ka + 102, w[3][0], w[3][1]);
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int grp = 0; grp < NG; ++grp) {
+            uint32_t b[2][2];
+            codes_to_h2(w[grp][0], b[0][0], b[0][1]);
+            codes_to_h2(w[grp][1], b[1][0], b[1][1]);
+            float acc[4];
+            mma_f16_z(acc, qa[grp][0], b[0][0], b[0][1]);
+            mma_f16(acc, qa[grp][1], b[1][0], b[1][1]);
+            const float2 sc = *reinterpret_cast<const float2 *>(sK + h * NG * 16 + grp * 16 +
+                                                                8 * t + 2 * c);
+            s0 = fmaf(sc.x, acc[0] + acc[2], s0);
+            s1 = fmaf(sc.y, acc[1] + acc[3], s1);
+          }
+          const bool v0 = row_ok && ((mh >> (8 * t + c)) & 1u);
+          const bool v1 = row_ok && ((mh >> (8 * t + 4 + c)) & 1u);
+          pr[h][t][0] = v0 ? s0 : -INFINITY;
+          pr[h][t][1] = v1 ? s1 : -INFINITY;
+          mloc = fmaxf(mloc, fmaxf(pr[h][t][0], pr[h][t][1]));
+        }
+      }
+      // ---- online softmax (base 2); a lane's tokens of a half are c, 4+c,
+      // 8+c, 12+c, the group's four lanes cover all sixteen
+      mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, 1));
+      mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, 2));
+      const float m_new = fmaxf(m_run, mloc);
+      const bool none = m_new == -INFINITY;
+      const float alpha = none ? 1.f : exp2f(m_run - m_new);
+      m_run = m_new;
+      float lsum = 0.f;
+#pragma unroll
+      for (int h = 0; h < NH; ++h)
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          pr[h][t][0] = none ? 0.f : exp2f(pr[h][t][0] - m_new);
+          pr[h][t][1] = none ? 0.f : exp2f(pr[h][t][1] - m_new);
+          lsum += pr[h][t][0] + pr[h][t][1];
+        }
+      l_run = l_run * alpha + lsum;
+      const float a0 = __shfl_sync(kFull, alpha, src0);
+      const float a1 = __shfl_sync(kFull, alpha, src1);
+      if (!__all_sync(kFull, a0 == 1.f && a1 == 1.f)) {
+#pragma unroll
+        for (int mt = 0; mt < 2 * NG; ++mt) {
+          oacc[mt][0] *= a0;
+          oacc[mt][1] *= a1;
+          oacc[mt][2] *= a0;
+          oacc[mt][3] *= a1;
+        }
+      }
+      // ---- O^T += V^T . (P * d)^T, per half and group
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const uint32_t mh = (mask >> (base + 16 * h)) & 0xffffu;
+        // the k-slots 2c, 2c+1, 2c+8, 2c+9 are tokens c, 4+c, 8+c, 12+c
+        const bool va0 = (mh >> c) & 1u, va1 = (mh >> (4 + c)) & 1u;
+        const bool vb0 = (mh >> (8 + c)) & 1u, vb1 = (mh >> (12 + c)) & 1u;
+        const uint32_t va = vst + (uint32_t)(16 * h + c) * pitch + seg + 2u + 4u * g;
+        const uint32_t p4 = 4u * pitch;
+#pragma unroll
+        for (int grp = 0; grp < NG; ++grp) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t a = va + k * p4 + 34u * grp;
+            wv[k] = (grp & 1) ? lds_code4<0>(a) : lds_code4<2>(a);
+          }
+          uint32_t o01[4], o23[4];
+          code_pairs_to_h2(wv[0], wv[1], o01);
+          code_pairs_to_h2(wv[2], wv[3], o23);
+          const float *sv = sV + h * NG * 16 + grp * 16;
+          const float2 s01 = *reinterpret_cast<const float2 *>(sv + 2 * c);
+          const float2 s23 = *reinterpret_cast<const float2 *>(sv + 8 + 2 * c);
+          const float pa0 = va0 ? pr[h][0][0] * s01.x : 0.f;
+          const float pa1 = va1 ? pr[h][0][1] * s01.y : 0.f;
+          const float pb0 = vb0 ? pr[h][1][0] * s23.x : 0.f;
+          const float pb1 = vb1 ? pr[h][1][1] * s23.y : 0.f;
+          uint32_t bq0, bq1;
+          if (HILO) {
+            uint32_t h0, l0, h1, l1;
+            split_h2(pa0, pa1, h0, l0);
+            split_h2(pb0, pb1, h1, l1);
+            bq0 = lo_col ? l0 : h0;
+            bq1 = lo_col ? l1 : h1;
+          } else {
+            bq0 = h2_bits(__floats2half2_rn(pa0, pa1));
+            bq1 = h2_bits(__floats2half2_rn(pb0, pb1));
+          }
+          if (!row_ok) bq0 = bq1 = 0u;
+          const uint32_t am0[4] = {o01[0], o01[1], o23[0], o23[1]};  // dims 4g, 4g+1
+          const uint32_t am1[4] = {o01[2], o01[3], o23[2], o23[3]};  // dims 4g+2, 4g+3
+          mma_f16(oacc[2 * grp], am0, bq0, bq1);
+          mma_f16(oacc[2 * grp + 1], am1, bq0, bq1);
+        }
+      }
+    }
+
+    if (flags & F_END) {
+      float l = l_run;
+      l += __shfl_xor_sync(kFull, l, 1);
+      l += __shfl_xor_sync(kFull, l, 2);
+      const size_t P = (size_t)blockIdx.x + seq;
+      const size_t hq0 = P * p.Hq + (size_t)kvh * G;
+      if (c == 0 && row_ok && !lo_col) {
+        p.part_ml[(hq0 + hrow) * 2 + 0] = m_run;
+        p.part_ml[(hq0 + hrow) * 2 + 1] = l;
+      }
+      // rows g, g+8 of m-tiles 2grp, 2grp+1 are dims 32grp + 4g + (0, 1, 2, 3)
+#pragma unroll
+      for (int grp = 0; grp < NG; ++grp) {
+        const float *o0 = oacc[2 * grp], *o1 = oacc[2 * grp + 1];
+        if (HILO) {
+          if (c < G)
+            *reinterpret_cast<float4 *>(p.part_o + (hq0 + c) * D + 32 * grp + 4 * g) =
+                make_float4(o0[0] + o0[1], o0[2] + o0[3], o1[0] + o1[1], o1[2] + o1[3]);
+        } else {
+          if (2 * c < G)
+            *reinterpret_cast<float4 *>(p.part_o + (hq0 + 2 * c) * D + 32 * grp + 4 * g) =
+                make_float4(o0[0], o0[2], o1[0], o1[2]);
+          if (2 * c + 1 < G)
+            *reinterpret_cast<float4 *>(p.part_o + (hq0 + 2 * c + 1) * D + 32 * grp + 4 * g) =
+                make_float4(o0[1], o0[3], o1[1], o1[3]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+  }
+}
+
 // Fused store of one sequence's new row (decode with append): convert
 // k_new[s] and v_new[s] to the pool format and write them into `cell` of
 // both pools, by the 32 lanes of the calling warp, with the arithmetic of
@@ -1187,7 +1537,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
                               p.n_cw);
     }
   }
-  if constexpr (MMA && FMT == MT_KV_Q8_0 && D <= 128) {
+  if constexpr (MMA && FMT == MT_KV_Q8_0 && D == 128) {
+    if (p.rows == 32)
+      consume_q8_direct<GP, 2>(p, full, empty, infos, abort_flag, ring, scratch, warp, lane);
+    else
+      consume_q8_direct<GP, 1>(p, full, empty, infos, abort_flag, ring, scratch, warp, lane);
+  } else if constexpr (MMA && FMT == MT_KV_Q8_0 && D <= 128) {
     consume_mma_q8<D, GP>(p, full, empty, infos, abort_flag, ring, smem + kHdrBytes, warp, lane);
   } else if constexpr (MMA) {
     consume_mma<FMT, D, GP>(p, full, empty, infos, abort_flag, ring, warp, lane);
@@ -1726,9 +2081,13 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
   // to align the ring, 16 bytes of tail
   const bool q8_mma = a->fmt == MT_KV_Q8_0 && (a->head_dim == 64 || a->head_dim == 128);
   const int simt_scratch = (kMaxConsumerWarps * (32 * GP + GP) * 4 + 127) & ~127;
-  // (per warp: K and V tiles of 16 rows, then their f32 group scales)
+  // (per warp: K and V tiles of 16 rows, then their f32 group scales; for
+  // head_dim 128 the operands come straight from the staged rows and only
+  // the f32 scale arrays are kept)
   const int tile_scratch =
-      kMaxConsumerWarps * 2 * 16 * ((2 * a->head_dim + 16) + (a->head_dim / 32) * 4);
+      a->head_dim == 128
+          ? kMaxConsumerWarps * kQ8dScaleFloats * 4
+          : kMaxConsumerWarps * 2 * 16 * ((2 * a->head_dim + 16) + (a->head_dim / 32) * 4);
   pl->scratch = q8_mma ? std::max(simt_scratch, tile_scratch) : simt_scratch;
   const int fixed = kHdrBytes + pl->scratch + 1024 + 16;
   int n_ctas = a->n_ctas;
