@@ -96,7 +96,7 @@ struct Params {
   int blk_pad;   // bytes of one staged K (or V) row chunk, padded to 128
   int rows;      // block rows per stage (block_size, or a divisor of it for wide rows)
   int pitch;     // shared-memory bytes between consecutive staged rows
-  int use_tmap;  // 1: stage blocks with swizzled tensor copies (f16 tensor-core path)
+  int use_tmap;  // 1: stage blocks with tensor copies (f16 / f32 swizzled, q8_0 padded)
   int scratch_bytes;  // shared-memory bytes between the header and the stage ring
   int ncb;       // 128-byte chunks per staged row (odd), tensor path
   int n_sub;     // partial records per (CTA, sequence) slot
@@ -967,7 +967,7 @@ __device__ __forceinline__ void mma_f16_z(float (&d)[4], const uint32_t (&a)[4],
 
 // Per-warp f32 scale arrays of the direct q8_0 consumer: K and V, for each
 // 16-row half of a stage, [group][score-column position].
-constexpr int kQ8dScaleFloats = 2 * 2 * 4 * 16;
+constexpr int kQ8dScaleFloatsPerHalf = 2 * 4 * 16;
 
 template <int GP, int NH>
 __device__ __forceinline__ void consume_q8_direct(const Params &p, uint64_t *full,
@@ -988,8 +988,8 @@ __device__ __forceinline__ void consume_q8_direct(const Params &p, uint64_t *ful
   const int src1 = HILO ? 8 * c : 8 * c + 4;
   const uint32_t seg = (uint32_t)kvh * (NG * 34);  // this head's bytes in a row
   const uint32_t pitch = (uint32_t)p.pitch;
-  float *sK = scr + (size_t)warp * kQ8dScaleFloats;  // [h][grp][16]
-  float *sV = sK + 2 * NG * 16;
+  float *sK = scr + (size_t)warp * (NH * kQ8dScaleFloatsPerHalf);  // [h][grp][16]
+  float *sV = sK + NH * NG * 16;
   // this lane's K row within a 16-row half (tile t adds 8): score column g
   const int krow = (g >> 1) + 4 * (g & 1);
 
@@ -1313,8 +1313,11 @@ __device__ __forceinline__ int append_block(const Params &p, int s) {
   return (c - 1) / p.bs;
 }
 
-template <int FMT, int D, int GP, bool MMA>
-__global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_constant__ Params p) {
+// MINB: CTAs per SM the kernel is compiled for (2 only for the direct q8_0
+// consumer with 16-row stages, whose registers then fit two resident CTAs).
+template <int FMT, int D, int GP, bool MMA, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
+    paged_decode_kernel(const __grid_constant__ Params p) {
   using C = Cfg<FMT, D, GP>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
@@ -1378,7 +1381,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_kernel(const __grid_
             // the whole stage (rows [base, base + rows)) in two tensor copies
             uint8_t *dk = ring + (size_t)slot * 2 * p.blk_pad;
             const int cell = phys * p.bs + base;
-            mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * p.blk_pad));
+            mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * p.rows * p.pitch));
             tma_block(dk, &p.tmap_k, cell, &full[slot], pol);
             tma_block(dk + p.blk_pad, &p.tmap_v, cell, &full[slot], pol);
           } else if (flags & F_DATA) {
@@ -2040,6 +2043,8 @@ struct Plan {
   int D, GP, wph, n_cw, stages, n_ctas, blk_pad, rows, smem;
   bool mma;
   int pitch, n_sub, ncb, scratch;
+  int q8_chunk;  // q8_0 staged through the word tensor map: chunk bytes (0: bulk copies)
+  bool two_per_sm;  // kernel compiled for two resident CTAs per SM
   size_t ws_status, ws_seq, ws_ml, ws_o, ws_total;
 };
 
@@ -2084,12 +2089,14 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
   // (per warp: K and V tiles of 16 rows, then their f32 group scales; for
   // head_dim 128 the operands come straight from the staged rows and only
   // the f32 scale arrays are kept)
+  const bool q8_direct = q8_mma && a->head_dim == 128;
   const int tile_scratch =
-      a->head_dim == 128
-          ? kMaxConsumerWarps * kQ8dScaleFloats * 4
-          : kMaxConsumerWarps * 2 * 16 * ((2 * a->head_dim + 16) + (a->head_dim / 32) * 4);
-  pl->scratch = q8_mma ? std::max(simt_scratch, tile_scratch) : simt_scratch;
-  const int fixed = kHdrBytes + pl->scratch + 1024 + 16;
+      q8_direct ? kMaxConsumerWarps * 2 * kQ8dScaleFloatsPerHalf * 4
+                : kMaxConsumerWarps * 2 * 16 * ((2 * a->head_dim + 16) + (a->head_dim / 32) * 4);
+  // (the direct q8_0 consumer uses only its scale arrays)
+  pl->scratch = q8_direct ? tile_scratch
+                          : (q8_mma ? std::max(simt_scratch, tile_scratch) : simt_scratch);
+  int fixed = kHdrBytes + pl->scratch + 1024 + 16;
   int n_ctas = a->n_ctas;
   const bool auto_ctas = n_ctas == 0;
   int smem_cap = 232448;
@@ -2124,11 +2131,33 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
   pl->mma = (a->fmt == MT_KV_F16 || (a->fmt == MT_KV_F32 && a->head_dim <= 128)) &&
             rb % 128 == 0 && pl->ncb <= 255 &&
             a->n_kv_heads * mma_wph <= kMaxConsumerWarps && fit(128 * pl->ncb, 16, rows, pad, stages);
-  // q8_0 pools: tensor-core consumers on per-warp converted tiles (d <= 128)
-  if (!pl->mma && q8_mma && fit((int)rb, 16, rows, pad, stages)) {
+  // q8_0 pools: tensor-core consumers (d <= 128). For head_dim 128 the rows
+  // are staged by a tensor copy whose box is wider than the row when the
+  // row is whole 32- or 16-byte chunks, so that the staged pitch is 8 or 24
+  // banks mod 32 (rows 4 apart share a bank group, rows 1 to 3 apart do
+  // not): the consumer's per-token loads then hit distinct banks.
+  pl->q8_chunk = 0;
+  int q8_pitch = (int)rb;
+  if (!pl->mma && q8_mma && a->head_dim == 128) {
+    if (rb % 32 == 0) {
+      const int nch = (int)(rb / 32);
+      q8_pitch = 32 * (nch | 1);
+      pl->q8_chunk = 32;
+    } else if (rb % 16 == 0) {
+      int nch = (int)(rb / 16);
+      while (nch % 4 != 2) ++nch;
+      q8_pitch = 16 * nch;
+      pl->q8_chunk = 16;
+    }
+    if (pl->q8_chunk && q8_pitch / pl->q8_chunk > 256) {  // a box dimension holds at most 256
+      pl->q8_chunk = 0;
+      q8_pitch = (int)rb;
+    }
+  }
+  if (!pl->mma && q8_mma && fit(q8_pitch, 16, rows, pad, stages)) {
     pl->mma = true;
     wph = 1;
-    pl->pitch = (int)rb;
+    pl->pitch = q8_pitch;
     pl->n_sub = 1;
   } else if (pl->mma) {
     wph = mma_wph;
@@ -2141,6 +2170,9 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
     wph = kMaxConsumerWarps / a->n_kv_heads;
     if (wph > nsteps) wph = nsteps;
     if (wph < 1) wph = 1;
+    // the FP32-core consumers keep their softmax rows in the scratch
+    pl->scratch = std::max(pl->scratch, simt_scratch);
+    fixed = kHdrBytes + pl->scratch + 1024 + 16;
     if (!fit((int)rb, 8, rows, pad, stages))
       return fail(MT_ERR_UNSUPPORTED, "paged decode: KV rows too wide to double-buffer 8 of them");
     pl->pitch = (int)rb;
@@ -2152,16 +2184,32 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
   // SM, each with stages sized for half of the SM's shared memory, so every
   // scheduler runs two consumer warps. With at most 4 warps per CTA (one per
   // scheduler) two CTAs always fit the per-scheduler register file.
-  if (auto_ctas && pl->n_cw <= 3) {
+  // The direct q8_0 consumer (one warp per KV head, long dependent chains per
+  // stage) also runs two CTAs per SM: 16-row stages in half the shared
+  // memory, and the kernel is compiled for two resident CTAs.
+  // (At block size 32 one CTA with whole-block stages does better: each warp
+  // then has two independent 16-row halves per stage.)
+  pl->two_per_sm = false;
+  if (auto_ctas && (pl->n_cw <= 3 || (q8_direct && pl->mma && a->block_size == 16))) {
     const int min_rows = pl->mma ? 16 : 8;
     int rows2 = 0, pad2 = 0, stages2 = 0;
-    const int cap1 = smem_cap;
+    const int cap1 = smem_cap, fixed1 = fixed, scratch1 = pl->scratch;
     smem_cap = (cap1 + 1024) / 2 - 1024;
-    if (fit(pl->pitch, min_rows, rows2, pad2, stages2) && stages2 >= 3) {
+    if (q8_direct) {
+      // 16-row stages: scale arrays for one half
+      pl->scratch = kMaxConsumerWarps * kQ8dScaleFloatsPerHalf * 4;
+      fixed = kHdrBytes + pl->scratch + 1024 + 16;
+    }
+    if (fit(pl->pitch, min_rows, rows2, pad2, stages2) && stages2 >= 3 &&
+        (!q8_direct || rows2 == 16)) {
       rows = rows2;
       pad = pad2;
       stages = stages2;
       n_ctas *= 2;
+      pl->two_per_sm = q8_direct;
+    } else {
+      fixed = fixed1;
+      pl->scratch = scratch1;
     }
     smem_cap = cap1;
   }
@@ -2180,11 +2228,11 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
   return MT_OK;
 }
 
-template <int FMT, int D, int GP, bool MMA>
-mt_status launch_decode(const Params &prm, const Plan &pl, cudaStream_t s) {
+template <int FMT, int D, int GP, bool MMA, int MINB>
+mt_status launch_decode_k(const Params &prm, const Plan &pl, cudaStream_t s) {
   static int configured_dev = -1;
   static int configured_smem = 0;
-  auto kern = paged_decode_kernel<FMT, D, GP, MMA>;
+  auto kern = paged_decode_kernel<FMT, D, GP, MMA, MINB>;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev || configured_smem < pl.smem) {
@@ -2212,6 +2260,14 @@ mt_status launch_decode(const Params &prm, const Plan &pl, cudaStream_t s) {
   return st;
 }
 
+template <int FMT, int D, int GP, bool MMA>
+mt_status launch_decode(const Params &prm, const Plan &pl, cudaStream_t s) {
+  if constexpr (MMA && FMT == MT_KV_Q8_0 && D == 128) {
+    if (pl.two_per_sm) return launch_decode_k<FMT, D, GP, MMA, 2>(prm, pl, s);
+  }
+  return launch_decode_k<FMT, D, GP, MMA, 1>(prm, pl, s);
+}
+
 template <int FMT, int D, bool MMA>
 mt_status dispatch_gp(const Params &prm, const Plan &pl, cudaStream_t s) {
   switch (pl.GP) {
@@ -2234,8 +2290,13 @@ mt_status dispatch_d(const Params &prm, const Plan &pl, cudaStream_t s) {
 
 // 3-D tensor map of a pool for the tensor-core path: [cells][row chunks of
 // 128 bytes][64 f16], box = (64, ncb, rows), 128-byte swizzle, zero fill.
+// q8_0 pools (head_dim 128): [cells][row chunks][32-bit words], box =
+// (chunk words, pitch / chunk, rows), no swizzle, zero fill.
 mt_status encode_pool_map(CUtensorMap *map, const void *pool, long long n_cells, size_t rb,
                           const Plan &pl) {
+  if (pl.q8_chunk)
+    return encode_pool_map_words(map, pool, n_cells, rb, pl.q8_chunk, pl.pitch / pl.q8_chunk,
+                                 pl.rows);
   return encode_pool_map_3d(map, pool, n_cells, rb, pl.ncb, pl.rows);
 }
 
@@ -2269,7 +2330,7 @@ mt_status fill_params(Params &prm, const mt_paged_attn_args *a, const Plan &pl, 
   prm.blk_pad = pl.blk_pad;
   prm.rows = pl.rows;
   prm.pitch = pl.pitch;
-  prm.use_tmap = (pl.mma && (a->fmt == MT_KV_F16 || a->fmt == MT_KV_F32)) ? 1 : 0;
+  prm.use_tmap = (pl.mma && (a->fmt == MT_KV_F16 || a->fmt == MT_KV_F32 || pl.q8_chunk)) ? 1 : 0;
   prm.scratch_bytes = pl.scratch;
   prm.ncb = pl.ncb;
   prm.n_sub = pl.n_sub;

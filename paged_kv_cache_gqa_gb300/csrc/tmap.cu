@@ -50,4 +50,24 @@ mt_status encode_pool_map_3d(CUtensorMap *map, const void *pool, long long n_cel
   return MT_OK;
 }
 
+mt_status encode_pool_map_words(CUtensorMap *map, const void *pool, long long n_cells, size_t rb,
+                                int chunk_bytes, int box_chunks, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn;
+  mt_status st = encode_fn(&fn);
+  if (st != MT_OK) return st;
+  const cuuint64_t dims[3] = {(cuuint64_t)(chunk_bytes / 4), (cuuint64_t)(rb / chunk_bytes),
+                              (cuuint64_t)n_cells};
+  const cuuint64_t strides[2] = {(cuuint64_t)chunk_bytes, (cuuint64_t)rb};
+  const cuuint32_t box[3] = {(cuuint32_t)(chunk_bytes / 4), (cuuint32_t)box_chunks,
+                             (cuuint32_t)box_rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(pool), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MT_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string((int)r) + ")");
+  return MT_OK;
+}
+
 }  // namespace mtkv

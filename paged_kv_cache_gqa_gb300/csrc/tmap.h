@@ -15,4 +15,15 @@ namespace mtkv {
 mt_status encode_pool_map_3d(CUtensorMap *map, const void *pool, long long n_cells, size_t rb,
                              int box_chunks, int box_rows);
 
+// 3-D tensor map of a pool seen as [cell][chunk of the row][32-bit words]:
+// n_cells cells of rb bytes (a multiple of chunk_bytes, which is 16 or 32),
+// box = (chunk_bytes / 4, box_chunks, box_rows), no swizzle, zero fill
+// outside the tensor. A box wider than the row (box_chunks > rb /
+// chunk_bytes) stages each row at a pitch of box_chunks * chunk_bytes
+// bytes, the extra chunks zero-filled; the q8_0 decode uses it to place
+// staged rows on different shared-memory banks. The pool must be 16-byte
+// aligned.
+mt_status encode_pool_map_words(CUtensorMap *map, const void *pool, long long n_cells, size_t rb,
+                                int chunk_bytes, int box_chunks, int box_rows);
+
 }  // namespace mtkv
