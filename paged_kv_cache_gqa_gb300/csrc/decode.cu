@@ -97,6 +97,7 @@ struct Params {
   int rows;      // block rows per stage (block_size, or a divisor of it for wide rows)
   int pitch;     // shared-memory bytes between consecutive staged rows
   int use_tmap;  // 1: stage blocks with tensor copies (f16 / f32 swizzled, q8_0 padded)
+  int pair;      // 1: a stage holds up to two blocks of one sequence (block_size 16, q8_0)
   int scratch_bytes;  // shared-memory bytes between the header and the stage ring
   int ncb;       // 128-byte chunks per staged row (odd), tensor path
   int n_sub;     // partial records per (CTA, sequence) slot
@@ -1043,16 +1044,34 @@ __device__ __forceinline__ void consume_q8_direct(const Params &p, uint64_t *ful
     if (flags & F_DATA) {
       const uint32_t kst = smem_u32(ring + (size_t)slot * 2 * p.blk_pad);
       const uint32_t vst = kst + (uint32_t)p.blk_pad;
-      // ---- group scales of both pools, per half, in score-column order
+      // ---- group scales of both pools, per half, in score-column order; a V
+      // scale of a row outside the mask is stored as 0 (its bits may be stale)
 #pragma unroll
-      for (int h = 0; h < NH; ++h)
+      for (int h = 0; h < NH; ++h) {
+        const uint32_t mh = (mask >> (base + 16 * h)) & 0xffffu;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           const int i = lane + 32 * k;          // [grp][pos]
           const int grp = i >> 4, pos = i & 15;
-          const uint32_t off = (uint32_t)(16 * h + q8d_col_token(pos)) * pitch + seg + 34u * grp;
-          sK[h * NG * 16 + i] = lds_f16f(kst + off);
-          sV[h * NG * 16 + i] = lds_f16f(vst + off);
+          const int tok = q8d_col_token(pos);
+          const uint32_t off = (uint32_t)(16 * h + tok) * pitch + seg + 34u * grp;
+          const float dk = lds_f16f(kst + off);
+          const float dv = lds_f16f(vst + off);
+          sK[h * NG * 16 + i] = dk;
+          sV[h * NG * 16 + i] = ((mh >> tok) & 1u) ? dv : 0.f;
+        }
+      }
+      // ---- every K code word of the stage, loaded before any conversion
+      uint32_t w[NH][2][NG][2];
+#pragma unroll
+      for (int h = 0; h < NH; ++h)
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const uint32_t ka = kst + (uint32_t)(16 * h + 8 * t + krow) * pitch + seg + 2u + 8u * c;
+          lds_code8<2>(ka, w[h][t][0][0], w[h][t][0][1]);
+          lds_code8<4>(ka + 34, w[h][t][1][0], w[h][t][1][1]);
+          lds_code8<6>(ka + 68, w[h][t][2][0], w[h][t][2][1]);
+          lds_code8<0>(ka + 102, w[h][t][3][0], w[h][t][3][1]);
         }
       __syncwarp();
       // ---- scores: two 8-column tiles per half
@@ -1063,18 +1082,12 @@ __device__ __forceinline__ void consume_q8_direct(const Params &p, uint64_t *ful
         const uint32_t mh = (mask >> (base + 16 * h)) & 0xffffu;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          const uint32_t ka = kst + (uint32_t)(16 * h + 8 * t + krow) * pitch + seg + 2u + 8u * c;
-          uint32_t w[NG][2];
-          lds_code8<2>(ka, w[0][0], w[0][1]);
-          lds_code8<4>(ka + 34, w[1][0], w[1][1]);
-          lds_code8<6>(ka + 68, w[2][0], w[2][1]);
-          lds_code8<0>(ka + 102, w[3][0], w[3][1]);
           float s0 = 0.f, s1 = 0.f;
 #pragma unroll
           for (int grp = 0; grp < NG; ++grp) {
             uint32_t b[2][2];
-            codes_to_h2(w[grp][0], b[0][0], b[0][1]);
-            codes_to_h2(w[grp][1], b[1][0], b[1][1]);
+            codes_to_h2(w[h][t][grp][0], b[0][0], b[0][1]);
+            codes_to_h2(w[h][t][grp][1], b[1][0], b[1][1]);
             float acc[4];
             mma_f16_z(acc, qa[grp][0], b[0][0], b[0][1]);
             mma_f16(acc, qa[grp][1], b[1][0], b[1][1]);
@@ -1089,6 +1102,19 @@ __device__ __forceinline__ void consume_q8_direct(const Params &p, uint64_t *ful
           pr[h][t][1] = v1 ? s1 : -INFINITY;
           mloc = fmaxf(mloc, fmaxf(pr[h][t][0], pr[h][t][1]));
         }
+      }
+      // ---- the V code words of the first half, loaded before the softmax
+      // (the k-slots 2c, 2c+1, 2c+8, 2c+9 are tokens c, 4+c, 8+c, 12+c)
+      const uint32_t p4 = 4u * pitch;
+      uint32_t wv[NG][4];
+      const uint32_t va0 = vst + (uint32_t)c * pitch + seg + 2u + 4u * g;
+      {
+        const uint32_t vr[4] = {va0, va0 + p4, va0 + 2 * p4, va0 + 3 * p4};
+#pragma unroll
+        for (int grp = 0; grp < NG; ++grp)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            wv[grp][k] = (grp & 1) ? lds_code4<0>(vr[k] + 34u * grp) : lds_code4<2>(vr[k] + 34u * grp);
       }
       // ---- online softmax (base 2); a lane's tokens of a half are c, 4+c,
       // 8+c, 12+c, the group's four lanes cover all sixteen
@@ -1122,30 +1148,28 @@ __device__ __forceinline__ void consume_q8_direct(const Params &p, uint64_t *ful
       // ---- O^T += V^T . (P * d)^T, per half and group
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
-        const uint32_t mh = (mask >> (base + 16 * h)) & 0xffffu;
-        // the k-slots 2c, 2c+1, 2c+8, 2c+9 are tokens c, 4+c, 8+c, 12+c
-        const bool va0 = (mh >> c) & 1u, va1 = (mh >> (4 + c)) & 1u;
-        const bool vb0 = (mh >> (8 + c)) & 1u, vb1 = (mh >> (12 + c)) & 1u;
-        const uint32_t va = vst + (uint32_t)(16 * h + c) * pitch + seg + 2u + 4u * g;
-        const uint32_t p4 = 4u * pitch;
+        if (h > 0) {
+          const uint32_t va = va0 + (uint32_t)(16 * h) * pitch;
+          const uint32_t vr[4] = {va, va + p4, va + 2 * p4, va + 3 * p4};
+#pragma unroll
+          for (int grp = 0; grp < NG; ++grp)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              wv[grp][k] = (grp & 1) ? lds_code4<0>(vr[k] + 34u * grp) : lds_code4<2>(vr[k] + 34u * grp);
+        }
 #pragma unroll
         for (int grp = 0; grp < NG; ++grp) {
-          uint32_t wv[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t a = va + k * p4 + 34u * grp;
-            wv[k] = (grp & 1) ? lds_code4<0>(a) : lds_code4<2>(a);
-          }
           uint32_t o01[4], o23[4];
-          code_pairs_to_h2(wv[0], wv[1], o01);
-          code_pairs_to_h2(wv[2], wv[3], o23);
+          code_pairs_to_h2(wv[grp][0], wv[grp][1], o01);
+          code_pairs_to_h2(wv[grp][2], wv[grp][3], o23);
+          // V scales of rows outside the mask are 0 and their p is 0
           const float *sv = sV + h * NG * 16 + grp * 16;
           const float2 s01 = *reinterpret_cast<const float2 *>(sv + 2 * c);
           const float2 s23 = *reinterpret_cast<const float2 *>(sv + 8 + 2 * c);
-          const float pa0 = va0 ? pr[h][0][0] * s01.x : 0.f;
-          const float pa1 = va1 ? pr[h][0][1] * s01.y : 0.f;
-          const float pb0 = vb0 ? pr[h][1][0] * s23.x : 0.f;
-          const float pb1 = vb1 ? pr[h][1][1] * s23.y : 0.f;
+          const float pa0 = pr[h][0][0] * s01.x;
+          const float pa1 = pr[h][0][1] * s01.y;
+          const float pb0 = pr[h][1][0] * s23.x;
+          const float pb1 = pr[h][1][1] * s23.y;
           uint32_t bq0, bq1;
           if (HILO) {
             uint32_t h0, l0, h1, l1;
@@ -1366,8 +1390,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
     bool alive = true;
     // Publish one stage. Lane 0 waits for the slot and issues; the others
     // learn the outcome through the shuffle.
-    auto emit = [&](int flags, int s, int r0, int r1, int phys, int base,
-                    uint32_t mask) -> bool {
+    auto emit = [&](int flags, int s, int r0, int r1, int phys, int base, uint32_t mask,
+                    int phys2 = -1) -> bool {
       const int slot = (int)(it % (uint32_t)S);
       const uint32_t round = it / (uint32_t)S;
       int okv = 1;
@@ -1377,7 +1401,19 @@ __global__ void __launch_bounds__(kThreads, MINB)
           okv = 0;
         if (okv) {
           infos[slot] = StageInfo{s, r0, r1, flags | (base << 8), (int)mask};
-          if ((flags & F_DATA) && p.use_tmap) {
+          if ((flags & F_DATA) && p.pair) {
+            // block phys in rows [0, bs), block phys2 (if any) in [bs, 2 bs):
+            // one tensor copy per block and pool
+            uint8_t *dk = ring + (size_t)slot * 2 * p.blk_pad;
+            const uint32_t half = (uint32_t)(p.bs * p.pitch);
+            mbar_arrive_expect_tx(&full[slot], (phys2 >= 0 ? 4u : 2u) * half);
+            tma_block(dk, &p.tmap_k, phys * p.bs, &full[slot], pol);
+            tma_block(dk + p.blk_pad, &p.tmap_v, phys * p.bs, &full[slot], pol);
+            if (phys2 >= 0) {
+              tma_block(dk + half, &p.tmap_k, phys2 * p.bs, &full[slot], pol);
+              tma_block(dk + p.blk_pad + half, &p.tmap_v, phys2 * p.bs, &full[slot], pol);
+            }
+          } else if ((flags & F_DATA) && p.use_tmap) {
             // the whole stage (rows [base, base + rows)) in two tensor copies
             uint8_t *dk = ring + (size_t)slot * 2 * p.blk_pad;
             const int cell = phys * p.bs + base;
@@ -1433,6 +1469,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
           if (lane == 0)
             bulk_prefetch_l2(p.q + (size_t)s * p.Hq * D, (uint32_t)(p.Hq * D * sizeof(float)));
           bool first = true;
+          int pend = -1;           // paired stages: block waiting for its partner
+          uint32_t pend_mask = 0;
           const int lb0 = lo / p.bs;
           // decode with append: the logical block of position ctx-1 when this
           // segment loads it (its new row is written just before the copy)
@@ -1484,6 +1522,22 @@ __global__ void __launch_bounds__(kThreads, MINB)
                   cmask &= row_bits(c0, c0 + p.rows);
                   if (!cmask) continue;
                 }
+                if (p.pair) {
+                  // hold the first block of a pair; emit both with the second
+                  if (pend < 0) {
+                    pend = phys;
+                    pend_mask = cmask;
+                    continue;
+                  }
+                  if (!emit(F_DATA | (first ? F_NEW : 0), s, 0, 2 * p.bs, pend, 0,
+                            pend_mask | (cmask << 16), phys)) {
+                    alive = false;
+                    break;
+                  }
+                  pend = -1;
+                  first = false;
+                  continue;
+                }
                 if (!emit(F_DATA | (first ? F_NEW : 0), s, max(r0, c0), min(r1, c0 + p.rows),
                           phys, c0, cmask)) {
                   alive = false;
@@ -1493,6 +1547,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
               }
               if (!alive) break;
             }
+          }
+          if (alive && pend >= 0) {
+            // the segment's last block without a partner
+            if (!emit(F_DATA | (first ? F_NEW : 0), s, 0, p.bs, pend, 0, pend_mask))
+              alive = false;
+            pend = -1;
+            first = false;
           }
           if (alive && !emit(F_END | (first ? F_NEW : 0), s, 0, 0, -1, 0, 0u)) alive = false;
           x = seg_hi;
@@ -2045,6 +2106,7 @@ struct Plan {
   int pitch, n_sub, ncb, scratch;
   int q8_chunk;  // q8_0 staged through the word tensor map: chunk bytes (0: bulk copies)
   bool two_per_sm;  // kernel compiled for two resident CTAs per SM
+  bool pair;        // q8_0 block size 16: two blocks per 32-row stage
   size_t ws_status, ws_seq, ws_ml, ws_o, ws_total;
 };
 
@@ -2154,7 +2216,26 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
       q8_pitch = (int)rb;
     }
   }
-  if (!pl->mma && q8_mma && fit(q8_pitch, 16, rows, pad, stages)) {
+  // At block size 16 the direct consumer takes two blocks of a sequence per
+  // 32-row stage (one tensor copy each), so that each warp works on two
+  // independent 16-row halves per stage as at block size 32.
+  pl->pair = false;
+  if (!pl->mma && q8_mma && pl->q8_chunk && a->block_size == 16) {
+    const int pad2 = (32 * q8_pitch + 127) & ~127;
+    const int st2 = std::min((smem_cap - fixed) / (2 * pad2), kMaxStages);
+    if (st2 >= 2) {
+      pl->pair = true;
+      pl->mma = true;
+      wph = 1;
+      pl->pitch = q8_pitch;
+      pl->n_sub = 1;
+      rows = 32;
+      pad = pad2;
+      stages = st2;
+    }
+  }
+  if (pl->pair) {
+  } else if (!pl->mma && q8_mma && fit(q8_pitch, 16, rows, pad, stages)) {
     pl->mma = true;
     wph = 1;
     pl->pitch = q8_pitch;
@@ -2184,29 +2265,37 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
   // SM, each with stages sized for half of the SM's shared memory, so every
   // scheduler runs two consumer warps. With at most 4 warps per CTA (one per
   // scheduler) two CTAs always fit the per-scheduler register file.
-  // The direct q8_0 consumer (one warp per KV head, long dependent chains per
-  // stage) also runs two CTAs per SM: 16-row stages in half the shared
-  // memory, and the kernel is compiled for two resident CTAs.
-  // (At block size 32 one CTA with whole-block stages does better: each warp
-  // then has two independent 16-row halves per stage.)
+  // The direct q8_0 consumer at block size 16 without paired stages (rows
+  // that are not whole 16-byte chunks) also runs two CTAs per SM: 16-row
+  // stages, and a kernel compiled for two resident CTAs when a CTA has more
+  // than 3 consumer warps. Paired stages keep their 32 rows and their
+  // two-half scale arrays.
   pl->two_per_sm = false;
-  if (auto_ctas && (pl->n_cw <= 3 || (q8_direct && pl->mma && a->block_size == 16))) {
+  if (auto_ctas && (pl->n_cw <= 3 || (q8_direct && pl->mma && !pl->pair && a->block_size == 16))) {
     const int min_rows = pl->mma ? 16 : 8;
     int rows2 = 0, pad2 = 0, stages2 = 0;
     const int cap1 = smem_cap, fixed1 = fixed, scratch1 = pl->scratch;
     smem_cap = (cap1 + 1024) / 2 - 1024;
-    if (q8_direct) {
+    bool fits;
+    if (pl->pair) {
+      rows2 = 32;
+      pad2 = (32 * pl->pitch + 127) & ~127;
+      stages2 = std::min((smem_cap - fixed) / (2 * pad2), kMaxStages);
+      fits = true;
+    } else if (q8_direct && pl->mma) {
       // 16-row stages: scale arrays for one half
       pl->scratch = kMaxConsumerWarps * kQ8dScaleFloatsPerHalf * 4;
       fixed = kHdrBytes + pl->scratch + 1024 + 16;
+      fits = fit(pl->pitch, min_rows, rows2, pad2, stages2) && rows2 == 16;
+    } else {
+      fits = fit(pl->pitch, min_rows, rows2, pad2, stages2);
     }
-    if (fit(pl->pitch, min_rows, rows2, pad2, stages2) && stages2 >= 3 &&
-        (!q8_direct || rows2 == 16)) {
+    if (fits && stages2 >= 3) {
       rows = rows2;
       pad = pad2;
       stages = stages2;
       n_ctas *= 2;
-      pl->two_per_sm = q8_direct;
+      pl->two_per_sm = q8_direct && pl->mma && pl->n_cw > 3;
     } else {
       fixed = fixed1;
       pl->scratch = scratch1;
@@ -2296,7 +2385,7 @@ mt_status encode_pool_map(CUtensorMap *map, const void *pool, long long n_cells,
                           const Plan &pl) {
   if (pl.q8_chunk)
     return encode_pool_map_words(map, pool, n_cells, rb, pl.q8_chunk, pl.pitch / pl.q8_chunk,
-                                 pl.rows);
+                                 pl.pair ? pl.rows / 2 : pl.rows);
   return encode_pool_map_3d(map, pool, n_cells, rb, pl.ncb, pl.rows);
 }
 
@@ -2331,6 +2420,7 @@ mt_status fill_params(Params &prm, const mt_paged_attn_args *a, const Plan &pl, 
   prm.rows = pl.rows;
   prm.pitch = pl.pitch;
   prm.use_tmap = (pl.mma && (a->fmt == MT_KV_F16 || a->fmt == MT_KV_F32 || pl.q8_chunk)) ? 1 : 0;
+  prm.pair = pl.pair ? 1 : 0;
   prm.scratch_bytes = pl.scratch;
   prm.ncb = pl.ncb;
   prm.n_sub = pl.n_sub;
