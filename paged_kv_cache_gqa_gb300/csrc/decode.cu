@@ -1082,7 +1082,7 @@ __device__ __forceinline__ void consume_q8_direct(const Params &p, uint64_t *ful
         const uint32_t mh = (mask >> (base + 16 * h)) & 0xffffu;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          float s0 = 0.f, s1 = 0.f;
+          float2 sv2 = make_float2(0.f, 0.f);
 #pragma unroll
           for (int grp = 0; grp < NG; ++grp) {
             uint32_t b[2][2];
@@ -1093,13 +1093,13 @@ __device__ __forceinline__ void consume_q8_direct(const Params &p, uint64_t *ful
             mma_f16(acc, qa[grp][1], b[1][0], b[1][1]);
             const float2 sc = *reinterpret_cast<const float2 *>(sK + h * NG * 16 + grp * 16 +
                                                                 8 * t + 2 * c);
-            s0 = fmaf(sc.x, acc[0] + acc[2], s0);
-            s1 = fmaf(sc.y, acc[1] + acc[3], s1);
+            // (hi + lo rows) times the tokens' group scales, two tokens at once
+            sv2 = f2_fma(sc, f2_add(make_float2(acc[0], acc[1]), make_float2(acc[2], acc[3])), sv2);
           }
           const bool v0 = row_ok && ((mh >> (8 * t + c)) & 1u);
           const bool v1 = row_ok && ((mh >> (8 * t + 4 + c)) & 1u);
-          pr[h][t][0] = v0 ? s0 : -INFINITY;
-          pr[h][t][1] = v1 ? s1 : -INFINITY;
+          pr[h][t][0] = v0 ? sv2.x : -INFINITY;
+          pr[h][t][1] = v1 ? sv2.y : -INFINITY;
           mloc = fmaxf(mloc, fmaxf(pr[h][t][0], pr[h][t][1]));
         }
       }
@@ -1166,20 +1166,18 @@ __device__ __forceinline__ void consume_q8_direct(const Params &p, uint64_t *ful
           const float *sv = sV + h * NG * 16 + grp * 16;
           const float2 s01 = *reinterpret_cast<const float2 *>(sv + 2 * c);
           const float2 s23 = *reinterpret_cast<const float2 *>(sv + 8 + 2 * c);
-          const float pa0 = pr[h][0][0] * s01.x;
-          const float pa1 = pr[h][0][1] * s01.y;
-          const float pb0 = pr[h][1][0] * s23.x;
-          const float pb1 = pr[h][1][1] * s23.y;
+          const float2 pa = f2_mul(make_float2(pr[h][0][0], pr[h][0][1]), s01);
+          const float2 pb = f2_mul(make_float2(pr[h][1][0], pr[h][1][1]), s23);
           uint32_t bq0, bq1;
           if (HILO) {
             uint32_t h0, l0, h1, l1;
-            split_h2(pa0, pa1, h0, l0);
-            split_h2(pb0, pb1, h1, l1);
+            split_h2x(pa, h0, l0);
+            split_h2x(pb, h1, l1);
             bq0 = lo_col ? l0 : h0;
             bq1 = lo_col ? l1 : h1;
           } else {
-            bq0 = h2_bits(__floats2half2_rn(pa0, pa1));
-            bq1 = h2_bits(__floats2half2_rn(pb0, pb1));
+            bq0 = h2_bits(__floats2half2_rn(pa.x, pa.y));
+            bq1 = h2_bits(__floats2half2_rn(pb.x, pb.y));
           }
           if (!row_ok) bq0 = bq1 = 0u;
           const uint32_t am0[4] = {o01[0], o01[1], o23[0], o23[1]};  // dims 4g, 4g+1

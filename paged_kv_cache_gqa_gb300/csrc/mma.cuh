@@ -42,4 +42,47 @@ __device__ __forceinline__ void split_h2(float x0, float x1, uint32_t &hi, uint3
   lo = h2_bits(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
 }
 
+// Packed f32x2 arithmetic (one instruction for two lanes, each lane rounded
+// exactly as the scalar instruction).
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
+  float2 r;
+  asm("{ .reg .b64 p, q, s; mov.b64 p, {%2, %3}; mov.b64 q, {%4, %5}; add.rn.f32x2 s, p, q; "
+      "mov.b64 {%0, %1}, s; }"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 f2_sub(float2 a, float2 b) {
+  float2 r;
+  asm("{ .reg .b64 p, q, s; mov.b64 p, {%2, %3}; mov.b64 q, {%4, %5}; sub.rn.f32x2 s, p, q; "
+      "mov.b64 {%0, %1}, s; }"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+  float2 r;
+  asm("{ .reg .b64 p, q, s; mov.b64 p, {%2, %3}; mov.b64 q, {%4, %5}; mul.rn.f32x2 s, p, q; "
+      "mov.b64 {%0, %1}, s; }"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{ .reg .b64 p, q, t, s; mov.b64 p, {%2, %3}; mov.b64 q, {%4, %5}; mov.b64 t, {%6, %7}; "
+      "fma.rn.f32x2 s, p, q, t; mov.b64 {%0, %1}, s; }"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+
+// split_h2 of a float pair with the residual taken by one packed subtraction
+__device__ __forceinline__ void split_h2x(float2 x, uint32_t &hi, uint32_t &lo) {
+  const __half2 h = __floats2half2_rn(x.x, x.y);
+  hi = h2_bits(h);
+  const float2 r = f2_sub(x, __half22float2(h));
+  lo = h2_bits(__floats2half2_rn(r.x, r.y));
+}
+
 }  // namespace mtkv
