@@ -72,6 +72,18 @@ struct StageInfo {
   int mask;   // valid rows of the block as bits (bit t: block row t), within [r0, r1)
 };
 
+// Position in the stage ring: slot and the parity of its round, advanced
+// without dividing by the (runtime) stage count.
+struct RingPos {
+  uint32_t slot = 0, phase = 0;
+  __device__ __forceinline__ void next(int S) {
+    if (++slot == (uint32_t)S) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 struct Params {
   CUtensorMap tmap_k;  // tensor-copy path (f16, f32 up to d 128): 3-D maps of the pools, see tma_block()
   CUtensorMap tmap_v;
@@ -317,11 +329,11 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
   float oacc[M::MTW][4];
   float m_run = -INFINITY, l_run = 0.f;
 
-  for (uint32_t it = 0;; ++it) {
-    const int slot = (int)(it % (uint32_t)S);
+  for (RingPos rp;; rp.next(S)) {
+    const int slot = (int)rp.slot;
     int okv = 1;
     if (lane == 0)
-      okv = mbar_wait_bounded(&full[slot], (it / (uint32_t)S) & 1u, abort_flag, p.wait_ns) ? 1 : 0;
+      okv = mbar_wait_bounded(&full[slot], rp.phase, abort_flag, p.wait_ns) ? 1 : 0;
     okv = __shfl_sync(kFull, okv, 0);
     if (!okv) {
       if (lane == 0) {
@@ -651,11 +663,11 @@ __device__ __forceinline__ void consume_mma_q8(const Params &p, uint64_t *full, 
   float oacc[M::MTW][4];
   float m_run = -INFINITY, l_run = 0.f;
 
-  for (uint32_t it = 0;; ++it) {
-    const int slot = (int)(it % (uint32_t)S);
+  for (RingPos rp;; rp.next(S)) {
+    const int slot = (int)rp.slot;
     int okv = 1;
     if (lane == 0)
-      okv = mbar_wait_bounded(&full[slot], (it / (uint32_t)S) & 1u, abort_flag, p.wait_ns) ? 1 : 0;
+      okv = mbar_wait_bounded(&full[slot], rp.phase, abort_flag, p.wait_ns) ? 1 : 0;
     okv = __shfl_sync(kFull, okv, 0);
     if (!okv) {
       if (lane == 0) {
@@ -993,16 +1005,17 @@ __device__ __forceinline__ void consume_q8_direct(const Params &p, uint64_t *ful
   float *sV = sK + NH * NG * 16;
   // this lane's K row within a 16-row half (tile t adds 8): score column g
   const int krow = (g >> 1) + 4 * (g & 1);
+  const uint32_t ring_s = smem_u32(ring);
 
   uint32_t qa[NG][2][4];
   float oacc[2 * NG][4];
   float m_run = -INFINITY, l_run = 0.f;
 
-  for (uint32_t it = 0;; ++it) {
-    const int slot = (int)(it % (uint32_t)S);
+  for (RingPos rp;; rp.next(S)) {
+    const int slot = (int)rp.slot;
     int okv = 1;
     if (lane == 0)
-      okv = mbar_wait_bounded(&full[slot], (it / (uint32_t)S) & 1u, abort_flag, p.wait_ns) ? 1 : 0;
+      okv = mbar_wait_bounded(&full[slot], rp.phase, abort_flag, p.wait_ns) ? 1 : 0;
     okv = __shfl_sync(kFull, okv, 0);
     if (!okv) {
       if (lane == 0) {
@@ -1042,7 +1055,7 @@ __device__ __forceinline__ void consume_q8_direct(const Params &p, uint64_t *ful
     }
 
     if (flags & F_DATA) {
-      const uint32_t kst = smem_u32(ring + (size_t)slot * 2 * p.blk_pad);
+      const uint32_t kst = ring_s + (uint32_t)slot * 2u * (uint32_t)p.blk_pad;
       const uint32_t vst = kst + (uint32_t)p.blk_pad;
       // ---- group scales of both pools, per half, in score-column order; a V
       // scale of a row outside the mask is stored as 0 (its bits may be stale)
@@ -1385,16 +1398,17 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const long long b1 = min((long long)total, b0 + per);
 
     uint32_t it = 0;
+    RingPos prp;  // slot and round parity of stage `it`
     bool alive = true;
     // Publish one stage. Lane 0 waits for the slot and issues; the others
     // learn the outcome through the shuffle.
     auto emit = [&](int flags, int s, int r0, int r1, int phys, int base, uint32_t mask,
                     int phys2 = -1) -> bool {
-      const int slot = (int)(it % (uint32_t)S);
-      const uint32_t round = it / (uint32_t)S;
+      const int slot = (int)prp.slot;
       int okv = 1;
       if (lane == 0) {
-        if (it >= (uint32_t)S && !mbar_wait_bounded(&empty[slot], (round - 1) & 1u, abort_flag,
+        // the slot's previous fill (round - 1) must have been released
+        if (it >= (uint32_t)S && !mbar_wait_bounded(&empty[slot], prp.phase ^ 1u, abort_flag,
                                                     p.wait_ns))
           okv = 0;
         if (okv) {
@@ -1435,7 +1449,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
         }
       }
       okv = __shfl_sync(kFull, okv, 0);
-      if (okv) ++it;
+      if (okv) {
+        ++it;
+        prp.next(S);
+      }
       return okv != 0;
     };
 
@@ -1635,11 +1652,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
   };
 
-  for (uint32_t it = 0;; ++it) {
-    const int slot = (int)(it % (uint32_t)S);
+  for (RingPos rp;; rp.next(S)) {
+    const int slot = (int)rp.slot;
     int okv = 1;
     if (lane == 0)
-      okv = mbar_wait_bounded(&full[slot], (it / (uint32_t)S) & 1u, abort_flag, p.wait_ns) ? 1 : 0;
+      okv = mbar_wait_bounded(&full[slot], rp.phase, abort_flag, p.wait_ns) ? 1 : 0;
     okv = __shfl_sync(kFull, okv, 0);
     if (!okv) {
       if (lane == 0) {
