@@ -152,11 +152,13 @@ mt_status mt_paged_attn_decode(const mt_paged_attn_args *args, void *workspace,
                                size_t workspace_bytes, mt_stream stream);
 
 /* Paged decode attention with the new token's K/V store fused in.
- * "KV Cache Design — cells, format, sessions", section 1 (the store writes
- * the cell the allocator resolved; the paged model resolves position p of
- * sequence s to cell block_table[s][p/bs]*bs + p%bs) and section 2 (the
- * fused decode family stores the new row into its cell in the same pass
- * that reads the cache). Equivalent to mt_kv_store of row s of k_new/v_new
+ * What is stored and where follows "KV Cache Design — cells, format,
+ * sessions", section 1 (the store writes the cell the allocator resolved;
+ * the paged model resolves position p of sequence s to cell
+ * block_table[s][p/bs]*bs + p%bs) and section 3 (the one store quantiser).
+ * Doing the store inside the decode launch is this library's own design:
+ * the page's fused family (projection, RoPE and store in one op) has no
+ * attention in it. Equivalent to mt_kv_store of row s of k_new/v_new
  * into the cell of position context_lens[s]-1 of every sequence with a
  * positive context length, followed by mt_paged_attn_decode(args): the
  * attention sees the new row when its position is inside the window.
@@ -295,7 +297,10 @@ mt_status mt_paged_attn_decode_cascade_append(const mt_paged_attn_args *args,
  * in it; nothing in it needs to start at zero, but calls whose kernels
  * overlap on the GPU race on it, so order them on one stream. The first
  * call on each device looks up the array's device address and caches it:
- * make that first call before any stream capture begins. */
+ * make that first call before any stream capture begins. The cached
+ * address belongs to the device's current context: after cudaDeviceReset
+ * (or anything else that destroys that context) it is stale, and this
+ * entry point must not be called again in the process. */
 mt_status mt_paged_attn_decode_static(const mt_paged_attn_args *args, uint32_t *status,
                                       mt_stream stream);
 
@@ -326,9 +331,15 @@ mt_status mt_check_moves(const mt_move *moves, int n_moves, int64_t n_cells, int
  * copy): consecutive moves share a launch (at most 1024, one CTA each) while
  * none writes rows another of them reads or writes; each move copies in
  * chunks of min(|dst-src|, len) rows in slide order with a barrier between
- * chunks. */
+ * chunks (runs that fit in shared memory move in one staged round).
+ *   status     device status word, or NULL. A staged move whose bounded wait
+ *              for its load runs out leaves its rows unmoved and sets
+ *              MT_STATUS_BIT_TIMEOUT here (mt_check_device_status then
+ *              returns MT_ERR_TIMEOUT); with NULL such a failure cannot be
+ *              reported, so callers that need the bit-exact guarantee pass
+ *              a word and check it. */
 mt_status mt_copy_cells(void *const *pools, int n_pools, size_t row_bytes, int64_t n_cells,
-                        const mt_move *moves, int n_moves, mt_stream stream);
+                        const mt_move *moves, int n_moves, uint32_t *status, mt_stream stream);
 
 /* Cold-tier int4 quantise — "Tiered KV cache — architecture", section
  * "The three-tier model": per block one float32 scale and ceil(n_elts/2)

@@ -108,7 +108,10 @@ __global__ void __launch_bounds__(32) copy_cells_staged_kernel(const __grid_cons
   mbar_arrive_expect_tx(&bar, bytes);
   bulk_g2s(buf, base + mv.src * b.row_bytes, bytes, &bar, policy_evict_first());
   if (!mbar_wait_bounded(&bar, 0, &abort_flag, 2000000000ull)) {
+    // nothing is written: report, and let the load land in shared memory
+    // (bounded again) before the CTA may retire
     report(status, MT_STATUS_BIT_TIMEOUT);
+    mbar_wait_bounded(&bar, 0, &abort_flag, 2000000000ull);
     return;
   }
   asm volatile(
@@ -127,7 +130,7 @@ using namespace mtkv;
 
 extern "C" mt_status mt_copy_cells(void *const *pools, int n_pools, size_t row_bytes,
                                    int64_t n_cells, const mt_move *moves, int n_moves,
-                                   mt_stream stream) {
+                                   uint32_t *status, mt_stream stream) {
   if (n_moves < 0 || n_pools < 0 || n_cells < 0)
     return fail(MT_ERR_INVALID_ARG, "mt_copy_cells: negative size");
   if (n_moves == 0 || n_pools == 0) return ok();
@@ -161,12 +164,9 @@ extern "C" mt_status mt_copy_cells(void *const *pools, int n_pools, size_t row_b
     if ((long long)m.len * (long long)row_bytes > kStagedMax) staged = false;
   long long batch_max_bytes = 0;
   if (staged) {
-    static bool attr_set = false;
-    if (!attr_set) {
-      cudaFuncSetAttribute(copy_cells_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kStagedMax);
-      attr_set = true;
-    }
+    st = kernel_smem(reinterpret_cast<const void *>(copy_cells_staged_kernel), kStagedMax,
+                     "cudaFuncSetAttribute(copy_cells staged smem)");
+    if (st != MT_OK) return st;
   }
 
   // Moves in one launch run concurrently, so none may write rows another one
@@ -207,7 +207,7 @@ extern "C" mt_status mt_copy_cells(void *const *pools, int n_pools, size_t row_b
     if (batch.n_moves == 0) return MT_OK;
     if (staged) {
       const dim3 grid((unsigned)batch.n_moves, (unsigned)batch.n_pools);
-      copy_cells_staged_kernel<<<grid, 32, (size_t)batch_max_bytes, s>>>(batch, nullptr);
+      copy_cells_staged_kernel<<<grid, 32, (size_t)batch_max_bytes, s>>>(batch, status);
       batch.n_moves = 0;
       reads.clear();
       writes.clear();

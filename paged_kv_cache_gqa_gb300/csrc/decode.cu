@@ -2334,24 +2334,11 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
 
 template <int FMT, int D, int GP, bool MMA, int MINB>
 mt_status launch_decode_k(const Params &prm, const Plan &pl, cudaStream_t s) {
-  static int configured_dev = -1;
-  static int configured_smem = 0;
   auto kern = paged_decode_kernel<FMT, D, GP, MMA, MINB>;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_dev != dev || configured_smem < pl.smem) {
-    mt_status st = cuda_check(
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem),
-        "cudaFuncSetAttribute(decode smem)");
-    if (st != MT_OK) return st;
-    st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         cudaSharedmemCarveoutMaxShared),
-                    "cudaFuncSetAttribute(decode carveout)");
-    if (st != MT_OK) return st;
-    configured_dev = dev;
-    configured_smem = pl.smem;
-  }
-  mt_status st = cuda_check(
+  mt_status st = kernel_smem(reinterpret_cast<const void *>(kern), pl.smem,
+                             "cudaFuncSetAttribute(decode smem)", true);
+  if (st != MT_OK) return st;
+  st = cuda_check(
       launch_pdl(kern, dim3(pl.n_ctas), dim3(32 * (pl.n_cw + 1)), pl.smem, s, prm),
       "paged decode launch");
   if (st != MT_OK) return st;
@@ -2736,7 +2723,11 @@ extern "C" mt_status mt_paged_attn_decode_append(const mt_paged_attn_args *a, co
 //    one stream, or use mt_paged_attn_decode with separate workspaces.
 //  * The first call on each device looks the array's device address up
 //    (cudaGetSymbolAddress, with that device current) and caches it; make
-//    that first call before any stream capture begins.
+//    that first call before any stream capture begins. The address is the
+//    array's in the device's current context: after cudaDeviceReset (or
+//    anything else that destroys and re-creates that context) the cached
+//    value is stale and this entry point must not be called again in the
+//    process.
 //  * The device status word is the caller's `status` (may be NULL), not part
 //    of the array.
 namespace mtkv {

@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -28,6 +29,29 @@ mt_status ok() {
 mt_status cuda_check(cudaError_t e, const char *what) {
   if (e == cudaSuccess) return MT_OK;
   return fail(MT_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+mt_status kernel_smem(const void *kern, int bytes, const char *what, bool max_carveout) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void *>, int> done;  // (device, kernel) -> bytes set
+  int dev = 0;
+  mt_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != MT_OK) return st;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(dev, kern);
+  const auto it = done.find(key);
+  if (it != done.end() && it->second >= bytes) return MT_OK;
+  st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
+                  what);
+  if (st != MT_OK) return st;
+  if (max_carveout) {
+    st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared),
+                    what);
+    if (st != MT_OK) return st;
+  }
+  done[key] = bytes;
+  return MT_OK;
 }
 
 mt_status device_info(DeviceInfo *out) {

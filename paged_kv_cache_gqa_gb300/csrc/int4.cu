@@ -315,21 +315,16 @@ extern "C" mt_status mt_kv_quant_int4(mt_kv_format fmt, const void *pool, int bl
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const auto *pp = static_cast<const uint8_t *>(pool);
   if (blk_bytes <= kQuantSmemMax && blk_bytes % 16 == 0) {
-    static bool attr_set[2] = {false, false};
     if (fmt == MT_KV_F16) {
-      if (!attr_set[0]) {
-        cudaFuncSetAttribute(int4_quant_smem_kernel<MT_KV_F16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemMax);
-        attr_set[0] = true;
-      }
+      mt_status st = kernel_smem(reinterpret_cast<const void *>(int4_quant_smem_kernel<MT_KV_F16>),
+                                 kQuantSmemMax, "cudaFuncSetAttribute(int4 quant smem)");
+      if (st != MT_OK) return st;
       int4_quant_smem_kernel<MT_KV_F16><<<n_blocks, 256, (size_t)blk_bytes, s>>>(
           pp, blk_bytes, n_elts, n_phys_blocks, blocks, scales, nibbles, status);
     } else {
-      if (!attr_set[1]) {
-        cudaFuncSetAttribute(int4_quant_smem_kernel<MT_KV_F32>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemMax);
-        attr_set[1] = true;
-      }
+      mt_status st = kernel_smem(reinterpret_cast<const void *>(int4_quant_smem_kernel<MT_KV_F32>),
+                                 kQuantSmemMax, "cudaFuncSetAttribute(int4 quant smem)");
+      if (st != MT_OK) return st;
       int4_quant_smem_kernel<MT_KV_F32><<<n_blocks, 256, (size_t)blk_bytes, s>>>(
           pp, blk_bytes, n_elts, n_phys_blocks, blocks, scales, nibbles, status);
     }

@@ -25,6 +25,12 @@ struct DeviceInfo {
 };
 mt_status device_info(DeviceInfo *out);
 
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device (a per-device setting): cached per (device, kernel) behind a
+// mutex, the return code checked. With max_carveout the kernel also prefers
+// the largest shared-memory carveout.
+mt_status kernel_smem(const void *kern, int bytes, const char *what, bool max_carveout = false);
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace mtkv

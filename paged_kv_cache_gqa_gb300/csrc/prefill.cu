@@ -307,18 +307,11 @@ __global__ void __launch_bounds__(mq::kThreads, 2)
 
 template <int FMT, int D, int GP>
 mt_status launch_t(const PrefillParams &p, int n_ctas, cudaStream_t s) {
-  static int configured_dev = -1;
   auto kern = prefill_kernel<FMT, D, GP>;
   constexpr int smem = mq::Cfg<FMT, D>::SMEM;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_dev != dev) {
-    mt_status st =
-        cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
-                   "cudaFuncSetAttribute(prefill smem)");
-    if (st != MT_OK) return st;
-    configured_dev = dev;
-  }
+  mt_status st = kernel_smem(reinterpret_cast<const void *>(kern), smem,
+                             "cudaFuncSetAttribute(prefill smem)");
+  if (st != MT_OK) return st;
   return cuda_check(launch_pdl(kern, dim3(n_ctas), dim3(mq::kThreads), smem, s, p),
                     "prefill kernel launch");
 }

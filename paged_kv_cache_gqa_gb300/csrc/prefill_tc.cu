@@ -907,18 +907,11 @@ __global__ void __launch_bounds__(128) prefill_tc_combine_kernel(const __grid_co
 
 template <int D, int GP, bool SPLIT>
 mt_status launch_t(const PrefillParams &p, const TcMaps &m, int n_ctas, cudaStream_t s) {
-  static int configured_dev = -1;
   auto kern = prefill_tc_kernel<D, GP, SPLIT>;
   constexpr int smem = TcCfg<D>::SMEM;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_dev != dev) {
-    mt_status st =
-        cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
-                   "cudaFuncSetAttribute(prefill tc smem)");
-    if (st != MT_OK) return st;
-    configured_dev = dev;
-  }
+  mt_status st = kernel_smem(reinterpret_cast<const void *>(kern), smem,
+                             "cudaFuncSetAttribute(prefill tc smem)");
+  if (st != MT_OK) return st;
   return cuda_check(launch_pdl(kern, dim3(n_ctas), dim3(kTcThreads), smem, s, p, m),
                     "prefill tc kernel launch");
 }

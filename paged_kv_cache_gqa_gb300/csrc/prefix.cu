@@ -294,18 +294,11 @@ namespace {
 
 template <int FMT, int D, int GP>
 mt_status launch_t(const PrefixParams &p, int n_ctas, cudaStream_t s) {
-  static int configured_dev = -1;
   auto kern = prefix_kernel<FMT, D, GP>;
   constexpr int smem = mq::Cfg<FMT, D>::SMEM;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_dev != dev) {
-    mt_status st =
-        cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
-                   "cudaFuncSetAttribute(prefix smem)");
-    if (st != MT_OK) return st;
-    configured_dev = dev;
-  }
+  mt_status st = kernel_smem(reinterpret_cast<const void *>(kern), smem,
+                             "cudaFuncSetAttribute(prefix smem)");
+  if (st != MT_OK) return st;
   return cuda_check(launch_pdl(kern, dim3(n_ctas), dim3(mq::kThreads), smem, s, p),
                     "prefix kernel launch");
 }

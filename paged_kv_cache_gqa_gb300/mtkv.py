@@ -103,7 +103,8 @@ def lib() -> ctypes.CDLL:
                                                     SZ, P]),
         "mt_order_moves": (I, [ctypes.POINTER(mt_move), I, ctypes.POINTER(I)]),
         "mt_check_moves": (I, [ctypes.POINTER(mt_move), I, I64, ctypes.POINTER(I)]),
-        "mt_copy_cells": (I, [ctypes.POINTER(P), I, SZ, I64, ctypes.POINTER(mt_move), I, P]),
+        "mt_copy_cells": (I, [ctypes.POINTER(P), I, SZ, I64, ctypes.POINTER(mt_move), I, U32P,
+                              P]),
         "mt_kv_quant_int4": (I, [I, P, I, I, I, I64, P, I, P, P, U32P, P]),
         "mt_kv_dequant_int4": (I, [I, P, I, I, I, I64, P, I, P, P, U32P, P]),
         "mt_kv_relayout": (I, [P, P, I, I64, I64, SZ, P]),
@@ -328,11 +329,12 @@ def mt_check_moves(moves, n_cells: int):
     return st, bad.value
 
 
-def mt_copy_cells(pools, row_bytes: int, n_cells: int, moves, stream=None) -> None:
+def mt_copy_cells(pools, row_bytes: int, n_cells: int, moves, status=None,
+                  stream=None) -> None:
     ptrs = (ctypes.c_void_p * max(1, len(pools)))(*[_ptr(p) for p in pools])
     arr = _moves_array(moves)
     _check(lib().mt_copy_cells(ptrs, len(pools), int(row_bytes), int(n_cells), arr, len(moves),
-                               _stream(stream)), "mt_copy_cells")
+                               _ptr(status), _stream(stream)), "mt_copy_cells")
 
 
 def mt_kv_quant_int4(fmt, pool, block_size, n_kv_heads, head_dim, n_phys_blocks, blocks,

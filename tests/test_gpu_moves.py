@@ -27,8 +27,11 @@ def test_compaction_moves_bit_exact(mt, row_bytes):
     rng = np.random.default_rng(41)
     pools = [rng.integers(0, 256, (n_cells, row_bytes), dtype=np.uint8) for _ in range(5)]
     devs = [to_dev(p) for p in pools]
-    mt.mt_copy_cells(devs, row_bytes, n_cells, ordered)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mt.mt_copy_cells(devs, row_bytes, n_cells, ordered, status=status)
     om.copy_cells(pools, ordered)
+    # a normal call (staged runs for 16-byte rows) leaves the status word clear
+    assert mt.mt_check_device_status(status) == mt.MT_OK
     for p, d in zip(pools, devs):
         assert np.array_equal(d.cpu().numpy(), p)
 

@@ -6,16 +6,17 @@ must stay out of the CUDA allocator) use this entry point: it keeps its
 split-K scratch in an array built into the library instead of a caller's
 workspace. These checks call it through the C ABI twice in a row, on two
 different workloads, and compare each result with the workspace entry point
-on the same inputs, within the parity tolerances; they also check that a call
-too large for the built-in array is refused. This file is named to be
-collected last.
+on the same inputs, within the parity tolerances; compare a call made right
+after a larger one (whose partial results are still in the shared array)
+directly with the CPU oracle; and check that a call too large for the
+built-in array is refused. This file is named to be collected last.
 """
 import numpy as np
 import pytest
 import torch
 
 from paged_kv_cache_gqa_gb300 import workloads
-from tests.gpu_util import TOL, oracle_pools, to_dev
+from tests.gpu_util import TOL, assert_close, assert_lse, oracle_decode, oracle_pools, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -70,6 +71,28 @@ def test_static_scratch_matches_workspace_on_two_calls_in_a_row(mt):
         fin = np.isfinite(l_ref)
         assert (np.isfinite(l_got) == fin).all()
         assert np.abs(l_got[fin] - l_ref[fin]).max() <= tol, w.name
+
+
+def test_static_scratch_matches_oracle_after_a_larger_call(mt):
+    # a larger call with other shapes leaves its partials in the shared
+    # array; the next call must not read any of them
+    big = workloads.llama3_f16(seed=64, n_seqs=24, ctx_lo=200, ctx_hi=3000)
+    kp, vp = oracle_pools(big)
+    a = _args(mt, big, to_dev(kp), to_dev(vp))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mt.mt_paged_attn_decode_static(a, status=status)
+    assert mt.mt_check_device_status(status) == 0
+    for w in (workloads.smollm2_f32(seed=65, n_seqs=3, ctx_lo=40, ctx_hi=300),
+              workloads.llama3_q8_prefix(seed=66, n_seqs=5, prefix=64, suffix_lo=3,
+                                         suffix_hi=90)):
+        kp, vp = oracle_pools(w)
+        a = _args(mt, w, to_dev(kp), to_dev(vp))
+        mt.mt_paged_attn_decode_static(a, status=status)
+        assert mt.mt_check_device_status(status) == 0
+        want, want_lse = oracle_decode(w, kp, vp)
+        got, got_lse = a._tensors[5].cpu().numpy(), a._tensors[7].cpu().numpy()
+        assert_close(got, want, TOL[w.fmt], f"{w.name} static")
+        assert_lse(got_lse, want_lse, TOL[w.fmt], f"{w.name} static")
 
 
 def test_static_scratch_refuses_calls_that_do_not_fit(mt):
