@@ -713,7 +713,7 @@ def run_extra(args, rank, world, local_rank):
                               "frac": round(c_bytes / (c_ms * 1e-3) / 1e9 / peak, 4)},
                "clocks": clk}
     elif args.workload == "q8_prefix":
-        w = workloads.llama3_q8_prefix(hist=False)
+        w = workloads.llama3_q8_prefix(hist=False, windows=args.windows)
         layers, ws, rb = _decode_setup(mtkv, w, 32, dev, g)
         cells = torch.from_numpy(w.new_cells).to(dev)
         groups = [(0, w.n_seqs, w.extra["prefix"] // w.block_size)]
@@ -749,8 +749,9 @@ def run_extra(args, rank, world, local_rank):
                "ms_per_step": round(ms, 4), "step_ms": sp, "frac_of_peak": round(value / peak, 4),
                "attended_tokens_per_s": round(32 * toks / (ms * 1e-3), 1),
                "config": {"workload": "llama3-8b-shaped q8_0 paged decode: 32 layers, 32 seqs "
-                                      "sharing a 4096-token prefix + U[64,1024] suffix, random "
-                                      "windows, 32/8 heads, head_dim 128, bs 32",
+                                      "sharing a 4096-token prefix + U[64,1024] suffix, " +
+                                      ("random windows" if args.windows else "no windows") +
+                                      ", 32/8 heads, head_dim 128, bs 32",
                           "prefix": ("cascade: shared blocks read once per group "
                                      "(mt_paged_attn_decode_cascade)" if cascade else
                                      "per-sequence decode (mt_paged_attn_decode)"),
@@ -928,6 +929,9 @@ def main():
     ap.add_argument("--prefix", default="cascade", choices=["cascade", "plain"],
                     help="q8_prefix workload: decode the shared prefix once per group "
                          "(mt_paged_attn_decode_cascade) or per sequence")
+    ap.add_argument("--windows", action=argparse.BooleanOptionalAction, default=True,
+                    help="q8_prefix workload: each query's random attn_span window (the "
+                         "configuration) or its whole context")
     ap.add_argument("--graph", action=argparse.BooleanOptionalAction, default=True,
                     help="replay the L-layer step as one captured CUDA graph")
     ap.add_argument("--layers", type=int, default=N_LAYERS,
