@@ -251,7 +251,10 @@ size_t mt_paged_attn_cascade_workspace_bytes(const mt_paged_attn_args *args,
  * tensor-core tile), instead of once per sequence; each sequence's private
  * suffix goes through the ordinary decode; the two partial results merge by
  * log-sum-exp ("KV Cache Design — cells, format, sessions", section 1: a
- * sequence reads another's prefix in place, within its window).
+ * sequence reads another's prefix in place, within its window; the
+ * set-valued window of the kv_map input — shared prefix plus private run —
+ * is the case that page names). All three window modes are accepted: none,
+ * spans, or kv_map runs (each row of a prefix tile then masks its own runs).
  *   groups    host array of n_groups (<= 64) disjoint groups; sequences in no
  *             group are decoded as usual. Each group's sequences must hold
  *             identical first n_prefix_blocks table entries (holes included):
@@ -260,7 +263,7 @@ size_t mt_paged_attn_cascade_workspace_bytes(const mt_paged_attn_args *args,
  *             being undefined.
  * Shapes the prefix kernel is not built for (head_dim 256) run the ordinary
  * decode. Errors as mt_paged_attn_decode, plus MT_ERR_INVALID_ARG for bad or
- * overlapping groups and MT_ERR_UNSUPPORTED for kv_map windows. */
+ * overlapping groups. */
 mt_status mt_paged_attn_decode_cascade(const mt_paged_attn_args *args,
                                        const mt_prefix_group *groups, int n_groups,
                                        void *workspace, size_t workspace_bytes, mt_stream stream);

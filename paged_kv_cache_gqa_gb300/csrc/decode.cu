@@ -2515,8 +2515,6 @@ mt_status cascade_plan(const mt_paged_attn_args *a, const Plan &pl,
   if (n_groups > kMaxPrefixGroups)
     return fail(MT_ERR_UNSUPPORTED, "cascade decode: at most 64 prefix groups");
   if (n_groups > 0 && !groups) return fail(MT_ERR_INVALID_ARG, "cascade decode: null groups");
-  if (n_groups > 0 && a->kv_map)
-    return fail(MT_ERR_UNSUPPORTED, "cascade decode: kv_map windows are not supported");
   std::vector<std::pair<int, int>> spans;
   for (int i = 0; i < n_groups; ++i) {
     const mt_prefix_group &g = groups[i];
@@ -2649,6 +2647,7 @@ mt_status cascade_decode(const mt_paged_attn_args *a, const mt_prefix_group *gro
       pp.table = a->block_table;
       pp.ctx = a->context_lens;
       pp.spans = a->spans;
+      pp.kv_map = a->kv_map;
       pp.status = prm.status;
       pp.B = prm.B;
       pp.Hq = prm.Hq;

@@ -146,6 +146,10 @@ __global__ void __launch_bounds__(mq::kThreads, 2)
   // loop walks the range (the copies run S-1 units ahead)
   __shared__ int phys_s[kUnitChunk + S];
   __shared__ int win_s[2 * mq::kWarps];
+  // kv_map windows: the runs of the tile's rows, clipped to the prefix
+  constexpr int R_RUNS = MT_KV_MAP_MAX_SPANS;
+  __shared__ int2 runs_s[kPrefixRows][R_RUNS];
+  const bool use_map = p.kv_map != nullptr;
   long long chunk0 = u_beg;
   load_unit_blocks(p, chunk0, (int)min((long long)kUnitChunk + S, u_end - chunk0), u_end, phys_s);
   __syncthreads();
@@ -215,6 +219,25 @@ __global__ void __launch_bounds__(mq::kThreads, 2)
         const bool ok = s < g.s1 && hg < p.G;
         lo_r[half] = hi_r[half] = 0;
         if (ok) prefix_window(p, s, g.nblk * bs, lo_r[half], hi_r[half]);
+        if (use_map) {
+          // the row's runs inside [0, min(ctx, prefix)); bounds = their span
+          int rl = INT_MAX, rh = INT_MIN;
+          for (int r = 0; r < R_RUNS; ++r) {
+            int a = 0, e = 0;
+            if (ok) {
+              const int32_t *rp = p.kv_map + ((size_t)s * R_RUNS + r) * 2;
+              a = max(rp[0], 0);
+              e = min(rp[0] + rp[1], hi_r[half]);
+            }
+            if (c4 == 0) runs_s[R][r] = make_int2(a, e);
+            if (e > a) {
+              rl = min(rl, a);
+              rh = max(rh, e);
+            }
+          }
+          lo_r[half] = rh > rl ? rl : 0;
+          hi_r[half] = rh > rl ? rh : 0;
+        }
         qrow[half] = ok ? p.q + ((size_t)s * p.Hq + (size_t)cur.kvh * p.G + hg) * D : nullptr;
       }
       mq::load_q<D>(st, qrow[0], qrow[1], p.qscale, c4);
@@ -247,8 +270,20 @@ __global__ void __launch_bounds__(mq::kThreads, 2)
 
     if (phys_s[u - chunk0] < 0) continue;  // hole (or flagged id)
     const int pos0 = cur.b * bs;
-    const uint32_t mk0 = mq::range_mask(lo_r[0], hi_r[0], pos0, bs);
-    const uint32_t mk1 = mq::range_mask(lo_r[1], hi_r[1], pos0, bs);
+    uint32_t mk0, mk1;
+    if (use_map) {
+      const int R0 = 16 * warp + gid;
+      mk0 = mk1 = 0u;
+#pragma unroll
+      for (int r = 0; r < R_RUNS; ++r) {
+        const int2 a0 = runs_s[R0][r], a1 = runs_s[R0 + 8][r];
+        mk0 |= mq::range_mask(a0.x, a0.y, pos0, bs);
+        mk1 |= mq::range_mask(a1.x, a1.y, pos0, bs);
+      }
+    } else {
+      mk0 = mq::range_mask(lo_r[0], hi_r[0], pos0, bs);
+      mk1 = mq::range_mask(lo_r[1], hi_r[1], pos0, bs);
+    }
     // rows of this warp with no position in the block skip the math
     const bool any = __any_sync(kAll, (mk0 | mk1) != 0u);
 

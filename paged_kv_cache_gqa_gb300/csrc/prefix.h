@@ -16,6 +16,7 @@ struct PrefixParams {
   const int32_t *table;
   const int32_t *ctx;
   const int32_t *spans;
+  const int32_t *kv_map;  // [B][MT_KV_MAP_MAX_SPANS][2] (start, len) runs, or null
   uint32_t *status;
   int B, Hq, Hkv, G, bs, max_blocks;
   long long n_phys;

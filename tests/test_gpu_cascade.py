@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import attention as oatt
 from oracle import moves as om
 from oracle import formats as ofmt
 from paged_kv_cache_gqa_gb300 import workloads
@@ -187,3 +188,54 @@ def test_cascade_with_fused_store(mt):
     assert np.array_equal(k_dev.cpu().numpy(), kp) and np.array_equal(v_dev.cpu().numpy(), vp)
     assert_close(out.cpu().numpy(), want, TOL["q8_0"], "cascade + fused store")
     assert_lse(lse.cpu().numpy(), want_lse, TOL["q8_0"], "cascade + fused store")
+
+
+def _prefix_map(rng, lens, n_prefix, extra):
+    """Set-valued windows: the shared prefix [0, n_prefix), one private run
+    after it, and `extra` random runs anywhere (some reaching into the
+    prefix, some past the context)."""
+    mp = np.zeros((len(lens), 8, 2), dtype=np.int32)
+    for s, c in enumerate(lens):
+        c = int(c)
+        mp[s, 0] = (0, n_prefix)
+        a = int(rng.integers(n_prefix, max(c, n_prefix + 1)))
+        mp[s, 1] = (a, int(rng.integers(1, max(c - a, 1) + 8)))
+        for r in range(2, 2 + extra):
+            mp[s, r] = (int(rng.integers(-4, c + 4)), int(rng.integers(-2, max(c // 4, 3))))
+    return mp
+
+
+@pytest.mark.parametrize("fmt,d,bs,hq,hkv,extra", [("f16", 128, 16, 32, 8, 0),
+                                                   ("q8_0", 128, 32, 32, 8, 3),
+                                                   ("f32", 64, 16, 9, 3, 2),
+                                                   ("q8_0", 64, 16, 8, 2, 6)])
+def test_cascade_kv_map_prefix_plus_private_run(mt, fmt, d, bs, hq, hkv, extra):
+    # "KV Cache Design — cells, format, sessions", section 1: a set-valued
+    # window (shared prefix + private run) goes through kv_map; the cascade
+    # must equal the plain kv_map decode of the oracle
+    rng = np.random.default_rng(90 + d + bs + extra)
+    w = workloads.llama3_f16(seed=91 + extra, n_seqs=11, ctx_lo=100, ctx_hi=400, fmt=fmt,
+                             block_size=bs, n_heads=hq, n_kv_heads=hkv, head_dim=d)
+    nblk = 3
+    groups = [(0, 6, nblk), (6, 11, nblk - 1)]
+    table = share(w.block_table, groups)
+    kp, vp = oracle_pools(w)
+    mp = _prefix_map(rng, w.context_lens, nblk * bs, extra)
+    mp[6:, 0] = ((nblk - 1) * bs) // 2, (nblk - 1) * bs  # the second group: part of its prefix
+    want, want_lse = oatt.paged_attn_decode_map(w.fmt, w.q, kp, vp, table, w.context_lens, mp,
+                                                w.n_heads, w.n_kv_heads, w.head_dim,
+                                                w.block_size, w.scale)
+    k_dev, v_dev = to_dev(kp), to_dev(vp)
+    q = to_dev(w.q)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((w.n_seqs, w.n_heads), float("nan"), device="cuda")
+    args = mt.paged_attn_args(w.fmt, q, k_dev, v_dev, to_dev(table), to_dev(w.context_lens), out,
+                              n_kv_heads=w.n_kv_heads, block_size=w.block_size,
+                              n_phys_blocks=w.n_phys_blocks, scale=w.scale, lse=lse,
+                              kv_map=to_dev(mp))
+    ws = torch.zeros(mt.mt_paged_attn_cascade_workspace_bytes(args, groups), dtype=torch.uint8,
+                     device="cuda")
+    mt.mt_paged_attn_decode_cascade(args, groups, ws)
+    assert mt.mt_check_device_status(ws) == 0, mt.mt_last_error()
+    assert_close(out.cpu().numpy(), want, TOL[w.fmt], f"{w.name} cascade kv_map")
+    assert_lse(lse.cpu().numpy(), want_lse, TOL[w.fmt], f"{w.name} cascade kv_map")

@@ -130,7 +130,7 @@ def test_kv_map_with_fused_store(mt):
     assert_lse(got_lse, want_lse, TOL[w.fmt], "kv_map + fused store")
 
 
-def test_kv_map_rejected_with_spans_or_cascade(mt):
+def test_kv_map_rejected_with_spans(mt):
     rng = np.random.default_rng(66)
     w = workloads.llama3_f16(seed=66, n_seqs=3, ctx_lo=30, ctx_hi=60)
     kp, vp = oracle_pools(w)
@@ -138,12 +138,3 @@ def test_kv_map_rejected_with_spans_or_cascade(mt):
     sp = np.stack([np.zeros(3), w.context_lens], axis=1).astype(np.int32)
     with pytest.raises(mt.MtError):
         decode_map(mt, w, kp, vp, mp, spans=sp)
-    q = to_dev(w.q)
-    out = torch.zeros_like(q)
-    args = mt.paged_attn_args(w.fmt, q, to_dev(kp), to_dev(vp), to_dev(w.block_table),
-                              to_dev(w.context_lens), out, n_kv_heads=w.n_kv_heads,
-                              block_size=w.block_size, n_phys_blocks=w.n_phys_blocks,
-                              scale=w.scale, kv_map=to_dev(mp))
-    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
-    with pytest.raises(mt.MtError):
-        mt.mt_paged_attn_decode_cascade(args, [(0, 3, 1)], ws)
