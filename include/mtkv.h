@@ -220,8 +220,9 @@ size_t mt_paged_prefill_workspace_bytes(const mt_paged_prefill_args *args);
  *   out[i][h] = sum_t softmax_t(scale * q[i][h] . k_t) v_t over the positions
  *   t <= p, t < ctx, not in a hole, inside the query's window;
  *   lse[i][h] = log sum_t exp(scale * q . k_t). No valid t: out 0, lse -inf.
- * Shapes built: head_dim 64 or 128, block_size 16 or 32, n_heads/n_kv_heads
- * <= 8, n_kv_heads <= 8 (others MT_ERR_UNSUPPORTED). Out-of-range block ids,
+ * Shapes built: head_dim 64 or 128 (and 256 for f16 and q8_0 pools),
+ * block_size 16 or 32, n_heads/n_kv_heads <= 8, n_kv_heads <= 8 (others
+ * MT_ERR_UNSUPPORTED). Out-of-range block ids,
  * query counts above the context length and query rows outside
  * [0, n_tokens) are skipped and flagged in the workspace status word. */
 mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *args, void *workspace,
@@ -261,8 +262,8 @@ size_t mt_paged_attn_cascade_workspace_bytes(const mt_paged_attn_args *args,
  *             the kernel checks this and flags a mismatch in the workspace
  *             status word (MT_ERR_DEVICE_CHECK), the affected outputs then
  *             being undefined.
- * Shapes the prefix kernel is not built for (head_dim 256) run the ordinary
- * decode. Errors as mt_paged_attn_decode, plus MT_ERR_INVALID_ARG for bad or
+ * Shapes the prefix kernel is not built for (f32 pools of head_dim 256) run
+ * the ordinary decode. Errors as mt_paged_attn_decode, plus MT_ERR_INVALID_ARG for bad or
  * overlapping groups. */
 mt_status mt_paged_attn_decode_cascade(const mt_paged_attn_args *args,
                                        const mt_prefix_group *groups, int n_groups,

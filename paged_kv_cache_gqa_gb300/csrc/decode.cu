@@ -2534,7 +2534,7 @@ mt_status cascade_plan(const mt_paged_attn_args *a, const Plan &pl,
   cp->rec_off = pl.ws_total;
   Cascade &c = cp->c;
   c = Cascade{};
-  cp->use = n_groups > 0 && prefix_supported(a->head_dim, a->block_size, pl.GP);
+  cp->use = n_groups > 0 && prefix_supported(a->fmt, a->head_dim, a->block_size, pl.GP);
   if (!cp->use) return MT_OK;
   c.n_groups = n_groups;
   c.gp = pl.GP;
@@ -2549,7 +2549,8 @@ mt_status cascade_plan(const mt_paged_attn_args *a, const Plan &pl,
   DeviceInfo di;
   mt_status st = device_info(&di);
   if (st != MT_OK) return st;
-  const long long ctas = std::min<long long>((long long)di.n_sm * prefix_ctas_per_sm(), units);
+  const long long ctas =
+      std::min<long long>((long long)di.n_sm * prefix_ctas_per_sm(a->head_dim), units);
   c.n_tiles = (int)tiles;
   c.n_units = units;
   c.n_ctas = ctas > 0 ? (int)ctas : 0;

@@ -51,7 +51,14 @@ struct Cfg {
   static constexpr int N_TILES = FMT == MT_KV_F32 ? 4 : FMT == MT_KV_Q8_0 ? 2 : 0;
   static constexpr int TILE_BYTES = N_TILES * kMaxBs * TP;
   static constexpr int SCALE_BYTES = FMT == MT_KV_Q8_0 ? 2 * NG * kMaxBs * 4 : 0;
-  static constexpr int SMEM = STAGES * RAW_STAGE + TILE_BYTES + SCALE_BYTES;
+  // head_dim above 128: the Q fragments would not fit in registers beside O,
+  // so each warp keeps its 16 rows of Q (high rows, then low rows, pitch
+  // 2d+16 bytes) in shared memory and reads them with ldmatrix per k-step
+  static constexpr bool QS = D > 128;
+  static constexpr int QTP = 2 * D + 16;
+  static constexpr int QS_WARP = 2 * 16 * QTP;
+  static constexpr int QS_BYTES = QS ? kWarps * QS_WARP : 0;
+  static constexpr int SMEM = STAGES * RAW_STAGE + TILE_BYTES + SCALE_BYTES + QS_BYTES;
 };
 
 
@@ -214,10 +221,33 @@ __device__ __forceinline__ uint32_t range_mask(int lo, int hi, int pos0, int bs)
 // gid + 8 (gid = lane / 4) of the MMA fragments.
 template <int D>
 struct Rows {
-  uint32_t qh[D / 16][4], ql[D / 16][4];  // A fragments of q * scale * log2(e)
+  static constexpr bool QS = D > 128;       // Q in shared memory (see Cfg::QS)
+  static constexpr int QTP = 2 * D + 16;
+  uint32_t qh[QS ? 1 : D / 16][4], ql[QS ? 1 : D / 16][4];  // A fragments of q*scale*log2(e)
+  uint32_t qs;                            // QS: shared address of the warp's Q rows
   float o[D / 8][4];                      // unnormalised output
   float m[2], l[2];                       // running max (base 2), partial sums
 };
+
+// The A fragments (high and low) of k-step ks of this warp's Q.
+template <int D>
+__device__ __forceinline__ void q_frags(const Rows<D> &st, int ks, int lane, uint32_t (&h)[4],
+                                        uint32_t (&l)[4]) {
+  if constexpr (Rows<D>::QS) {
+    // ldmatrix.x4: lanes 0-7 rows 0-7 / cols 0-7, 8-15 rows 8-15 / cols 0-7,
+    // 16-23 rows 0-7 / cols 8-15, 24-31 rows 8-15 / cols 8-15
+    const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t a = st.qs + (uint32_t)(r * Rows<D>::QTP + ks * 32 + (lane >> 4) * 16);
+    ldsm_x4(a, h[0], h[1], h[2], h[3]);
+    ldsm_x4(a + 16 * Rows<D>::QTP, l[0], l[1], l[2], l[3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      h[i] = st.qh[ks][i];
+      l[i] = st.ql[ks][i];
+    }
+  }
+}
 
 // Start rows gid / gid+8 with query rows q0 / q1 (null: padding row).
 template <int D>
@@ -233,15 +263,30 @@ __device__ __forceinline__ void load_q(Rows<D> &st, const float *q0, const float
         x0 = *reinterpret_cast<const float2 *>(qrow + 16 * ks + 2 * c4);
         x1 = *reinterpret_cast<const float2 *>(qrow + 16 * ks + 2 * c4 + 8);
       }
-      // A fragment: regs 0/2 hold row gid (cols 2c, 2c+8), 1/3 row gid+8
-      split_h2(x0.x * qscale, x0.y * qscale, st.qh[ks][half], st.ql[ks][half]);
-      split_h2(x1.x * qscale, x1.y * qscale, st.qh[ks][half + 2], st.ql[ks][half + 2]);
+      if constexpr (Rows<D>::QS) {
+        // rows gid / gid+8 of the warp's Q tile, cols 16ks + 2c and +8
+        uint32_t h0, l0, h1, l1;
+        split_h2(x0.x * qscale, x0.y * qscale, h0, l0);
+        split_h2(x1.x * qscale, x1.y * qscale, h1, l1);
+        const int r = (threadIdx.x & 31) / 4 + 8 * half;
+        uint8_t *t = reinterpret_cast<uint8_t *>(__cvta_shared_to_generic(st.qs)) +
+                     r * Rows<D>::QTP + (16 * ks + 2 * c4) * 2;
+        *reinterpret_cast<uint32_t *>(t) = h0;
+        *reinterpret_cast<uint32_t *>(t + 16) = h1;
+        *reinterpret_cast<uint32_t *>(t + 16 * Rows<D>::QTP) = l0;
+        *reinterpret_cast<uint32_t *>(t + 16 * Rows<D>::QTP + 16) = l1;
+      } else {
+        // A fragment: regs 0/2 hold row gid (cols 2c, 2c+8), 1/3 row gid+8
+        split_h2(x0.x * qscale, x0.y * qscale, st.qh[ks][half], st.ql[ks][half]);
+        split_h2(x1.x * qscale, x1.y * qscale, st.qh[ks][half + 2], st.ql[ks][half + 2]);
+      }
     }
     st.m[half] = -INFINITY;
     st.l[half] = 0.f;
   }
 #pragma unroll
   for (int nd = 0; nd < D / 8; ++nd) st.o[nd][0] = st.o[nd][1] = st.o[nd][2] = st.o[nd][3] = 0.f;
+  if constexpr (Rows<D>::QS) __syncwarp();  // the warp's Q rows are written
 }
 
 // Row sums of the quad (the 4 threads sharing rows gid, gid + 8).
@@ -266,8 +311,6 @@ __device__ __forceinline__ void unit(Rows<D> &st, const uint8_t *kt, const uint8
   constexpr int ND = D / 8;
   const int c4 = lane & 3;
   const int NT = bs / 8;
-  auto &qh = st.qh;
-  auto &ql = st.ql;
   auto &o = st.o;
   auto &m_r = st.m;
   auto &l_r = st.l;
@@ -280,6 +323,11 @@ __device__ __forceinline__ void unit(Rows<D> &st, const uint8_t *kt, const uint8
   const uint32_t ka = smem_u32(kt + (lane & 7) * C::TP) + (lane >> 3) * 16;
 #pragma unroll
   for (int k2 = 0; k2 < D / 32; ++k2) {
+    // Q's A fragments of the group's two k-steps (registers, or shared
+    // memory for head_dim 256)
+    uint32_t qh[2][4], ql[2][4];
+    q_frags<D>(st, 2 * k2, lane, qh[0], ql[0]);
+    q_frags<D>(st, 2 * k2 + 1, lane, qh[1], ql[1]);
     uint32_t bf[4][4];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
@@ -288,14 +336,14 @@ __device__ __forceinline__ void unit(Rows<D> &st, const uint8_t *kt, const uint8
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
         if (nt < NT) {
-          mma_f16(sc[nt], qh[2 * k2], bf[nt][0], bf[nt][1]);
-          mma_f16(sc[nt], qh[2 * k2 + 1], bf[nt][2], bf[nt][3]);
+          mma_f16(sc[nt], qh[0], bf[nt][0], bf[nt][1]);
+          mma_f16(sc[nt], qh[1], bf[nt][2], bf[nt][3]);
         }
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
         if (nt < NT) {
-          mma_f16(sc[nt], ql[2 * k2], bf[nt][0], bf[nt][1]);
-          mma_f16(sc[nt], ql[2 * k2 + 1], bf[nt][2], bf[nt][3]);
+          mma_f16(sc[nt], ql[0], bf[nt][0], bf[nt][1]);
+          mma_f16(sc[nt], ql[1], bf[nt][2], bf[nt][3]);
         }
     } else if constexpr (FMT == MT_KV_Q8_0) {
       // one 32-dim group: its own accumulators, then times the scales
@@ -304,15 +352,15 @@ __device__ __forceinline__ void unit(Rows<D> &st, const uint8_t *kt, const uint8
       for (int nt = 0; nt < 4; ++nt) {
         acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
         if (nt < NT) {
-          mma_f16(acc[nt], qh[2 * k2], bf[nt][0], bf[nt][1]);
-          mma_f16(acc[nt], qh[2 * k2 + 1], bf[nt][2], bf[nt][3]);
+          mma_f16(acc[nt], qh[0], bf[nt][0], bf[nt][1]);
+          mma_f16(acc[nt], qh[1], bf[nt][2], bf[nt][3]);
         }
       }
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
         if (nt < NT) {
-          mma_f16(acc[nt], ql[2 * k2], bf[nt][0], bf[nt][1]);
-          mma_f16(acc[nt], ql[2 * k2 + 1], bf[nt][2], bf[nt][3]);
+          mma_f16(acc[nt], ql[0], bf[nt][0], bf[nt][1]);
+          mma_f16(acc[nt], ql[1], bf[nt][2], bf[nt][3]);
         }
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
@@ -330,12 +378,12 @@ __device__ __forceinline__ void unit(Rows<D> &st, const uint8_t *kt, const uint8
         if (nt < NT) {
           uint32_t l0, l1, l2, l3;
           ldsm_x4(ka + nt * 8 * C::TP + k2 * 64 + kMaxBs * C::TP, l0, l1, l2, l3);
-          mma_f16(sc[nt], qh[2 * k2], bf[nt][0], bf[nt][1]);
-          mma_f16(sc[nt], qh[2 * k2 + 1], bf[nt][2], bf[nt][3]);
-          mma_f16(sc[nt], ql[2 * k2], bf[nt][0], bf[nt][1]);
-          mma_f16(sc[nt], ql[2 * k2 + 1], bf[nt][2], bf[nt][3]);
-          mma_f16(sc[nt], qh[2 * k2], l0, l1);
-          mma_f16(sc[nt], qh[2 * k2 + 1], l2, l3);
+          mma_f16(sc[nt], qh[0], bf[nt][0], bf[nt][1]);
+          mma_f16(sc[nt], qh[1], bf[nt][2], bf[nt][3]);
+          mma_f16(sc[nt], ql[0], bf[nt][0], bf[nt][1]);
+          mma_f16(sc[nt], ql[1], bf[nt][2], bf[nt][3]);
+          mma_f16(sc[nt], qh[0], l0, l1);
+          mma_f16(sc[nt], qh[1], l2, l3);
         }
     }
   }

@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(mq::kThreads, 2)
   }
 
   mq::Rows<D> st;
+  if constexpr (C::QS) st.qs = smem_u32(smem + C::SMEM - C::QS_BYTES) + warp * C::QS_WARP;
   int lo_r[2] = {0, 0}, hi_r[2] = {0, 0};  // each row's window bounds (causal, ctx included)
   int orow[2] = {-1, -1};                  // (query row * Hq + head), -1: padding row
   int ulo = 0, uhi = 0;                    // union of the tile's windows
@@ -328,7 +329,11 @@ mt_status launch_d(int gp, const PrefillParams &p, int n_ctas, cudaStream_t s) {
 
 template <int FMT>
 mt_status launch_f(int d, int gp, const PrefillParams &p, int n_ctas, cudaStream_t s) {
-  return d == 64 ? launch_d<FMT, 64>(gp, p, n_ctas, s) : launch_d<FMT, 128>(gp, p, n_ctas, s);
+  if (d == 64) return launch_d<FMT, 64>(gp, p, n_ctas, s);
+  if constexpr (FMT != MT_KV_F32) {
+    if (d == 256) return launch_d<FMT, 256>(gp, p, n_ctas, s);
+  }
+  return launch_d<FMT, 128>(gp, p, n_ctas, s);
 }
 
 int pad_g(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : G <= 8 ? 8 : 0; }
@@ -356,11 +361,12 @@ extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void 
     return fail(MT_ERR_INVALID_ARG, "prefill: n_heads must be a multiple of n_kv_heads");
   const int G = a->n_heads / a->n_kv_heads;
   const int GP = pad_g(G);
-  if ((a->head_dim != 64 && a->head_dim != 128) || (a->block_size != 16 && a->block_size != 32) ||
-      GP == 0)
+  const bool d_ok = a->head_dim == 64 || a->head_dim == 128 ||
+                    (a->head_dim == 256 && a->fmt != MT_KV_F32);
+  if (!d_ok || (a->block_size != 16 && a->block_size != 32) || GP == 0)
     return fail(MT_ERR_UNSUPPORTED,
-                "prefill: head_dim 64 or 128, block_size 16 or 32, at most 8 query heads per "
-                "KV head");
+                "prefill: head_dim 64 or 128 (256 for f16 and q8_0 pools), block_size 16 or 32, "
+                "at most 8 query heads per KV head");
   if (a->spans && a->kv_map)
     return fail(MT_ERR_INVALID_ARG, "prefill: spans and kv_map are two window modes: pass one");
   if ((long long)a->max_blocks * a->block_size > 0x7fffffffLL)

@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(mq::kThreads, 2)
   }
 
   mq::Rows<D> st;
+  if constexpr (C::QS) st.qs = smem_u32(smem + C::SMEM - C::QS_BYTES) + warp * C::QS_WARP;
   int lo_r[2] = {0, 0}, hi_r[2] = {0, 0};
   int cur_T = -1;
   int ulo = 0, uhi = 0;  // union of the current tile's windows
@@ -309,21 +310,28 @@ __global__ void __launch_bounds__(mq::kThreads, 2)
 
 }  // namespace
 
-bool prefix_supported(int head_dim, int block_size, int gp) {
-  return (head_dim == 64 || head_dim == 128) && (block_size == 16 || block_size == 32) &&
-         (gp == 1 || gp == 2 || gp == 4 || gp == 8);
+bool prefix_supported(mt_kv_format fmt, int head_dim, int block_size, int gp) {
+  const bool d = head_dim == 64 || head_dim == 128 || (head_dim == 256 && fmt != MT_KV_F32);
+  return d && (block_size == 16 || block_size == 32) && (gp == 1 || gp == 2 || gp == 4 || gp == 8);
 }
 
 int prefix_smem_bytes(mt_kv_format fmt, int head_dim) {
-  const bool d64 = head_dim == 64;
   switch (fmt) {
-    case MT_KV_F32: return d64 ? mq::Cfg<MT_KV_F32, 64>::SMEM : mq::Cfg<MT_KV_F32, 128>::SMEM;
-    case MT_KV_F16: return d64 ? mq::Cfg<MT_KV_F16, 64>::SMEM : mq::Cfg<MT_KV_F16, 128>::SMEM;
-    default: return d64 ? mq::Cfg<MT_KV_Q8_0, 64>::SMEM : mq::Cfg<MT_KV_Q8_0, 128>::SMEM;
+    case MT_KV_F32:
+      return head_dim == 64 ? mq::Cfg<MT_KV_F32, 64>::SMEM : mq::Cfg<MT_KV_F32, 128>::SMEM;
+    case MT_KV_F16:
+      return head_dim == 64    ? mq::Cfg<MT_KV_F16, 64>::SMEM
+             : head_dim == 128 ? mq::Cfg<MT_KV_F16, 128>::SMEM
+                               : mq::Cfg<MT_KV_F16, 256>::SMEM;
+    default:
+      return head_dim == 64    ? mq::Cfg<MT_KV_Q8_0, 64>::SMEM
+             : head_dim == 128 ? mq::Cfg<MT_KV_Q8_0, 128>::SMEM
+                               : mq::Cfg<MT_KV_Q8_0, 256>::SMEM;
   }
 }
 
-int prefix_ctas_per_sm() { return 2; }
+// head_dim 256 keeps Q in shared memory (about 200 KB per CTA): one per SM
+int prefix_ctas_per_sm(int head_dim) { return head_dim == 256 ? 1 : 2; }
 
 namespace {
 
@@ -350,7 +358,11 @@ mt_status launch_d(int gp, const PrefixParams &p, int n_ctas, cudaStream_t s) {
 
 template <int FMT>
 mt_status launch_f(int head_dim, int gp, const PrefixParams &p, int n_ctas, cudaStream_t s) {
-  return head_dim == 64 ? launch_d<FMT, 64>(gp, p, n_ctas, s) : launch_d<FMT, 128>(gp, p, n_ctas, s);
+  if (head_dim == 64) return launch_d<FMT, 64>(gp, p, n_ctas, s);
+  if constexpr (FMT != MT_KV_F32) {
+    if (head_dim == 256) return launch_d<FMT, 256>(gp, p, n_ctas, s);
+  }
+  return launch_d<FMT, 128>(gp, p, n_ctas, s);
 }
 
 }  // namespace

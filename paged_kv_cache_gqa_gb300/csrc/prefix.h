@@ -25,13 +25,13 @@ struct PrefixParams {
   Cascade c;
 };
 
-// Whether the prefix kernel is built for this shape (head_dim 64 or 128,
-// block_size 16 or 32, padded query group <= 8).
-bool prefix_supported(int head_dim, int block_size, int gp);
+// Whether the prefix kernel is built for this shape (head_dim 64 or 128, and
+// 256 for f16 and q8_0 pools; block_size 16 or 32; padded query group <= 8).
+bool prefix_supported(mt_kv_format fmt, int head_dim, int block_size, int gp);
 // Dynamic shared memory of the prefix kernel for (format, head_dim).
 int prefix_smem_bytes(mt_kv_format fmt, int head_dim);
-// CTAs of the prefix kernel that can be resident on the device at once.
-int prefix_ctas_per_sm();
+// CTAs of the prefix kernel resident per SM for this head_dim.
+int prefix_ctas_per_sm(int head_dim);
 mt_status launch_prefix(mt_kv_format fmt, int head_dim, int gp, const PrefixParams &p, int n_ctas,
                         cudaStream_t stream);
 

@@ -116,7 +116,10 @@ def test_cascade_q8_prefix_windows(mt):
 
 @pytest.mark.parametrize("fmt,d,bs,hq,hkv", [("q8_0", 64, 16, 2, 2), ("q8_0", 128, 16, 16, 2),
                                              ("f16", 64, 32, 8, 1), ("f32", 128, 32, 4, 4),
-                                             ("f16", 128, 16, 6, 2)])
+                                             ("f16", 128, 16, 6, 2),
+                                             # head_dim 256: Q rows kept in shared memory
+                                             ("f16", 256, 16, 16, 4), ("q8_0", 256, 32, 8, 2),
+                                             ("q8_0", 256, 16, 5, 1)])
 def test_cascade_shape_grid(mt, fmt, d, bs, hq, hkv):
     w = workloads.llama3_f16(seed=25 + d + bs + hq, n_seqs=7, ctx_lo=20, ctx_hi=150, fmt=fmt,
                              block_size=bs, n_heads=hq, n_kv_heads=hkv, head_dim=d)
@@ -128,9 +131,13 @@ def test_cascade_holes_in_prefix_and_fallback_shape(mt):
     t = w.block_table.copy()
     t[:, 1] = -1  # a hole inside the shared prefix, in every sequence
     check(mt, w, [(0, 6, 4)], table=t)
-    # head_dim 256 has no prefix kernel: the call runs the plain decode
+    # the long-context shape (head_dim 256, f16) takes the prefix kernel too;
+    # f32 pools of head_dim 256 have none and run the plain decode
     w2 = workloads.longctx_f16_int4(seed=27, n_seqs=3, ctx=400)
     check(mt, w2, [(0, 3, 5)])
+    w3 = workloads.llama3_f16(seed=29, n_seqs=4, ctx_lo=100, ctx_hi=200, fmt="f32", n_heads=4,
+                              n_kv_heads=2, head_dim=256)
+    check(mt, w3, [(0, 4, 3)])
 
 
 def test_cascade_broken_promise_is_flagged(mt):

@@ -121,7 +121,12 @@ def test_prefill_kv_map_runs(mt, fmt):
 
 @pytest.mark.parametrize("fmt,d,bs,hq,hkv", [("f16", 64, 32, 8, 1), ("q8_0", 64, 16, 2, 2),
                                              ("f16", 128, 16, 5, 5), ("f32", 128, 32, 4, 2),
-                                             ("q8_0", 128, 32, 24, 4)])
+                                             ("q8_0", 128, 32, 24, 4),
+                                             # head_dim 256 (the (256, 16) dispatch tuple of
+                                             # "Tiered KV cache — architecture", "Kernel
+                                             # dispatch"): Q rows kept in shared memory
+                                             ("f16", 256, 16, 16, 4), ("q8_0", 256, 16, 8, 2),
+                                             ("f16", 256, 32, 6, 2), ("q8_0", 256, 32, 3, 3)])
 def test_prefill_shape_grid(mt, fmt, d, bs, hq, hkv):
     rng = np.random.default_rng(55 + d + bs + hq)
     w = workloads.llama3_f16(seed=55 + d + hq, n_seqs=4, ctx_lo=1, ctx_hi=160, fmt=fmt,
@@ -169,8 +174,11 @@ def test_prefill_rejects_bad_arguments(mt):
     mp = random_map(rng, w, q_start)
     with pytest.raises(mt.MtError):
         run_prefill(mt, w, q, q_start, kp, vp, spans=sp, kv_map=mp)
-    w2 = workloads.longctx_f16_int4(seed=59, n_seqs=1, ctx=64)  # head_dim 256: not built
+    # f32 pools of head_dim 256 have no multi-query kernel
+    w2 = workloads.llama3_f16(seed=59, n_seqs=1, ctx_lo=40, ctx_hi=64, fmt="f32", n_heads=4,
+                              n_kv_heads=2, head_dim=256)
     q2, qs2 = make_queries(w2, rng, 4)
     kp2, vp2 = oracle_pools(w2)
-    with pytest.raises(mt.MtError):
+    with pytest.raises(mt.MtError) as e:
         run_prefill(mt, w2, q2, qs2, kp2, vp2)
+    assert e.value.status == mt.MT_ERR_UNSUPPORTED
