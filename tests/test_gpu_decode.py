@@ -145,6 +145,11 @@ SHAPES = [  # fmt, head_dim, block_size, n_heads, n_kv_heads
     ("f16", 128, 32, 24, 4), ("f16", 64, 16, 21, 3), ("f16", 128, 16, 5, 5),
     ("q8_0", 64, 16, 6, 2), ("q8_0", 128, 32, 32, 8), ("q8_0", 256, 16, 16, 4),
     ("q8_0", 128, 16, 8, 1), ("q8_0", 64, 32, 9, 3),
+    # head_dim 128 q8_0 on the direct-operand consumer: paired 16-row blocks
+    # (32-byte chunks at 8 heads, 16-byte chunks at 2), whole 32-row blocks
+    # through the 16-byte-chunk map (6 heads), query groups 1, 4 and 8
+    ("q8_0", 128, 16, 32, 8), ("q8_0", 128, 16, 16, 2), ("q8_0", 128, 32, 6, 6),
+    ("q8_0", 128, 16, 12, 4),
 ]
 
 

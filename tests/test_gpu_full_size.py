@@ -117,6 +117,36 @@ def test_full_smollm2_f32_step(mt):
     _fused_step(mt, w, 3002, None)
 
 
+@pytest.mark.parametrize("bs", [16, 32])
+def test_full_llama3_q8_0_decode(mt, bs):
+    # the Llama-3-shaped batch (64 sequences, context log-uniform in
+    # [512, 16384], 32/8 heads, d 128) with q8_0 pools, one decode call in the
+    # launch configuration the per-format benchmark times (default grid,
+    # paired 16-row blocks at block size 16). The sampled sequences' blocks
+    # hold N(0,1) rows stored by the oracle's quantiser; the other blocks are
+    # zero (scale 0, codes 0: valid q8_0 cells)
+    w = workloads.llama3_f16(fmt="q8_0", block_size=bs, hist=False)
+    seqs = _sample(w, 4, 3010 + bs)
+    rb = ofmt.row_bytes("q8_0", w.n_kv_heads, w.head_dim)
+    kp = np.zeros((w.n_cells, rb), np.uint8)
+    vp = np.zeros((w.n_cells, rb), np.uint8)
+    rng = np.random.default_rng(3011 + bs)
+    row = w.n_kv_heads * w.head_dim
+    for s in seqs:
+        nb = -(-int(w.context_lens[s]) // bs)
+        cells = (w.block_table[s, :nb].astype(np.int64)[:, None] * bs + np.arange(bs)).reshape(-1)
+        x = rng.standard_normal((2, nb * bs, row), dtype=np.float32)
+        kp[cells] = ofmt.encode_rows("q8_0", x[0], w.n_kv_heads, w.head_dim)
+        vp[cells] = ofmt.encode_rows("q8_0", x[1], w.n_kv_heads, w.head_dim)
+    args, out, lse = _args(mt, w, to_dev(kp), to_dev(vp), lse=True)
+    ws = torch.zeros(mt.mt_paged_attn_workspace_bytes(args), dtype=torch.uint8, device="cuda")
+    mt.mt_paged_attn_decode(args, ws)
+    assert mt.mt_check_device_status(ws) == 0, mt.mt_last_error()
+    want, want_lse = oracle_decode(w, kp, vp, seqs=seqs)
+    _check(w, out.cpu().numpy(), want, seqs, f"q8_0 bs {bs} full size", lse.cpu().numpy(),
+           want_lse)
+
+
 @pytest.mark.parametrize("prefix", ["cascade", "plain"])
 def test_full_q8_prefix_windows(mt, prefix):
     # 32 sequences sharing a 4096-token prefix (refcount 32) plus private
