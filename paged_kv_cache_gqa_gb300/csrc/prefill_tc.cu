@@ -21,8 +21,10 @@
 //     its P.V has run; holes are not read at all;
 //   * one MMA warp computes S(c) = Q_hi K^T + Q_lo K^T (M = 128, N = 128,
 //     f16 in, f32 accumulated in tensor memory; q = Q_hi + Q_lo to ~2^-22, so
-//     scores keep float32 accuracy) into the S buffer as soon as the softmax
-//     has loaded the previous chunk's scores into registers;
+//     scores keep float32 accuracy; Q read from tensor memory, so only K
+//     takes shared-memory bandwidth) into one of two S buffers, as soon as the
+//     P.V of the chunk two back (which used that buffer) has run: S(c + 1) is
+//     computed while the softmax works on S(c);
 //     another computes O += P(c) V(c) once the probabilities of chunk c are
 //     in tensor memory (P read from tensor memory, V MN-major straight from
 //     its stage), after zeroing the V rows of holes and past the context (P
@@ -33,16 +35,17 @@
 //     tensor-memory lanes 32 (w % 4) .. + 31; each takes 64 of the 128 score
 //     columns and half of O): load S, mask it, exchange the row maximum with
 //     the partner through shared memory and a two-warp named barrier, run the
-//     online softmax, and store f16 probabilities into one of two P buffers
-//     in tensor memory. The output row is rescaled only when the running
-//     maximum grows by more than 2^8 (probabilities then stay below 256,
-//     exact in f16); a tile's output is normalised once at the end.
+//     online softmax, and store f16 probabilities over the scores they came
+//     from (each thread over its own columns, already in registers). The
+//     output row is rescaled only when the running maximum grows by more than
+//     2^8 (probabilities then stay below 256, exact in f16); a tile's output
+//     is normalised once at the end.
 // The next tile's Q is built during the current tile, a slice of 8 dims per
-// chunk, as high / low f16 pairs in spare tensor-memory columns (each slice's
-// global loads issued at a chunk's start and used at its end); once the last
-// S of a tile is complete it is copied into the shared Q tiles, so the next
-// tile's first scores are computed while the last chunk's softmax and the
-// output of the current tile run.
+// chunk, as high / low f16 pairs staged in shared memory (each slice's global
+// loads issued at a chunk's start and used at its end); once the last S of a
+// tile is complete it is copied into the Q columns of tensor memory, so the
+// next tile's first scores are computed while the last chunk's softmax and
+// the output of the current tile run.
 #include <limits.h>
 #include <math.h>
 
@@ -67,11 +70,13 @@ constexpr int kMmaWarpS = 10;   // issues S = Q K^T
 constexpr int kMmaWarpO = 11;   // issues O += P V
 constexpr int kTcThreads = 384;
 constexpr int kChunk = 128;        // tokens per chunk
-// tensor-memory columns: S [0, 128); O [128, 128 + d); P (f16 pairs) double
-// buffer [256, 320), [320, 384); the next tile's Q as f16 pairs, high [384,
-// 448) and low [448, 512)
-constexpr int kOCol = kChunk;
-constexpr int kPCol = 256;
+// tensor-memory columns: S double buffer [0, 128), [128, 256) (S(x) in buffer
+// x % 2; P(x) as f16 pairs over the scores it came from: the thread owning
+// score columns [64 h, 64 h + 64) writes their 32 probability pairs to
+// [64 h, 64 h + 32)); O [256, 256 + d); the tile's Q as f16 pairs (the A
+// operand of S), high [384, 384 + d / 2) and low [448, 448 + d / 2)
+constexpr int kSCols = kChunk;
+constexpr int kOCol = 2 * kChunk;
 constexpr int kQHiCol = 384;
 constexpr int kQLoCol = 448;
 constexpr uint32_t kTmemCols = 512;
@@ -80,11 +85,12 @@ constexpr int kMaxSplit = 16;       // pieces per tile when tiles are fewer than
 template <int D>
 struct TcCfg {
   static constexpr int HALVES = D / 64;                 // 64-dim halves of a head
-  static constexpr int QB = HALVES * kTcRows * 128;     // one Q tile (hi or lo)
+  static constexpr int QSTAGE = D * 512;  // the next tile's Q staged: 128 rows x D x (high, low) f16
   static constexpr int KVB = HALVES * kChunk * 128;     // K (or V) of one chunk
   static constexpr int STAGE = 2 * KVB;                 // K and V of one chunk
   static constexpr int STAGES = D == 64 ? 4 : 2;
-  static constexpr int SMEM = 1024 + 2 * QB + STAGES * STAGE;
+  static constexpr int OSTAGE = kSoftWarps * 2048;      // output staging, 2 KB per softmax warp
+  static constexpr int SMEM = 1024 + QSTAGE + STAGES * STAGE + OSTAGE;
 };
 static_assert(TcCfg<128>::SMEM + 8 * 1024 <= 227 * 1024, "shared memory");
 static_assert(TcCfg<64>::SMEM + 8 * 1024 <= 227 * 1024, "shared memory");
@@ -218,35 +224,99 @@ struct RowOf {
   }
 };
 
-// Write the row's query as a high / low f16 pair into the two Q tiles (this
-// thread's half of the head dims; zeros for rows that hold no query).
+// Write the row's query as high / low f16 pairs into the Q columns of tensor
+// memory (this thread's half of the head dims, dims (2c, 2c + 1) in column
+// c of each; zeros for rows that hold no query).
 template <int D, int GP>
 __device__ __forceinline__ void write_q(const PrefillParams &p, const Tile &tl, int row, int hc,
-                                        uint8_t *qhi, uint8_t *qlo) {
+                                        uint32_t q_hi_t, uint32_t q_lo_t) {
   const RowOf<GP> r(p, tl, row);
-  const float *qrow = p.q + ((size_t)(r.ok ? r.i : 0) * p.Hq + (size_t)tl.kvh * p.G + r.hg) * D;
-#pragma unroll 4
-  for (int e = hc * (D / 2); e < (hc + 1) * (D / 2); e += 8) {
-    float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-    if (r.ok) {
-      x0 = *reinterpret_cast<const float4 *>(qrow + e);
-      x1 = *reinterpret_cast<const float4 *>(qrow + e + 4);
+  const float *qrow =
+      p.q + ((size_t)(r.ok ? r.i : 0) * p.Hq + (size_t)tl.kvh * p.G + r.hg) * D + hc * (D / 2);
+#pragma unroll
+  for (int w16 = 0; w16 < D / 4; w16 += 16) {  // 16 columns = 32 dims per step
+    uint32_t h[16], l[16];
+#pragma unroll
+    for (int j = 0; j < 16; j += 4) {
+      float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+      if (r.ok) {
+        x0 = *reinterpret_cast<const float4 *>(qrow + 2 * (w16 + j));
+        x1 = *reinterpret_cast<const float4 *>(qrow + 2 * (w16 + j) + 4);
+      }
+      uint32_t hh[4], ll[4];
+      split8(x0, x1, p.qscale, hh, ll);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        h[j + t] = hh[t];
+        l[j + t] = ll[t];
+      }
     }
-    uint32_t h[4], l[4];
-    const float qs = p.qscale;
-    split_h2(x0.x * qs, x0.y * qs, h[0], l[0]);
-    split_h2(x0.z * qs, x0.w * qs, h[1], l[1]);
-    split_h2(x1.x * qs, x1.y * qs, h[2], l[2]);
-    split_h2(x1.z * qs, x1.w * qs, h[3], l[3]);
-    const uint32_t off = (uint32_t)((e >> 6) * kTcRows * 128) + tc::sw128(row, (e & 63) >> 3);
-    *reinterpret_cast<uint4 *>(qhi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4 *>(qlo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+    tc::st16u(q_hi_t + w16, h);
+    tc::st16u(q_lo_t + w16, l);
   }
 }
 
-// Tensor maps of the two pools: [cell][128-byte chunk][64 f16], box (64, 1, bs).
+// Write this thread's DH-float half row (o, times `mul`; zeros when `zero`)
+// to `dst` (null: not stored), through the warp's 2 KB staging buffer `buf`.
+// Each pass moves four float4 of every row of the warp, transposed, so that
+// one store instruction writes 8 rows x 64 contiguous bytes (whole sectors)
+// rather than 32 rows' scattered 16-byte pieces: a tile's output leaves in
+// a quarter of the requests.
+template <int DH>
+__device__ __forceinline__ void store_half_rows(const float (&o)[DH], float mul, bool zero,
+                                                float *dst, float4 *buf, int lane) {
+  float *rows[4];  // the destination of row 8 k + lane / 4 of the warp
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    rows[k] = reinterpret_cast<float *>(
+        __shfl_sync(kAll, reinterpret_cast<unsigned long long>(dst), 8 * k + (lane >> 2)));
+#pragma unroll
+  for (int q = 0; q < DH / 16; ++q) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float *v = o + 16 * q + 4 * j;
+      buf[j * 32 + lane] = zero ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                : make_float4(v[0] * mul, v[1] * mul, v[2] * mul, v[3] * mul);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 v = buf[(lane & 3) * 32 + 8 * k + (lane >> 2)];
+      if (rows[k]) *reinterpret_cast<float4 *>(rows[k] + 16 * q + 4 * (lane & 3)) = v;
+    }
+    __syncwarp();
+  }
+}
+
+// One tensor store of box (32, heads, rows) from shared memory at `src`,
+// into the output at (dim x, head y, row z); tracked by this thread's bulk
+// group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z,
+                                             uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// This thread's bulk stores have read their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// This thread's bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Tensor maps of the two pools: [cell][128-byte chunk][64 f16], box (64, 1,
+// bs); and, when o_ok, of the output as [row][head][dim], box (32, G, 32 /
+// GP): the (query, head) rows one softmax warp holds.
 struct TcMaps {
-  CUtensorMap k, v;
+  CUtensorMap k, v, o;
+  int o_ok;
 };
 
 // SPLIT: the launch may cut tiles into pieces (records given); without it the
@@ -260,17 +330,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ int ts[kMaxPrefillSeqs + 1];
   __shared__ uint32_t tmem_slot;
-  __shared__ __align__(8) uint64_t k_full[ST], k_free[ST], v_full[ST], v_free[ST], s_full,
-      s_free, p_full[2], pv_done[2], q_full, o_free, drain[2];
+  __shared__ __align__(8) uint64_t k_full[ST], k_free[ST], v_full[ST], v_free[ST], s_full[2],
+      p_full[2], pv_done[2], q_full, o_free, drain[2];
   __shared__ uint64_t mask_s[2][ST][2];  // [K / V] staged rows that hold data (not a hole, < ctx)
   __shared__ uint64_t smask_s[2][2];     // the same for the chunk of S(x), by x % 2
   __shared__ float pm_s[2][2][kTcRows];  // partial row maxima: [chunk parity][half][row]
   __shared__ float pl_s[2][kTcRows];     // partial row sums at the tile end
   __shared__ int abort_s;
   uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t *qhi = base;
-  uint8_t *qlo = base + C::QB;
-  uint8_t *ring = base + 2 * C::QB;
+  uint8_t *qstage = base;  // the next tile's Q, staged
+  uint8_t *ring = base + C::QSTAGE;
   pdl_enter();
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -305,9 +374,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&v_full[k], 1);
       mbar_init(&v_free[k], 1);
     }
-    mbar_init(&s_full, 2);  // the MMAs' commit + the issuing thread (smask_s written)
-    mbar_init(&s_free, kSoftWarps);
     for (int k = 0; k < 2; ++k) {
+      mbar_init(&s_full[k], 2);  // the MMAs' commit + the issuing thread (smask_s written)
       mbar_init(&p_full[k], kSoftWarps);
       mbar_init(&pv_done[k], 1);
     }
@@ -433,8 +501,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr uint32_t idesc_s = tc::idesc_f16(kTcRows, kChunk, false);
     constexpr uint32_t idesc_o = tc::idesc_f16(kTcRows, D, true);
     // descriptor bases, advanced per operand by whole 16-byte units
-    const uint64_t d_qhi = tc::desc_sw128(smem_u32(qhi), 16, 1024);
-    const uint64_t d_qlo = tc::desc_sw128(smem_u32(qlo), 16, 1024);
     const uint64_t d_k = tc::desc_sw128(smem_u32(ring), 16, 1024);
     const uint64_t d_v = tc::desc_sw128(smem_u32(ring) + C::KVB, kChunk * 128, 1024);
     int g = 0;
@@ -449,11 +515,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int c = un.cb; c < un.ce; ++c) {
         const int x = g + (c - un.cb), st = x % ST;
         if (role == 0) {
-          // S(x) = Q_hi K^T + Q_lo K^T, once K of chunk x is staged and the
-          // softmax has loaded S(x - 1) (and read its row mask)
+          // S(x) = Q_hi K^T + Q_lo K^T into buffer x % 2, once K of chunk x
+          // is staged and P(x - 2) V has run (the softmax has then read
+          // S(x - 2) and its row mask, and P(x - 2) is no longer needed)
           if (!mbar_wait_bounded(&k_full[st], (uint32_t)(x / ST) & 1u, &abort_s, wait_ns) ||
-              (x >= 1 &&
-               !mbar_wait_bounded(&s_free, (uint32_t)(x - 1) & 1u, &abort_s, wait_ns))) {
+              (x >= 2 && !mbar_wait_bounded(&pv_done[x & 1], (uint32_t)((x - 2) >> 1) & 1u,
+                                            &abort_s, wait_ns))) {
             fine = false;
             break;
           }
@@ -464,19 +531,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             smask_s[x & 1][0] = mask_s[0][st][0];
             smask_s[x & 1][1] = mask_s[0][st][1];
             const uint64_t kd = tc::desc_advance(d_k, (uint32_t)(st * C::STAGE));
-            const uint32_t dcol = tmem;
+            const uint32_t dcol = tmem + (uint32_t)((x & 1) * kSCols);
 #pragma unroll
             for (int hf = 0; hf < C::HALVES; ++hf)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t qo = (uint32_t)(hf * kTcRows * 128 + kk * 32);
+                // dims [64 hf + 16 kk, + 16): Q columns 32 hf + 8 kk of each half
+                const uint32_t qc = (uint32_t)(hf * 32 + kk * 8);
                 const uint64_t bd = tc::desc_advance(kd, (uint32_t)(hf * kChunk * 128 + kk * 32));
-                tc::mma_f16(dcol, tc::desc_advance(d_qhi, qo), bd, idesc_s, hf + kk > 0);
-                tc::mma_f16(dcol, tc::desc_advance(d_qlo, qo), bd, idesc_s, true);
+                tc::mma_f16_ts(dcol, tmem + kQHiCol + qc, bd, idesc_s, hf + kk > 0);
+                tc::mma_f16_ts(dcol, tmem + kQLoCol + qc, bd, idesc_s, true);
               }
-            tc::commit(&s_full);
+            tc::commit(&s_full[x & 1]);
             tc::commit(&k_free[st]);
-            mbar_arrive(&s_full);
+            mbar_arrive(&s_full[x & 1]);
           }
           __syncwarp();
           continue;
@@ -507,14 +575,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc::fence_after();
         if (lane == 0) {
-          // O += P V (P from tensor memory; V MN-major: LBO = the distance
-          // between its 64-dim halves)
+          // O += P V (P from tensor memory, in S buffer x % 2: tokens
+          // [16 kk, 16 kk + 16) at column 64 (kk / 4) + 8 (kk % 4); V MN-major:
+          // LBO = the distance between its 64-dim halves)
           const uint64_t vd = tc::desc_advance(d_v, (uint32_t)(st * C::STAGE));
-          const uint32_t pa = tmem + (uint32_t)(kPCol + (x & 1) * (kChunk / 2));
+          const uint32_t pa = tmem + (uint32_t)((x & 1) * kSCols);
 #pragma unroll
           for (int kk = 0; kk < kChunk / 16; ++kk)
-            tc::mma_f16_ts(tmem + kOCol, pa + kk * 8, tc::desc_advance(vd, kk * 2048), idesc_o,
-                           c > un.cb || kk > 0);
+            tc::mma_f16_ts(tmem + kOCol, pa + (kk >> 2) * 64 + (kk & 3) * 8,
+                           tc::desc_advance(vd, kk * 2048), idesc_o, c > un.cb || kk > 0);
           tc::commit(&pv_done[x & 1]);
           tc::commit(&v_free[st]);
         }
@@ -531,6 +600,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int row = tid & (kTcRows - 1), hc = tid >> 7, pair = 1 + (warp & 3);
     const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // lanes of this row
     constexpr int HC = kChunk / 2;  // score columns per thread: [HC hc, HC hc + HC)
+    float4 *obuf = reinterpret_cast<float4 *>(ring + ST * C::STAGE) + warp * 128;
+    // this warp's region of the Q staging area: the next tile's Q slices of
+    // its threads during a tile, its output rows for the tensor stores at the
+    // tile's end (one 4 KB box per 32-dim block)
+    uint8_t *wreg = qstage + (size_t)warp * (C::QSTAGE / kSoftWarps);
+    bool ost_pending = false;  // tensor stores issued from wreg, maybe still reading it
+    auto ost_free = [&]() {
+      if (ost_pending) {
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+        ost_pending = false;
+      }
+    };
     // this row's record of unit u (split tiles): max, sum, destination, O
     auto record = [&](int u) -> float * {
       return p.rec + ((size_t)u * kTcRows + row) * (D + 4);
@@ -553,12 +635,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               make_float4(-INFINITY, 0.f, __int_as_float(dest_of(e.tl)), 0.f);
       }
     }
+    // this thread's Q columns in tensor memory: high / low pairs at columns
+    // kQHiCol / kQLoCol + hc * D / 4 + [0, D / 4)
+    const uint32_t q_hi_t = t_row + (uint32_t)(kQHiCol + hc * (D / 4));
+    const uint32_t q_lo_t = t_row + (uint32_t)(kQLoCol + hc * (D / 4));
     int u = blockIdx.x;
     Unit un;
     bool have = live_unit(u, un);
     if (have) {
-      write_q<D, GP>(p, un.tl, row, hc, qhi, qlo);
-      tc::fence_proxy_shared();
+      write_q<D, GP>(p, un.tl, row, hc, q_hi_t, q_lo_t);
+      tc::wait_st();
+      tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&q_full);
     }
@@ -580,11 +667,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + e));
         }
       }
-      // the next tile's Q, slice k = dims [8k, 8k + 8) of this thread's half row:
-      // high / low pairs at columns kQHiCol / kQLoCol + hc * D / 4 + 4k
+      // the next tile's Q, slice k = dims [8k, 8k + 8) of this thread's half
+      // row, staged in the warp's shared-memory region as 16-byte groups:
+      // high pairs in group k, low pairs in group NSL + k (group g of lane l
+      // at 512 g + 16 l, so a warp's accesses cover consecutive words)
       constexpr int NSL = D / 16;
-      const uint32_t q_hi_t = t_row + (uint32_t)(kQHiCol + hc * (D / 4));
-      const uint32_t q_lo_t = t_row + (uint32_t)(kQLoCol + hc * (D / 4));
+      uint4 *qst = reinterpret_cast<uint4 *>(wreg) + lane;
       auto load_slice = [&](int k, float4 &a, float4 &b) {
         a = b = make_float4(0.f, 0.f, 0.f, 0.f);
         if (qn) {
@@ -595,8 +683,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       auto store_slice = [&](int k, const float4 &a, const float4 &b) {
         uint32_t h[4], l[4];
         split8(a, b, p.qscale, h, l);
-        tc::st4u(q_hi_t + 4 * k, h[0], h[1], h[2], h[3]);
-        tc::st4u(q_lo_t + 4 * k, l[0], l[1], l[2], l[3]);
+        qst[k * 32] = make_uint4(h[0], h[1], h[2], h[3]);
+        qst[(NSL + k) * 32] = make_uint4(l[0], l[1], l[2], l[3]);
       };
       const RowOf<GP> rw(p, tl, row);
       if (hc == 0 && rw.j < tl.n && rw.hg < p.G && !rw.in)
@@ -628,57 +716,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float4 qa, qb;
         if (slice) load_slice(lc, qa, qb);
         // ---- S(x) complete
-        fine = mbar_wait_bounded(&s_full, (uint32_t)x & 1u, &abort_s, wait_ns) && fine;
+        fine = mbar_wait_bounded(&s_full[x & 1], (uint32_t)(x >> 1) & 1u, &abort_s, wait_ns) &&
+               fine;
         tc::fence_after();
         if (last && have_next) {
-          // every S of this tile is done: the rest of the next tile's Q is
-          // staged, then all of it moves into the shared Q tiles
+          // every S of this tile is done, so its Q columns are free: the
+          // rest of the next tile's Q is staged, then all of it moves into
+          // the Q columns
+          ost_free();
           for (int k = lc; k < NSL; ++k) {
             float4 a, b;
             load_slice(k, a, b);
             store_slice(k, a, b);
           }
-          tc::wait_st();
 #pragma unroll
           for (int half = 0; half < 2; ++half) {  // high, then low
-            uint8_t *qt = half ? qlo : qhi;
-            const uint32_t src = half ? q_lo_t : q_hi_t;
+            const uint32_t dst = half ? q_lo_t : q_hi_t;
 #pragma unroll
             for (int w16 = 0; w16 < D / 4; w16 += 16) {
-              float v[16];
-              tc::ld16(src + w16, v);
-              tc::wait_ld();
+              uint32_t w[16];
 #pragma unroll
-              for (int j = 0; j < 16; j += 4) {
-                const int e = hc * (D / 2) + 2 * (w16 + j);  // first of the 8 dims
-                const uint32_t off =
-                    (uint32_t)((e >> 6) * kTcRows * 128) + tc::sw128(row, (e & 63) >> 3);
-                *reinterpret_cast<uint4 *>(qt + off) =
-                    make_uint4(__float_as_uint(v[j]), __float_as_uint(v[j + 1]),
-                               __float_as_uint(v[j + 2]), __float_as_uint(v[j + 3]));
+              for (int j = 0; j < 4; ++j) {
+                const uint4 gq = qst[(half * NSL + w16 / 4 + j) * 32];
+                w[4 * j] = gq.x;
+                w[4 * j + 1] = gq.y;
+                w[4 * j + 2] = gq.z;
+                w[4 * j + 3] = gq.w;
               }
+              tc::st16u(dst + w16, w);
             }
           }
-          tc::fence_proxy_shared();
+          tc::wait_st();
+          tc::fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&q_full);
         }
-        // ---- S(x): load this thread's 64 columns, then hand the buffer back
+        // ---- S(x): this thread's 64 columns of buffer x % 2 into registers
+        const uint32_t s_row = t_row + (uint32_t)((x & 1) * kSCols + hc * HC);
         float sv[HC];
 #pragma unroll
         for (int c16 = 0; c16 < HC; c16 += 16) {
           float v[16];
-          tc::ld16(t_row + (uint32_t)(hc * HC + c16), v);
+          tc::ld16(s_row + (uint32_t)c16, v);
 #pragma unroll
           for (int e = 0; e < 16; ++e) sv[c16 + e] = v[e];
         }
         const uint64_t vm = smask_s[x & 1][hc];
-        // P tile x % 2 is free once P(x-2) V has run: polled now, used below
-        const bool p_free = x < 2 || mbar_try_wait(&pv_done[x & 1], (uint32_t)((x - 2) >> 1) & 1u);
         tc::wait_ld();
-        tc::fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free);
         // ---- mask: the row's window, then the staged rows that hold data
         const int pos0 = c * kChunk + hc * HC;  // position of this thread's first column
         uint64_t mk = 0;
@@ -742,14 +826,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc::wait_st();
         }
-        // ---- probabilities into P tile x % 2
-        if (!p_free)
-          fine = mbar_wait_bounded(&pv_done[x & 1], (uint32_t)((x - 2) >> 1) & 1u, &abort_s,
-                                   wait_ns) &&
-                 fine;
+        // ---- probabilities over this thread's own (already loaded) scores
         float ls[4] = {0.f, 0.f, 0.f, 0.f};  // two packed pairs of partial sums
         const float mr = m_run == -INFINITY ? 0.f : m_run;  // all sv are -inf then: p = 0
-        const uint32_t p_row = t_row + (uint32_t)(kPCol + (x & 1) * (kChunk / 2) + hc * (HC / 2));
+        const uint32_t p_row = s_row;
 #pragma unroll
         for (int e = 0; e < HC; e += 32) {
           uint32_t h[16];
@@ -768,7 +848,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[x & 1]);
-        if (slice) store_slice(lc, qa, qb);
+        if (slice) {
+          ost_free();
+          store_slice(lc, qa, qb);
+        }
       }
       if (!fine) break;
       const int x_last = g + (un.ce - un.cb) - 1;
@@ -802,10 +885,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (n_split > 1) {
         // a piece of a split tile: the unnormalised record, merged later
         float *rr = record(u);
-#pragma unroll
-        for (int e = 0; e < DH; e += 4)
-          *reinterpret_cast<float4 *>(rr + 4 + hc * DH + e) =
-              make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+        store_half_rows<DH>(o, 1.f, false, rr + 4 + hc * DH, obuf, lane);
         if (hc == 0)
           *reinterpret_cast<float4 *>(rr) =
               make_float4(m_run, l_row, __int_as_float(dest_of(tl)), 0.f);
@@ -816,13 +896,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       const bool any = l_row > 0.f;
       const float inv = any ? 1.f / l_row : 0.f;
-      if (rw.in) {
-        float *dst = p.out + ((size_t)rw.i * p.Hq + (size_t)tl.kvh * p.G + rw.hg) * D + hc * DH;
+      // the warp's 32 rows are QW whole queries of the tile: when all are
+      // queries of the sequence, its rows leave by tensor stores from its
+      // region (box row (query, head) = (lane / GP, lane % GP) packed over
+      // the G real heads; 16-byte chunk c of box row k at c ^ (k % 8), the
+      // 128-byte swizzle), so the warp moves on without waiting for them
+      constexpr int QW = 32 / GP;
+      const int jq0 = tl.qt * TQ + (warp & 3) * QW;
+      const int i0 = p.q_start[tl.s] + jq0;  // the warp's first query row
+      if (maps.o_ok && jq0 + QW <= tl.n && i0 >= 0 && i0 + QW <= p.n_tok) {
+        ost_free();
+        const int k = (lane / GP) * p.G + rw.hg;
+        if (rw.hg < p.G) {
 #pragma unroll
-        for (int e = 0; e < DH; e += 4)
-          *reinterpret_cast<float4 *>(dst + e) =
-              any ? make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv)
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int j = 0; j < DH / 32; ++j) {
+            uint8_t *brow = wreg + j * 4096 + k * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const float *v = o + 32 * j + 4 * c;
+              *reinterpret_cast<float4 *>(brow + ((c ^ (k & 7)) << 4)) =
+                  any ? make_float4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+        }
+        tc::fence_proxy_shared();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int j = 0; j < DH / 32; ++j)
+            tma_store_3d(&maps.o, hc * DH + 32 * j, tl.kvh * p.G, i0, smem_u32(wreg + j * 4096));
+          bulk_commit();
+        }
+        ost_pending = true;
+      } else {
+        store_half_rows<DH>(
+            o, inv, !any,
+            rw.in ? p.out + ((size_t)rw.i * p.Hq + (size_t)tl.kvh * p.G + rw.hg) * D + hc * DH
+                  : nullptr,
+            obuf, lane);
       }
       if (rw.in && p.lse && hc == 0)
         p.lse[(size_t)rw.i * p.Hq + (size_t)tl.kvh * p.G + rw.hg] =
@@ -831,6 +943,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       u = u2;
       have = have_next;
     }
+    // the output's tensor stores land before the CTA (and its shared memory) ends
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   if (!fine) {
     abort_s = 1;  // the other roles stop waiting within a few polls
@@ -955,6 +1070,15 @@ mt_status launch_prefill_tc(const PrefillParams &p, int head_dim, int gp, int n_
   if (st != MT_OK) return st;
   st = encode_pool_map_3d(&m.v, p.v_pool, n_cells, (size_t)p.row_bytes, 1, p.bs);
   if (st != MT_OK) return st;
+  // the output by tensor stores when it is 16-byte aligned (else every row
+  // is stored by the softmax threads themselves)
+  m.o_ok = 0;
+  if ((reinterpret_cast<uintptr_t>(p.out) & 15u) == 0 && p.n_tok > 0) {
+    const int gpe = gp == 1 || gp == 2 || gp == 4 ? gp : 8;  // as launch_g instantiates
+    st = encode_out_map_f32(&m.o, p.out, p.n_tok, p.Hq, head_dim, p.G, 32 / gpe);
+    if (st != MT_OK) return st;
+    m.o_ok = 1;
+  }
   return head_dim == 64 ? launch_d<64>(gp, p, m, n_ctas, stream)
                         : launch_d<128>(gp, p, m, n_ctas, stream);
 }

@@ -78,3 +78,18 @@ def test_prefill_tc_more_sequences_than_one_launch(mt):
     q, q_start = make_queries(w, rng, 6)
     kp, vp = oracle_pools(w)
     check_pools(mt, w, q, q_start, kp, vp)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(12, 2, 128), (6, 2, 128), (16, 8, 64), (8, 8, 128)])
+def test_prefill_tc_output_boxes(mt, hq, hkv, d):
+    # a softmax warp's 32 rows are 32 / GP whole queries; when all are queries
+    # of the sequence they leave by tensor stores of box (32 dims, G heads,
+    # 32 / GP queries), else by the threads' own stores: query groups of 6
+    # and 3 (padded to 8 and 4: the box packs the real heads), 2 and 1, with
+    # query counts that end sequences inside a warp's block
+    rng = np.random.default_rng(84 + hq + d)
+    w = workloads.llama3_f16(seed=84 + hq + d, n_seqs=4, ctx_lo=300, ctx_hi=700, n_heads=hq,
+                             n_kv_heads=hkv, head_dim=d)
+    q, q_start = make_queries(w, rng, 150)
+    kp, vp = oracle_pools(w)
+    check_pools(mt, w, q, q_start, kp, vp)
