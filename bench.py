@@ -804,8 +804,9 @@ def run_extra(args, rank, world, local_rank):
         # fewer than the SMs)
         long_ = args.workload == "prefill_f16_long"
         n_seqs_p, ctx_p, n_q = (1, 32768, 256) if long_ else (16, 2048, 512)
+        pfmt = args.prefill_format
         w = workloads.llama3_f16(seed=SEED + 9, n_seqs=n_seqs_p, ctx_lo=ctx_p, ctx_hi=ctx_p,
-                                 hist=False)
+                                 hist=False, fmt=pfmt)
         layers, _, rb = _decode_setup(mtkv, w, 8, dev, g)
         table = torch.from_numpy(w.block_table).to(dev)
         ctx_d = torch.from_numpy(w.context_lens).to(dev)
@@ -814,7 +815,7 @@ def run_extra(args, rank, world, local_rank):
         for kp, vp, _a, _kn in layers:
             q = torch.randn(n_q * w.n_seqs, w.n_heads, w.head_dim, generator=g, device=dev)
             out = torch.empty_like(q)
-            a = mtkv.prefill_args("f16", q, kp, vp, table, ctx_d, q_start, out,
+            a = mtkv.prefill_args(pfmt, q, kp, vp, table, ctx_d, q_start, out,
                                   n_kv_heads=w.n_kv_heads, block_size=w.block_size,
                                   n_phys_blocks=w.n_phys_blocks, scale=w.scale)
             calls.append(a)
@@ -835,10 +836,11 @@ def run_extra(args, rank, world, local_rank):
         ctx0 = int(w.context_lens[0])
         pairs = w.n_seqs * sum(ctx0 - n_q + j + 1 for j in range(n_q))
         flop = 4.0 * pairs * w.n_heads * w.head_dim
-        kv_bytes = 2 * int(w.context_lens.sum()) * w.n_kv_heads * w.head_dim * 2
+        kv_bytes = 2 * int(w.context_lens.sum()) * rb
         tflops = len(calls) * flop / (ms * 1e-3) / 1e12
         tpeak = _tensor_peak()
-        res = {"metric": "paged prefill attention TFLOP/s (f16 operands, f32 accumulate)",
+        res = {"metric": "paged prefill attention TFLOP/s (f16 operands, f32 accumulate)"
+                         + ("" if pfmt == "f16" else f", {pfmt} pools"),
                "value": round(tflops, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
                "step_ms": sp,
                "ms_per_call": round(ms / len(calls), 5),
@@ -849,7 +851,7 @@ def run_extra(args, rank, world, local_rank):
                             "note": "useful FLOPs (4 * pairs * heads * head_dim); the kernel "
                                     "also multiplies the low half of q and padding rows"},
                "kv_GB_per_s": round(len(calls) * kv_bytes / (ms * 1e-3) / 1e9, 1),
-               "config": {"workload": f"llama3-8b-shaped f16 chunked prefill: {n_seqs_p} "
+               "config": {"workload": f"llama3-8b-shaped {pfmt} chunked prefill: {n_seqs_p} "
                                       f"seqs x ctx {ctx_p}, last {n_q} positions as "
                                       "queries, 32/8 heads, head_dim 128, bs 16, 8 layers"},
                "clocks": clk}
@@ -921,6 +923,9 @@ def main():
                     choices=["llama3_f16", "smollm2_f32", "q8_prefix", "longctx_int4",
                              "llama3_formats", "prefill_f16", "prefill_f16_long"],
                     help="llama3_f16 is the benchmark line; the others measure the other kernels")
+    ap.add_argument("--prefill-format", default="f16", choices=["f16", "q8_0", "f32"],
+                    help="KV pool format of the prefill workloads (f16: the tcgen05 kernel; "
+                         "q8_0 and f32: the mma.sync multi-query kernel)")
     ap.add_argument("--store", default=None, choices=["fused", "separate"],
                     help="store each layer's new row inside the decode launch "
                          "(mt_paged_attn_decode_append) or with its own mt_kv_store launch; "

@@ -39,7 +39,22 @@ constexpr uint64_t kPrefillWsBytes = 256;
 // (the kernel splits only while tiles are fewer than CTAs).
 constexpr int kSplitCtas = 160;
 
-// Bytes of split records a call may need: 0 unless the f16 tensor-core kernel
+// q8_0 pools on the tcgen05 kernel: the call's blocks staged as f16 rows
+// (launch_stage_q8_f16): a table of n_seqs x max_blocks staged ids, then the
+// K and the V f16 pools of n_seqs x max_blocks x block_size rows. 0 when the
+// call does not stage (other formats and shapes; staged ids that would not
+// fit the kernel's 32-bit cell indices: the mma.sync kernel runs instead).
+size_t q8_stage_bytes(const mt_paged_prefill_args *a) {
+  if (a->fmt != MT_KV_Q8_0 || !prefill_tc_supported(a->fmt, a->head_dim, a->block_size))
+    return 0;
+  const long long cells = (long long)a->n_seqs * a->max_blocks * a->block_size;
+  if (cells <= 0 || cells >= (1LL << 31)) return 0;
+  auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  return up((size_t)a->n_seqs * a->max_blocks * 4) +
+         2 * up((size_t)cells * a->n_kv_heads * a->head_dim * 2);
+}
+
+// Bytes of split records a call may need: 0 unless the tensor-core kernel
 // runs and the query count leaves fewer tiles than kSplitCtas (every sequence
 // has at least ceil(n_s / TQ) tiles per KV head, so the tile count is at
 // least Hkv * ceil(n_tokens / TQ)).
@@ -346,7 +361,7 @@ using namespace mtkv;
 extern "C" size_t mt_paged_prefill_workspace_bytes(const mt_paged_prefill_args *a) {
   if (!a) return 0;
   const int G = a->n_kv_heads > 0 && a->n_heads % a->n_kv_heads == 0 ? a->n_heads / a->n_kv_heads : 0;
-  return kPrefillWsBytes + prefill_rec_bytes(a, G > 0 ? pad_g(G) : 0);
+  return kPrefillWsBytes + prefill_rec_bytes(a, G > 0 ? pad_g(G) : 0) + q8_stage_bytes(a);
 }
 
 extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void *workspace,
@@ -376,11 +391,14 @@ extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void 
       !a->out)
     return fail(MT_ERR_INVALID_ARG, "prefill: null pointer");
   const size_t rec_bytes = prefill_rec_bytes(a, GP);
-  if (!workspace || workspace_bytes < kPrefillWsBytes + rec_bytes)
+  const size_t stage_bytes = q8_stage_bytes(a);
+  const size_t need = kPrefillWsBytes + rec_bytes + stage_bytes;
+  if (!workspace || workspace_bytes < need)
     return fail(MT_ERR_INVALID_ARG, "prefill: workspace missing or too small (need " +
-                                        std::to_string(kPrefillWsBytes + rec_bytes) + " bytes)");
-  if (!aligned16(a->k_pool) || !aligned16(a->v_pool) || !aligned16(a->q) || !aligned16(a->out))
-    return fail(MT_ERR_INVALID_ARG, "prefill: q, pools and out must be 16-byte aligned");
+                                        std::to_string(need) + " bytes)");
+  if (!aligned16(a->k_pool) || !aligned16(a->v_pool) || !aligned16(a->q) || !aligned16(a->out) ||
+      !aligned16(workspace))
+    return fail(MT_ERR_INVALID_ARG, "prefill: q, pools, out and workspace must be 16-byte aligned");
   DeviceInfo di;
   mt_status st = device_info(&di);
   if (st != MT_OK) return st;
@@ -412,17 +430,37 @@ extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void 
     p.rec_units = 2 * kSplitCtas;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // f16 pools, and q8_0 pools staged as f16 rows, run the tcgen05 kernel
+  const bool tc = a->fmt == MT_KV_F16 ? prefill_tc_supported(a->fmt, a->head_dim, a->block_size)
+                                      : stage_bytes > 0;
+  const int32_t *table = a->block_table;
+  if (stage_bytes) {
+    uint8_t *ws = static_cast<uint8_t *>(workspace) + kPrefillWsBytes + rec_bytes;
+    const size_t tb = ((size_t)a->n_seqs * a->max_blocks * 4 + 255) & ~(size_t)255;
+    const size_t pb = (stage_bytes - tb) / 2;
+    int32_t *table16 = reinterpret_cast<int32_t *>(ws);
+    uint8_t *k16 = ws + tb, *v16 = ws + tb + pb;
+    st = launch_stage_q8_f16(p.k_pool, p.v_pool, a->block_table, a->context_lens, a->n_seqs,
+                             a->max_blocks, a->block_size, a->n_phys_blocks, a->n_kv_heads,
+                             a->head_dim, (int)rb, k16, v16, table16, p.status, di.n_sm * 4, s);
+    if (st != MT_OK) return st;
+    table = table16;
+    p.k_pool = k16;
+    p.v_pool = v16;
+    p.n_phys = (long long)a->n_seqs * a->max_blocks;
+    p.row_bytes = a->n_kv_heads * a->head_dim * 2;
+  }
   // sequences are independent: launch in chunks of kMaxPrefillSeqs (query
   // rows stay absolute, so only the per-sequence arrays are offset)
   for (int s0 = 0; s0 < a->n_seqs; s0 += kMaxPrefillSeqs) {
     p.B = std::min(kMaxPrefillSeqs, a->n_seqs - s0);
-    p.table = a->block_table + (size_t)s0 * a->max_blocks;
+    p.table = table + (size_t)s0 * a->max_blocks;
     p.ctx = a->context_lens + s0;
     p.q_start = a->q_start + s0;
-    if (prefill_tc_supported(a->fmt, a->head_dim, a->block_size)) {
-      // f16 pools: the tcgen05 kernel, one CTA (all 512 tensor-memory
-      // columns, ~198 KB of shared memory for head_dim 128) per SM, then the
-      // merge of split tiles (returns at once when nothing was split)
+    if (tc) {
+      // the tcgen05 kernel, one CTA (all 512 tensor-memory columns, ~198 KB
+      // of shared memory for head_dim 128) per SM, then the merge of split
+      // tiles (returns at once when nothing was split)
       st = launch_prefill_tc(p, a->head_dim, GP, di.n_sm, s);
       if (st != MT_OK) return st;
       st = launch_prefill_tc_combine(p, a->head_dim, di.n_sm, s);

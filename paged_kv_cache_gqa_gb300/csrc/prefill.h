@@ -38,8 +38,23 @@ struct PrefillParams {
   int rec_units;
 };
 
-// tcgen05 prefill kernel (f16 pools, head_dim 64 or 128, block_size 16 or 32).
+// tcgen05 prefill kernel (f16 pools, head_dim 64 or 128, block_size 16 or 32;
+// q8_0 pools of those shapes through rows staged as f16, below).
 bool prefill_tc_supported(mt_kv_format fmt, int head_dim, int block_size);
+
+// q8_0 pools on the tcgen05 kernel: the blocks a prefill call reads, staged
+// as f16 rows. Block b of sequence s (of the n_seqs sequences of `table`,
+// max_blocks entries each) becomes staged block s * max_blocks + b: its bs
+// rows of n_kv_heads * head_dim values, value = code * scale rounded once to
+// the nearest f16, are written to k16 / v16 (rows of n_kv_heads * head_dim * 2
+// bytes), and table16[s][b] = that id; holes, blocks past the context and
+// out-of-range ids (flagged in *status) become -1. A staged value beyond the
+// f16 range is flagged too (it reads as infinite).
+mt_status launch_stage_q8_f16(const uint8_t *k_pool, const uint8_t *v_pool, const int32_t *table,
+                              const int32_t *ctx, int n_seqs, int max_blocks, int bs,
+                              long long n_phys, int n_kv_heads, int head_dim, int row_bytes,
+                              uint8_t *k16, uint8_t *v16, int32_t *table16, uint32_t *status,
+                              int n_ctas, cudaStream_t stream);
 // Merge the split pieces' records of the last tcgen05 launch (returns at once
 // when it did not split).
 mt_status launch_prefill_tc_combine(const PrefillParams &p, int head_dim, int n_ctas,

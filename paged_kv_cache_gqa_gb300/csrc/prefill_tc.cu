@@ -63,18 +63,20 @@ namespace {
 
 constexpr unsigned kAll = 0xffffffffu;
 constexpr int kTcRows = 128;       // rows per tile = tensor-memory lanes
-constexpr int kSoftWarps = 8;      // two threads per row
-constexpr int kLoadWarpK = 8;
-constexpr int kLoadWarpV = 9;
-constexpr int kMmaWarpS = 10;   // issues S = Q K^T
-constexpr int kMmaWarpO = 11;   // issues O += P V
-constexpr int kTcThreads = 384;
-constexpr int kChunk = 128;        // tokens per chunk
+constexpr int kTPR = 2;                    // softmax threads per row
+constexpr int kSoftWarps = 4 * kTPR;       // warps w, w + 4, ... share lanes 32 (w % 4) ..
+constexpr int kLoadWarpK = kSoftWarps;
+constexpr int kLoadWarpV = kSoftWarps + 1;
+constexpr int kMmaWarpS = kSoftWarps + 2;  // issues S = Q K^T
+constexpr int kMmaWarpO = kSoftWarps + 3;  // issues O += P V
+constexpr int kTcThreads = 32 * (kSoftWarps + 4);
+constexpr int kChunk = 128;                // tokens per chunk
+constexpr int kHC = kChunk / kTPR;         // score columns per softmax thread
 // tensor-memory columns: S double buffer [0, 128), [128, 256) (S(x) in buffer
 // x % 2; P(x) as f16 pairs over the scores it came from: the thread owning
-// score columns [64 h, 64 h + 64) writes their 32 probability pairs to
-// [64 h, 64 h + 32)); O [256, 256 + d); the tile's Q as f16 pairs (the A
-// operand of S), high [384, 384 + d / 2) and low [448, 448 + d / 2)
+// score columns [kHC h, kHC h + kHC) writes their kHC / 2 probability pairs
+// to [kHC h, kHC h + kHC / 2)); O [256, 256 + d); the tile's Q as f16 pairs
+// (the A operand of S), high [384, 384 + d / 2) and low [448, 448 + d / 2)
 constexpr int kSCols = kChunk;
 constexpr int kOCol = 2 * kChunk;
 constexpr int kQHiCol = 384;
@@ -89,11 +91,19 @@ struct TcCfg {
   static constexpr int KVB = HALVES * kChunk * 128;     // K (or V) of one chunk
   static constexpr int STAGE = 2 * KVB;                 // K and V of one chunk
   static constexpr int STAGES = D == 64 ? 4 : 2;
-  static constexpr int OSTAGE = kSoftWarps * 2048;      // output staging, 2 KB per softmax warp
-  static constexpr int SMEM = 1024 + QSTAGE + STAGES * STAGE + OSTAGE;
+  static constexpr int SMEM = 1024 + QSTAGE + STAGES * STAGE;
+  // per softmax thread: dims of its part of the row (Q and O), Q slices of 8
+  // dims; its warp's region of the Q staging area, and the output box
+  // width (dims) of the tensor stores
+  static constexpr int DT = D / kTPR;
+  static constexpr int NSL = DT / 8;
+  static constexpr int REGION = QSTAGE / kSoftWarps;
+  static constexpr int CB = DT < 32 ? DT : 32;
+  static_assert(REGION >= 2 * NSL * 512 && REGION >= (DT / CB) * 32 * CB * 4, "staging region");
+  static_assert(DT >= 16 && (CB == 16 || CB == 32), "output box");
 };
-static_assert(TcCfg<128>::SMEM + 8 * 1024 <= 227 * 1024, "shared memory");
-static_assert(TcCfg<64>::SMEM + 8 * 1024 <= 227 * 1024, "shared memory");
+static_assert(TcCfg<128>::SMEM + 12 * 1024 <= 227 * 1024, "shared memory");
+static_assert(TcCfg<64>::SMEM + 12 * 1024 <= 227 * 1024, "shared memory");
 
 // 2^x by the hardware approximation (relative error ~2^-22, 2^-inf = 0):
 // far below the f16 rounding the probabilities get right after.
@@ -137,14 +147,27 @@ __device__ __forceinline__ void tma_rows(uint32_t dst, const CUtensorMap *map, i
       : "memory");
 }
 
-// Two-warp named barrier (ids 1..4: warps w and w + 4) that also ANDs a flag.
+// Named barrier of the kTPR warps that share a row quarter (ids 1..4: warps
+// w, w + 4, ...) that also ORs a flag.
+__device__ __forceinline__ bool pair_vote_or(int id, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; barrier.red.or.pred q, %2, %3, p; "
+      "selp.u32 %0, 1, 0, q; }"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(id), "n"(32 * kTPR)
+      : "memory");
+  return r != 0;
+}
+
+// The same barrier, ANDing a flag.
 __device__ __forceinline__ bool pair_sync_and(int id, bool v) {
   uint32_t r;
   asm volatile(
-      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; barrier.red.and.pred q, %2, 64, p; "
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; barrier.red.and.pred q, %2, %3, p; "
       "selp.u32 %0, 1, 0, q; }"
       : "=r"(r)
-      : "r"(v ? 1u : 0u), "r"(id)
+      : "r"(v ? 1u : 0u), "r"(id), "n"(32 * kTPR)
       : "memory");
   return r != 0;
 }
@@ -224,71 +247,64 @@ struct RowOf {
   }
 };
 
+// W consecutive 32-bit tensor-memory columns of this thread's lane (W a
+// multiple of 8).
+template <int W>
+__device__ __forceinline__ void st_words(uint32_t taddr, const uint32_t (&w)[W]) {
+  if constexpr (W % 16 == 0) {
+#pragma unroll
+    for (int b = 0; b < W; b += 16) tc::st16u(taddr + b, *reinterpret_cast<const uint32_t(*)[16]>(w + b));
+  } else {
+    static_assert(W == 8, "column count");
+    tc::st8u(taddr, w);
+  }
+}
+
 // Write the row's query as high / low f16 pairs into the Q columns of tensor
-// memory (this thread's half of the head dims, dims (2c, 2c + 1) in column
-// c of each; zeros for rows that hold no query).
+// memory (this thread's D / kTPR dims, dims (2c, 2c + 1) in column c of
+// each; zeros for rows that hold no query).
 template <int D, int GP>
 __device__ __forceinline__ void write_q(const PrefillParams &p, const Tile &tl, int row, int hc,
                                         uint32_t q_hi_t, uint32_t q_lo_t) {
+  constexpr int DT = D / kTPR, W = DT / 2;
   const RowOf<GP> r(p, tl, row);
   const float *qrow =
-      p.q + ((size_t)(r.ok ? r.i : 0) * p.Hq + (size_t)tl.kvh * p.G + r.hg) * D + hc * (D / 2);
+      p.q + ((size_t)(r.ok ? r.i : 0) * p.Hq + (size_t)tl.kvh * p.G + r.hg) * D + hc * DT;
+  uint32_t h[W], l[W];
 #pragma unroll
-  for (int w16 = 0; w16 < D / 4; w16 += 16) {  // 16 columns = 32 dims per step
-    uint32_t h[16], l[16];
-#pragma unroll
-    for (int j = 0; j < 16; j += 4) {
-      float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-      if (r.ok) {
-        x0 = *reinterpret_cast<const float4 *>(qrow + 2 * (w16 + j));
-        x1 = *reinterpret_cast<const float4 *>(qrow + 2 * (w16 + j) + 4);
-      }
-      uint32_t hh[4], ll[4];
-      split8(x0, x1, p.qscale, hh, ll);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        h[j + t] = hh[t];
-        l[j + t] = ll[t];
-      }
+  for (int j = 0; j < W; j += 4) {  // 8 dims per step
+    float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+    if (r.ok) {
+      x0 = *reinterpret_cast<const float4 *>(qrow + 2 * j);
+      x1 = *reinterpret_cast<const float4 *>(qrow + 2 * j + 4);
     }
-    tc::st16u(q_hi_t + w16, h);
-    tc::st16u(q_lo_t + w16, l);
+    uint32_t hh[4], ll[4];
+    split8(x0, x1, p.qscale, hh, ll);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      h[j + t] = hh[t];
+      l[j + t] = ll[t];
+    }
   }
+  st_words<W>(q_hi_t, h);
+  st_words<W>(q_lo_t, l);
 }
 
-// Write this thread's DH-float half row (o, times `mul`; zeros when `zero`)
-// to `dst` (null: not stored), through the warp's 2 KB staging buffer `buf`.
-// Each pass moves four float4 of every row of the warp, transposed, so that
-// one store instruction writes 8 rows x 64 contiguous bytes (whole sectors)
-// rather than 32 rows' scattered 16-byte pieces: a tile's output leaves in
-// a quarter of the requests.
-template <int DH>
-__device__ __forceinline__ void store_half_rows(const float (&o)[DH], float mul, bool zero,
-                                                float *dst, float4 *buf, int lane) {
-  float *rows[4];  // the destination of row 8 k + lane / 4 of the warp
+// This thread's DT output values (o, times `mul`; zeros when `zero`) to
+// `dst` (null: not stored), by the thread's own 16-byte stores: rows that
+// the output's tensor stores do not take (a warp's block of queries that
+// runs past its sequence) and the pieces of split tiles.
+template <int DT>
+__device__ __forceinline__ void store_part(const float (&o)[DT], float mul, bool zero, float *dst) {
+  if (!dst) return;
 #pragma unroll
-  for (int k = 0; k < 4; ++k)
-    rows[k] = reinterpret_cast<float *>(
-        __shfl_sync(kAll, reinterpret_cast<unsigned long long>(dst), 8 * k + (lane >> 2)));
-#pragma unroll
-  for (int q = 0; q < DH / 16; ++q) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float *v = o + 16 * q + 4 * j;
-      buf[j * 32 + lane] = zero ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                : make_float4(v[0] * mul, v[1] * mul, v[2] * mul, v[3] * mul);
-    }
-    __syncwarp();
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float4 v = buf[(lane & 3) * 32 + 8 * k + (lane >> 2)];
-      if (rows[k]) *reinterpret_cast<float4 *>(rows[k] + 16 * q + 4 * (lane & 3)) = v;
-    }
-    __syncwarp();
-  }
+  for (int e = 0; e < DT; e += 4)
+    *reinterpret_cast<float4 *>(dst + e) =
+        zero ? make_float4(0.f, 0.f, 0.f, 0.f)
+             : make_float4(o[e] * mul, o[e + 1] * mul, o[e + 2] * mul, o[e + 3] * mul);
 }
 
-// One tensor store of box (32, heads, rows) from shared memory at `src`,
+// One tensor store of box (CB, heads, rows) from shared memory at `src`,
 // into the output at (dim x, head y, row z); tracked by this thread's bulk
 // group.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z,
@@ -312,8 +328,8 @@ __device__ __forceinline__ void bulk_wait_all() {
 }
 
 // Tensor maps of the two pools: [cell][128-byte chunk][64 f16], box (64, 1,
-// bs); and, when o_ok, of the output as [row][head][dim], box (32, G, 32 /
-// GP): the (query, head) rows one softmax warp holds.
+// bs); and, when o_ok, of the output as [row][head][dim], box (CB, G, 32 /
+// GP): a block of the (query, head) rows one softmax warp holds.
 struct TcMaps {
   CUtensorMap k, v, o;
   int o_ok;
@@ -334,8 +350,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       p_full[2], pv_done[2], q_full, o_free, drain[2];
   __shared__ uint64_t mask_s[2][ST][2];  // [K / V] staged rows that hold data (not a hole, < ctx)
   __shared__ uint64_t smask_s[2][2];     // the same for the chunk of S(x), by x % 2
-  __shared__ float pm_s[2][2][kTcRows];  // partial row maxima: [chunk parity][half][row]
-  __shared__ float pl_s[2][kTcRows];     // partial row sums at the tile end
+  __shared__ float pm_s[2][kTPR][kTcRows];  // partial row maxima: [chunk parity][part][row]
+  __shared__ float pl_s[kTPR][kTcRows];     // partial row sums at the tile end
   __shared__ int abort_s;
   uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *qstage = base;  // the next tile's Q, staged
@@ -576,13 +592,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::fence_after();
         if (lane == 0) {
           // O += P V (P from tensor memory, in S buffer x % 2: tokens
-          // [16 kk, 16 kk + 16) at column 64 (kk / 4) + 8 (kk % 4); V MN-major:
-          // LBO = the distance between its 64-dim halves)
+          // [16 kk, 16 kk + 16) at column kHC (kk / J) + 8 (kk % J), J = kHC /
+          // 16 K steps per softmax thread's columns; V MN-major: LBO = the
+          // distance between its 64-dim halves)
           const uint64_t vd = tc::desc_advance(d_v, (uint32_t)(st * C::STAGE));
           const uint32_t pa = tmem + (uint32_t)((x & 1) * kSCols);
 #pragma unroll
           for (int kk = 0; kk < kChunk / 16; ++kk)
-            tc::mma_f16_ts(tmem + kOCol, pa + (kk >> 2) * 64 + (kk & 3) * 8,
+            tc::mma_f16_ts(tmem + kOCol, pa + (kk / (kHC / 16)) * kHC + (kk % (kHC / 16)) * 8,
                            tc::desc_advance(vd, kk * 2048), idesc_o, c > un.cb || kk > 0);
           tc::commit(&pv_done[x & 1]);
           tc::commit(&v_free[st]);
@@ -597,14 +614,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (!mbar_wait_bounded(&drain[role], 0, &abort_s, wait_ns)) fine = false;
   } else {
     // ============================================================= softmax
+    // thread (row, hc): score columns [HC hc, HC hc + HC) of each chunk, Q
+    // and O dims [DT hc, DT hc + DT)
     const int row = tid & (kTcRows - 1), hc = tid >> 7, pair = 1 + (warp & 3);
     const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // lanes of this row
-    constexpr int HC = kChunk / 2;  // score columns per thread: [HC hc, HC hc + HC)
-    float4 *obuf = reinterpret_cast<float4 *>(ring + ST * C::STAGE) + warp * 128;
+    constexpr int HC = kHC, DT = C::DT;
+    constexpr uint64_t kFull = HC == 64 ? ~0ull : (1ull << HC) - 1ull;
     // this warp's region of the Q staging area: the next tile's Q slices of
     // its threads during a tile, its output rows for the tensor stores at the
-    // tile's end (one 4 KB box per 32-dim block)
-    uint8_t *wreg = qstage + (size_t)warp * (C::QSTAGE / kSoftWarps);
+    // tile's end (one box of 32 rows x CB dims per CB-dim block)
+    uint8_t *wreg = qstage + (size_t)warp * C::REGION;
     bool ost_pending = false;  // tensor stores issued from wreg, maybe still reading it
     auto ost_free = [&]() {
       if (ost_pending) {
@@ -628,7 +647,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         unit_of<GP>(p, ts, n_tiles, n_split, ue, e);
         if (e.ce > e.cb) continue;
         float *rr = record(ue);
-        for (int d0 = hc * (D / 2); d0 < (hc + 1) * (D / 2); d0 += 4)
+        for (int d0 = hc * DT; d0 < (hc + 1) * DT; d0 += 4)
           *reinterpret_cast<float4 *>(rr + 4 + d0) = make_float4(0.f, 0.f, 0.f, 0.f);
         if (hc == 0)
           *reinterpret_cast<float4 *>(rr) =
@@ -636,9 +655,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     // this thread's Q columns in tensor memory: high / low pairs at columns
-    // kQHiCol / kQLoCol + hc * D / 4 + [0, D / 4)
-    const uint32_t q_hi_t = t_row + (uint32_t)(kQHiCol + hc * (D / 4));
-    const uint32_t q_lo_t = t_row + (uint32_t)(kQLoCol + hc * (D / 4));
+    // kQHiCol / kQLoCol + hc * DT / 2 + [0, DT / 2)
+    const uint32_t q_hi_t = t_row + (uint32_t)(kQHiCol + hc * (DT / 2));
+    const uint32_t q_lo_t = t_row + (uint32_t)(kQLoCol + hc * (DT / 2));
     int u = blockIdx.x;
     Unit un;
     bool have = live_unit(u, un);
@@ -657,21 +676,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       Unit nxu;
       const bool have_next = live_unit(u2, nxu);
       const Tile &nx = nxu.tl;
-      const float *qn = nullptr;  // this thread's half of its next-tile query row (or none)
+      const float *qn = nullptr;  // this thread's part of its next-tile query row (or none)
       if (have_next) {
         const RowOf<GP> rn(p, nx, row);
         if (rn.ok) {
-          qn = p.q + ((size_t)rn.i * p.Hq + (size_t)nx.kvh * p.G + rn.hg) * D + hc * (D / 2);
+          qn = p.q + ((size_t)rn.i * p.Hq + (size_t)nx.kvh * p.G + rn.hg) * D + hc * DT;
 #pragma unroll
-          for (int e = 0; e < D / 2; e += 32)
+          for (int e = 0; e < DT; e += 32)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + e));
         }
       }
-      // the next tile's Q, slice k = dims [8k, 8k + 8) of this thread's half
-      // row, staged in the warp's shared-memory region as 16-byte groups:
-      // high pairs in group k, low pairs in group NSL + k (group g of lane l
-      // at 512 g + 16 l, so a warp's accesses cover consecutive words)
-      constexpr int NSL = D / 16;
+      // the next tile's Q, slice k = dims [8k, 8k + 8) of this thread's part
+      // of the row, staged in the warp's shared-memory region as 16-byte
+      // groups: high pairs in group k, low pairs in group NSL + k (group g of
+      // lane l at 512 g + 16 l, so a warp's accesses cover consecutive words)
+      constexpr int NSL = C::NSL;
       uint4 *qst = reinterpret_cast<uint4 *>(wreg) + lane;
       auto load_slice = [&](int k, float4 &a, float4 &b) {
         a = b = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -731,27 +750,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
 #pragma unroll
           for (int half = 0; half < 2; ++half) {  // high, then low
-            const uint32_t dst = half ? q_lo_t : q_hi_t;
+            uint32_t w[DT / 2];
 #pragma unroll
-            for (int w16 = 0; w16 < D / 4; w16 += 16) {
-              uint32_t w[16];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const uint4 gq = qst[(half * NSL + w16 / 4 + j) * 32];
-                w[4 * j] = gq.x;
-                w[4 * j + 1] = gq.y;
-                w[4 * j + 2] = gq.z;
-                w[4 * j + 3] = gq.w;
-              }
-              tc::st16u(dst + w16, w);
+            for (int j = 0; j < NSL; ++j) {
+              const uint4 gq = qst[(half * NSL + j) * 32];
+              w[4 * j] = gq.x;
+              w[4 * j + 1] = gq.y;
+              w[4 * j + 2] = gq.z;
+              w[4 * j + 3] = gq.w;
             }
+            st_words<DT / 2>(half ? q_lo_t : q_hi_t, w);
           }
           tc::wait_st();
           tc::fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&q_full);
         }
-        // ---- S(x): this thread's 64 columns of buffer x % 2 into registers
+        // ---- S(x): this thread's HC columns of buffer x % 2 into registers
         const uint32_t s_row = t_row + (uint32_t)((x & 1) * kSCols + hc * HC);
         float sv[HC];
 #pragma unroll
@@ -761,7 +776,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) sv[c16 + e] = v[e];
         }
-        const uint64_t vm = smask_s[x & 1][hc];
+        const uint64_t vm = (smask_s[x & 1][(hc * HC) >> 6] >> ((hc * HC) & 63)) & kFull;
         tc::wait_ld();
         // ---- mask: the row's window, then the staged rows that hold data
         const int pos0 = c * kChunk + hc * HC;  // position of this thread's first column
@@ -775,56 +790,67 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         mk &= vm;
         // most chunks are wholly readable: only partial ones pay for the mask
-        if (mk != ~0ull) {
-          const uint32_t m0 = (uint32_t)mk, m1 = (uint32_t)(mk >> 32);
+        if (mk != kFull) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            sv[e] = (m0 & (1u << e)) ? sv[e] : -INFINITY;
-            sv[e + 32] = (m1 & (1u << e)) ? sv[e + 32] : -INFINITY;
+          for (int h32 = 0; h32 < HC; h32 += 32) {
+            const uint32_t m = (uint32_t)(mk >> h32);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sv[h32 + e] = (m & (1u << e)) ? sv[h32 + e] : -INFINITY;
           }
         }
-        // row maximum: 4 independent chains of 3-input maxima over 16 columns each
-        float mq[4];
+        // row maximum: independent chains of 3-input maxima over 16 columns each
+        float mq[HC / 16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < HC / 16; ++j) {
           const float *v = sv + 16 * j;
           float m = max3f(v[0], v[1], v[2]);
 #pragma unroll
           for (int e = 3; e < 15; e += 2) m = max3f(m, v[e], v[e + 1]);
           mq[j] = fmaxf(m, v[15]);
         }
-        pm_s[x & 1][hc][row] = fmaxf(max3f(mq[0], mq[1], mq[2]), mq[3]);
-        // both halves of the row (and their waits) meet here; a wait that ran
-        // out on either side ends the pair's loop at the same point
-        if (!pair_sync_and(pair, fine)) {
-          fine = false;
-          break;
-        }
-        const float mloc = fmaxf(pm_s[x & 1][0][row], pm_s[x & 1][1][row]);
-        // ---- online softmax, rescaling O only when the maximum grows past 2^8
-        const float m_new = fmaxf(m_run, mloc);
-        float scale_o = 1.f;
-        if (m_new != -INFINITY && (m_run == -INFINITY || m_new > m_run + 8.f)) {
-          scale_o = m_run == -INFINITY ? 1.f : exp2f(m_run - m_new);
-          l_run *= scale_o;
-          m_run = m_new;
-        }
-        if (c > un.cb && __any_sync(kAll, scale_o != 1.f)) {
-          // P(x-1) V has been added to O
-          fine = mbar_wait_bounded(&pv_done[(x - 1) & 1], (uint32_t)((x - 1) >> 1) & 1u, &abort_s,
-                                   wait_ns) &&
-                 fine;
-          tc::fence_after();
-#pragma unroll 1
-          for (int c16 = hc * (D / 2); c16 < (hc + 1) * (D / 2); c16 += 16) {
-            float v[16];
-            tc::ld16(t_row + kOCol + c16, v);
-            tc::wait_ld();
+        float mown = mq[0];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] *= scale_o;
-            tc::st16(t_row + kOCol + c16, v);
+        for (int j = 1; j < HC / 16; ++j) mown = fmaxf(mown, mq[j]);
+        // ---- online softmax, rescaling O only when the maximum grows past 2^8.
+        // The row's running maximum changes only when one of its scores passes
+        // m_run + 8 (or on its first finite score), so the row's parts exchange
+        // their maxima only then: one vote of their warps decides (and carries
+        // the waits' outcome; a wait that ran out in any part ends the row's
+        // loop at the same point)
+        const bool grow = mown != -INFINITY && (m_run == -INFINITY || mown > m_run + 8.f);
+        if (pair_vote_or(pair, grow || !fine)) {
+          pm_s[x & 1][hc][row] = mown;
+          if (!pair_sync_and(pair, fine)) {
+            fine = false;
+            break;
           }
-          tc::wait_st();
+          float mloc = pm_s[x & 1][0][row];
+#pragma unroll
+          for (int h = 1; h < kTPR; ++h) mloc = fmaxf(mloc, pm_s[x & 1][h][row]);
+          const float m_new = fmaxf(m_run, mloc);
+          float scale_o = 1.f;
+          if (m_new != -INFINITY && (m_run == -INFINITY || m_new > m_run + 8.f)) {
+            scale_o = m_run == -INFINITY ? 1.f : exp2f(m_run - m_new);
+            l_run *= scale_o;
+            m_run = m_new;
+          }
+          if (c > un.cb && __any_sync(kAll, scale_o != 1.f)) {
+            // P(x-1) V has been added to O
+            fine = mbar_wait_bounded(&pv_done[(x - 1) & 1], (uint32_t)((x - 1) >> 1) & 1u,
+                                     &abort_s, wait_ns) &&
+                   fine;
+            tc::fence_after();
+#pragma unroll 1
+            for (int c16 = hc * DT; c16 < (hc + 1) * DT; c16 += 16) {
+              float v[16];
+              tc::ld16(t_row + kOCol + c16, v);
+              tc::wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) v[e] *= scale_o;
+              tc::st16(t_row + kOCol + c16, v);
+            }
+            tc::wait_st();
+          }
         }
         // ---- probabilities over this thread's own (already loaded) scores
         float ls[4] = {0.f, 0.f, 0.f, 0.f};  // two packed pairs of partial sums
@@ -861,14 +887,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                wait_ns) &&
              fine;
       tc::fence_after();
-      // this thread's half of the output row out of tensor memory (every load
-      // in flight, one wait), then O is handed to the next tile's first P.V
-      constexpr int DH = D / 2;
-      float o[DH];
+      // this thread's part of the output row out of tensor memory (every
+      // load in flight, one wait), then O is handed to the next tile's first P.V
+      float o[DT];
 #pragma unroll
-      for (int c16 = 0; c16 < DH; c16 += 16) {
+      for (int c16 = 0; c16 < DT; c16 += 16) {
         float v[16];
-        tc::ld16(t_row + (uint32_t)(kOCol + hc * DH + c16), v);
+        tc::ld16(t_row + (uint32_t)(kOCol + hc * DT + c16), v);
 #pragma unroll
         for (int e = 0; e < 16; ++e) o[c16 + e] = v[e];
       }
@@ -881,11 +906,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fine = false;
         break;
       }
-      const float l_row = pl_s[0][row] + pl_s[1][row];
+      float l_row = pl_s[0][row];
+#pragma unroll
+      for (int h = 1; h < kTPR; ++h) l_row += pl_s[h][row];
       if (n_split > 1) {
         // a piece of a split tile: the unnormalised record, merged later
         float *rr = record(u);
-        store_half_rows<DH>(o, 1.f, false, rr + 4 + hc * DH, obuf, lane);
+        store_part<DT>(o, 1.f, false, rr + 4 + hc * DT);
         if (hc == 0)
           *reinterpret_cast<float4 *>(rr) =
               make_float4(m_run, l_row, __int_as_float(dest_of(tl)), 0.f);
@@ -898,23 +925,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float inv = any ? 1.f / l_row : 0.f;
       // the warp's 32 rows are QW whole queries of the tile: when all are
       // queries of the sequence, its rows leave by tensor stores from its
-      // region (box row (query, head) = (lane / GP, lane % GP) packed over
-      // the G real heads; 16-byte chunk c of box row k at c ^ (k % 8), the
-      // 128-byte swizzle), so the warp moves on without waiting for them
-      constexpr int QW = 32 / GP;
+      // region, one box of CB dims per block (box row (query, head) = (lane
+      // / GP, lane % GP) packed over the G real heads; the 16-byte chunk c of
+      // box row k at c ^ (k % 8) for 128-byte rows, c ^ ((k / 2) % 4) for
+      // 64-byte rows: the tensor map's swizzle), so the warp moves on
+      // without waiting for them
+      constexpr int QW = 32 / GP, CB = C::CB, BOX = 32 * CB * 4;
       const int jq0 = tl.qt * TQ + (warp & 3) * QW;
       const int i0 = p.q_start[tl.s] + jq0;  // the warp's first query row
       if (maps.o_ok && jq0 + QW <= tl.n && i0 >= 0 && i0 + QW <= p.n_tok) {
         ost_free();
         const int k = (lane / GP) * p.G + rw.hg;
+        const int sw = CB == 32 ? (k & 7) : ((k >> 1) & 3);
         if (rw.hg < p.G) {
 #pragma unroll
-          for (int j = 0; j < DH / 32; ++j) {
-            uint8_t *brow = wreg + j * 4096 + k * 128;
+          for (int j = 0; j < DT / CB; ++j) {
+            uint8_t *brow = wreg + j * BOX + k * (CB * 4);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const float *v = o + 32 * j + 4 * c;
-              *reinterpret_cast<float4 *>(brow + ((c ^ (k & 7)) << 4)) =
+            for (int c = 0; c < CB / 4; ++c) {
+              const float *v = o + CB * j + 4 * c;
+              *reinterpret_cast<float4 *>(brow + ((c ^ sw) << 4)) =
                   any ? make_float4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv)
                       : make_float4(0.f, 0.f, 0.f, 0.f);
             }
@@ -924,17 +954,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
         if (lane == 0) {
 #pragma unroll
-          for (int j = 0; j < DH / 32; ++j)
-            tma_store_3d(&maps.o, hc * DH + 32 * j, tl.kvh * p.G, i0, smem_u32(wreg + j * 4096));
+          for (int j = 0; j < DT / CB; ++j)
+            tma_store_3d(&maps.o, hc * DT + CB * j, tl.kvh * p.G, i0, smem_u32(wreg + j * BOX));
           bulk_commit();
         }
         ost_pending = true;
       } else {
-        store_half_rows<DH>(
+        store_part<DT>(
             o, inv, !any,
-            rw.in ? p.out + ((size_t)rw.i * p.Hq + (size_t)tl.kvh * p.G + rw.hg) * D + hc * DH
-                  : nullptr,
-            obuf, lane);
+            rw.in ? p.out + ((size_t)rw.i * p.Hq + (size_t)tl.kvh * p.G + rw.hg) * D + hc * DT
+                  : nullptr);
       }
       if (rw.in && p.lse && hc == 0)
         p.lse[(size_t)rw.i * p.Hq + (size_t)tl.kvh * p.G + rw.hg] =
@@ -1020,6 +1049,94 @@ __global__ void __launch_bounds__(128) prefill_tc_combine_kernel(const __grid_co
   }
 }
 
+// q8_0 rows -> f16 rows for the tensor-core prefill. A CTA per (sequence,
+// block) unit at a time: the block's bs rows of K (then of V), contiguous in
+// the pool, arrive in shared memory by asynchronous copies (16 bytes each
+// when the row size allows, else 4), then thread t converts 32-value groups
+// t, t + 256, ... (each group: an f16 scale, then 32 int8 codes, 34 bytes at
+// a 2-byte alignment) into 64 contiguous bytes of f16 rows: each value is
+// code * scale rounded once to the nearest f16.
+template <int CH>
+__device__ __forceinline__ void stage_copy(uint32_t dst, const void *src) {
+  if constexpr (CH == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+template <int CH>
+__global__ void __launch_bounds__(256) stage_q8_f16_kernel(
+    const uint8_t *__restrict__ k_pool, const uint8_t *__restrict__ v_pool,
+    const int32_t *__restrict__ table, const int32_t *__restrict__ ctx, int n_seqs,
+    int max_blocks, int bs, long long n_phys, int n_groups, int row_bytes,
+    uint8_t *__restrict__ k16, uint8_t *__restrict__ v16, int32_t *__restrict__ table16,
+    uint32_t *status) {
+  extern __shared__ __align__(16) uint8_t raw[];  // bs rows of row_bytes
+  pdl_enter();
+  const int tid = threadIdx.x;
+  const long long n_units = (long long)n_seqs * max_blocks;
+  const size_t rb16 = (size_t)n_groups * 64;
+  const int blk_bytes = bs * row_bytes;
+  for (long long unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+    const int s = (int)(unit / max_blocks), b = (int)(unit % max_blocks);
+    const int c = max(ctx[s], 0);
+    int phys = b * bs < c ? table[unit] : -1;
+    if (phys < -1 || (phys >= 0 && (long long)phys >= n_phys)) {
+      if (tid == 0) report(status, MT_STATUS_BIT_DEVICE_CHECK);
+      phys = -1;
+    }
+    if (tid == 0) table16[unit] = phys >= 0 ? (int32_t)unit : -1;
+    if (phys < 0) continue;
+    const int n_valid = min(bs, c - b * bs);  // rows inside the context
+    bool big = false;
+#pragma unroll 1
+    for (int kv = 0; kv < 2; ++kv) {
+      const uint8_t *src = (kv ? v_pool : k_pool) + (size_t)phys * blk_bytes;
+      for (int o = tid * CH; o < blk_bytes; o += 256 * CH) stage_copy<CH>(smem_u32(raw + o), src + o);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      __syncthreads();
+      uint8_t *dst = (kv ? v16 : k16) + (size_t)unit * bs * rb16;
+      for (int gi = tid; gi < bs * n_groups; gi += 256) {
+        const int r = gi / n_groups, g = gi - r * n_groups;
+        const uint16_t *gp = reinterpret_cast<const uint16_t *>(raw + r * row_bytes + g * 34);
+        const __half dh = __ushort_as_half(gp[0]);
+        const __half2 d2 = __halves2half2(dh, dh);
+        // codes exactly as f16 (the bit pattern 0x64XX is 1024 + XX: codes
+        // + 128 as bytes, minus 1152), then one f16 multiply by the scale:
+        // the exact product rounded to the nearest f16
+        const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          const uint32_t b4 = ((uint32_t)gp[2 + j] << 16 | gp[1 + j]) ^ 0x80808080u;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            uint32_t hb = __byte_perm(b4, 0x64646464u, t ? 0x4342 : 0x4140);
+            __half2 h = __hsub2(*reinterpret_cast<__half2 *>(&hb), bias);
+            h = __hmul2(h, d2);
+            w[j + t] = *reinterpret_cast<uint32_t *>(&h);
+          }
+        }
+        // a product rounds to infinity only if |scale| * 128 can reach 65520
+        if (r < n_valid && fabsf(__half2float(dh)) * 128.f >= 65504.f) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const __half2 h = *reinterpret_cast<const __half2 *>(&w[j]);
+            big |= __hisinf(__low2half(h)) || __hisinf(__high2half(h));
+          }
+        }
+        uint4 *o = reinterpret_cast<uint4 *>(dst + (size_t)r * rb16 + (size_t)g * 64);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          o[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+      }
+      __syncthreads();  // the buffer is refilled next
+    }
+    if (big) report(status, MT_STATUS_BIT_DEVICE_CHECK);
+  }
+}
+
 template <int D, int GP, bool SPLIT>
 mt_status launch_t(const PrefillParams &p, const TcMaps &m, int n_ctas, cudaStream_t s) {
   auto kern = prefill_tc_kernel<D, GP, SPLIT>;
@@ -1049,8 +1166,24 @@ mt_status launch_d(int gp, const PrefillParams &p, const TcMaps &m, int n_ctas, 
 }  // namespace
 
 bool prefill_tc_supported(mt_kv_format fmt, int head_dim, int block_size) {
-  return fmt == MT_KV_F16 && (head_dim == 64 || head_dim == 128) &&
+  return (fmt == MT_KV_F16 || fmt == MT_KV_Q8_0) && (head_dim == 64 || head_dim == 128) &&
          (block_size == 16 || block_size == 32);
+}
+
+mt_status launch_stage_q8_f16(const uint8_t *k_pool, const uint8_t *v_pool, const int32_t *table,
+                              const int32_t *ctx, int n_seqs, int max_blocks, int bs,
+                              long long n_phys, int n_kv_heads, int head_dim, int row_bytes,
+                              uint8_t *k16, uint8_t *v16, int32_t *table16, uint32_t *status,
+                              int n_ctas, cudaStream_t stream) {
+  const long long units = (long long)n_seqs * max_blocks;
+  if (units == 0) return MT_OK;
+  const int grid = (int)std::min<long long>(units, (long long)n_ctas);
+  const size_t smem = (size_t)bs * row_bytes;  // at most 32 rows of 8 x 4 x 34 bytes: 34 KB
+  auto kern = (row_bytes % 16 == 0) ? stage_q8_f16_kernel<16> : stage_q8_f16_kernel<4>;
+  return cuda_check(launch_pdl(kern, dim3(grid), dim3(256), smem, stream, k_pool, v_pool, table,
+                               ctx, n_seqs, max_blocks, bs, n_phys, n_kv_heads * head_dim / 32,
+                               row_bytes, k16, v16, table16, status),
+                    "q8_0 -> f16 staging launch");
 }
 
 mt_status launch_prefill_tc_combine(const PrefillParams &p, int head_dim, int n_ctas,
@@ -1075,7 +1208,8 @@ mt_status launch_prefill_tc(const PrefillParams &p, int head_dim, int gp, int n_
   m.o_ok = 0;
   if ((reinterpret_cast<uintptr_t>(p.out) & 15u) == 0 && p.n_tok > 0) {
     const int gpe = gp == 1 || gp == 2 || gp == 4 ? gp : 8;  // as launch_g instantiates
-    st = encode_out_map_f32(&m.o, p.out, p.n_tok, p.Hq, head_dim, p.G, 32 / gpe);
+    const int cb = std::min(head_dim / kTPR, 32);             // TcCfg<D>::CB
+    st = encode_out_map_f32(&m.o, p.out, p.n_tok, p.Hq, head_dim, cb, p.G, 32 / gpe);
     if (st != MT_OK) return st;
     m.o_ok = 1;
   }

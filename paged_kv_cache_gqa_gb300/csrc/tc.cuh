@@ -146,6 +146,14 @@ __device__ __forceinline__ void st4u(uint32_t taddr, uint32_t w0, uint32_t w1, u
                : "memory");
 }
 
+// 8 consecutive 32-bit columns of this thread's lane from raw words.
+__device__ __forceinline__ void st8u(uint32_t taddr, const uint32_t (&w)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+      : "memory");
+}
+
 // 16 consecutive 32-bit columns of this thread's lane from raw words.
 __device__ __forceinline__ void st16u(uint32_t taddr, const uint32_t (&w)[16]) {
   asm volatile(

@@ -27,11 +27,11 @@ mt_status encode_pool_map_words(CUtensorMap *map, const void *pool, long long n_
                                 int chunk_bytes, int box_chunks, int box_rows);
 
 // 3-D tensor map of a float32 output [row][head][dim] (n_rows x n_heads x
-// head_dim, rows of n_heads * head_dim floats), box = (32, box_heads,
-// box_rows), 128-byte swizzle: the prefill kernel stores a warp's output
-// rows through it. The output must be 16-byte aligned and head_dim a
-// multiple of 32.
+// head_dim, rows of n_heads * head_dim floats), box = (box_dims, box_heads,
+// box_rows) with box_dims 32 (128-byte swizzle) or 16 (64-byte swizzle):
+// the prefill kernel stores a warp's output rows through it. The output
+// must be 16-byte aligned and head_dim a multiple of box_dims.
 mt_status encode_out_map_f32(CUtensorMap *map, float *out, long long n_rows, int n_heads,
-                             int head_dim, int box_heads, int box_rows);
+                             int head_dim, int box_dims, int box_heads, int box_rows);
 
 }  // namespace mtkv

@@ -93,3 +93,38 @@ def test_prefill_tc_output_boxes(mt, hq, hkv, d):
     q, q_start = make_queries(w, rng, 150)
     kp, vp = oracle_pools(w)
     check_pools(mt, w, q, q_start, kp, vp)
+
+
+@pytest.mark.parametrize("d,bs,hq,hkv", [(128, 16, 32, 8), (128, 32, 12, 2), (64, 16, 8, 2)])
+def test_prefill_tc_q8_0_staged(mt, d, bs, hq, hkv):
+    # q8_0 pools run the tcgen05 kernel on rows staged as f16 (code * scale
+    # rounded once to f16): contexts of several 128-token chunks, many tiles,
+    # a hole, against the oracle's exact dequantisation at the q8_0 tolerance
+    rng = np.random.default_rng(86 + d + bs + hq)
+    w = workloads.llama3_f16(seed=86 + d + bs, n_seqs=3, ctx_lo=500, ctx_hi=900, fmt="q8_0",
+                             block_size=bs, n_heads=hq, n_kv_heads=hkv, head_dim=d)
+    table = w.block_table.copy()
+    table[1, 2] = -1
+    w = dataclasses.replace(w, block_table=table)
+    q, q_start = make_queries(w, rng, 260)
+    kp, vp = oracle_pools(w)
+    check_pools(mt, w, q, q_start, kp, vp)
+
+
+def test_prefill_tc_q8_0_staged_flags_bad_ids(mt):
+    # an out-of-range block id is flagged by the staging pass and read as a
+    # hole; the other sequence's rows are unaffected
+    rng = np.random.default_rng(87)
+    w = workloads.llama3_f16(seed=87, n_seqs=2, ctx_lo=300, ctx_hi=400, fmt="q8_0")
+    q, q_start = make_queries(w, rng, 40)
+    kp, vp = oracle_pools(w)
+    table = w.block_table.copy()
+    table[0, 3] = w.n_phys_blocks + 5
+    got, _, st = run_prefill(mt, w, q, q_start, kp, vp, table=table)
+    assert st == mt.MT_ERR_DEVICE_CHECK
+    holed = table.copy()
+    holed[0, 3] = -1
+    want, _ = oatt.paged_attn_prefill(w.fmt, q, kp, vp, holed, w.context_lens, q_start, None,
+                                      None, w.n_heads, w.n_kv_heads, w.head_dim, w.block_size,
+                                      w.scale)
+    assert_close(got, want, TOL[w.fmt], "q8_0 staged prefill with a bad id")
