@@ -207,7 +207,10 @@ typedef struct {
 } mt_paged_prefill_args;
 
 /* Workspace bytes mt_paged_attn_prefill needs (its first 4 bytes are the
- * device status word; zero them once after allocating). */
+ * device status word; zero them once after allocating). For q8_0 pools of
+ * head_dim 64 or 128 it includes the f16 staging of the call's blocks:
+ * n_seqs x max_blocks x block_size rows of n_kv_heads x head_dim f16 for K
+ * and for V (plus a table of n_seqs x max_blocks ids). */
 size_t mt_paged_prefill_workspace_bytes(const mt_paged_prefill_args *args);
 
 /* Multi-query (prefill, or chunked prefill) attention through the paged
@@ -224,7 +227,16 @@ size_t mt_paged_prefill_workspace_bytes(const mt_paged_prefill_args *args);
  * block_size 16 or 32, n_heads/n_kv_heads <= 8, n_kv_heads <= 8 (others
  * MT_ERR_UNSUPPORTED). Out-of-range block ids,
  * query counts above the context length and query rows outside
- * [0, n_tokens) are skipped and flagged in the workspace status word. */
+ * [0, n_tokens) are skipped and flagged in the workspace status word.
+ * Arithmetic: f16 pools (head_dim 64, 128) run on the 5th-generation tensor
+ * cores with q split into high and low f16 halves (scores to ~2^-22) and
+ * f16 probabilities; q8_0 pools of those head sizes take the same kernel
+ * after a pass that stages each block the call reads as f16 rows, every
+ * value code * scale rounded once to the nearest f16 (relative error <=
+ * 2^-11, inside the q8_0 tolerance; a staged value beyond the f16 range is
+ * flagged in the status word); other pools run a warp-level tensor-core
+ * kernel that keeps codes exact and applies scales in float32. The
+ * workspace must be 16-byte aligned. */
 mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *args, void *workspace,
                                 size_t workspace_bytes, mt_stream stream);
 

@@ -442,7 +442,7 @@ extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void 
     uint8_t *k16 = ws + tb, *v16 = ws + tb + pb;
     st = launch_stage_q8_f16(p.k_pool, p.v_pool, a->block_table, a->context_lens, a->n_seqs,
                              a->max_blocks, a->block_size, a->n_phys_blocks, a->n_kv_heads,
-                             a->head_dim, (int)rb, k16, v16, table16, p.status, di.n_sm * 4, s);
+                             a->head_dim, (int)rb, k16, v16, table16, p.status, di.n_sm * 8, s);
     if (st != MT_OK) return st;
     table = table16;
     p.k_pool = k16;
