@@ -1367,7 +1367,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = p.stages;
-  pdl_enter();
+  // the successor may start launching at once; every role waits for the
+  // predecessor (pdl_wait) before its first access to memory an earlier
+  // kernel of the stream may write: the producer first plans its range from
+  // the context lengths, windows and block table, which no kernel of this
+  // library writes, so that work overlaps the predecessor's tail
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -1382,17 +1387,15 @@ __global__ void __launch_bounds__(kThreads, MINB)
   if (warp == p.n_cw) {
     // ------------------------------------------------------ producer warp
     const uint64_t pol = policy_evict_first();
-    // pass 1: total stream length (CTA 0 also publishes the prefix)
+    // pass 1: total stream length
     int total = 0;
     for (int base = 0; base < p.B; base += 32) {
       const int s = base + lane;
       int lo, hi;
       const int nb = s < p.B ? seq_window(p, s, lo, hi) : 0;
       const int incl = warp_incl_scan(nb, lane);
-      if (blockIdx.x == 0 && s < p.B) p.seq_start[s] = total + incl - nb;
       total += __shfl_sync(kFull, incl, 31);
     }
-    if (blockIdx.x == 0 && lane == 0) p.seq_start[p.B] = total;
     const int per = total > 0 ? (total + (int)gridDim.x - 1) / (int)gridDim.x : 0;
     const long long b0 = (long long)blockIdx.x * per;
     const long long b1 = min((long long)total, b0 + per);
@@ -1456,9 +1459,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
       return okv != 0;
     };
 
+    // pass 2: first sequence whose blocks reach past b0
+    int s_first = p.B, start_first = 0;
     if (b0 < b1) {
-      // pass 2: first sequence whose blocks reach past b0
-      int s_first = p.B, start_first = 0, run = 0;
+      int run = 0;
       for (int base = 0; base < p.B; base += 32) {
         const int s = base + lane;
         int lo, hi;
@@ -1473,6 +1477,23 @@ __global__ void __launch_bounds__(kThreads, MINB)
         }
         run += __shfl_sync(kFull, incl, 31);
       }
+    }
+    pdl_wait();
+    if (blockIdx.x == 0) {
+      // CTA 0 publishes each sequence's first stream position (the combine
+      // reads it), now that the predecessor no longer reads the workspace
+      int run = 0;
+      for (int base = 0; base < p.B; base += 32) {
+        const int s = base + lane;
+        int lo, hi;
+        const int nb = s < p.B ? seq_window(p, s, lo, hi) : 0;
+        const int incl = warp_incl_scan(nb, lane);
+        if (s < p.B) p.seq_start[s] = run + incl - nb;
+        run += __shfl_sync(kFull, incl, 31);
+      }
+      if (lane == 0) p.seq_start[p.B] = run;
+    }
+    if (b0 < b1) {
       long long x = b0;
       int start = start_first;
       for (int s = s_first; alive && x < b1 && s < p.B; ++s) {
@@ -1596,6 +1617,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   }
 
   if (warp >= p.n_cw) return;
+  pdl_wait();
   if (p.k_new) {
     // Appended rows outside every window are read by no CTA: the consumer
     // warps of CTA s mod grid write them while the first stages load. The
