@@ -10,7 +10,15 @@
  *    device memory; calls that need scratch take a caller-provided
  *    workspace whose size comes from the matching *_workspace_bytes call.
  *  - Execution: compute calls are asynchronous on `stream` (a cudaStream_t;
- *    NULL is the legacy default stream). Arguments that can be checked on
+ *    NULL is the legacy default stream). Their kernels are launched with
+ *    programmatic dependent launch: a kernel may start while the previous
+ *    kernel of the stream finishes, and waits for it before touching memory
+ *    that kernel may write. The decode kernels read their context lengths,
+ *    windows (spans, kv_map) and block tables before that wait, so these
+ *    arrays must not be written by a kernel of the stream that lets its
+ *    dependents launch early (griddepcontrol.launch_dependents) before it
+ *    completes; copies, and kernels that do not, are waited for as usual.
+ *    Arguments that can be checked on
  *    the host are checked before anything is launched; a failed check
  *    returns a status and launches nothing. Checks that need device data
  *    (block ids, context lengths, cells) run inside the kernels: an
