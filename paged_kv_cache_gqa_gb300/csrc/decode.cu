@@ -51,6 +51,7 @@
 #include <algorithm>
 #include <mutex>
 #include <string>
+#include <type_traits>
 #include <vector>
 
 namespace mtkv {
@@ -399,14 +400,18 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
         wrote = true;
         __syncwarp();
       }
+      // The stage's NT 8-token tiles (NT = rows / 8, a constant per branch)
+      // are all computed, without per-tile conditions, so that their chains
+      // interleave: rows outside the stage's mask get score -inf and their V
+      // rows are zero (above).
+      auto run_stage = [&](auto nt_c) {
+      constexpr int NT = decltype(nt_c)::value;
       // ---- S = Qhl . K^T over the stage's 8-token tiles
-      float pr[4][2];
+      float pr[NT][2];
       float mloc = -INFINITY;
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        pr[t][0] = pr[t][1] = -INFINITY;
-        const int t0 = 8 * t;
-        if (t0 >= p.bs || t0 + 8 <= r0 || t0 >= r1) continue;
+      for (int t = 0; t < NT; ++t) {
+        const int t0 = base + 8 * t;  // block row of the tile's first token
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         if constexpr (FMT == MT_KV_F32) {
           // B fragment of k-step ks: token t0 + g, dims 16 ks + 2c (+1) and + 8
@@ -448,7 +453,7 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
       m_run = m_new;
       float lsum = 0.f;
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
+      for (int t = 0; t < NT; ++t) {
         pr[t][0] = none ? 0.f : exp2f(pr[t][0] - m_new);
         pr[t][1] = none ? 0.f : exp2f(pr[t][1] - m_new);
         lsum += pr[t][0] + pr[t][1];
@@ -467,9 +472,8 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
       }
       // ---- O^T += V^T . P^T over 16-token chunks
 #pragma unroll
-      for (int kc = 0; kc < 2; ++kc) {
-        const int t0 = 16 * kc;
-        if (t0 >= p.bs || t0 + 16 <= r0 || t0 >= r1) continue;
+      for (int kc = 0; kc < NT / 2; ++kc) {
+        const int t0 = base + 16 * kc;
         uint32_t b0, b1;
         if (M::HILO) {
           uint32_t h0, l0, h1, l1;
@@ -512,6 +516,11 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
           }
         }
       }
+      };
+      if (p.rows == 16)
+        run_stage(std::integral_constant<int, 2>{});
+      else
+        run_stage(std::integral_constant<int, 4>{});
       if (wrote) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
 
