@@ -412,7 +412,9 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         const int t0 = base + 8 * t;  // block row of the tile's first token
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        // two accumulators (alternate products), so the tile's MMAs form two
+        // dependent chains of half the length
+        float acc[4] = {0.f, 0.f, 0.f, 0.f}, acd[4] = {0.f, 0.f, 0.f, 0.f};
         if constexpr (FMT == MT_KV_F32) {
           // B fragment of k-step ks: token t0 + g, dims 16 ks + 2c (+1) and + 8
           const int krow = t0 + g - base;
@@ -425,7 +427,7 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
             split_h2(k0.x, k0.y, h0, l0);
             split_h2(k1.x, k1.y, h1, l1);
             mma_f16(acc, qa[ks], h0, h1);
-            mma_f16(acc, qa[ks], l0, l1);
+            mma_f16(acd, qa[ks], l0, l1);
           }
         } else {
           const int krow = t0 + (lane & 7) - base;
@@ -435,11 +437,12 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
             uint32_t b0, b1, b2, b3;
             ldsm_x4(swz(kst, krow, ke + ks * 16, p.ncb), b0, b1, b2, b3);
             mma_f16(acc, qa[ks], b0, b1);
-            mma_f16(acc, qa[ks + 1], b2, b3);
+            mma_f16(acd, qa[ks + 1], b2, b3);
           }
         }
         const int tk = t0 + 2 * c;
-        const float s0 = acc[0] + acc[2], s1 = acc[1] + acc[3];
+        const float s0 = (acc[0] + acd[0]) + (acc[2] + acd[2]);
+        const float s1 = (acc[1] + acd[1]) + (acc[3] + acd[3]);
         pr[t][0] = (row_ok && ((mask >> tk) & 1u)) ? s0 : -INFINITY;
         pr[t][1] = (row_ok && ((mask >> (tk + 1)) & 1u)) ? s1 : -INFINITY;
         mloc = fmaxf(mloc, fmaxf(pr[t][0], pr[t][1]));
