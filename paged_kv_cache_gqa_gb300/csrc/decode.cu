@@ -473,20 +473,24 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
           oacc[mt][3] *= a1;
         }
       }
-      // ---- O^T += V^T . P^T over 16-token chunks
+      // ---- O^T += V^T . P^T over 16-token chunks (an 8-row stage, f32 pools
+      // with wide rows: one chunk whose tokens 8..15 have P = 0 and V = 0)
+      constexpr int NKC = NT >= 2 ? NT / 2 : 1;
 #pragma unroll
-      for (int kc = 0; kc < NT / 2; ++kc) {
+      for (int kc = 0; kc < NKC; ++kc) {
         const int t0 = base + 16 * kc;
+        const float p10 = NT >= 2 ? pr[(2 * kc + 1) % NT][0] : 0.f;
+        const float p11 = NT >= 2 ? pr[(2 * kc + 1) % NT][1] : 0.f;
         uint32_t b0, b1;
         if (M::HILO) {
           uint32_t h0, l0, h1, l1;
           split_h2(pr[2 * kc][0], pr[2 * kc][1], h0, l0);
-          split_h2(pr[2 * kc + 1][0], pr[2 * kc + 1][1], h1, l1);
+          split_h2(p10, p11, h1, l1);
           b0 = lo_col ? l0 : h0;
           b1 = lo_col ? l1 : h1;
         } else {
           b0 = h2_bits(__floats2half2_rn(pr[2 * kc][0], pr[2 * kc][1]));
-          b1 = h2_bits(__floats2half2_rn(pr[2 * kc + 1][0], pr[2 * kc + 1][1]));
+          b1 = h2_bits(__floats2half2_rn(p10, p11));
         }
         if (!row_ok) b0 = b1 = 0u;
         if constexpr (FMT == MT_KV_F32) {
@@ -499,6 +503,10 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
 #pragma unroll
             for (int q = 0; q < 4; ++q) {  // (dim + 8 (q & 1), token + 8 (q >> 1))
               const int r = tr + 8 * (q >> 1), e = fe + 8 * (q & 1);
+              if (NT == 1 && q >= 2) {
+                v[2 * q] = v[2 * q + 1] = 0.f;
+                continue;
+              }
               v[2 * q] = lds_f32(swz32(vst, r, e, p.ncb));
               v[2 * q + 1] = lds_f32(swz32(vst, r + 1, e, p.ncb));
             }
@@ -520,10 +528,20 @@ __device__ __forceinline__ void consume_mma(const Params &p, uint64_t *full, uin
         }
       }
       };
-      if (p.rows == 16)
-        run_stage(std::integral_constant<int, 2>{});
-      else
-        run_stage(std::integral_constant<int, 4>{});
+      if constexpr (FMT == MT_KV_F32) {
+        if (p.rows == 8) {
+          run_stage(std::integral_constant<int, 1>{});
+        } else if (p.rows == 16) {
+          run_stage(std::integral_constant<int, 2>{});
+        } else {
+          run_stage(std::integral_constant<int, 4>{});
+        }
+      } else {
+        if (p.rows == 16)
+          run_stage(std::integral_constant<int, 2>{});
+        else
+          run_stage(std::integral_constant<int, 4>{});
+      }
       if (wrote) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
 
@@ -2239,9 +2257,11 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
   pl->ncb = nc | 1;  // odd number of 128-byte lines per staged row
   // (f32 pools: head_dim 64 and 128; at 256 the split operands do not fit in
   // registers and those pools stay on the FP32-core consumers)
+  // (f32 pools whose 16-row stages do not fit twice take 8-row stages)
   pl->mma = (a->fmt == MT_KV_F16 || (a->fmt == MT_KV_F32 && a->head_dim <= 128)) &&
             rb % 128 == 0 && pl->ncb <= 255 &&
-            a->n_kv_heads * mma_wph <= kMaxConsumerWarps && fit(128 * pl->ncb, 16, rows, pad, stages);
+            a->n_kv_heads * mma_wph <= kMaxConsumerWarps &&
+            fit(128 * pl->ncb, a->fmt == MT_KV_F32 ? 8 : 16, rows, pad, stages);
   // q8_0 pools: tensor-core consumers (d <= 128). For head_dim 128 the rows
   // are staged by a tensor copy whose box is wider than the row when the
   // row is whole 32- or 16-byte chunks, so that the staged pitch is 8 or 24

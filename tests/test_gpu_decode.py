@@ -141,6 +141,8 @@ def test_longctx_holes_and_int4_round_trip(mt):
 
 SHAPES = [  # fmt, head_dim, block_size, n_heads, n_kv_heads
     ("f32", 64, 16, 4, 2), ("f32", 128, 32, 8, 8), ("f32", 256, 16, 2, 1),
+    # f32 rows of 8 x 128 floats: 8-row tensor-core stages (query groups 4, 1)
+    ("f32", 128, 16, 32, 8), ("f32", 128, 16, 7, 7),
     ("f16", 64, 32, 8, 1), ("f16", 128, 16, 32, 8), ("f16", 256, 16, 16, 4),
     ("f16", 128, 32, 24, 4), ("f16", 64, 16, 21, 3), ("f16", 128, 16, 5, 5),
     ("q8_0", 64, 16, 6, 2), ("q8_0", 128, 32, 32, 8), ("q8_0", 256, 16, 16, 4),
