@@ -99,7 +99,6 @@ struct Params {
   float *lse;
   float *part_o;       // [P][Hq][D] unnormalised partial outputs
   float *part_ml;      // [P][Hq][2] partial (max, sum) in base-2 logits
-  int32_t *seq_start;  // [B+1] stream offset of each sequence's first block
   uint32_t *status;
   const float *k_new;  // [B][Hkv*D] rows appended at position ctx-1, or null
   const float *v_new;
@@ -1509,20 +1508,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
       }
     }
     pdl_wait();
-    if (blockIdx.x == 0) {
-      // CTA 0 publishes each sequence's first stream position (the combine
-      // reads it), now that the predecessor no longer reads the workspace
-      int run = 0;
-      for (int base = 0; base < p.B; base += 32) {
-        const int s = base + lane;
-        int lo, hi;
-        const int nb = s < p.B ? seq_window(p, s, lo, hi) : 0;
-        const int incl = warp_incl_scan(nb, lane);
-        if (s < p.B) p.seq_start[s] = run + incl - nb;
-        run += __shfl_sync(kFull, incl, 31);
-      }
-      if (lane == 0) p.seq_start[p.B] = run;
-    }
     if (b0 < b1) {
       long long x = b0;
       int start = start_first;
@@ -1986,7 +1971,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
 template <int D>
 __global__ void __launch_bounds__(256) splitk_combine_kernel(const Params p) {
   constexpr int DV = D / 32;
-  pdl_enter();
+  pdl_trigger();
   // With few (s, h) pairs, wps warps share one pair's partial list (each a
   // contiguous share) and merge their results through shared memory.
   __shared__ float red_s[8][2 + D];
@@ -1996,8 +1981,24 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(const Params p) {
   const int kw = warp % wps;
   const bool live = w < p.B * p.Hq;
   const int s = live ? w / p.Hq : 0, h = live ? w % p.Hq : 0;
-  const int T = p.seq_start[p.B];
-  const int beg = p.seq_start[s], end = p.seq_start[s + 1];
+  // the sequence's first stream position and the stream length follow from
+  // the context lengths and windows (read-only inputs, the decode's own
+  // arithmetic), so they are computed before waiting for the decode
+  int T = 0, beg = 0, end = 0;
+  for (int base = 0; base < p.B; base += 32) {
+    const int sl = base + lane;
+    int lo, hi, nb = 0;
+    if (sl < p.B) nb = seq_window(p, sl, lo, hi);
+    const int incl = warp_incl_scan(nb, lane);
+    if (s >= base && s < base + 32) {
+      const int incl_s = __shfl_sync(kFull, incl, s - base);
+      const int nb_s = __shfl_sync(kFull, nb, s - base);
+      beg = T + incl_s - nb_s;
+      end = T + incl_s;
+    }
+    T += __shfl_sync(kFull, incl, 31);
+  }
+  pdl_wait();
   const int per = T > 0 ? (T + p.n_ctas - 1) / p.n_ctas : 1;
   float acc[DV];
 #pragma unroll
@@ -2174,7 +2175,7 @@ struct Plan {
   int q8_chunk;  // q8_0 staged through the word tensor map: chunk bytes (0: bulk copies)
   bool two_per_sm;  // kernel compiled for two resident CTAs per SM
   bool pair;        // q8_0 block size 16: two blocks per 32-row stage
-  size_t ws_status, ws_seq, ws_ml, ws_o, ws_total;
+  size_t ws_status, ws_ml, ws_o, ws_total;
 };
 
 int pad_group(int G) {
@@ -2379,8 +2380,7 @@ mt_status make_plan(const mt_paged_attn_args *a, Plan *pl, bool need_device) {
   const size_t P = ((size_t)n_ctas + (size_t)a->n_seqs) * pl->n_sub;
   auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
   pl->ws_status = 0;
-  pl->ws_seq = 256;
-  pl->ws_ml = pl->ws_seq + up(((size_t)a->n_seqs + 1) * 4);
+  pl->ws_ml = 256;
   pl->ws_o = pl->ws_ml + up(P * a->n_heads * 2 * 4);
   pl->ws_total = pl->ws_o + up(P * a->n_heads * (size_t)a->head_dim * 4);
   return MT_OK;
@@ -2461,7 +2461,6 @@ mt_status fill_params(Params &prm, const mt_paged_attn_args *a, const Plan &pl, 
   prm.k_new = nullptr;
   prm.v_new = nullptr;
   prm.casc.n_groups = 0;
-  prm.seq_start = reinterpret_cast<int32_t *>(ws + pl.ws_seq);
   prm.part_ml = reinterpret_cast<float *>(ws + pl.ws_ml);
   prm.part_o = reinterpret_cast<float *>(ws + pl.ws_o);
   prm.B = a->n_seqs;
