@@ -128,3 +128,18 @@ def test_prefill_tc_q8_0_staged_flags_bad_ids(mt):
                                       None, w.n_heads, w.n_kv_heads, w.head_dim, w.block_size,
                                       w.scale)
     assert_close(got, want, TOL[w.fmt], "q8_0 staged prefill with a bad id")
+
+
+def test_prefill_tc_q8_0_staged_flags_f16_overflow(mt):
+    # a q8_0 group whose values reach past the f16 range (scale 600, codes
+    # 127: 76 200) cannot be staged as f16: the staging pass flags it
+    rng = np.random.default_rng(88)
+    w = workloads.llama3_f16(seed=88, n_seqs=2, ctx_lo=100, ctx_hi=200, fmt="q8_0")
+    q, q_start = make_queries(w, rng, 20)
+    kp, vp = oracle_pools(w)
+    cell = int(w.block_table[0, 0]) * w.block_size  # position 0 of sequence 0
+    kp = kp.copy()
+    kp[cell, 0:2] = np.frombuffer(np.float16(600.0).tobytes(), dtype=np.uint8)
+    kp[cell, 2:34] = 127
+    _, _, st = run_prefill(mt, w, q, q_start, kp, vp)
+    assert st == mt.MT_ERR_DEVICE_CHECK
