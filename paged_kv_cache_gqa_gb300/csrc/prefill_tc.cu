@@ -1050,9 +1050,10 @@ __global__ void __launch_bounds__(128) prefill_tc_combine_kernel(const __grid_co
 }
 
 // q8_0 rows -> f16 rows for the tensor-core prefill. A CTA per (sequence,
-// block) unit at a time: the block's bs rows of K (then of V), contiguous in
-// the pool, arrive in shared memory by asynchronous copies (16 bytes each
-// when the row size allows, else 4), then thread t converts 32-value groups
+// block) unit at a time: the block's bs rows of K and its bs rows of V, each
+// contiguous in its pool, arrive in shared memory together by asynchronous
+// copies (16 bytes each when the row size allows, else 4), then thread t
+// converts 32-value groups
 // t, t + 256, ... (each group: an f16 scale, then 32 int8 codes, 34 bytes at
 // a 2-byte alignment) into 64 contiguous bytes of f16 rows: each value is
 // code * scale rounded once to the nearest f16.
@@ -1071,7 +1072,7 @@ __global__ void __launch_bounds__(256) stage_q8_f16_kernel(
     int max_blocks, int bs, long long n_phys, int n_groups, int row_bytes,
     uint8_t *__restrict__ k16, uint8_t *__restrict__ v16, int32_t *__restrict__ table16,
     uint32_t *status) {
-  extern __shared__ __align__(16) uint8_t raw[];  // bs rows of row_bytes
+  extern __shared__ __align__(16) uint8_t raw[];  // bs rows of K, then bs rows of V
   pdl_enter();
   const int tid = threadIdx.x;
   const long long n_units = (long long)n_seqs * max_blocks;
@@ -1090,16 +1091,22 @@ __global__ void __launch_bounds__(256) stage_q8_f16_kernel(
     const int n_valid = min(bs, c - b * bs);  // rows inside the context
     bool big = false;
 #pragma unroll 1
+    // the block's K rows, then its V rows, all in flight at once
     for (int kv = 0; kv < 2; ++kv) {
       const uint8_t *src = (kv ? v_pool : k_pool) + (size_t)phys * blk_bytes;
-      for (int o = tid * CH; o < blk_bytes; o += 256 * CH) stage_copy<CH>(smem_u32(raw + o), src + o);
-      asm volatile("cp.async.commit_group;" ::: "memory");
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-      __syncthreads();
+      for (int o = tid * CH; o < blk_bytes; o += 256 * CH)
+        stage_copy<CH>(smem_u32(raw + kv * blk_bytes + o), src + o);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+#pragma unroll 1
+    for (int kv = 0; kv < 2; ++kv) {
+      const uint8_t *rows = raw + kv * blk_bytes;
       uint8_t *dst = (kv ? v16 : k16) + (size_t)unit * bs * rb16;
       for (int gi = tid; gi < bs * n_groups; gi += 256) {
         const int r = gi / n_groups, g = gi - r * n_groups;
-        const uint16_t *gp = reinterpret_cast<const uint16_t *>(raw + r * row_bytes + g * 34);
+        const uint16_t *gp = reinterpret_cast<const uint16_t *>(rows + r * row_bytes + g * 34);
         const __half dh = __ushort_as_half(gp[0]);
         const __half2 d2 = __halves2half2(dh, dh);
         // codes exactly as f16 (the bit pattern 0x64XX is 1024 + XX: codes
@@ -1131,8 +1138,8 @@ __global__ void __launch_bounds__(256) stage_q8_f16_kernel(
         for (int j = 0; j < 4; ++j)
           o[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
       }
-      __syncthreads();  // the buffer is refilled next
     }
+    __syncthreads();  // the buffer is refilled for the next unit
     if (big) report(status, MT_STATUS_BIT_DEVICE_CHECK);
   }
 }
@@ -1178,8 +1185,12 @@ mt_status launch_stage_q8_f16(const uint8_t *k_pool, const uint8_t *v_pool, cons
   const long long units = (long long)n_seqs * max_blocks;
   if (units == 0) return MT_OK;
   const int grid = (int)std::min<long long>(units, (long long)n_ctas);
-  const size_t smem = (size_t)bs * row_bytes;  // at most 32 rows of 8 x 4 x 34 bytes: 34 KB
+  // K and V rows of one block: at most 2 x 32 rows of 8 x 4 x 34 bytes, 68 KB
+  const size_t smem = 2 * (size_t)bs * row_bytes;
   auto kern = (row_bytes % 16 == 0) ? stage_q8_f16_kernel<16> : stage_q8_f16_kernel<4>;
+  mt_status st = kernel_smem(reinterpret_cast<const void *>(kern), (int)smem,
+                             "cudaFuncSetAttribute(q8_0 staging smem)");
+  if (st != MT_OK) return st;
   return cuda_check(launch_pdl(kern, dim3(grid), dim3(256), smem, stream, k_pool, v_pool, table,
                                ctx, n_seqs, max_blocks, bs, n_phys, n_kv_heads * head_dim / 32,
                                row_bytes, k16, v16, table16, status),
