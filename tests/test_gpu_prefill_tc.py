@@ -143,3 +143,18 @@ def test_prefill_tc_q8_0_staged_flags_f16_overflow(mt):
     kp[cell, 2:34] = 127
     _, _, st = run_prefill(mt, w, q, q_start, kp, vp)
     assert st == mt.MT_ERR_DEVICE_CHECK
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8_0"])
+def test_prefill_tc_split_long_context(mt, fmt):
+    # one chunk of a long prompt: ~100 queries at the end of a context of
+    # 3000-4000 positions leave 32 tiles for 152 CTAs, so each tile's ~30
+    # chunks are cut into pieces whose records the combine merges (f16, and
+    # q8_0 through the staged rows)
+    rng = np.random.default_rng(89)
+    w = workloads.llama3_f16(seed=89, n_seqs=1, ctx_lo=3000, ctx_hi=4000, fmt=fmt)
+    n = 100
+    q_start = np.array([0, n], dtype=np.int32)
+    q = rng.standard_normal((n, w.n_heads, w.head_dim)).astype(np.float32)
+    kp, vp = oracle_pools(w)
+    check_pools(mt, w, q, q_start, kp, vp)
