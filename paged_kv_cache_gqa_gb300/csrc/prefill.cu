@@ -11,6 +11,12 @@
 // modes, read as logical positions). out = softmax-weighted V, lse = the
 // natural log-sum-exp of the scaled logits.
 //
+// Which kernel: head_dim 64 and 128 run the tcgen05 kernel (prefill_tc.cu) —
+// f16 pools directly, q8_0 pools after a pass that stages the call's blocks
+// as f16 rows, f32 pools after one that stages them as high / low f16 pairs.
+// The kernel below takes head_dim 256 (f16, q8_0) and calls too large to
+// stage.
+//
 // How (GB300): a tile is 64 rows (query token, head) of one KV head — 64/GP
 // consecutive queries of one sequence times the GP (padded) heads of the
 // group — and every block of the sequence up to the tile's last position.
@@ -39,19 +45,21 @@ constexpr uint64_t kPrefillWsBytes = 256;
 // (the kernel splits only while tiles are fewer than CTAs).
 constexpr int kSplitCtas = 160;
 
-// q8_0 pools on the tcgen05 kernel: the call's blocks staged as f16 rows
-// (launch_stage_q8_f16): a table of n_seqs x max_blocks staged ids, then the
-// K and the V f16 pools of n_seqs x max_blocks x block_size rows. 0 when the
-// call does not stage (other formats and shapes; staged ids that would not
-// fit the kernel's 32-bit cell indices: the mma.sync kernel runs instead).
-size_t q8_stage_bytes(const mt_paged_prefill_args *a) {
-  if (a->fmt != MT_KV_Q8_0 || !prefill_tc_supported(a->fmt, a->head_dim, a->block_size))
-    return 0;
+// q8_0 and f32 pools on the tcgen05 kernel: the call's blocks staged as f16
+// rows (launch_stage_q8_f16) or high / low f16 rows (launch_stage_f32_pair):
+// a table of n_seqs x max_blocks staged ids, then the K and the V staged
+// pools of n_seqs x max_blocks x block_size rows (2 or 4 bytes per value). 0
+// when the call does not stage (f16 pools, other shapes; staged ids that
+// would not fit the kernel's 32-bit cell indices: the mma.sync kernel runs
+// instead).
+size_t tc_stage_bytes(const mt_paged_prefill_args *a) {
+  if (a->fmt == MT_KV_F16 || !prefill_tc_supported(a->fmt, a->head_dim, a->block_size)) return 0;
   const long long cells = (long long)a->n_seqs * a->max_blocks * a->block_size;
   if (cells <= 0 || cells >= (1LL << 31)) return 0;
   auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  const size_t vb = a->fmt == MT_KV_F32 ? 4 : 2;
   return up((size_t)a->n_seqs * a->max_blocks * 4) +
-         2 * up((size_t)cells * a->n_kv_heads * a->head_dim * 2);
+         2 * up((size_t)cells * a->n_kv_heads * a->head_dim * vb);
 }
 
 // Bytes of split records a call may need: 0 unless the tensor-core kernel
@@ -361,7 +369,7 @@ using namespace mtkv;
 extern "C" size_t mt_paged_prefill_workspace_bytes(const mt_paged_prefill_args *a) {
   if (!a) return 0;
   const int G = a->n_kv_heads > 0 && a->n_heads % a->n_kv_heads == 0 ? a->n_heads / a->n_kv_heads : 0;
-  return kPrefillWsBytes + prefill_rec_bytes(a, G > 0 ? pad_g(G) : 0) + q8_stage_bytes(a);
+  return kPrefillWsBytes + prefill_rec_bytes(a, G > 0 ? pad_g(G) : 0) + tc_stage_bytes(a);
 }
 
 extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void *workspace,
@@ -391,7 +399,7 @@ extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void 
       !a->out)
     return fail(MT_ERR_INVALID_ARG, "prefill: null pointer");
   const size_t rec_bytes = prefill_rec_bytes(a, GP);
-  const size_t stage_bytes = q8_stage_bytes(a);
+  const size_t stage_bytes = tc_stage_bytes(a);
   const size_t need = kPrefillWsBytes + rec_bytes + stage_bytes;
   if (!workspace || workspace_bytes < need)
     return fail(MT_ERR_INVALID_ARG, "prefill: workspace missing or too small (need " +
@@ -430,9 +438,11 @@ extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void 
     p.rec_units = 2 * kSplitCtas;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // f16 pools, and q8_0 pools staged as f16 rows, run the tcgen05 kernel
+  // f16 pools, and q8_0 / f32 pools staged as f16 / high-low f16 rows, run
+  // the tcgen05 kernel
   const bool tc = a->fmt == MT_KV_F16 ? prefill_tc_supported(a->fmt, a->head_dim, a->block_size)
                                       : stage_bytes > 0;
+  const bool pair = a->fmt == MT_KV_F32;
   const int32_t *table = a->block_table;
   if (stage_bytes) {
     uint8_t *ws = static_cast<uint8_t *>(workspace) + kPrefillWsBytes + rec_bytes;
@@ -440,15 +450,22 @@ extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void 
     const size_t pb = (stage_bytes - tb) / 2;
     int32_t *table16 = reinterpret_cast<int32_t *>(ws);
     uint8_t *k16 = ws + tb, *v16 = ws + tb + pb;
-    st = launch_stage_q8_f16(p.k_pool, p.v_pool, a->block_table, a->context_lens, a->n_seqs,
-                             a->max_blocks, a->block_size, a->n_phys_blocks, a->n_kv_heads,
-                             a->head_dim, (int)rb, k16, v16, table16, p.status, di.n_sm * 8, s);
+    if (pair)
+      st = launch_stage_f32_pair(static_cast<const float *>(a->k_pool),
+                                 static_cast<const float *>(a->v_pool), a->block_table,
+                                 a->context_lens, a->n_seqs, a->max_blocks, a->block_size,
+                                 a->n_phys_blocks, a->n_kv_heads, a->head_dim, k16, v16, table16,
+                                 p.status, di.n_sm * 8, s);
+    else
+      st = launch_stage_q8_f16(p.k_pool, p.v_pool, a->block_table, a->context_lens, a->n_seqs,
+                               a->max_blocks, a->block_size, a->n_phys_blocks, a->n_kv_heads,
+                               a->head_dim, (int)rb, k16, v16, table16, p.status, di.n_sm * 8, s);
     if (st != MT_OK) return st;
     table = table16;
     p.k_pool = k16;
     p.v_pool = v16;
     p.n_phys = (long long)a->n_seqs * a->max_blocks;
-    p.row_bytes = a->n_kv_heads * a->head_dim * 2;
+    p.row_bytes = a->n_kv_heads * a->head_dim * (pair ? 4 : 2);
   }
   // sequences are independent: launch in chunks of kMaxPrefillSeqs (query
   // rows stay absolute, so only the per-sequence arrays are offset)
@@ -461,7 +478,7 @@ extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void 
       // the tcgen05 kernel, one CTA (all 512 tensor-memory columns, ~198 KB
       // of shared memory for head_dim 128) per SM, then the merge of split
       // tiles (returns at once when nothing was split)
-      st = launch_prefill_tc(p, a->head_dim, GP, di.n_sm, s);
+      st = launch_prefill_tc(p, a->head_dim, GP, pair, di.n_sm, s);
       if (st != MT_OK) return st;
       st = launch_prefill_tc_combine(p, a->head_dim, di.n_sm, s);
       if (st != MT_OK) return st;

@@ -39,7 +39,7 @@ struct PrefillParams {
 };
 
 // tcgen05 prefill kernel (f16 pools, head_dim 64 or 128, block_size 16 or 32;
-// q8_0 pools of those shapes through rows staged as f16, below).
+// q8_0 and f32 pools of those shapes through staged rows, below).
 bool prefill_tc_supported(mt_kv_format fmt, int head_dim, int block_size);
 
 // q8_0 pools on the tcgen05 kernel: the blocks a prefill call reads, staged
@@ -55,11 +55,23 @@ mt_status launch_stage_q8_f16(const uint8_t *k_pool, const uint8_t *v_pool, cons
                               long long n_phys, int n_kv_heads, int head_dim, int row_bytes,
                               uint8_t *k16, uint8_t *v16, int32_t *table16, uint32_t *status,
                               int n_ctas, cudaStream_t stream);
+// f32 pools on the tcgen05 kernel: the blocks a prefill call reads, staged
+// as high / low f16 pairs, numbered as launch_stage_q8_f16 numbers them. A
+// staged row is the high f16 image of the row's n_kv_heads * head_dim values
+// (x rounded to the nearest f16), then the low one (x - high, rounded): rows
+// of n_kv_heads * head_dim * 4 bytes in k16 / v16. A value whose high part is
+// infinite (outside the f16 range) is flagged in *status.
+mt_status launch_stage_f32_pair(const float *k_pool, const float *v_pool, const int32_t *table,
+                                const int32_t *ctx, int n_seqs, int max_blocks, int bs,
+                                long long n_phys, int n_kv_heads, int head_dim, uint8_t *k16,
+                                uint8_t *v16, int32_t *table16, uint32_t *status, int n_ctas,
+                                cudaStream_t stream);
 // Merge the split pieces' records of the last tcgen05 launch (returns at once
 // when it did not split).
 mt_status launch_prefill_tc_combine(const PrefillParams &p, int head_dim, int n_ctas,
                                     cudaStream_t stream);
-mt_status launch_prefill_tc(const PrefillParams &p, int head_dim, int gp, int n_ctas,
+// pair: the pools' rows are high / low f16 images (launch_stage_f32_pair).
+mt_status launch_prefill_tc(const PrefillParams &p, int head_dim, int gp, bool pair, int n_ctas,
                             cudaStream_t stream);
 
 }  // namespace mtkv

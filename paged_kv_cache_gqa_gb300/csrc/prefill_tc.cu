@@ -1,5 +1,6 @@
 // Multi-query (prefill) paged attention on the 5th-generation tensor cores
-// (tcgen05, tensor-memory accumulators), for f16 pools.
+// (tcgen05, tensor-memory accumulators), for f16 pools; q8_0 pools staged as
+// f16 rows and f32 pools staged as high / low f16 pairs take the same kernel.
 //
 // What is computed — exactly what prefill.cu computes (see there): for query
 // row i of sequence s at position ctx - n + j, softmax-weighted V over the
@@ -84,13 +85,16 @@ constexpr int kQLoCol = 448;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxSplit = 16;       // pieces per tile when tiles are fewer than CTAs
 
-template <int D>
+// PAIR: the pools hold each value as a high / low f16 pair (f32 pools,
+// staged), so a chunk's K (or V) is two f16 images, high then low.
+template <int D, bool PAIR>
 struct TcCfg {
   static constexpr int HALVES = D / 64;                 // 64-dim halves of a head
   static constexpr int QSTAGE = D * 512;  // the next tile's Q staged: 128 rows x D x (high, low) f16
-  static constexpr int KVB = HALVES * kChunk * 128;     // K (or V) of one chunk
+  static constexpr int PART = HALVES * kChunk * 128;    // one f16 image of a chunk's K (or V)
+  static constexpr int KVB = (PAIR ? 2 : 1) * PART;     // K (or V) of one chunk
   static constexpr int STAGE = 2 * KVB;                 // K and V of one chunk
-  static constexpr int STAGES = D == 64 ? 4 : 2;
+  static constexpr int STAGES = (D == 64 ? 4 : 2) / (PAIR ? 2 : 1);
   static constexpr int SMEM = 1024 + QSTAGE + STAGES * STAGE;
   // per softmax thread: dims of its part of the row (Q and O), Q slices of 8
   // dims; its warp's region of the Q staging area, and the output box
@@ -102,8 +106,10 @@ struct TcCfg {
   static_assert(REGION >= 2 * NSL * 512 && REGION >= (DT / CB) * 32 * CB * 4, "staging region");
   static_assert(DT >= 16 && (CB == 16 || CB == 32), "output box");
 };
-static_assert(TcCfg<128>::SMEM + 12 * 1024 <= 227 * 1024, "shared memory");
-static_assert(TcCfg<64>::SMEM + 12 * 1024 <= 227 * 1024, "shared memory");
+static_assert(TcCfg<128, false>::SMEM + 12 * 1024 <= 227 * 1024, "shared memory");
+static_assert(TcCfg<64, false>::SMEM + 12 * 1024 <= 227 * 1024, "shared memory");
+static_assert(TcCfg<128, true>::SMEM + 12 * 1024 <= 227 * 1024, "shared memory");
+static_assert(TcCfg<64, true>::SMEM + 12 * 1024 <= 227 * 1024, "shared memory");
 
 // 2^x by the hardware approximation (relative error ~2^-22, 2^-inf = 0):
 // far below the f16 rounding the probabilities get right after.
@@ -336,11 +342,14 @@ struct TcMaps {
 };
 
 // SPLIT: the launch may cut tiles into pieces (records given); without it the
-// piece count is the constant 1 and every unit is a whole tile.
-template <int D, int GP, bool SPLIT>
+// piece count is the constant 1 and every unit is a whole tile. PAIR: rows of
+// the pools are a high f16 image of the values, then a low one (f32 pools,
+// staged): S takes Q_lo K_hi and Q_hi K_lo besides Q_hi K_hi, and P.V
+// takes P_lo V_hi and P_hi V_lo besides P_hi V_hi.
+template <int D, int GP, bool SPLIT, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ TcMaps maps) {
-  using C = TcCfg<D>;
+  using C = TcCfg<D, PAIR>;
   constexpr int ST = C::STAGES;
   constexpr int R_RUNS = MT_KV_MAP_MAX_SPANS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -487,16 +496,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
           mask_s[kv][st][0] = ((uint64_t)w1 << 32) | w0;
           mask_s[kv][st][1] = ((uint64_t)w3 << 32) | w2;
-          mbar_arrive_expect_tx(&full[st], (uint32_t)(n_valid * C::HALVES * 128) << bs_shift);
+          mbar_arrive_expect_tx(&full[st], (uint32_t)(n_valid * C::KVB / kChunk) << bs_shift);
         }
         __syncwarp();
-        // one copy per (block, 64-dim half): lane = k * HALVES + h
+        // one copy per (block, 64-dim half): lane = k * HALVES + h (PAIR: and
+        // one of the low image, Hkv heads further along the row)
         const int k = lane / C::HALVES, h = lane % C::HALVES;
         const int pk = __shfl_sync(kAll, phys, k & 31);
         if (k < nb && pk >= 0) {
           const uint32_t dst = smem_u32(ring) + (uint32_t)(st * C::STAGE + kv * C::KVB +
                                                            h * (kChunk * 128) + (k << bs_shift) * 128);
           tma_rows(dst, map, tl.kvh * C::HALVES + h, pk << bs_shift, &full[st]);
+          if constexpr (PAIR)
+            tma_rows(dst + C::PART, map, (p.Hkv + tl.kvh) * C::HALVES + h, pk << bs_shift,
+                     &full[st]);
         }
       }
       un = nx;
@@ -557,6 +570,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint64_t bd = tc::desc_advance(kd, (uint32_t)(hf * kChunk * 128 + kk * 32));
                 tc::mma_f16_ts(dcol, tmem + kQHiCol + qc, bd, idesc_s, hf + kk > 0);
                 tc::mma_f16_ts(dcol, tmem + kQLoCol + qc, bd, idesc_s, true);
+                if constexpr (PAIR)
+                  tc::mma_f16_ts(dcol, tmem + kQHiCol + qc, tc::desc_advance(bd, C::PART),
+                                 idesc_s, true);
               }
             tc::commit(&s_full[x & 1]);
             tc::commit(&k_free[st]);
@@ -573,8 +589,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint64_t vm0 = mask_s[1][st][0], vm1 = mask_s[1][st][1];
         if ((vm0 & vm1) != ~0ull) {
           uint8_t *vt = ring + (size_t)st * C::STAGE + C::KVB;
-          for (int u = lane; u < kChunk * C::HALVES * 8; u += 32) {
-            const int line = u >> 3, r = line & (kChunk - 1);  // line = half * 128 + row
+          for (int u = lane; u < C::KVB / 16; u += 32) {
+            // line = (image * HALVES + half) * 128 + row
+            const int line = u >> 3, r = line & (kChunk - 1);
             if (!(((r < 64 ? vm0 : vm1) >> (r & 63)) & 1ull))
               *reinterpret_cast<uint4 *>(vt + (size_t)line * 128 + (u & 7) * 16) =
                   make_uint4(0, 0, 0, 0);
@@ -598,9 +615,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint64_t vd = tc::desc_advance(d_v, (uint32_t)(st * C::STAGE));
           const uint32_t pa = tmem + (uint32_t)((x & 1) * kSCols);
 #pragma unroll
-          for (int kk = 0; kk < kChunk / 16; ++kk)
-            tc::mma_f16_ts(tmem + kOCol, pa + (kk / (kHC / 16)) * kHC + (kk % (kHC / 16)) * 8,
-                           tc::desc_advance(vd, kk * 2048), idesc_o, c > un.cb || kk > 0);
+          for (int kk = 0; kk < kChunk / 16; ++kk) {
+            const uint32_t pc = pa + (kk / (kHC / 16)) * kHC + (kk % (kHC / 16)) * 8;
+            const uint64_t vk = tc::desc_advance(vd, kk * 2048);
+            tc::mma_f16_ts(tmem + kOCol, pc, vk, idesc_o, c > un.cb || kk > 0);
+            if constexpr (PAIR) {
+              // P_lo: the second half of the thread's columns
+              tc::mma_f16_ts(tmem + kOCol, pc + kHC / 2, vk, idesc_o, true);
+              tc::mma_f16_ts(tmem + kOCol, pc, tc::desc_advance(vk, C::PART), idesc_o, true);
+            }
+          }
           tc::commit(&pv_done[x & 1]);
           tc::commit(&v_free[st]);
         }
@@ -856,18 +880,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float ls[4] = {0.f, 0.f, 0.f, 0.f};  // two packed pairs of partial sums
         const float mr = m_run == -INFINITY ? 0.f : m_run;  // all sv are -inf then: p = 0
         const uint32_t p_row = s_row;
+        if constexpr (PAIR) {
+          // p as high and low f16 (p = high + low to ~2^-22): the high pairs
+          // over the first HC / 2 of the thread's columns, the low over the rest
 #pragma unroll
-        for (int e = 0; e < HC; e += 32) {
-          uint32_t h[16];
+          for (int e = 0; e < HC; e += 16) {
+            uint32_t h[8], l[8];
 #pragma unroll
-          for (int k2 = 0; k2 < 16; ++k2) {
-            float u, w;
-            add2(sv[e + 2 * k2], sv[e + 2 * k2 + 1], -mr, u, w);
-            const float a = ex2(u), b = ex2(w);
-            acc2(ls[2 * (k2 & 1)], ls[2 * (k2 & 1) + 1], a, b);
-            h[k2] = h2_bits(__floats2half2_rn(a, b));
+            for (int k2 = 0; k2 < 8; ++k2) {
+              float u, w;
+              add2(sv[e + 2 * k2], sv[e + 2 * k2 + 1], -mr, u, w);
+              const float a = ex2(u), b = ex2(w);
+              acc2(ls[2 * (k2 & 1)], ls[2 * (k2 & 1) + 1], a, b);
+              split_h2(a, b, h[k2], l[k2]);
+            }
+            tc::st8u(p_row + (uint32_t)(e / 2), h);
+            tc::st8u(p_row + (uint32_t)(HC / 2 + e / 2), l);
           }
-          tc::st16u(p_row + (uint32_t)(e / 2), h);
+        } else {
+#pragma unroll
+          for (int e = 0; e < HC; e += 32) {
+            uint32_t h[16];
+#pragma unroll
+            for (int k2 = 0; k2 < 16; ++k2) {
+              float u, w;
+              add2(sv[e + 2 * k2], sv[e + 2 * k2 + 1], -mr, u, w);
+              const float a = ex2(u), b = ex2(w);
+              acc2(ls[2 * (k2 & 1)], ls[2 * (k2 & 1) + 1], a, b);
+              h[k2] = h2_bits(__floats2half2_rn(a, b));
+            }
+            tc::st16u(p_row + (uint32_t)(e / 2), h);
+          }
         }
         l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         tc::wait_st();
@@ -1144,10 +1187,63 @@ __global__ void __launch_bounds__(256) stage_q8_f16_kernel(
   }
 }
 
-template <int D, int GP, bool SPLIT>
+// f32 rows -> high / low f16 rows for the tensor-core prefill: value x
+// becomes high = x rounded to the nearest f16 and low = (x - high) rounded
+// to the nearest f16 (high + low = x to ~2^-22 relative for |x| inside the
+// f16 range; a value whose high part is infinite is flagged). A staged row
+// is the high image of the row's hd values, then the low image (hd * 4
+// bytes, as the f32 row). A CTA per (sequence, block) unit at a time, each
+// thread converting 4 consecutive values per step.
+__global__ void __launch_bounds__(256) stage_f32_pair_kernel(
+    const float *__restrict__ k_pool, const float *__restrict__ v_pool,
+    const int32_t *__restrict__ table, const int32_t *__restrict__ ctx, int n_seqs,
+    int max_blocks, int bs, long long n_phys, int hd, uint8_t *__restrict__ k16,
+    uint8_t *__restrict__ v16, int32_t *__restrict__ table16, uint32_t *status) {
+  pdl_enter();
+  const int tid = threadIdx.x, n4 = hd / 4;
+  const long long n_units = (long long)n_seqs * max_blocks;
+  for (long long unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+    const int s = (int)(unit / max_blocks), b = (int)(unit % max_blocks);
+    const int c = max(ctx[s], 0);
+    int phys = b * bs < c ? table[unit] : -1;
+    if (phys < -1 || (phys >= 0 && (long long)phys >= n_phys)) {
+      if (tid == 0) report(status, MT_STATUS_BIT_DEVICE_CHECK);
+      phys = -1;
+    }
+    if (tid == 0) table16[unit] = phys >= 0 ? (int32_t)unit : -1;
+    if (phys < 0) continue;
+    const int n_valid = min(bs, c - b * bs);  // rows inside the context
+    bool big = false;
+#pragma unroll 1
+    for (int kv = 0; kv < 2; ++kv) {
+      const float4 *src =
+          reinterpret_cast<const float4 *>((kv ? v_pool : k_pool) + (size_t)phys * bs * hd);
+      uint2 *dst = reinterpret_cast<uint2 *>((kv ? v16 : k16) + (size_t)unit * bs * hd * 4);
+      for (int i = tid; i < bs * n4; i += 256) {
+        const int r = i / n4, e = i - r * n4;
+        const float4 x = __ldg(src + i);
+        uint32_t h0, l0, h1, l1;
+        split_h2(x.x, x.y, h0, l0);
+        split_h2(x.z, x.w, h1, l1);
+        uint2 *row = dst + (size_t)r * (hd / 2);  // hd * 4 bytes = hd / 2 eight-byte words
+        row[e] = make_uint2(h0, h1);
+        row[n4 + e] = make_uint2(l0, l1);
+        if (r < n_valid) {
+          const __half2 a = *reinterpret_cast<const __half2 *>(&h0);
+          const __half2 d = *reinterpret_cast<const __half2 *>(&h1);
+          big |= __hisinf(__low2half(a)) || __hisinf(__high2half(a)) ||
+                 __hisinf(__low2half(d)) || __hisinf(__high2half(d));
+        }
+      }
+    }
+    if (big) report(status, MT_STATUS_BIT_DEVICE_CHECK);
+  }
+}
+
+template <int D, int GP, bool SPLIT, bool PAIR>
 mt_status launch_t(const PrefillParams &p, const TcMaps &m, int n_ctas, cudaStream_t s) {
-  auto kern = prefill_tc_kernel<D, GP, SPLIT>;
-  constexpr int smem = TcCfg<D>::SMEM;
+  auto kern = prefill_tc_kernel<D, GP, SPLIT, PAIR>;
+  constexpr int smem = TcCfg<D, PAIR>::SMEM;
   mt_status st = kernel_smem(reinterpret_cast<const void *>(kern), smem,
                              "cudaFuncSetAttribute(prefill tc smem)");
   if (st != MT_OK) return st;
@@ -1155,26 +1251,27 @@ mt_status launch_t(const PrefillParams &p, const TcMaps &m, int n_ctas, cudaStre
                     "prefill tc kernel launch");
 }
 
-template <int D, bool SPLIT>
+template <int D, bool SPLIT, bool PAIR>
 mt_status launch_g(int gp, const PrefillParams &p, const TcMaps &m, int n_ctas, cudaStream_t s) {
   switch (gp) {
-    case 1: return launch_t<D, 1, SPLIT>(p, m, n_ctas, s);
-    case 2: return launch_t<D, 2, SPLIT>(p, m, n_ctas, s);
-    case 4: return launch_t<D, 4, SPLIT>(p, m, n_ctas, s);
-    default: return launch_t<D, 8, SPLIT>(p, m, n_ctas, s);
+    case 1: return launch_t<D, 1, SPLIT, PAIR>(p, m, n_ctas, s);
+    case 2: return launch_t<D, 2, SPLIT, PAIR>(p, m, n_ctas, s);
+    case 4: return launch_t<D, 4, SPLIT, PAIR>(p, m, n_ctas, s);
+    default: return launch_t<D, 8, SPLIT, PAIR>(p, m, n_ctas, s);
   }
 }
 
-template <int D>
+template <int D, bool PAIR>
 mt_status launch_d(int gp, const PrefillParams &p, const TcMaps &m, int n_ctas, cudaStream_t s) {
-  return p.rec ? launch_g<D, true>(gp, p, m, n_ctas, s) : launch_g<D, false>(gp, p, m, n_ctas, s);
+  return p.rec ? launch_g<D, true, PAIR>(gp, p, m, n_ctas, s)
+               : launch_g<D, false, PAIR>(gp, p, m, n_ctas, s);
 }
 
 }  // namespace
 
 bool prefill_tc_supported(mt_kv_format fmt, int head_dim, int block_size) {
-  return (fmt == MT_KV_F16 || fmt == MT_KV_Q8_0) && (head_dim == 64 || head_dim == 128) &&
-         (block_size == 16 || block_size == 32);
+  return (fmt == MT_KV_F16 || fmt == MT_KV_Q8_0 || fmt == MT_KV_F32) &&
+         (head_dim == 64 || head_dim == 128) && (block_size == 16 || block_size == 32);
 }
 
 mt_status launch_stage_q8_f16(const uint8_t *k_pool, const uint8_t *v_pool, const int32_t *table,
@@ -1197,6 +1294,20 @@ mt_status launch_stage_q8_f16(const uint8_t *k_pool, const uint8_t *v_pool, cons
                     "q8_0 -> f16 staging launch");
 }
 
+mt_status launch_stage_f32_pair(const float *k_pool, const float *v_pool, const int32_t *table,
+                                const int32_t *ctx, int n_seqs, int max_blocks, int bs,
+                                long long n_phys, int n_kv_heads, int head_dim, uint8_t *k16,
+                                uint8_t *v16, int32_t *table16, uint32_t *status, int n_ctas,
+                                cudaStream_t stream) {
+  const long long units = (long long)n_seqs * max_blocks;
+  if (units == 0) return MT_OK;
+  const int grid = (int)std::min<long long>(units, (long long)n_ctas);
+  return cuda_check(launch_pdl(stage_f32_pair_kernel, dim3(grid), dim3(256), 0, stream, k_pool,
+                               v_pool, table, ctx, n_seqs, max_blocks, bs, n_phys,
+                               n_kv_heads * head_dim, k16, v16, table16, status),
+                    "f32 -> high / low f16 staging launch");
+}
+
 mt_status launch_prefill_tc_combine(const PrefillParams &p, int head_dim, int n_ctas,
                                     cudaStream_t stream) {
   if (!p.rec) return MT_OK;
@@ -1205,9 +1316,10 @@ mt_status launch_prefill_tc_combine(const PrefillParams &p, int head_dim, int n_
                     "prefill tc combine launch");
 }
 
-mt_status launch_prefill_tc(const PrefillParams &p, int head_dim, int gp, int n_ctas,
+mt_status launch_prefill_tc(const PrefillParams &p, int head_dim, int gp, bool pair, int n_ctas,
                             cudaStream_t stream) {
-  // the pools as [cell][128-byte chunk][64 f16]; one copy = bs cells of one chunk
+  // the pools as [cell][128-byte chunk][64 f16] (pair: the chunks of the high
+  // image, then those of the low); one copy = bs cells of one chunk
   const long long n_cells = p.n_phys * p.bs;
   TcMaps m;
   mt_status st = encode_pool_map_3d(&m.k, p.k_pool, n_cells, (size_t)p.row_bytes, 1, p.bs);
@@ -1219,13 +1331,16 @@ mt_status launch_prefill_tc(const PrefillParams &p, int head_dim, int gp, int n_
   m.o_ok = 0;
   if ((reinterpret_cast<uintptr_t>(p.out) & 15u) == 0 && p.n_tok > 0) {
     const int gpe = gp == 1 || gp == 2 || gp == 4 ? gp : 8;  // as launch_g instantiates
-    const int cb = std::min(head_dim / kTPR, 32);             // TcCfg<D>::CB
+    const int cb = std::min(head_dim / kTPR, 32);             // TcCfg<D, PAIR>::CB
     st = encode_out_map_f32(&m.o, p.out, p.n_tok, p.Hq, head_dim, cb, p.G, 32 / gpe);
     if (st != MT_OK) return st;
     m.o_ok = 1;
   }
-  return head_dim == 64 ? launch_d<64>(gp, p, m, n_ctas, stream)
-                        : launch_d<128>(gp, p, m, n_ctas, stream);
+  if (pair)
+    return head_dim == 64 ? launch_d<64, true>(gp, p, m, n_ctas, stream)
+                          : launch_d<128, true>(gp, p, m, n_ctas, stream);
+  return head_dim == 64 ? launch_d<64, false>(gp, p, m, n_ctas, stream)
+                        : launch_d<128, false>(gp, p, m, n_ctas, stream);
 }
 
 }  // namespace mtkv

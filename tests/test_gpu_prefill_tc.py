@@ -1,9 +1,11 @@
-"""GPU parity of the tcgen05 prefill kernel (f16 pools) at sizes that drive
-its pipeline: contexts of many 128-token chunks, more tiles than CTAs (tile
+"""GPU parity of the tcgen05 prefill kernel (f16 pools; q8_0 pools staged as
+f16 rows, f32 pools staged as high / low f16 pairs) at sizes that drive its
+pipeline: contexts of many 128-token chunks, more tiles than CTAs (tile
 changes with the next tile's query staged during the current one), running
 maxima that grow past the lazy-rescale threshold in every chunk, and more
-sequences than one launch takes. The oracle and tolerance are those of the
-other prefill tests (f16: 2e-3 on outputs and log-sum-exp).
+sequences than one launch takes. The oracle and tolerances are those of the
+other prefill tests (f16 and q8_0: 2e-3, f32: 1e-4, on outputs and
+log-sum-exp).
 """
 import dataclasses
 
@@ -47,14 +49,16 @@ def test_prefill_tc_long_contexts_many_tiles(mt):
     check_pools(mt, w, q, q_start, kp, vp)
 
 
+@pytest.mark.parametrize("fmt", ["f16", "f32"])
 @pytest.mark.parametrize("d", [64, 128])
-def test_prefill_tc_rescales_growing_maxima(mt, d):
+def test_prefill_tc_rescales_growing_maxima(mt, d, fmt):
     # scores that grow by ~8.5 (base 2) per 128 tokens: every chunk raises the
     # running maximum past the 2^8 threshold, so the output row in tensor
-    # memory is rescaled in every chunk
+    # memory is rescaled in every chunk (f32: probabilities up to 2^8 as
+    # high / low f16 pairs)
     rng = np.random.default_rng(82 + d)
     w = workloads.llama3_f16(seed=82 + d, n_seqs=2, ctx_lo=500, ctx_hi=640, n_heads=4,
-                             n_kv_heads=1, head_dim=d)
+                             n_kv_heads=1, head_dim=d, fmt=fmt)
     u = np.ones(d, dtype=np.float32) / np.sqrt(d)
     k_hist = w.k_hist.copy()
     for s in range(w.n_seqs):
@@ -145,12 +149,44 @@ def test_prefill_tc_q8_0_staged_flags_f16_overflow(mt):
     assert st == mt.MT_ERR_DEVICE_CHECK
 
 
-@pytest.mark.parametrize("fmt", ["f16", "q8_0"])
+@pytest.mark.parametrize("d,bs,hq,hkv", [(128, 16, 32, 8), (128, 32, 12, 2), (64, 16, 8, 2),
+                                         (64, 32, 9, 3)])
+def test_prefill_tc_f32_paired(mt, d, bs, hq, hkv):
+    # f32 pools run the tcgen05 kernel on rows staged as high / low f16
+    # pairs (x = high + low to ~2^-22), scores and P.V each from three
+    # products: contexts of several 128-token chunks, many tiles, a hole,
+    # against the oracle at the f32 tolerance
+    rng = np.random.default_rng(90 + d + bs + hq)
+    w = workloads.llama3_f16(seed=90 + d + bs, n_seqs=3, ctx_lo=500, ctx_hi=900, fmt="f32",
+                             block_size=bs, n_heads=hq, n_kv_heads=hkv, head_dim=d)
+    table = w.block_table.copy()
+    table[1, 2] = -1
+    w = dataclasses.replace(w, block_table=table)
+    q, q_start = make_queries(w, rng, 260)
+    kp, vp = oracle_pools(w)
+    check_pools(mt, w, q, q_start, kp, vp)
+
+
+def test_prefill_tc_f32_flags_f16_overflow(mt):
+    # an f32 value outside the f16 range (1e5) has no high / low f16 pair:
+    # the staging pass flags it
+    rng = np.random.default_rng(91)
+    w = workloads.llama3_f16(seed=91, n_seqs=2, ctx_lo=100, ctx_hi=200, fmt="f32")
+    q, q_start = make_queries(w, rng, 20)
+    kp, vp = oracle_pools(w)
+    cell = int(w.block_table[1, 0]) * w.block_size + 3  # position 3 of sequence 1
+    vp = vp.copy()
+    vp[cell, 5 * 4:6 * 4] = np.frombuffer(np.float32(1.0e5).tobytes(), dtype=np.uint8)
+    _, _, st = run_prefill(mt, w, q, q_start, kp, vp)
+    assert st == mt.MT_ERR_DEVICE_CHECK
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "f32"])
 def test_prefill_tc_split_long_context(mt, fmt):
     # one chunk of a long prompt: ~100 queries at the end of a context of
     # 3000-4000 positions leave 32 tiles for 152 CTAs, so each tile's ~30
     # chunks are cut into pieces whose records the combine merges (f16, and
-    # q8_0 through the staged rows)
+    # q8_0 and f32 through their staged rows)
     rng = np.random.default_rng(89)
     w = workloads.llama3_f16(seed=89, n_seqs=1, ctx_lo=3000, ctx_hi=4000, fmt=fmt)
     n = 100
