@@ -19,7 +19,8 @@
 //     ahead) and stage its K and its V head slices with one tensor copy (TMA,
 //     128-byte swizzle) per block and 64-dim half into two rings of stages; a
 //     K stage is refilled as soon as its scores are computed, a V stage once
-//     its P.V has run; holes are not read at all;
+//     its P.V has run (a ring of a single stage, f32 pools at head_dim 128,
+//     fills and frees each stage by halves); holes are not read at all;
 //   * one MMA warp computes S(c) = Q_hi K^T + Q_lo K^T (M = 128, N = 128,
 //     f16 in, f32 accumulated in tensor memory; q = Q_hi + Q_lo to ~2^-22, so
 //     scores keep float32 accuracy; Q read from tensor memory, so only K
@@ -351,11 +352,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ TcMaps maps) {
   using C = TcCfg<D, PAIR>;
   constexpr int ST = C::STAGES;
+  // a ring of one stage (PAIR, head_dim 128) fills and frees each stage in
+  // two halves with barriers of their own, so half of the next chunk loads
+  // while the MMAs read the other: K by 64-dim half (S takes one after the
+  // other), V by 64-token half (P.V likewise)
+  constexpr int NSB = ST == 1 ? 2 : 1;
+  static_assert(NSB == 1 || C::HALVES == 2, "K halves");
   constexpr int R_RUNS = MT_KV_MAP_MAX_SPANS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ int ts[kMaxPrefillSeqs + 1];
   __shared__ uint32_t tmem_slot;
-  __shared__ __align__(8) uint64_t k_full[ST], k_free[ST], v_full[ST], v_free[ST], s_full[2],
+  __shared__ __align__(8) uint64_t k_full[ST * NSB], k_free[ST * NSB], v_full[ST * NSB],
+      v_free[ST * NSB], s_full[2],
       p_full[2], pv_done[2], q_full, o_free, drain[2];
   __shared__ uint64_t mask_s[2][ST][2];  // [K / V] staged rows that hold data (not a hole, < ctx)
   __shared__ uint64_t smask_s[2][2];     // the same for the chunk of S(x), by x % 2
@@ -393,7 +401,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) ts[p.B] = run;
   }
   if (tid == 0) {
-    for (int k = 0; k < ST; ++k) {
+    for (int k = 0; k < ST * NSB; ++k) {
       mbar_init(&k_full[k], 1);
       mbar_init(&k_free[k], 1);
       mbar_init(&v_full[k], 1);
@@ -474,11 +482,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int phys = raw_next;
         raw_next = c + 1 < un.ce ? fetch(tl, c + 1) : (have_next ? fetch(nx.tl, nx.cb) : -1);
         const int st = g % ST;
-        if (g >= ST &&
-            !mbar_wait_bounded(&empty[st], (uint32_t)((g / ST) - 1) & 1u, &abort_s, wait_ns)) {
-          fine = false;
-          break;
-        }
         if (phys < -1 || (phys >= 0 && (long long)phys >= p.n_phys)) {
           report(p.status, MT_STATUS_BIT_DEVICE_CHECK);
           phys = -1;
@@ -492,24 +495,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t w1 = __reduce_or_sync(kAll, (uint32_t)(m0 >> 32));
         const uint32_t w2 = __reduce_or_sync(kAll, (uint32_t)m1);
         const uint32_t w3 = __reduce_or_sync(kAll, (uint32_t)(m1 >> 32));
-        const int n_valid = __popc(__ballot_sync(kAll, phys >= 0));
-        if (lane == 0) {
-          mask_s[kv][st][0] = ((uint64_t)w1 << 32) | w0;
-          mask_s[kv][st][1] = ((uint64_t)w3 << 32) | w2;
-          mbar_arrive_expect_tx(&full[st], (uint32_t)(n_valid * C::KVB / kChunk) << bs_shift);
-        }
-        __syncwarp();
+        const uint64_t mw0 = ((uint64_t)w1 << 32) | w0, mw1 = ((uint64_t)w3 << 32) | w2;
         // one copy per (block, 64-dim half): lane = k * HALVES + h (PAIR: and
-        // one of the low image, Hkv heads further along the row)
+        // one of the low image, Hkv heads further along the row); with two
+        // barriers per stage, the copy's half of the stage: its dim half (K)
+        // or its token half (V)
         const int k = lane / C::HALVES, h = lane % C::HALVES;
         const int pk = __shfl_sync(kAll, phys, k & 31);
-        if (k < nb && pk >= 0) {
-          const uint32_t dst = smem_u32(ring) + (uint32_t)(st * C::STAGE + kv * C::KVB +
-                                                           h * (kChunk * 128) + (k << bs_shift) * 128);
-          tma_rows(dst, map, tl.kvh * C::HALVES + h, pk << bs_shift, &full[st]);
-          if constexpr (PAIR)
-            tma_rows(dst + C::PART, map, (p.Hkv + tl.kvh) * C::HALVES + h, pk << bs_shift,
-                     &full[st]);
+        const int sub = NSB == 1 ? 0 : kv ? (k << bs_shift) >> 6 : h;
+        bool waited = true;
+#pragma unroll
+        for (int j = 0; j < NSB; ++j) {
+          uint64_t *fb = &full[st * NSB + j];
+          if (g >= ST && !mbar_wait_bounded(&empty[st * NSB + j], (uint32_t)((g / ST) - 1) & 1u,
+                                            &abort_s, wait_ns)) {
+            // the copies already issued to the stage's first half land first
+            for (int j2 = 0; j2 < j; ++j2)
+              mbar_wait_bounded(&full[st * NSB + j2], (uint32_t)(g / ST) & 1u, &abort_s, wait_ns);
+            waited = false;
+            break;
+          }
+          const bool mine = k < nb && pk >= 0 && sub == j;
+          const uint32_t n_copies = __popc(__ballot_sync(kAll, mine));
+          if (lane == 0) {
+            // the row masks go with the first barrier (K: S reads both
+            // before its first MMA); V's token halves each with their own
+            if (NSB == 1 || kv == 0) {
+              if (j == 0) {
+                mask_s[kv][st][0] = mw0;
+                mask_s[kv][st][1] = mw1;
+              }
+            } else {
+              mask_s[kv][st][j] = j ? mw1 : mw0;
+            }
+            mbar_arrive_expect_tx(fb, (n_copies * (PAIR ? 2u : 1u) * 128u) << bs_shift);
+          }
+          __syncwarp();
+          if (mine) {
+            const uint32_t dst = smem_u32(ring) +
+                                 (uint32_t)(st * C::STAGE + kv * C::KVB + h * (kChunk * 128) +
+                                            (k << bs_shift) * 128);
+            tma_rows(dst, map, tl.kvh * C::HALVES + h, pk << bs_shift, fb);
+            if constexpr (PAIR)
+              tma_rows(dst + C::PART, map, (p.Hkv + tl.kvh) * C::HALVES + h, pk << bs_shift, fb);
+          }
+        }
+        if (!waited) {
+          fine = false;
+          break;
         }
       }
       un = nx;
@@ -520,7 +553,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int k = 0; k < ST; ++k) {
       if (g <= k) continue;
       const int gl = g - 1 - ((g - 1 - k) % ST);
-      if (!mbar_wait_bounded(&full[k], (uint32_t)(gl / ST) & 1u, &abort_s, wait_ns)) fine = false;
+      for (int j = 0; j < NSB; ++j)
+        if (!mbar_wait_bounded(&full[k * NSB + j], (uint32_t)(gl / ST) & 1u, &abort_s, wait_ns))
+          fine = false;
     }
   } else if (warp == kMmaWarpS || warp == kMmaWarpO) {
     // ================================================================= MMA
@@ -545,90 +580,135 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int x = g + (c - un.cb), st = x % ST;
         if (role == 0) {
           // S(x) = Q_hi K^T + Q_lo K^T into buffer x % 2, once K of chunk x
-          // is staged and P(x - 2) V has run (the softmax has then read
-          // S(x - 2) and its row mask, and P(x - 2) is no longer needed)
-          if (!mbar_wait_bounded(&k_full[st], (uint32_t)(x / ST) & 1u, &abort_s, wait_ns) ||
+          // is staged (two barriers per stage: its dim halves one after the
+          // other, each freed once its MMAs are done) and P(x - 2) V has run
+          // (the softmax has then read S(x - 2) and its row mask, and P(x -
+          // 2) is no longer needed)
+          if (!mbar_wait_bounded(&k_full[st * NSB], (uint32_t)(x / ST) & 1u, &abort_s, wait_ns) ||
               (x >= 2 && !mbar_wait_bounded(&pv_done[x & 1], (uint32_t)((x - 2) >> 1) & 1u,
                                             &abort_s, wait_ns))) {
             fine = false;
             break;
           }
-          tc::fence_after();
-          if (lane == 0) {
-            // the chunk's row mask goes with S(x) (the K stage may be refilled
-            // as soon as S(x) is done); published by this thread's arrive below
-            smask_s[x & 1][0] = mask_s[0][st][0];
-            smask_s[x & 1][1] = mask_s[0][st][1];
-            const uint64_t kd = tc::desc_advance(d_k, (uint32_t)(st * C::STAGE));
-            const uint32_t dcol = tmem + (uint32_t)((x & 1) * kSCols);
+          const uint64_t kd = tc::desc_advance(d_k, (uint32_t)(st * C::STAGE));
+          const uint32_t dcol = tmem + (uint32_t)((x & 1) * kSCols);
+          bool staged = true;
 #pragma unroll
-            for (int hf = 0; hf < C::HALVES; ++hf)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                // dims [64 hf + 16 kk, + 16): Q columns 32 hf + 8 kk of each half
-                const uint32_t qc = (uint32_t)(hf * 32 + kk * 8);
-                const uint64_t bd = tc::desc_advance(kd, (uint32_t)(hf * kChunk * 128 + kk * 32));
-                tc::mma_f16_ts(dcol, tmem + kQHiCol + qc, bd, idesc_s, hf + kk > 0);
-                tc::mma_f16_ts(dcol, tmem + kQLoCol + qc, bd, idesc_s, true);
-                if constexpr (PAIR)
-                  tc::mma_f16_ts(dcol, tmem + kQHiCol + qc, tc::desc_advance(bd, C::PART),
-                                 idesc_s, true);
+          for (int j = 0; j < NSB; ++j) {
+            if (j > 0 && !mbar_wait_bounded(&k_full[st * NSB + j], (uint32_t)(x / ST) & 1u,
+                                            &abort_s, wait_ns)) {
+              staged = false;
+              break;
+            }
+            tc::fence_after();
+            if (lane == 0) {
+              if (j == 0) {
+                // the chunk's row mask goes with S(x) (the K stage may be
+                // refilled as soon as S(x) is done); published by this
+                // thread's arrive below
+                smask_s[x & 1][0] = mask_s[0][st][0];
+                smask_s[x & 1][1] = mask_s[0][st][1];
               }
-            tc::commit(&s_full[x & 1]);
-            tc::commit(&k_free[st]);
-            mbar_arrive(&s_full[x & 1]);
+#pragma unroll
+              for (int hf = j * (C::HALVES / NSB); hf < (j + 1) * (C::HALVES / NSB); ++hf)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                  // dims [64 hf + 16 kk, + 16): Q columns 32 hf + 8 kk of each half
+                  const uint32_t qc = (uint32_t)(hf * 32 + kk * 8);
+                  const uint64_t bd =
+                      tc::desc_advance(kd, (uint32_t)(hf * kChunk * 128 + kk * 32));
+                  tc::mma_f16_ts(dcol, tmem + kQHiCol + qc, bd, idesc_s, hf + kk > 0);
+                  tc::mma_f16_ts(dcol, tmem + kQLoCol + qc, bd, idesc_s, true);
+                  if constexpr (PAIR)
+                    tc::mma_f16_ts(dcol, tmem + kQHiCol + qc, tc::desc_advance(bd, C::PART),
+                                   idesc_s, true);
+                }
+              if (j == NSB - 1) {
+                tc::commit(&s_full[x & 1]);
+                tc::commit(&k_free[st * NSB + j]);
+                mbar_arrive(&s_full[x & 1]);
+              } else {
+                tc::commit(&k_free[st * NSB + j]);
+              }
+            }
+            __syncwarp();
           }
-          __syncwarp();
+          if (!staged) {
+            fine = false;
+            break;
+          }
           continue;
         }
-        // P.V: V of chunk x staged; its rows without data (holes, past the context) -> 0
-        if (!mbar_wait_bounded(&v_full[st], (uint32_t)(x / ST) & 1u, &abort_s, wait_ns)) {
-          fine = false;
-          break;
-        }
-        const uint64_t vm0 = mask_s[1][st][0], vm1 = mask_s[1][st][1];
-        if ((vm0 & vm1) != ~0ull) {
-          uint8_t *vt = ring + (size_t)st * C::STAGE + C::KVB;
-          for (int u = lane; u < C::KVB / 16; u += 32) {
-            // line = (image * HALVES + half) * 128 + row
-            const int line = u >> 3, r = line & (kChunk - 1);
-            if (!(((r < 64 ? vm0 : vm1) >> (r & 63)) & 1ull))
+        // P.V: V of chunk x staged (two barriers per stage: its token halves
+        // one after the other, each freed once its MMAs are done); its rows
+        // without data (holes, past the context) -> 0 first
+        uint8_t *vt = ring + (size_t)st * C::STAGE + C::KVB;
+        auto zero_rows = [&](int th, uint64_t m) {
+          // token half th: u = ((image * HALVES + dim half) * 64 + row) * 8 + 16-byte part
+          for (int u = lane; u < C::KVB / 32; u += 32) {
+            const int r = (u >> 3) & 63, line = (u >> 9) * kChunk + th * 64 + r;
+            if (!((m >> r) & 1ull))
               *reinterpret_cast<uint4 *>(vt + (size_t)line * 128 + (u & 7) * 16) =
                   make_uint4(0, 0, 0, 0);
           }
-          tc::fence_proxy_shared();
+        };
+        bool staged = true;
+#pragma unroll
+        for (int j = 0; j < NSB; ++j) {
+          if (!mbar_wait_bounded(&v_full[st * NSB + j], (uint32_t)(x / ST) & 1u, &abort_s,
+                                 wait_ns)) {
+            staged = false;
+            break;
+          }
+          bool zeroed = false;
+#pragma unroll
+          for (int th = j * (2 / NSB); th < (j + 1) * (2 / NSB); ++th) {
+            const uint64_t m = mask_s[1][st][th];
+            if (m != ~0ull) {
+              zero_rows(th, m);
+              zeroed = true;
+            }
+          }
+          if (zeroed) {
+            tc::fence_proxy_shared();
+            __syncwarp();
+          }
+          // P(x) written; before the tile's first P.V, the previous output read out
+          if (j == 0 &&
+              (!mbar_wait_bounded(&p_full[x & 1], (uint32_t)(x >> 1) & 1u, &abort_s, wait_ns) ||
+               (c == un.cb && k > 0 &&
+                !mbar_wait_bounded(&o_free, (uint32_t)(k - 1) & 1u, &abort_s, wait_ns)))) {
+            staged = false;
+            break;
+          }
+          tc::fence_after();
+          if (lane == 0) {
+            // O += P V (P from tensor memory, in S buffer x % 2: tokens
+            // [16 kk, 16 kk + 16) at column kHC (kk / J) + 8 (kk % J), J = kHC /
+            // 16 K steps per softmax thread's columns; V MN-major: LBO = the
+            // distance between its 64-dim halves)
+            const uint64_t vd = tc::desc_advance(d_v, (uint32_t)(st * C::STAGE));
+            const uint32_t pa = tmem + (uint32_t)((x & 1) * kSCols);
+#pragma unroll
+            for (int kk = j * (kChunk / 16 / NSB); kk < (j + 1) * (kChunk / 16 / NSB); ++kk) {
+              const uint32_t pc = pa + (kk / (kHC / 16)) * kHC + (kk % (kHC / 16)) * 8;
+              const uint64_t vk = tc::desc_advance(vd, kk * 2048);
+              tc::mma_f16_ts(tmem + kOCol, pc, vk, idesc_o, c > un.cb || kk > 0);
+              if constexpr (PAIR) {
+                // P_lo: the second half of the thread's columns
+                tc::mma_f16_ts(tmem + kOCol, pc + kHC / 2, vk, idesc_o, true);
+                tc::mma_f16_ts(tmem + kOCol, pc, tc::desc_advance(vk, C::PART), idesc_o, true);
+              }
+            }
+            if (j == NSB - 1) tc::commit(&pv_done[x & 1]);
+            tc::commit(&v_free[st * NSB + j]);
+          }
           __syncwarp();
         }
-        // P(x) written; before the tile's first P.V, the previous output read out
-        if (!mbar_wait_bounded(&p_full[x & 1], (uint32_t)(x >> 1) & 1u, &abort_s, wait_ns) ||
-            (c == un.cb && k > 0 &&
-             !mbar_wait_bounded(&o_free, (uint32_t)(k - 1) & 1u, &abort_s, wait_ns))) {
+        if (!staged) {
           fine = false;
           break;
         }
-        tc::fence_after();
-        if (lane == 0) {
-          // O += P V (P from tensor memory, in S buffer x % 2: tokens
-          // [16 kk, 16 kk + 16) at column kHC (kk / J) + 8 (kk % J), J = kHC /
-          // 16 K steps per softmax thread's columns; V MN-major: LBO = the
-          // distance between its 64-dim halves)
-          const uint64_t vd = tc::desc_advance(d_v, (uint32_t)(st * C::STAGE));
-          const uint32_t pa = tmem + (uint32_t)((x & 1) * kSCols);
-#pragma unroll
-          for (int kk = 0; kk < kChunk / 16; ++kk) {
-            const uint32_t pc = pa + (kk / (kHC / 16)) * kHC + (kk % (kHC / 16)) * 8;
-            const uint64_t vk = tc::desc_advance(vd, kk * 2048);
-            tc::mma_f16_ts(tmem + kOCol, pc, vk, idesc_o, c > un.cb || kk > 0);
-            if constexpr (PAIR) {
-              // P_lo: the second half of the thread's columns
-              tc::mma_f16_ts(tmem + kOCol, pc + kHC / 2, vk, idesc_o, true);
-              tc::mma_f16_ts(tmem + kOCol, pc, tc::desc_advance(vk, C::PART), idesc_o, true);
-            }
-          }
-          tc::commit(&pv_done[x & 1]);
-          tc::commit(&v_free[st]);
-        }
-        __syncwarp();
       }
       g += un.ce - un.cb;
     }
