@@ -215,10 +215,11 @@ typedef struct {
 } mt_paged_prefill_args;
 
 /* Workspace bytes mt_paged_attn_prefill needs (its first 4 bytes are the
- * device status word; zero them once after allocating). For q8_0 pools of
- * head_dim 64 or 128 it includes the f16 staging of the call's blocks:
- * n_seqs x max_blocks x block_size rows of n_kv_heads x head_dim f16 for K
- * and for V (plus a table of n_seqs x max_blocks ids). */
+ * device status word; zero them once after allocating). For q8_0 and f32
+ * pools of head_dim 64 or 128 it includes the staging of the call's blocks:
+ * n_seqs x max_blocks x block_size rows of n_kv_heads x head_dim f16 (q8_0)
+ * or f16 pairs (f32) for K and for V, plus a table of n_seqs x max_blocks
+ * ids. */
 size_t mt_paged_prefill_workspace_bytes(const mt_paged_prefill_args *args);
 
 /* Multi-query (prefill, or chunked prefill) attention through the paged
@@ -242,9 +243,13 @@ size_t mt_paged_prefill_workspace_bytes(const mt_paged_prefill_args *args);
  * after a pass that stages each block the call reads as f16 rows, every
  * value code * scale rounded once to the nearest f16 (relative error <=
  * 2^-11, inside the q8_0 tolerance; a staged value beyond the f16 range is
- * flagged in the status word); other pools run a warp-level tensor-core
- * kernel that keeps codes exact and applies scales in float32. The
- * workspace must be 16-byte aligned. */
+ * flagged in the status word); f32 pools of those head sizes after a pass
+ * that stages each value x as an f16 pair (x rounded, and the remainder
+ * rounded: x to ~2^-22 relative), scores and P.V each from three products
+ * (float32 accuracy; a value beyond the f16 range is flagged); head_dim 256
+ * runs a warp-level tensor-core kernel that keeps codes exact and applies
+ * scales in float32. The workspace (mt_paged_prefill_workspace_bytes) holds
+ * the staged rows of q8_0 and f32 calls and must be 16-byte aligned. */
 mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *args, void *workspace,
                                 size_t workspace_bytes, mt_stream stream);
 
