@@ -6,7 +6,8 @@ decode call in seconds, so each decode test runs the whole call on the GPU
 and compares a seeded sample of sequences — always including the longest
 and the shortest — with all their heads (f32 KV 1e-4, f16 and q8_0 2e-3);
 where the oracle is cheap enough (SmolLM2-shaped f32, the q8_0 shared
-prefix) every sequence is compared. Everything whose result must be
+prefix) every sequence is compared; the chunked prefill call compares a
+seeded sample of its query rows. Everything whose result must be
 bit-exact is compared in full: the stored rows (the whole pools after the
 call, so nothing else was written), the int4 scales, nibbles and
 dequantised blocks of every cold block, the 60 pools after the 1000-move
@@ -145,6 +146,67 @@ def test_full_llama3_q8_0_decode(mt, bs):
     want, want_lse = oracle_decode(w, kp, vp, seqs=seqs)
     _check(w, out.cpu().numpy(), want, seqs, f"q8_0 bs {bs} full size", lse.cpu().numpy(),
            want_lse)
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "f32"])
+def test_full_llama3_prefill(mt, fmt):
+    # the chunked-prefill benchmark's call: 16 sequences at context 2048 whose
+    # last 512 positions are queries (8192 query rows), 32/8 heads, d 128,
+    # bs 16, in its launch configuration (f16 pools directly, q8_0 and f32
+    # through their staging passes). A seeded sample of query rows of four
+    # sequences (always each one's first and last query) is checked with all
+    # heads: sampled row j of sequence s is the oracle's one-query sequence
+    # at context ctx - n + j + 1 over the same blocks
+    n_q = 512
+    w = workloads.llama3_f16(seed=3020, n_seqs=16, ctx_lo=2048, ctx_hi=2048, hist=False, fmt=fmt)
+    g = _gen(3021)
+    rng = np.random.default_rng(3023)
+    seqs = sorted({0, w.n_seqs - 1} | set(rng.choice(w.n_seqs, 2, replace=False).tolist()))
+    if fmt == "q8_0":
+        # the sampled sequences' blocks hold N(0,1) rows stored by the
+        # oracle's quantiser; the other blocks are zero (valid q8_0 cells)
+        rb = ofmt.row_bytes("q8_0", w.n_kv_heads, w.head_dim)
+        kp = np.zeros((w.n_cells, rb), np.uint8)
+        vp = np.zeros((w.n_cells, rb), np.uint8)
+        xr = np.random.default_rng(3022)
+        bs = w.block_size
+        for s in seqs:
+            nb = -(-int(w.context_lens[s]) // bs)
+            cells = (w.block_table[s, :nb].astype(np.int64)[:, None] * bs
+                     + np.arange(bs)).reshape(-1)
+            x = xr.standard_normal((2, nb * bs, w.n_kv_heads * w.head_dim), dtype=np.float32)
+            kp[cells] = ofmt.encode_rows("q8_0", x[0], w.n_kv_heads, w.head_dim)
+            vp[cells] = ofmt.encode_rows("q8_0", x[1], w.n_kv_heads, w.head_dim)
+        k_dev, v_dev = to_dev(kp), to_dev(vp)
+    else:
+        k_dev, v_dev = _randn_pools(w, g, torch.float32 if fmt == "f32" else torch.float16)
+        kp, vp = _host_bytes(k_dev), _host_bytes(v_dev)
+    q = torch.randn(n_q * w.n_seqs, w.n_heads, w.head_dim, generator=g, device="cuda")
+    q_start = torch.arange(0, n_q * w.n_seqs + 1, n_q, dtype=torch.int32, device="cuda")
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((q.shape[0], w.n_heads), float("nan"), device="cuda")
+    a = mt.prefill_args(fmt, q, k_dev, v_dev, to_dev(w.block_table), to_dev(w.context_lens),
+                        q_start, out, n_kv_heads=w.n_kv_heads, block_size=w.block_size,
+                        n_phys_blocks=w.n_phys_blocks, scale=w.scale, lse=lse)
+    ws = torch.zeros(mt.mt_paged_prefill_workspace_bytes(a), dtype=torch.uint8, device="cuda")
+    mt.mt_paged_attn_prefill(a, ws)
+    assert mt.mt_check_device_status(ws) == 0, mt.mt_last_error()
+    got, got_lse = out.cpu().numpy(), lse.cpu().numpy()
+    assert np.isfinite(got).all(), f"{fmt} prefill full size: non-finite output"
+    rows, ctx_sub, tab_sub = [], [], []
+    for s in seqs:
+        c = int(w.context_lens[s])
+        for j in sorted({0, n_q - 1} | set(rng.choice(n_q, 4, replace=False).tolist())):
+            rows.append(s * n_q + j)
+            ctx_sub.append(c - n_q + j + 1)
+            tab_sub.append(w.block_table[s])
+    q_sub = q.cpu().numpy()[rows]
+    want, want_lse = oatt.paged_attn_prefill(
+        fmt, q_sub, kp, vp, np.stack(tab_sub), np.array(ctx_sub, np.int32),
+        np.arange(len(rows) + 1, dtype=np.int32), None, None, w.n_heads, w.n_kv_heads,
+        w.head_dim, w.block_size, w.scale)
+    assert_close(got[rows], want, TOL[fmt], f"{fmt} prefill full size")
+    assert_lse(got_lse[rows], want_lse, TOL[fmt], f"{fmt} prefill full size")
 
 
 @pytest.mark.parametrize("prefix", ["cascade", "plain"])
