@@ -924,8 +924,9 @@ def main():
                              "llama3_formats", "prefill_f16", "prefill_f16_long"],
                     help="llama3_f16 is the benchmark line; the others measure the other kernels")
     ap.add_argument("--prefill-format", default="f16", choices=["f16", "q8_0", "f32"],
-                    help="KV pool format of the prefill workloads (f16: the tcgen05 kernel; "
-                         "q8_0 and f32: the mma.sync multi-query kernel)")
+                    help="KV pool format of the prefill workloads (all on the tcgen05 "
+                         "kernel: q8_0 after staging as f16 rows, f32 after staging as "
+                         "high/low f16 pairs)")
     ap.add_argument("--store", default=None, choices=["fused", "separate"],
                     help="store each layer's new row inside the decode launch "
                          "(mt_paged_attn_decode_append) or with its own mt_kv_store launch; "
