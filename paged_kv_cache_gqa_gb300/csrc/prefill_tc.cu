@@ -1111,64 +1111,87 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-// Merge the pieces of split tiles: one warp per tile row, lane l owns output
-// dims [l D/32, (l + 1) D/32); by log-sum-exp over the pieces' (max, sum)
-// records, then normalised. Rows of no query (destination -1) are skipped.
+// Merge the pieces of split tiles: one warp per tile row (the grid's warps
+// take the launch's tile rows in turn), lane l owns output dims [l D/32,
+// (l + 1) D/32); by log-sum-exp over the pieces' (max, sum) records, then
+// normalised. A row's headers and the outputs of its first kB pieces are
+// all requested before any is used, so a row of up to kB pieces costs one
+// L2 round trip. Rows of no query (destination -1) are skipped.
 template <int D>
-__global__ void __launch_bounds__(128) prefill_tc_combine_kernel(const __grid_constant__ PrefillParams p) {
-  constexpr int DV = D / 32;
+__global__ void __launch_bounds__(256) prefill_tc_combine_kernel(const __grid_constant__ PrefillParams p) {
+  constexpr int DV = D / 32, kB = 4;
   pdl_enter();
   const int n_tiles = p.rec_hdr[0], n_split = p.rec_hdr[1];
   if (n_split <= 1) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31;
   const size_t pstride = (size_t)kTcRows * (D + 4);  // from one piece of a tile to the next
-  for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-    for (int r = warp; r < kTcRows; r += 4) {
-      const float *rr = p.rec + ((size_t)t * n_split * kTcRows + r) * (D + 4);
-      float m = -INFINITY, l = 0.f;
-      int dst = -1;
-      if (lane < n_split) {
-        const float4 h = __ldcg(reinterpret_cast<const float4 *>(rr + lane * pstride));
-        m = h.x;
-        l = h.y;
-        dst = __float_as_int(h.z);
-      }
-      if (!(l > 0.f)) m = -INFINITY;
-      float M = m;
-      int d = dst;
+  const int n_rows = n_tiles * kTcRows;
+  for (int w = blockIdx.x * 8 + (threadIdx.x >> 5); w < n_rows; w += gridDim.x * 8) {
+    const int t = w / kTcRows, r = w % kTcRows;
+    const float *rr = p.rec + ((size_t)t * n_split * kTcRows + r) * (D + 4);
+    float m = -INFINITY, l = 0.f;
+    int dst = -1;
+    if (lane < n_split) {
+      const float4 h = __ldcg(reinterpret_cast<const float4 *>(rr + lane * pstride));
+      m = h.x;
+      l = h.y;
+      dst = __float_as_int(h.z);
+    }
+    // this lane's dims of pieces [j0, j0 + kB)
+    float v[kB][DV];
+    auto load = [&](int j0) {
 #pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        M = fmaxf(M, __shfl_xor_sync(kAll, M, o));
-        d = max(d, __shfl_xor_sync(kAll, d, o));
-      }
-      if (d < 0) continue;
-      const float f = m == -INFINITY ? 0.f : exp2f(m - M);
-      float L = l * f;
+      for (int jj = 0; jj < kB; ++jj) {
+        if (j0 + jj < n_split) {
+          const float *op = rr + (j0 + jj) * pstride + 4 + lane * DV;
 #pragma unroll
-      for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(kAll, L, o);
-      float acc[DV];
+          for (int e = 0; e < DV; e += 2) {
+            const float2 x = __ldcg(reinterpret_cast<const float2 *>(op + e));
+            v[jj][e] = x.x;
+            v[jj][e + 1] = x.y;
+          }
+        } else {
 #pragma unroll
-      for (int e = 0; e < DV; ++e) acc[e] = 0.f;
-      for (int j = 0; j < n_split; ++j) {
-        const float fj = __shfl_sync(kAll, f, j);
-        if (fj == 0.f) continue;
-        const float *op = rr + j * pstride + 4 + lane * DV;
-#pragma unroll
-        for (int e = 0; e < DV; e += 2) {
-          const float2 v = __ldcg(reinterpret_cast<const float2 *>(op + e));
-          acc[e] = fmaf(fj, v.x, acc[e]);
-          acc[e + 1] = fmaf(fj, v.y, acc[e + 1]);
+          for (int e = 0; e < DV; ++e) v[jj][e] = 0.f;
         }
       }
-      const bool any = L > 0.f;
-      const float inv = any ? 1.f / L : 0.f;
-      float *out = p.out + (size_t)d * D + lane * DV;
+    };
+    load(0);
+    if (!(l > 0.f)) m = -INFINITY;
+    float M = m;
+    int d = dst;
 #pragma unroll
-      for (int e = 0; e < DV; e += 2)
-        *reinterpret_cast<float2 *>(out + e) = make_float2(acc[e] * inv, acc[e + 1] * inv);
-      if (p.lse && lane == 0)
-        p.lse[d] = any ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+    for (int o = 16; o; o >>= 1) {
+      M = fmaxf(M, __shfl_xor_sync(kAll, M, o));
+      d = max(d, __shfl_xor_sync(kAll, d, o));
     }
+    if (d < 0) continue;
+    const float f = m == -INFINITY ? 0.f : exp2f(m - M);
+    float L = l * f;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(kAll, L, o);
+    float acc[DV];
+#pragma unroll
+    for (int e = 0; e < DV; ++e) acc[e] = 0.f;
+    for (int j0 = 0; j0 < n_split; j0 += kB) {
+      if (j0 > 0) load(j0);
+#pragma unroll
+      for (int jj = 0; jj < kB; ++jj) {
+        const float fs = __shfl_sync(kAll, f, (j0 + jj) & 31);
+        const float fj = j0 + jj < n_split ? fs : 0.f;  // the same in every lane
+        if (fj == 0.f) continue;  // an empty piece (or none): not read into the sum
+#pragma unroll
+        for (int e = 0; e < DV; ++e) acc[e] = fmaf(fj, v[jj][e], acc[e]);
+      }
+    }
+    const bool any = L > 0.f;
+    const float inv = any ? 1.f / L : 0.f;
+    float *out = p.out + (size_t)d * D + lane * DV;
+#pragma unroll
+    for (int e = 0; e < DV; e += 2)
+      *reinterpret_cast<float2 *>(out + e) = make_float2(acc[e] * inv, acc[e + 1] * inv);
+    if (p.lse && lane == 0)
+      p.lse[d] = any ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
   }
 }
 
@@ -1391,8 +1414,10 @@ mt_status launch_stage_f32_pair(const float *k_pool, const float *v_pool, const 
 mt_status launch_prefill_tc_combine(const PrefillParams &p, int head_dim, int n_ctas,
                                     cudaStream_t stream) {
   if (!p.rec) return MT_OK;
+  // a split launch has fewer tiles (of 128 rows) than SMs: a warp per row,
+  // 8 warps per CTA, 4 CTAs per SM
   auto kern = head_dim == 64 ? prefill_tc_combine_kernel<64> : prefill_tc_combine_kernel<128>;
-  return cuda_check(launch_pdl(kern, dim3(n_ctas), dim3(128), 0, stream, p),
+  return cuda_check(launch_pdl(kern, dim3(4 * n_ctas), dim3(256), 0, stream, p),
                     "prefill tc combine launch");
 }
 
