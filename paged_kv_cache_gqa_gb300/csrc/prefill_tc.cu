@@ -1198,11 +1198,11 @@ __global__ void __launch_bounds__(256) prefill_tc_combine_kernel(const __grid_co
 // q8_0 rows -> f16 rows for the tensor-core prefill. A CTA per (sequence,
 // block) unit at a time: the block's bs rows of K and its bs rows of V, each
 // contiguous in its pool, arrive in shared memory together by asynchronous
-// copies (16 bytes each when the row size allows, else 4), then thread t
-// converts 32-value groups
-// t, t + 256, ... (each group: an f16 scale, then 32 int8 codes, 34 bytes at
-// a 2-byte alignment) into 64 contiguous bytes of f16 rows: each value is
-// code * scale rounded once to the nearest f16.
+// copies (16 bytes each when the row size allows, else 4), then four
+// threads per 32-value group (an f16 scale, then 32 int8 codes, 34 bytes at
+// a 2-byte alignment) each convert 8 of its values into 16 bytes of the
+// group's 64 bytes of f16 rows, so a warp's stores cover 512 contiguous
+// bytes: each value is code * scale rounded once to the nearest f16.
 template <int CH>
 __device__ __forceinline__ void stage_copy(uint32_t dst, const void *src) {
   if constexpr (CH == 16)
@@ -1250,8 +1250,11 @@ __global__ void __launch_bounds__(256) stage_q8_f16_kernel(
     for (int kv = 0; kv < 2; ++kv) {
       const uint8_t *rows = raw + kv * blk_bytes;
       uint8_t *dst = (kv ? v16 : k16) + (size_t)unit * bs * rb16;
-      for (int gi = tid; gi < bs * n_groups; gi += 256) {
-        const int r = gi / n_groups, g = gi - r * n_groups;
+      // quarter q of group g of row r: codes [8q, 8q + 8) -> output bytes
+      // [16q, 16q + 16) of the group's 64
+      for (int gi = tid; gi < bs * n_groups * 4; gi += 256) {
+        const int q = gi & 3, gq = gi >> 2;
+        const int r = gq / n_groups, g = gq - r * n_groups;
         const uint16_t *gp = reinterpret_cast<const uint16_t *>(rows + r * row_bytes + g * 34);
         const __half dh = __ushort_as_half(gp[0]);
         const __half2 d2 = __halves2half2(dh, dh);
@@ -1259,10 +1262,11 @@ __global__ void __launch_bounds__(256) stage_q8_f16_kernel(
         // + 128 as bytes, minus 1152), then one f16 multiply by the scale:
         // the exact product rounded to the nearest f16
         const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-        uint32_t w[16];
+        uint32_t w[4];
 #pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-          const uint32_t b4 = ((uint32_t)gp[2 + j] << 16 | gp[1 + j]) ^ 0x80808080u;
+        for (int j = 0; j < 4; j += 2) {
+          const uint32_t b4 =
+              ((uint32_t)gp[2 + 4 * q + j] << 16 | gp[1 + 4 * q + j]) ^ 0x80808080u;
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             uint32_t hb = __byte_perm(b4, 0x64646464u, t ? 0x4342 : 0x4140);
@@ -1274,15 +1278,13 @@ __global__ void __launch_bounds__(256) stage_q8_f16_kernel(
         // a product rounds to infinity only if |scale| * 128 can reach 65520
         if (r < n_valid && fabsf(__half2float(dh)) * 128.f >= 65504.f) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < 4; ++j) {
             const __half2 h = *reinterpret_cast<const __half2 *>(&w[j]);
             big |= __hisinf(__low2half(h)) || __hisinf(__high2half(h));
           }
         }
-        uint4 *o = reinterpret_cast<uint4 *>(dst + (size_t)r * rb16 + (size_t)g * 64);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          o[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        *reinterpret_cast<uint4 *>(dst + (size_t)r * rb16 + (size_t)g * 64 + q * 16) =
+            make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
     __syncthreads();  // the buffer is refilled for the next unit
