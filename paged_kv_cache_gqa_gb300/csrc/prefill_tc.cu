@@ -21,7 +21,8 @@
 //     K stage is refilled as soon as its scores are computed, a V stage once
 //     its P.V has run (a ring of a single stage, f32 pools at head_dim 128,
 //     fills and frees each stage by halves); holes are not read at all;
-//   * one MMA warp computes S(c) = Q_hi K^T + Q_lo K^T (M = 128, N = 128,
+//   * one MMA warp computes S(c) = Q_hi K^T + Q_lo K^T (paired mode: + Q_hi
+//     K_lo^T, K being K_hi + K_lo) (M = 128, N = 128,
 //     f16 in, f32 accumulated in tensor memory; q = Q_hi + Q_lo to ~2^-22, so
 //     scores keep float32 accuracy; Q read from tensor memory, so only K
 //     takes shared-memory bandwidth) into one of two S buffers, as soon as the
@@ -77,7 +78,8 @@ constexpr int kHC = kChunk / kTPR;         // score columns per softmax thread
 // tensor-memory columns: S double buffer [0, 128), [128, 256) (S(x) in buffer
 // x % 2; P(x) as f16 pairs over the scores it came from: the thread owning
 // score columns [kHC h, kHC h + kHC) writes their kHC / 2 probability pairs
-// to [kHC h, kHC h + kHC / 2)); O [256, 256 + d); the tile's Q as f16 pairs
+// to [kHC h, kHC h + kHC / 2), and in the paired mode the pairs of the low
+// parts to [kHC h + kHC / 2, kHC h + kHC)); O [256, 256 + d); the tile's Q as f16 pairs
 // (the A operand of S), high [384, 384 + d / 2) and low [448, 448 + d / 2)
 constexpr int kSCols = kChunk;
 constexpr int kOCol = 2 * kChunk;
