@@ -248,7 +248,9 @@ size_t mt_paged_prefill_workspace_bytes(const mt_paged_prefill_args *args);
  * rounded: x to ~2^-22 relative), scores and P.V each from three products
  * (float32 accuracy; a value beyond the f16 range is flagged); head_dim 256
  * runs a warp-level tensor-core kernel that keeps codes exact and applies
- * scales in float32. The workspace (mt_paged_prefill_workspace_bytes) holds
+ * scales in float32. A q8_0 or f32 call whose staged rows (n_seqs x
+ * max_blocks x block_size) would reach 2^31 returns MT_ERR_UNSUPPORTED. The
+ * workspace (mt_paged_prefill_workspace_bytes) holds
  * the staged rows of q8_0 and f32 calls and must be 16-byte aligned. */
 mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *args, void *workspace,
                                 size_t workspace_bytes, mt_stream stream);

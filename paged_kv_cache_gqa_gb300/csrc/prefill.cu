@@ -14,8 +14,7 @@
 // Which kernel: head_dim 64 and 128 run the tcgen05 kernel (prefill_tc.cu) —
 // f16 pools directly, q8_0 pools after a pass that stages the call's blocks
 // as f16 rows, f32 pools after one that stages them as high / low f16 pairs.
-// The kernel below takes head_dim 256 (f16, q8_0) and calls too large to
-// stage.
+// The kernel below takes head_dim 256 (f16, q8_0).
 //
 // How (GB300): a tile is 64 rows (query token, head) of one KV head — 64/GP
 // consecutive queries of one sequence times the GP (padded) heads of the
@@ -50,8 +49,7 @@ constexpr int kSplitCtas = 160;
 // a table of n_seqs x max_blocks staged ids, then the K and the V staged
 // pools of n_seqs x max_blocks x block_size rows (2 or 4 bytes per value). 0
 // when the call does not stage (f16 pools, other shapes; staged ids that
-// would not fit the kernel's 32-bit cell indices: the mma.sync kernel runs
-// instead).
+// would not fit the kernel's 32-bit cell indices: the call is refused).
 size_t tc_stage_bytes(const mt_paged_prefill_args *a) {
   if (a->fmt == MT_KV_F16 || !prefill_tc_supported(a->fmt, a->head_dim, a->block_size)) return 0;
   const long long cells = (long long)a->n_seqs * a->max_blocks * a->block_size;
@@ -350,15 +348,6 @@ mt_status launch_d(int gp, const PrefillParams &p, int n_ctas, cudaStream_t s) {
   }
 }
 
-template <int FMT>
-mt_status launch_f(int d, int gp, const PrefillParams &p, int n_ctas, cudaStream_t s) {
-  if (d == 64) return launch_d<FMT, 64>(gp, p, n_ctas, s);
-  if constexpr (FMT != MT_KV_F32) {
-    if (d == 256) return launch_d<FMT, 256>(gp, p, n_ctas, s);
-  }
-  return launch_d<FMT, 128>(gp, p, n_ctas, s);
-}
-
 int pad_g(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : G <= 8 ? 8 : 0; }
 
 }  // namespace
@@ -443,6 +432,10 @@ extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void 
   const bool tc = a->fmt == MT_KV_F16 ? prefill_tc_supported(a->fmt, a->head_dim, a->block_size)
                                       : stage_bytes > 0;
   const bool pair = a->fmt == MT_KV_F32;
+  if (!tc && a->head_dim != 256)
+    return fail(MT_ERR_UNSUPPORTED,
+                "prefill: q8_0 / f32 call too large to stage (n_seqs * max_blocks * block_size "
+                "cells must stay below 2^31)");
   const int32_t *table = a->block_table;
   if (stage_bytes) {
     uint8_t *ws = static_cast<uint8_t *>(workspace) + kPrefillWsBytes + rec_bytes;
@@ -484,12 +477,10 @@ extern "C" mt_status mt_paged_attn_prefill(const mt_paged_prefill_args *a, void 
       if (st != MT_OK) return st;
       continue;
     }
+    // head_dim 256 (f16, q8_0): the mma.sync kernel
     const int n_ctas = di.n_sm * 2;
-    switch (a->fmt) {
-      case MT_KV_F32: st = launch_f<MT_KV_F32>(a->head_dim, GP, p, n_ctas, s); break;
-      case MT_KV_F16: st = launch_f<MT_KV_F16>(a->head_dim, GP, p, n_ctas, s); break;
-      default: st = launch_f<MT_KV_Q8_0>(a->head_dim, GP, p, n_ctas, s); break;
-    }
+    st = a->fmt == MT_KV_F16 ? launch_d<MT_KV_F16, 256>(GP, p, n_ctas, s)
+                             : launch_d<MT_KV_Q8_0, 256>(GP, p, n_ctas, s);
     if (st != MT_OK) return st;
   }
   return ok();
