@@ -110,6 +110,16 @@ def test_prefill_q8_with_spans(mt):
     check(mt, w, q, q_start, spans=random_spans(rng, w, q_start))
 
 
+def test_prefill_f32_with_spans(mt):
+    # f32 pools (staged as high / low f16 pairs) with a random [lo, hi)
+    # window per query, contexts of a few chunks
+    rng = np.random.default_rng(60)
+    w = workloads.llama3_f16(seed=60, n_seqs=4, ctx_lo=100, ctx_hi=400, fmt="f32",
+                             n_heads=8, n_kv_heads=2, head_dim=128)
+    q, q_start = make_queries(w, rng, 40)
+    check(mt, w, q, q_start, spans=random_spans(rng, w, q_start))
+
+
 @pytest.mark.parametrize("fmt", ["f16", "q8_0", "f32"])
 def test_prefill_kv_map_runs(mt, fmt):
     rng = np.random.default_rng(54)
@@ -135,9 +145,10 @@ def test_prefill_shape_grid(mt, fmt, d, bs, hq, hkv):
     check(mt, w, q, q_start)
 
 
-def test_prefill_holes_and_empty(mt):
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "f32"])
+def test_prefill_holes_and_empty(mt, fmt):
     rng = np.random.default_rng(56)
-    w = workloads.llama3_f16(seed=56, n_seqs=5, ctx_lo=40, ctx_hi=200)
+    w = workloads.llama3_f16(seed=56, n_seqs=5, ctx_lo=40, ctx_hi=200, fmt=fmt)
     table = w.block_table.copy()
     table[0, 1] = -1
     table[3, 0] = -1

@@ -167,6 +167,25 @@ def test_prefill_tc_f32_paired(mt, d, bs, hq, hkv):
     check_pools(mt, w, q, q_start, kp, vp)
 
 
+def test_prefill_tc_f32_staged_flags_bad_ids(mt):
+    # an out-of-range block id is flagged by the f32 staging pass and read as
+    # a hole; the other rows are unaffected
+    rng = np.random.default_rng(92)
+    w = workloads.llama3_f16(seed=92, n_seqs=2, ctx_lo=300, ctx_hi=400, fmt="f32")
+    q, q_start = make_queries(w, rng, 40)
+    kp, vp = oracle_pools(w)
+    table = w.block_table.copy()
+    table[1, 4] = w.n_phys_blocks + 7
+    got, _, st = run_prefill(mt, w, q, q_start, kp, vp, table=table)
+    assert st == mt.MT_ERR_DEVICE_CHECK
+    holed = table.copy()
+    holed[1, 4] = -1
+    want, _ = oatt.paged_attn_prefill(w.fmt, q, kp, vp, holed, w.context_lens, q_start, None,
+                                      None, w.n_heads, w.n_kv_heads, w.head_dim, w.block_size,
+                                      w.scale)
+    assert_close(got, want, TOL[w.fmt], "f32 staged prefill with a bad id")
+
+
 def test_prefill_tc_f32_flags_f16_overflow(mt):
     # an f32 value outside the f16 range (1e5) has no high / low f16 pair:
     # the staging pass flags it
