@@ -2,8 +2,8 @@
 and its host-side logic agrees with the oracle (no GPU needed).
 
 Host-side entry points tested here: mt_kv_row_bytes, mt_order_moves,
-mt_check_moves, mt_kv_grow_capacity, and the argument checks that run
-before any launch.
+mt_check_moves, mt_kv_grow_capacity, mt_paged_prefill_workspace_bytes, and
+the argument checks that run before any launch.
 """
 import os
 import re
@@ -125,3 +125,36 @@ def test_host_checks_reject_before_launch(mt):
     assert st == mt.MT_ERR_INVALID_ARG and "old_cap" in mt.mt_last_error()
     st = mt.lib().mt_kv_quant_int4(2, None, 16, 4, 256, 10, None, 1, None, None, None, None)
     assert st == mt.MT_ERR_UNSUPPORTED
+
+
+def _prefill_ws(mt, fmt, n_seqs, n_tokens, hq, hkv, d, bs, max_blocks):
+    a = mt.mt_paged_prefill_args()
+    a.fmt = mt._fmt(fmt)
+    a.n_seqs, a.n_tokens, a.n_heads, a.n_kv_heads, a.head_dim = n_seqs, n_tokens, hq, hkv, d
+    a.block_size, a.max_blocks, a.n_phys_blocks = bs, max_blocks, n_seqs * max_blocks
+    return mt.mt_paged_prefill_workspace_bytes(a)
+
+
+def test_prefill_workspace_holds_the_staged_rows(mt):
+    # the header's contract: q8_0 and f32 pools of head_dim 64 / 128 add the
+    # staging of the call's blocks, n_seqs x max_blocks x block_size rows of
+    # n_kv_heads x head_dim values as f16 (q8_0) or high / low f16 pairs
+    # (f32), for K and for V, plus a table of n_seqs x max_blocks ids; f16
+    # pools and head_dim 256 stage nothing
+    B, mb, bs, hq, hkv = 16, 128, 16, 32, 8
+    for d in (64, 128):
+        rows = B * mb * bs
+        base = _prefill_ws(mt, "f16", B, 8192, hq, hkv, d, bs, mb)
+        assert 0 < base <= 4096
+        q8 = _prefill_ws(mt, "q8_0", B, 8192, hq, hkv, d, bs, mb)
+        f32 = _prefill_ws(mt, "f32", B, 8192, hq, hkv, d, bs, mb)
+        need_q8 = 2 * rows * hkv * d * 2 + B * mb * 4
+        need_f32 = 2 * rows * hkv * d * 4 + B * mb * 4
+        assert need_q8 <= q8 - base < need_q8 + 4096
+        assert need_f32 <= f32 - base < need_f32 + 4096
+    d256 = [_prefill_ws(mt, f, B, 8192, 16, 4, 256, bs, mb) for f in ("f16", "q8_0")]
+    assert d256[0] == d256[1] == base
+    # few query rows (fewer tiles than SMs can take): room for the split
+    # records, 2 x 160 units of 128 rows x (head_dim + 4) floats
+    few = _prefill_ws(mt, "f16", 1, 100, hq, hkv, 128, bs, mb)
+    assert few - base >= 2 * 160 * 128 * (128 + 4) * 4
