@@ -794,19 +794,23 @@ def run_extra(args, rank, world, local_rank):
                                       "KV format: 64 seqs, ctx log-uniform [512,16384], 32/8 "
                                       "heads, head_dim 128; 4 rotated pool pairs per format"},
                "clocks": clk}
-    elif args.workload in ("prefill_f16", "prefill_f16_long"):
+    elif args.workload in ("prefill_f16", "prefill_f16_long", "prefill_smollm2"):
         # chunked prefill through the paged cache, Llama-3-8B-shaped heads, f16
         # pools, the queries' K/V rows already stored; 8 layers with their own
         # pools, so successive calls do not hit in L2. prefill_f16: 16
         # sequences at context 2048 whose last 512 positions are the queries;
         # prefill_f16_long: one sequence at context 32768 whose last 256
         # positions are the queries (one chunk of a long prompt: 64 tiles,
-        # fewer than the SMs)
+        # fewer than the SMs); prefill_smollm2: SmolLM2-135M heads (9/3,
+        # head_dim 64), 8 sequences at context 4096 whose last 512 positions
+        # are the queries
         long_ = args.workload == "prefill_f16_long"
-        n_seqs_p, ctx_p, n_q = (1, 32768, 256) if long_ else (16, 2048, 512)
+        smol = args.workload == "prefill_smollm2"
+        n_seqs_p, ctx_p, n_q = (1, 32768, 256) if long_ else (8, 4096, 512) if smol else (16, 2048, 512)
         pfmt = args.prefill_format
+        heads = dict(n_heads=9, n_kv_heads=3, head_dim=64) if smol else {}
         w = workloads.llama3_f16(seed=SEED + 9, n_seqs=n_seqs_p, ctx_lo=ctx_p, ctx_hi=ctx_p,
-                                 hist=False, fmt=pfmt)
+                                 hist=False, fmt=pfmt, **heads)
         layers, _, rb = _decode_setup(mtkv, w, 8, dev, g)
         table = torch.from_numpy(w.block_table).to(dev)
         ctx_d = torch.from_numpy(w.context_lens).to(dev)
@@ -851,9 +855,11 @@ def run_extra(args, rank, world, local_rank):
                             "note": "useful FLOPs (4 * pairs * heads * head_dim); the kernel "
                                     "also multiplies the low half of q and padding rows"},
                "kv_GB_per_s": round(len(calls) * kv_bytes / (ms * 1e-3) / 1e9, 1),
-               "config": {"workload": f"llama3-8b-shaped {pfmt} chunked prefill: {n_seqs_p} "
-                                      f"seqs x ctx {ctx_p}, last {n_q} positions as "
-                                      "queries, 32/8 heads, head_dim 128, bs 16, 8 layers"},
+               "config": {"workload": f"{'smollm2-135m' if smol else 'llama3-8b'}-shaped {pfmt} "
+                                      f"chunked prefill: {n_seqs_p} seqs x ctx {ctx_p}, last "
+                                      f"{n_q} positions as queries, "
+                                      f"{w.n_heads}/{w.n_kv_heads} heads, head_dim "
+                                      f"{w.head_dim}, bs 16, 8 layers"},
                "clocks": clk}
     elif args.workload == "longctx_int4":
         w = workloads.longctx_f16_int4(hist=False)
@@ -921,7 +927,8 @@ def main():
                          "runs it: one whole layer over all host cores, three times")
     ap.add_argument("--workload", default="llama3_f16",
                     choices=["llama3_f16", "smollm2_f32", "q8_prefix", "longctx_int4",
-                             "llama3_formats", "prefill_f16", "prefill_f16_long"],
+                             "llama3_formats", "prefill_f16", "prefill_f16_long",
+                             "prefill_smollm2"],
                     help="llama3_f16 is the benchmark line; the others measure the other kernels")
     ap.add_argument("--prefill-format", default="f16", choices=["f16", "q8_0", "f32"],
                     help="KV pool format of the prefill workloads (all on the tcgen05 "
